@@ -1,0 +1,275 @@
+"""CPU oracle of grouped MoE prefill -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference legs of ``bench.py`` may import or run this module.  The product
+path (the CUDA library and its Python binding) never calls it, and this
+module imports nothing from the product package.
+
+What it computes follows the page "perf(ds4): batch heterogeneous MoE prefill
+by expert" (Luce-Org/lucebox PR #640), Summary: tokens are routed to their
+top-k of up to 256 routed experts; a route histogram, an exclusive prefix over
+the expert counts and a scatter put token rows in expert-major order; grouped
+gate/up projections with SwiGLU and a grouped down projection run per expert;
+a weighted combine brings the expert outputs back to token order, and masked
+(non-owned) routes contribute exactly zero ("Summary" and "Correctness and
+validation").  The combine is the fused expert-major route combine of the page
+"perf(ds4): accelerate ROCm decode and long-context selection" (PR #667),
+lucebox8 A/B section, whose qualification on the page "perf(ds4): extend
+sparse prefill scheduling to 10K" (PR #684, "Historical qualification")
+includes a byte-exact signed-zero case.
+
+Everything floating-point is evaluated in float64 with no intermediate
+rounding.  The integer results (ids, counts, offsets, the permutation) are the
+plain definitions: a stable sort, a bincount, a cumulative sum.
+
+Readings of points the pages leave open (each one is also listed in the
+design notes of the repository):
+
+* top-k order: experts sorted by logit descending, ties to the lower expert
+  id; -0.0 and +0.0 compare equal.
+* gate weights: softmax over the k selected logits (identical to a softmax
+  over all experts renormalised over the selected k).
+* the mask applies after selection: a masked route keeps its slot and its
+  weight, is left out of the histogram, the scatter and the combine, and the
+  remaining weights are NOT renormalised.
+* row order inside an expert segment: ascending route index r = t*k + s.
+* SwiGLU: silu(x.Wg) * (x.Wu) with silu(a) = a / (1 + exp(-a)), no clamp.
+* combine: out[t] starts at +0.0 and adds w[t,s] * y(t,s) for ascending s,
+  skipping masked slots (never multiplying them).
+
+Storage: ``w_gate``/``w_up`` are [E][f][d] and ``w_down`` is [E][d][f]
+(K-contiguous rows).  A weight argument may also be a callable
+``e -> (w_gate_e, w_up_e, w_down_e)`` so that a caller can fetch one expert at
+a time from a bank that does not fit in host memory.
+
+Pins (tests marked "not gpu" check each function against something other
+than itself): hand-derived golden fixtures, brute-force top-k over all
+orderings on tiny inputs, a closed-form two-expert softmax, counting and
+permutation invariants, the E=1/k=1 reduction to a dense SwiGLU FFN, the k=E
+reduction to a full softmax mixture, and the all-masked exact +0.0 case.
+No function here is unpinned.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# A1: top-k routing
+# ---------------------------------------------------------------------------
+
+def route_topk(logits, k: int):
+    """Top-k expert ids and their gate weights for every token.
+
+    Page "perf(ds4): batch heterogeneous MoE prefill by expert", Summary
+    (routed experts, up to 256 of them); the page "perf(ds4): extend sparse
+    prefill scheduling to 10K", Summary (native top-6 routing is preserved).
+
+    Returns ``ids`` int32 [T][k] (descending logit, ties to the lower id) and
+    ``w`` float64 [T][k], the softmax of the k selected logits.
+    """
+    logits = np.asarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    expert = np.arange(E)
+    for t in range(T):
+        # Stable order by (-logit, expert id).  np.lexsort sorts by the LAST key
+        # first, so the logit key comes last.  -0.0 and +0.0 compare equal.
+        order = np.lexsort((expert, -logits[t].astype(np.float64)))
+        chosen = order[:k]
+        ids[t] = chosen
+        sel = logits[t, chosen].astype(np.float64)
+        z = np.exp(sel - sel[0])           # sel[0] is the largest selected logit
+        w[t] = z / z.sum()
+    return ids, w
+
+
+# ---------------------------------------------------------------------------
+# A2 / A3: route histogram and exclusive prefix
+# ---------------------------------------------------------------------------
+
+def _unmasked(ids, mask):
+    ids = np.asarray(ids)
+    if mask is None:
+        return np.ones(ids.shape, dtype=bool)
+    return np.asarray(mask).reshape(ids.shape) == 0
+
+
+def route_histogram(ids, mask, E: int):
+    """counts[e] = number of unmasked routes whose expert is e.
+
+    Page "perf(ds4): batch heterogeneous MoE prefill by expert", Summary
+    (GPU-native route histogram for up to 256 experts; masked owner routes are
+    not computed here).
+    """
+    ids = np.asarray(ids)
+    keep = _unmasked(ids, mask)
+    return np.bincount(ids[keep].ravel(), minlength=E).astype(np.int32)
+
+
+def prefix_offsets(counts):
+    """offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]  (length E+1).
+
+    Page "perf(ds4): batch heterogeneous MoE prefill by expert", Summary
+    (exclusive prefix over the expert counts).
+    """
+    counts = np.asarray(counts, dtype=np.int64)
+    offsets = np.zeros(counts.size + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    return offsets.astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# A4: scatter to expert-major order
+# ---------------------------------------------------------------------------
+
+def scatter_permutation(ids, mask):
+    """Expert-major permutation of the unmasked routes.
+
+    Page "perf(ds4): batch heterogeneous MoE prefill by expert", Summary
+    (GPU-native scatter); row order within an expert keeps the route order,
+    as the page "perf(ds4): extend sparse prefill scheduling to 10K" asks of
+    selected rows (Summary: selected-row order is preserved).
+
+    Returns ``row_of_route`` int32 [T*k] (-1 for a masked route) and
+    ``route_of_row`` int32 [T*k] (-1 for the unused rows R .. T*k-1), where
+    R is the number of unmasked routes.
+    """
+    ids = np.asarray(ids)
+    flat = ids.reshape(-1)
+    keep = _unmasked(ids, mask).reshape(-1)
+    routes = np.nonzero(keep)[0]                       # ascending route index
+    order = np.argsort(flat[routes], kind="stable")    # group by expert, keep route order
+    route_of_row = np.full(flat.size, -1, dtype=np.int32)
+    route_of_row[: routes.size] = routes[order]
+    row_of_route = np.full(flat.size, -1, dtype=np.int32)
+    row_of_route[routes[order]] = np.arange(routes.size, dtype=np.int32)
+    return row_of_route, route_of_row
+
+
+def scatter_rows(x, route_of_row, k: int):
+    """xs[i] = x[token of route route_of_row[i]] for the R used rows."""
+    x = np.asarray(x)
+    used = np.asarray(route_of_row)
+    used = used[used >= 0]
+    return x[used // k]
+
+
+# ---------------------------------------------------------------------------
+# A5 / A6: per-expert SwiGLU FFN
+# ---------------------------------------------------------------------------
+
+def silu(a):
+    """silu(a) = a / (1 + exp(-a)); exp overflow gives -0.0, never NaN."""
+    a = np.asarray(a, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
+
+
+def _expert(weights, e):
+    if callable(weights):
+        wg, wu, wd = weights(e)
+    else:
+        wg, wu, wd = weights[0][e], weights[1][e], weights[2][e]
+    return (np.asarray(wg, dtype=np.float64), np.asarray(wu, dtype=np.float64),
+            np.asarray(wd, dtype=np.float64))
+
+
+def expert_ffn(rows, w_gate_e, w_up_e, w_down_e):
+    """y = (silu(x.Wg) * (x.Wu)) . Wd for each row x, in float64.
+
+    Page "perf(ds4): batch heterogeneous MoE prefill by expert", Summary
+    (grouped gate/up/down projections per expert); the SwiGLU between them is
+    the "DS4 SwiGLU split op" of the page "perf(ggml): reuse ROCmFP4 weights
+    across q=4 columns".  Storage: w_gate_e, w_up_e [f][d]; w_down_e [d][f].
+    """
+    x = np.asarray(rows, dtype=np.float64)
+    g = x @ np.asarray(w_gate_e, dtype=np.float64).T    # [n][f]
+    u = x @ np.asarray(w_up_e, dtype=np.float64).T      # [n][f]
+    h = silu(g) * u                                      # [n][f]
+    return h @ np.asarray(w_down_e, dtype=np.float64).T  # [n][d]
+
+
+def grouped_ffn(xs, offsets, weights):
+    """Expert outputs y [R][d]: rows offsets[e] .. offsets[e+1]-1 go through expert e.
+
+    Page "perf(ds4): batch heterogeneous MoE prefill by expert", Summary
+    (one grouped gate/up/down graph instead of a serial graph per active
+    expert).  Experts with no rows are skipped.
+    """
+    xs = np.asarray(xs, dtype=np.float64)
+    offsets = np.asarray(offsets)
+    E = offsets.size - 1
+    y = np.zeros((int(offsets[E]), xs.shape[1]), dtype=np.float64)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            y[lo:hi] = expert_ffn(xs[lo:hi], *_expert(weights, e))
+    return y
+
+
+# ---------------------------------------------------------------------------
+# A7: weighted combine back to token order
+# ---------------------------------------------------------------------------
+
+def combine(y, row_of_route, w, T: int, k: int):
+    """out[t] = +0.0 + sum over ascending unmasked slots s of w[t,s] * y[row(t,s)].
+
+    Page "perf(ds4): accelerate ROCm decode and long-context selection",
+    lucebox8 A/B (fused expert-major combine replacing the reduce/multiply
+    launches); page "perf(ds4): batch heterogeneous MoE prefill by expert",
+    Summary (masked owner routes are exact zero contributions).
+    """
+    y = np.asarray(y, dtype=np.float64)
+    rows = np.asarray(row_of_route).reshape(T, k)
+    w = np.asarray(w, dtype=np.float64).reshape(T, k)
+    d = y.shape[1] if y.ndim == 2 else 0
+    out = np.zeros((T, d), dtype=np.float64)          # +0.0 everywhere
+    for s in range(k):
+        used = rows[:, s] >= 0
+        out[used] += w[used, s, None] * y[rows[used, s]]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The whole path, and a per-token form for spot checks at full size
+# ---------------------------------------------------------------------------
+
+def moe_forward(logits, x, weights, k: int, mask=None):
+    """Every intermediate of the path for one chunk, as a dict."""
+    logits = np.asarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    ids, w = route_topk(logits, k)
+    counts = route_histogram(ids, mask, E)
+    offsets = prefix_offsets(counts)
+    row_of_route, route_of_row = scatter_permutation(ids, mask)
+    xs = scatter_rows(x, route_of_row, k)
+    y = grouped_ffn(xs, offsets, weights)
+    out = combine(y, row_of_route, w, T, k)
+    return {"ids": ids, "w": w, "counts": counts, "offsets": offsets,
+            "row_of_route": row_of_route, "route_of_row": route_of_row,
+            "xs": xs, "y": y, "out": out}
+
+
+def token_outputs(tokens, ids, w, mask, x, weights):
+    """out[t] for the listed tokens, evaluated route by route from the definition.
+
+    Same result as ``moe_forward(...)["out"][tokens]`` (up to float64
+    rounding order) without running the other tokens: used to spot-check
+    full-size runs on a sample of tokens.
+    """
+    ids = np.asarray(ids)
+    w = np.asarray(w, dtype=np.float64)
+    keep = _unmasked(ids, mask)
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros((len(tokens), x.shape[1]), dtype=np.float64)
+    for i, t in enumerate(tokens):
+        for s in range(ids.shape[1]):
+            if keep[t, s]:
+                y = expert_ffn(x[t][None, :], *_expert(weights, int(ids[t, s])))[0]
+                out[i] += w[t, s] * y
+    return out
