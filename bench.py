@@ -1,0 +1,442 @@
+"""Benchmark of grouped MoE prefill on GB300 (one JSON line on stdout).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole path (top-k routing, histogram, prefix,
+scatter, grouped gate/up+SwiGLU, grouped down, combine) over one synthetic
+prefill chunk already resident in HBM.  The default workload is the
+2048-token chunk (E=256, top-6, d=4096, f=2048, 10% of routes masked).
+Under torchrun each rank runs an independent replica on its own GPU with its
+own seed (no data-path collective); value = tokens of all ranks / the
+slowest rank's time.
+
+--impl reference times the CPU oracle (float64, numpy) on the host cores on a
+bounded sample of the same workload, as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "grouped MoE prefill tokens/s (T=401/2048/8192, E=256, top-6); % of roofline"
+UNIT = "tokens/s"
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+        self.t_start = self.t_end = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu_index), "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def mark(self, start: bool):
+        if start:
+            self.t_start = time.time()
+        else:
+            self.t_end = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.45)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        # samples while the GPU was busy (clock above idle) are the "under load" ones
+        busy = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def _workload(name: str, rank: int):
+    from workloads import CONFIGS
+    cfg = CONFIGS[name]
+    if rank:
+        cfg = cfg.replace(seed=cfg.seed + 1000 * rank)
+    return cfg
+
+
+def _oracle_inputs(inp, tokens):
+    """Host (float64) copies of the inputs a token sample needs: its logits, rows, mask and experts."""
+    from oracle import moe_oracle as mo
+    cfg = inp["cfg"]
+    logits = inp["logits"].float().cpu().numpy()[tokens]
+    x = inp["x"].float().cpu().numpy()[tokens]
+    mask = None if inp["mask"] is None else inp["mask"].cpu().numpy()[tokens]
+    ids, _ = mo.route_topk(logits, cfg.k)
+    experts = sorted(set(ids.ravel().tolist()))
+    bank = {}
+    for e in experts:
+        bank[e] = tuple(t[e].float().cpu().numpy() for t in (inp["w_gate"], inp["w_up"], inp["w_down"]))
+    zero = None
+    def get(e):
+        nonlocal zero
+        if e in bank:
+            return bank[e]
+        if zero is None:
+            zero = (np.zeros((cfg.f, cfg.d), np.float32), np.zeros((cfg.f, cfg.d), np.float32),
+                    np.zeros((cfg.d, cfg.f), np.float32))
+        return zero
+    return logits, x, mask, get
+
+
+def _time_oracle(inp, n_tokens: int):
+    """Seconds the oracle takes for the whole path over the first n_tokens tokens."""
+    from oracle import moe_oracle as mo
+    cfg = inp["cfg"]
+    cache = inp.setdefault("_oracle_sample", {})
+    if n_tokens not in cache:
+        cache.clear()
+        cache[n_tokens] = _oracle_inputs(inp, list(range(n_tokens)))
+    logits, x, mask, get = cache[n_tokens]
+    t0 = time.perf_counter()
+    mo.moe_forward(logits, x, get, cfg.k, mask)
+    return time.perf_counter() - t0
+
+
+MAX_ORACLE_TOKENS = 16  # bounds the host copy of the sampled experts (<= 96 experts, fp32)
+
+
+def _size_oracle_sample(inp, budget_s: float):
+    t1 = _time_oracle(inp, 1)
+    n = int(max(1, min(inp["cfg"].T, MAX_ORACLE_TOKENS, budget_s / max(t1, 1e-3))))
+    return n, t1
+
+
+def _cpu_desc():
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return model
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    from workloads import make_inputs
+    cfg = _workload(args.workload, 0)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(cfg, device="cpu", weights_device=dev)
+    per_step_budget = max(0.05, args.reference_budget_s / max(1, args.steps + args.warmup))
+    n, _ = _size_oracle_sample(inp, per_step_budget)
+    for _ in range(args.warmup):
+        _time_oracle(inp, n)
+    total = 0.0
+    for _ in range(args.steps):
+        total += _time_oracle(inp, n)
+    value = n * args.steps / total
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} tokens of the {cfg.T}-token chunk per step (numpy float64)",
+                         "cpu": _cpu_desc()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sparse_moe_expert_top_gb300", "csrc", n), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(kernel: str, workload: str, units: float):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    ent = rec.get(kernel, {}).get(workload)
+    if not ent or ent.get("src_hash") != _src_hash(*ent.get("sources", [])):
+        return None
+    return ent["dram_bytes_per_launch"]
+
+
+def run_ours(args, rank: int, world: int):
+    from sparse_moe_expert_top_gb300 import build as _build
+    _build.build()
+    from sparse_moe_expert_top_gb300 import moe as M
+    from workloads import make_inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg = _workload(args.workload, rank)
+    inp = make_inputs(cfg, device=dev)
+    T, E, k, d, f = cfg.T, cfg.E, cfg.k, cfg.d, cfg.f
+    dtype = inp["x"].dtype
+    bufs = M.MoEBuffers(T, E, k, d, f, dtype, device=dev)
+    logits, x, mask = inp["logits"], inp["x"], inp["mask"]
+    wg, wu, wd = inp["w_gate"], inp["w_up"], inp["w_down"]
+
+    names = ("topk", "histogram", "prefix", "scatter", "gate_up", "down", "combine")
+
+    def step(events=None):
+        b = bufs
+        calls = (
+            lambda: M.moe_route_topk(logits, k, b.ids, b.w),
+            lambda: M.moe_route_histogram(b.ids, mask, E, b.counts, b.ws),
+            lambda: M.moe_prefix_offsets(b.counts, T, k, b.offsets, b.ws),
+            lambda: M.moe_scatter_rows(x, b.ids, mask, b.offsets, b.xs, b.row_of_route, b.route_of_row, b.ws),
+            lambda: M.moe_grouped_gate_up(b.xs, b.offsets, wg, wu, b.h),
+            lambda: M.moe_grouped_down(b.h, b.offsets, wd, b.y),
+            lambda: M.moe_combine(b.y, b.row_of_route, b.w, b.out),
+        )
+        for i, c in enumerate(calls):
+            if events is not None:
+                events[i][0].record()
+            c()
+            if events is not None:
+                events[i][1].record()
+
+    for _ in range(args.warmup):
+        step()
+    M.moe_check_device_error()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in names] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    start.record()
+    for s in range(args.steps):
+        step(ev[s])
+    end.record()
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    clk = clocks.stop()
+    M.moe_check_device_error()
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+    per_kernel = {n: statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
+                  for i, n in enumerate(names)}
+
+    # ---- end to end through the public API: pinned host inputs in, output out
+    h_logits = logits.cpu().pin_memory()
+    h_x = x.cpu().pin_memory()
+    h_mask = None if mask is None else mask.cpu().pin_memory()
+    h_out = torch.empty(T, d, dtype=torch.float32).pin_memory()
+    d_logits, d_x = torch.empty_like(logits), torch.empty_like(x)
+    d_mask = None if mask is None else torch.empty_like(mask)
+    h2d = h_logits.numel() * 4 + h_x.numel() * h_x.element_size() + (0 if h_mask is None else h_mask.numel())
+    d2h = h_out.numel() * 4
+
+    def e2e_step():
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        if d_mask is not None:
+            d_mask.copy_(h_mask, non_blocking=True)
+        out = M.moe_forward(d_logits, d_x, d_mask, wg, wu, wd, k, bufs)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_s = float(te.item())
+    assert torch.equal(h_out, bufs.out.cpu()), "end-to-end output differs from the device-resident run"
+
+    if rank != 0:
+        return
+
+    # ---- roofline of the dominant kernel (grouped gate/up + SwiGLU)
+    counts = bufs.counts.cpu().numpy()
+    R = int(counts.sum())
+    touched = int(np.count_nonzero(counts))
+    es = 2 if dtype == torch.bfloat16 else 4
+    gate_up_bytes = touched * 2 * f * d * es + R * d * es + R * f * es
+    down_bytes = touched * d * f * es + R * f * es + R * d * 4
+    peaks = _peaks()
+    gu_ms = per_kernel["gate_up"]
+    achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
+    traffic = _profiled_traffic("gate_up", cfg.name, R)
+    roofline = {"kernel": "moe_grouped_gate_up (ffn_tc_kernel<gated>)", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": traffic, "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": gate_up_bytes, "avg_launch_ms": gu_ms}
+    # whole-path roofline: the slower of FLOPs at the dense bf16 tensor peak
+    # and the path's algorithmic bytes at HBM bandwidth
+    flops = 6.0 * R * d * f
+    path_bytes = (T * E * 4 + T * k * 8                      # routing
+                  + T * d * es + R * d * es                  # scatter
+                  + gate_up_bytes + down_bytes               # grouped FFN
+                  + R * d * 4 + T * d * 4)                   # combine
+    t_roof = max(flops / (peaks["bf16_tflops_sustained"] * 1e12), path_bytes / (peaks["hbm_gbs"] * 1e9))
+    ms_per_step = elapsed_ms / args.steps
+    value = world * T * args.steps / (elapsed_ms * 1e-3)
+
+    # ---- CPU baseline: the oracle on the host cores, bounded sample
+    cpu = None
+    if not args.no_cpu_baseline:
+        n, _ = _size_oracle_sample(inp, args.cpu_budget_s)
+        secs = _time_oracle(inp, n)
+        cpu = {"value": n / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"first {n} of {T} tokens, whole path in float64 (numpy, BLAS on all cores), "
+                         f"{secs:.1f} s", "cpu": _cpu_desc()}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "T": T, "d": d, "f": f, "E": E, "k": k, "mask_p": cfg.mask_p,
+                   "routes_unmasked": R, "experts_touched": touched,
+                   "l2": f"inputs larger than L2: {touched * 3 * d * f * es / 1e9:.1f} GB of touched expert "
+                         "weights streamed per step (L2 129 MB), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "e2e": {"value": world * T * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (7 if dtype == torch.bfloat16 else 9),
+        "roofline": roofline,
+        "path_roofline": {"flops": flops, "bytes": path_bytes, "t_roof_ms": t_roof * 1e3,
+                          "frac": t_roof * 1e3 / ms_per_step,
+                          "tflops": flops / (ms_per_step * 1e-3) / 1e12},
+        "kernels_ms": per_kernel,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="prefill_t2048")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--reference-budget-s", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

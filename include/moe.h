@@ -1,0 +1,199 @@
+/*
+ * moe.h -- C-ABI of the GB300 (sm_103a) grouped MoE prefill library.
+ *
+ * The path computed here is the heterogeneous MoE prefill batched by expert
+ * of the page "perf(ds4): batch heterogeneous MoE prefill by expert"
+ * (Luce-Org/lucebox PR #640), Summary: every token is routed to its top-k of
+ * up to 256 routed experts; a route histogram, an exclusive prefix over the
+ * expert counts and a scatter put the token rows in expert-major order;
+ * grouped gate/up projections with SwiGLU and a grouped down projection run
+ * per expert; a weighted combine returns the expert outputs to token order,
+ * and masked (non-owned) routes contribute exactly zero.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *   its description says otherwise.  The library never allocates device
+ *   memory and never frees caller memory.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every call only enqueues work on `stream` and returns; nothing
+ *   synchronises except moe_check_device_error().
+ * - Matrices are dense and row-major.  Notation: T tokens, E experts
+ *   (1..256), k experts per token (1..min(E,16)), d hidden size, f expert FFN
+ *   size, R = number of unmasked routes (<= T*k), "route" r = t*k + s for
+ *   token t and slot s.
+ * - Expert weights are stored K-contiguous (the nn.Linear convention):
+ *   w_gate and w_up are [E][f][d], w_down is [E][d][f].
+ * - Compact (expert-major) buffers xs, h and y are sized for the worst case,
+ *   T*k rows ("capacity"); rows R .. T*k-1 are zero-filled by the call that
+ *   produces the buffer.  R itself stays on the device in offsets[E].
+ * - Operand types: MOE_BF16 (bf16 operands, fp32 accumulation in tensor
+ *   memory, h stored as bf16) or MOE_F32 (fp32 operands and fp32 FMA
+ *   arithmetic, h stored as fp32).  y and out are always fp32.
+ * - Row starts of x, xs, h, y and out must be 16-byte aligned: the base
+ *   pointers must be 16-byte aligned and d*sizeof(operand), f*sizeof(operand)
+ *   multiples of 16 bytes.  The bf16 tensor-core path needs d and f to be
+ *   multiples of 128.
+ * - Errors: a call returns MOE_ERR_INVALID_ARG without enqueuing anything
+ *   when an argument is out of range, null where it must not be, or
+ *   misaligned; MOE_ERR_UNSUPPORTED when the current device is not an
+ *   sm_103 GPU or the operand type is unknown; MOE_ERR_CUDA when a launch
+ *   fails (moe_last_cuda_error() gives the cudaError_t).  Conditions that are
+ *   only visible on the device (inconsistent offsets, a bounded wait that ran
+ *   out) set a sticky device error word instead; moe_check_device_error()
+ *   reports and clears it.
+ * - The calls keep no host state between calls apart from a per-device
+ *   cache (SM count, kernel attributes, the address of the device error
+ *   word); they are safe to call from several host threads.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* bad size, null pointer or misalignment (host check), or bad offsets (device check) */
+    MOE_ERR_UNSUPPORTED = 2,  /* not an sm_103 device, or an unknown operand type */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed; see moe_last_cuda_error() */
+    MOE_ERR_TIMEOUT = 4       /* a bounded wait inside a kernel ran out (device error word) */
+} moe_status;
+
+typedef enum moe_dtype {
+    MOE_F32 = 0,
+    MOE_BF16 = 1
+} moe_dtype;
+
+/* Library version as 10000*major + 100*minor + patch. */
+int moe_version(void);
+
+/* Static text for a status code (never NULL). */
+const char* moe_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call made by this library on this
+ * host thread (0 if none). */
+int moe_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears the sticky device error word
+ * of the current device.  Returns MOE_OK, MOE_ERR_TIMEOUT (a bounded wait in
+ * a kernel ran out; that kernel's outputs are undefined) or
+ * MOE_ERR_INVALID_ARG (a kernel found inconsistent offsets and skipped its
+ * work). */
+moe_status moe_check_device_error(void* stream);
+
+/* Bytes of scratch workspace `ws` needed by moe_route_histogram,
+ * moe_prefix_offsets, moe_scatter_rows and moe_forward for T tokens and
+ * k slots.  The workspace must be zero-filled once before its first use
+ * (e.g. cudaMemset); the calls leave it ready for the next call.  One
+ * workspace serves one stream at a time.  T >= 0, 1 <= k <= 16. */
+moe_status moe_workspace_size(int T, int k, size_t* bytes);
+
+/* A1 -- top-k routing.  Page "perf(ds4): batch heterogeneous MoE prefill by
+ * expert", Summary (routed experts, up to 256) and page "perf(ds4): extend
+ * sparse prefill scheduling to 10K", Summary (native top-6 routing).
+ *   logits [T][E] fp32 (finite values).
+ *   ids    [T][k] int32 out: the k largest logits in descending order, ties
+ *          to the lower expert id (-0.0 equals +0.0).
+ *   w      [T][k] fp32 out: softmax over the k selected logits. */
+moe_status moe_route_topk(const float* logits, int T, int E, int k,
+                          int32_t* ids, float* w, void* stream);
+
+/* A2 -- route histogram.  Page "perf(ds4): batch heterogeneous MoE prefill
+ * by expert", Summary (GPU-native route histogram for up to 256 experts).
+ *   ids    [T][k] int32, each in [0, E).
+ *   mask   [T][k] uint8 or NULL; nonzero = route masked (owned elsewhere),
+ *          not counted.
+ *   counts [E] int32 out: unmasked routes per expert.
+ *   ws     workspace (moe_workspace_size); receives per-chunk counts and the
+ *          stable rank of every route inside its chunk. */
+moe_status moe_route_histogram(const int32_t* ids, const uint8_t* mask, int T, int k, int E,
+                               int32_t* counts, void* ws, void* stream);
+
+/* A3 -- exclusive prefix over expert counts.  Same page, Summary
+ * (GPU-native prefix).
+ *   counts  [E] int32 from moe_route_histogram with the same T, k, E, ws.
+ *   offsets [E+1] int32 out: offsets[0] = 0, offsets[e+1] = offsets[e] +
+ *           counts[e]; offsets[E] = R.
+ *   ws      the workspace moe_route_histogram filled; per-chunk counts are
+ *           turned into per-chunk row bases for the scatter. */
+moe_status moe_prefix_offsets(const int32_t* counts, int T, int k, int E,
+                              int32_t* offsets, void* ws, void* stream);
+
+/* A4 -- scatter to expert-major order.  Same page, Summary (GPU-native
+ * scatter) and "Correctness and validation" (compact destinations are
+ * zero-initialised).
+ *   x            [T][d] operand type `dtype`.
+ *   ids, mask    as for moe_route_histogram (same values).
+ *   offsets      [E+1] from moe_prefix_offsets.
+ *   xs           [T*k][d] out: row offsets[e] + j holds the token row of the
+ *                j-th unmasked route to expert e in ascending route order;
+ *                rows R .. T*k-1 are zero-filled.
+ *   row_of_route [T*k] int32 out: compact row of route r, -1 when masked.
+ *   route_of_row [T*k] int32 out: route of compact row i, -1 for i >= R.
+ *   ws           the workspace moe_prefix_offsets prepared. */
+moe_status moe_scatter_rows(const void* x, int dtype, const int32_t* ids, const uint8_t* mask,
+                            const int32_t* offsets, int T, int k, int d, int E,
+                            void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                            void* ws, void* stream);
+
+/* A5 -- grouped gate/up projection with SwiGLU.  Same page, Summary
+ * (grouped gate/up MMID graphs instead of a serial graph per active expert);
+ * the SwiGLU is the "DS4 SwiGLU split op" of the page "perf(ggml): reuse
+ * ROCmFP4 weights across q=4 columns".
+ *   xs      [cap][d] compact rows (moe_scatter_rows), cap = capacity rows.
+ *   offsets [E+1] expert segments of xs; offsets[E] <= cap (checked on the
+ *           device: a violation skips the work and sets MOE_ERR_INVALID_ARG
+ *           in the device error word).
+ *   w_gate, w_up [E][f][d].
+ *   h       [cap][f] out: h[i] = silu(xs[i].Wg_e) * (xs[i].Wu_e) for the
+ *           expert e whose segment holds row i; rows R .. cap-1 zero-filled.
+ * bf16: tcgen05 tensor cores, fp32 accumulation, h rounded to bf16.
+ * fp32: fp32 FMA, h fp32. */
+moe_status moe_grouped_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                               const void* w_gate, const void* w_up, int dtype, void* h, void* stream);
+
+/* A6 -- grouped down projection.  Same page, Summary (grouped down MMID).
+ *   h       [cap][f] from moe_grouped_gate_up.
+ *   w_down  [E][d][f].
+ *   y       [cap][d] fp32 out: y[i] = h[i].Wd_e; rows R .. cap-1
+ *           zero-filled. */
+moe_status moe_grouped_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                            const void* w_down, int dtype, float* y, void* stream);
+
+/* A5 + A6 in one call (two kernels on `stream`). */
+moe_status moe_grouped_ffn(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                           const void* w_gate, const void* w_up, const void* w_down, int dtype,
+                           void* h, float* y, void* stream);
+
+/* A7 -- weighted combine back to token order.  Page "perf(ds4): accelerate
+ * ROCm decode and long-context selection", lucebox8 A/B (fused expert-major
+ * route combine) and page "perf(ds4): batch heterogeneous MoE prefill by
+ * expert", Summary (masked owner routes are exact zero contributions).
+ *   y            [cap][d] fp32 expert outputs.
+ *   row_of_route [T*k] int32, -1 = masked (skipped, never multiplied).
+ *   w            [T][k] fp32 gate weights.
+ *   out          [T][d] fp32 out: out[t] = +0.0 + sum over ascending
+ *                unmasked s of w[t][s] * y[row_of_route[t*k+s]], fp32
+ *                fused multiply-adds in that fixed order (deterministic). */
+moe_status moe_combine(const float* y, const int32_t* row_of_route, const float* w,
+                       int T, int k, int d, float* out, void* stream);
+
+/* The whole path (A1..A7) on `stream`, with every intermediate written to
+ * the caller's buffers (shapes as above; mask may be NULL). */
+moe_status moe_forward(const float* logits, const void* x, const uint8_t* mask,
+                       int T, int E, int k, int d, int f,
+                       const void* w_gate, const void* w_up, const void* w_down, int dtype,
+                       int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                       void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                       void* h, float* y, float* out, void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

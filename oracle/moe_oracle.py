@@ -179,19 +179,45 @@ def _expert(weights, e):
             np.asarray(wd, dtype=np.float64))
 
 
-def expert_ffn(rows, w_gate_e, w_up_e, w_down_e):
-    """y = (silu(x.Wg) * (x.Wu)) . Wd for each row x, in float64.
+def expert_swiglu(rows, w_gate_e, w_up_e):
+    """h = silu(x.Wg) * (x.Wu) for each row x, in float64 (gate/up step).
 
     Page "perf(ds4): batch heterogeneous MoE prefill by expert", Summary
-    (grouped gate/up/down projections per expert); the SwiGLU between them is
-    the "DS4 SwiGLU split op" of the page "perf(ggml): reuse ROCmFP4 weights
-    across q=4 columns".  Storage: w_gate_e, w_up_e [f][d]; w_down_e [d][f].
+    (grouped gate/up projections); the SwiGLU is the "DS4 SwiGLU split op" of
+    the page "perf(ggml): reuse ROCmFP4 weights across q=4 columns".
+    Storage: w_gate_e, w_up_e [f][d].
     """
     x = np.asarray(rows, dtype=np.float64)
     g = x @ np.asarray(w_gate_e, dtype=np.float64).T    # [n][f]
     u = x @ np.asarray(w_up_e, dtype=np.float64).T      # [n][f]
-    h = silu(g) * u                                      # [n][f]
-    return h @ np.asarray(w_down_e, dtype=np.float64).T  # [n][d]
+    return silu(g) * u                                   # [n][f]
+
+
+def expert_down(h, w_down_e):
+    """y = h . Wd for each row h, in float64 (down step).  Storage: w_down_e [d][f]."""
+    return np.asarray(h, dtype=np.float64) @ np.asarray(w_down_e, dtype=np.float64).T  # [n][d]
+
+
+def expert_ffn(rows, w_gate_e, w_up_e, w_down_e):
+    """y = (silu(x.Wg) * (x.Wu)) . Wd for each row x: the gate/up step then the down step."""
+    return expert_down(expert_swiglu(rows, w_gate_e, w_up_e), w_down_e)
+
+
+def grouped_swiglu(xs, offsets, weights):
+    """h [R][f]: rows offsets[e] .. offsets[e+1]-1 go through expert e's gate/up step."""
+    xs = np.asarray(xs, dtype=np.float64)
+    offsets = np.asarray(offsets)
+    E = offsets.size - 1
+    h = None
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            wg, wu, _ = _expert(weights, e)
+            he = expert_swiglu(xs[lo:hi], wg, wu)
+            if h is None:
+                h = np.zeros((int(offsets[E]), he.shape[1]), dtype=np.float64)
+            h[lo:hi] = he
+    return h
 
 
 def grouped_ffn(xs, offsets, weights):

@@ -1,0 +1,165 @@
+// C-ABI plumbing: device cache, sticky device error word, status strings,
+// grouped FFN dispatch and the whole-path convenience call.
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+// Sticky device error word (bits moe::DEVERR_*), one per device that loads
+// the library.  Kernels receive its address as an argument.
+__device__ unsigned g_moe_device_error;
+
+namespace moe {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+bool g_ready[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+thread_local int g_last_cuda_error = 0;
+
+}  // namespace
+
+moe_status cuda_status(cudaError_t err) {
+    if (err == cudaSuccess) return MOE_OK;
+    g_last_cuda_error = static_cast<int>(err);
+    return MOE_ERR_CUDA;
+}
+
+moe_status device_info(DeviceInfo* info) {
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_ready[dev]) {
+        DeviceInfo di{};
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev));
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev));
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
+        if (di.cc_major != 10 || di.cc_minor != 3) return MOE_ERR_UNSUPPORTED;
+        void* p = nullptr;
+        MOE_CUDA_TRY(cudaGetSymbolAddress(&p, g_moe_device_error));
+        di.error_word = static_cast<unsigned*>(p);
+        g_info[dev] = di;
+        g_ready[dev] = true;
+    }
+    *info = g_info[dev];
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_version(void) { return 100; }
+
+extern "C" const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported device or operand type";
+        case MOE_ERR_CUDA: return "CUDA call failed";
+        case MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" moe_status moe_check_device_error(void* stream) {
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    unsigned word = 0;
+    MOE_CUDA_TRY(cudaMemcpy(&word, di.error_word, sizeof(word), cudaMemcpyDeviceToHost));
+    if (word == 0) return MOE_OK;
+    const unsigned zero = 0;
+    MOE_CUDA_TRY(cudaMemcpy(di.error_word, &zero, sizeof(zero), cudaMemcpyHostToDevice));
+    return (word & DEVERR_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_INVALID_ARG;
+}
+
+namespace {
+
+moe_status check_ffn_args(const int32_t* offsets, int cap, int E, int d, int f, int dtype) {
+    const int es = dtype_size(dtype);
+    if (es == 0) return MOE_ERR_UNSUPPORTED;
+    MOE_REQUIRE(offsets && cap >= 0 && E >= 1 && E <= kMaxExperts && d >= 1 && f >= 1);
+    MOE_REQUIRE((static_cast<size_t>(d) * es) % 16 == 0 && (static_cast<size_t>(f) * es) % 16 == 0);
+    if (dtype == MOE_BF16) MOE_REQUIRE(d % 128 == 0 && f % 128 == 0);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_grouped_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                          const void* w_gate, const void* w_up, int dtype, void* h,
+                                          void* stream) {
+    moe_status st = check_ffn_args(offsets, cap, E, d, f, dtype);
+    if (st != MOE_OK) return st;
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(xs && w_gate && w_up && h);
+    MOE_REQUIRE(aligned16(xs) && aligned16(w_gate) && aligned16(w_up) && aligned16(h));
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == MOE_BF16) return launch_ffn_tc_gate_up(xs, offsets, cap, E, d, f, w_gate, w_up, h, s, di);
+    return launch_ffn_simt_gate_up(static_cast<const float*>(xs), offsets, cap, E, d, f,
+                                   static_cast<const float*>(w_gate), static_cast<const float*>(w_up),
+                                   static_cast<float*>(h), s, di);
+}
+
+extern "C" moe_status moe_grouped_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                                       const void* w_down, int dtype, float* y, void* stream) {
+    moe_status st = check_ffn_args(offsets, cap, E, d, f, dtype);
+    if (st != MOE_OK) return st;
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(h && w_down && y);
+    MOE_REQUIRE(aligned16(h) && aligned16(w_down) && aligned16(y));
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == MOE_BF16) return launch_ffn_tc_down(h, offsets, cap, E, d, f, w_down, y, s, di);
+    return launch_ffn_simt_down(static_cast<const float*>(h), offsets, cap, E, d, f,
+                                static_cast<const float*>(w_down), y, s, di);
+}
+
+extern "C" moe_status moe_grouped_ffn(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                      const void* w_gate, const void* w_up, const void* w_down, int dtype,
+                                      void* h, float* y, void* stream) {
+    moe_status st = moe_grouped_gate_up(xs, offsets, cap, E, d, f, w_gate, w_up, dtype, h, stream);
+    if (st != MOE_OK) return st;
+    return moe_grouped_down(h, offsets, cap, E, d, f, w_down, dtype, y, stream);
+}
+
+extern "C" moe_status moe_forward(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k,
+                                  int d, int f, const void* w_gate, const void* w_up, const void* w_down, int dtype,
+                                  int32_t* ids, float* w, int32_t* counts, int32_t* offsets, void* xs,
+                                  int32_t* row_of_route, int32_t* route_of_row, void* h, float* y, float* out,
+                                  void* ws, void* stream) {
+    // validate everything before the first launch so that a bad argument
+    // enqueues nothing
+    moe_status st = check_ffn_args(offsets, T * k, E, d, f, dtype);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && k <= E && d % 4 == 0);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && w_gate && w_up && w_down && ids && w && counts && xs && row_of_route &&
+                route_of_row && h && y && out && ws);
+    MOE_REQUIRE(aligned16(x) && aligned16(xs) && aligned16(h) && aligned16(y) && aligned16(out) &&
+                aligned16(ws) && aligned16(w_gate) && aligned16(w_up) && aligned16(w_down));
+    const int cap = T * k;
+    if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
+    if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
+    if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+    if ((st = moe_scatter_rows(x, dtype, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
+                               stream)) != MOE_OK)
+        return st;
+    if ((st = moe_grouped_ffn(xs, offsets, cap, E, d, f, w_gate, w_up, w_down, dtype, h, y, stream)) != MOE_OK)
+        return st;
+    return moe_combine(y, row_of_route, w, T, k, d, out, stream);
+}

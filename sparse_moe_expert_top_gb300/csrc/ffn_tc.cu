@@ -1,0 +1,577 @@
+// Grouped expert FFN on the sm_103a tensor cores (operand type MOE_BF16).
+//
+// Page "perf(ds4): batch heterogeneous MoE prefill by expert" (Luce-Org/
+// lucebox PR #640), Summary: one grouped gate/up and one grouped down
+// projection over all active experts instead of a serial graph per expert.
+// Page "perf(ds4): unify gfx1151 sparse-prefill stack" (PR #685),
+// Composition: adaptive sparse-MoE tiles and a persistent compact work queue.
+//
+// GB300 design
+// ------------
+// Prefill chunks give each expert few rows (median 9 at 401 tokens, ~19 at
+// 2048), so the work is streaming the touched experts' weights from HBM.
+// The kernel therefore swaps the GEMM operands: the WEIGHT tile is the
+// M = 128 operand of tcgen05.mma and the expert's compact token rows form N
+// (a multiple of 16, at most 128 per work item).  Each weight byte is loaded
+// once per 128 rows, and an expert with 9 rows issues N = 16 MMAs instead of
+// padding 9 rows up to an M = 128 tile.  (The pages' adaptive tile width on
+// RDNA is the same idea.)
+//
+// Work item = (expert e, 128-row slice mt of the output features, 128-row
+// slice nt of the expert's compact rows).  Items are numbered expert-major,
+// then mt, then nt, so CTAs working at the same time on the nt slices of one
+// expert share its weight tile through L2.  The kernel is persistent: one
+// CTA per SM takes items blockIdx.x, blockIdx.x + gridDim.x, ...; every CTA
+// derives the same item table from `offsets` in its prologue, so ragged
+// per-expert row counts (including empty experts) need no host round trip.
+//
+// Roles (192 threads): warp 0 lane 0 issues TMA loads into a ring of shared-
+// memory stages (128B-swizzled, 64 K-elements per stage); warp 1 lane 0
+// issues tcgen05.mma into a double-buffered TMEM accumulator (gate and up
+// accumulators side by side for the SwiGLU stage); warps 2-5 read the
+// accumulator with tcgen05.ld, apply SwiGLU (gate/up) and store rows.
+// Every mbarrier wait is bounded: when it runs out the kernel records
+// DEVERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and returns.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;        // MMA M: weight rows per tile
+constexpr int BN = 128;        // compact rows per work item (MMA N <= BN)
+constexpr int BK = 64;         // K elements per stage (one 128-byte swizzle atom of bf16)
+constexpr int UMMA_K = 16;     // K per tcgen05.mma of kind::f16
+constexpr int kBoxRows = 16;   // compact rows per TMA box
+constexpr int kThreads = 192;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+template <bool GATED>
+struct Cfg {
+    static constexpr int kA = GATED ? 2 : 1;  // weight operands per stage
+    static constexpr int kStages = GATED ? 4 : 6;
+    static constexpr int kATileBytes = BM * BK * 2;
+    static constexpr int kBTileBytes = BN * BK * 2;
+    static constexpr int kStageBytes = kA * kATileBytes + kBTileBytes;
+    static constexpr int kAccCols = kA * BN;
+    static constexpr int kTmemCols = 2 * kAccCols;  // two accumulator buffers
+    static constexpr int kCtrlBytes = 4096;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 1024;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase of `bar` with parity `parity` to complete.
+// Returns false (after flagging the CTA and the device error word on a
+// time-out) when the wait is abandoned.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* err) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_try_wait(addr, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(addr, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(err, DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: used while draining copies and
+// MMAs that are already in flight.
+__device__ __noinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(addr, parity) && global_ns() - t0 < kWaitLimitNs) {
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major, 128B-swizzled operand tile:
+// rows of 128 bytes, 8-row core groups 1024 bytes apart (stride byte
+// offset), descriptor version 1, swizzle mode 2 (128B).  The leading byte
+// offset is unused for this layout.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
+// and B, both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Work-item table
+// ---------------------------------------------------------------------------
+
+struct Item {
+    int e, mt, row0, rows;
+};
+
+// item_off[e] = first item of expert e (exclusive scan), ntiles[e] = compact
+// row slices of expert e.  Items of one expert are ordered mt-major, nt-minor.
+__device__ __forceinline__ Item decode_item(int it, const int* item_off, const int* ntiles, const int32_t* offsets,
+                                            int E) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (item_off[mid] <= it) lo = mid;
+        else hi = mid - 1;
+    }
+    Item r;
+    r.e = lo;
+    const int local = it - item_off[lo];
+    const int n = ntiles[lo];
+    r.mt = local / n;
+    const int nt = local - r.mt * n;
+    const int seg_lo = __ldg(offsets + lo), seg_hi = __ldg(offsets + lo + 1);
+    r.row0 = seg_lo + nt * BN;
+    r.rows = min(BN, seg_hi - r.row0);
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.  GATED: out = h (bf16 [cap][M]) = silu(A0 . xs) * (A1 . xs) with
+// A0 = w_gate, A1 = w_up, M = f, K = d.  Otherwise out = y (fp32 [cap][M]) =
+// A0 . h with A0 = w_down, M = d, K = f.
+// ---------------------------------------------------------------------------
+
+template <bool GATED>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
+                  const __grid_constant__ CUtensorMap map_b, const int32_t* __restrict__ offsets, int cap, int E,
+                  int K, int M, void* __restrict__ out, unsigned* err) {
+    using C = Cfg<GATED>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* ctrl = smem + C::kStages * C::kStageBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* acc_full = empty + C::kStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* issued = reinterpret_cast<int*>(tmem_slot + 2);  // last phase issued per stage, -1 = none
+    int* item_off = issued + C::kStages;                  // E + 1 entries
+    int* ntiles = item_off + kMaxExperts + 1;             // E entries
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_kb = K / BK;
+    const int n_mt = M / BM;
+
+    // ---- prologue: barriers, TMEM, item table --------------------------------
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            issued[s] = -1;
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&map_a0);
+        if (GATED) prefetch_tmap(&map_a1);
+        prefetch_tmap(&map_b);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 2) {
+        // validate the segments and count the compact-row slices of every expert
+        bool bad = false;
+        for (int e = lane; e < E; e += 32) {
+            const int lo = offsets[e], hi = offsets[e + 1];
+            const bool seg_bad = lo < 0 || hi < lo || hi > cap;
+            bad |= seg_bad;
+            ntiles[e] = seg_bad ? 0 : (hi - lo + BN - 1) / BN;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        __syncwarp();
+        // exclusive scan of the item counts ntiles[e] * n_mt: lane j owns
+        // experts [j*per, (j+1)*per)
+        const int per = (E + 31) / 32;
+        int local = 0;
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e < E && !bad) local += ntiles[e] * n_mt;
+        }
+        int incl = local;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - local;
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e < E) {
+                item_off[e] = run;
+                run += bad ? 0 : ntiles[e] * n_mt;
+            }
+        }
+        if (lane == 31) item_off[E] = run;
+        if (bad && lane == 0) atomicOr(err, DEVERR_OFFSETS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_items = item_off[E];
+
+    if (warp == 0) {
+        // ---- TMA producer -------------------------------------------------
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const Item item = decode_item(it, item_off, ntiles, offsets, E);
+                const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
+                const uint32_t bytes = C::kA * C::kATileBytes + n16 * kBoxRows * BK * 2;
+                const int wy = item.e * M + item.mt * BM;
+                for (int kb = 0; kb < n_kb; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + s * C::kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    issued[s] = static_cast<int>(ph);
+                    tma_load_2d(st, &map_a0, &full[s], kb * BK, wy, pol_w);
+                    if (GATED) tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * BK, wy, pol_w);
+                    uint8_t* bdst = st + C::kA * C::kATileBytes;
+                    for (int j = 0; j < n16; ++j)
+                        tma_load_2d(bdst + j * kBoxRows * 128, &map_b, &full[s], kb * BK, item.row0 + j * kBoxRows,
+                                    pol_x);
+                    if (++s == C::kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer ---------------------------------------------------
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int local = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++local) {
+                const Item item = decode_item(it, item_off, ntiles, offsets, E);
+                const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
+                const uint32_t idesc = idesc_bf16(BM, n16 * kBoxRows);
+                const int buf = local & 1;
+                const uint32_t acc_ph = static_cast<uint32_t>(local >> 1) & 1u;
+                if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, abort_flag, err)) break;
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::kAccCols);
+                for (int kb = 0; kb < n_kb; ++kb) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(smem + s * C::kStageBytes);
+                    const uint32_t a1 = a0 + C::kATileBytes;
+                    const uint32_t b = a0 + C::kA * C::kATileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        const uint64_t bd = sdesc_sw128(b + kk * UMMA_K * 2);
+                        umma_bf16(d0, sdesc_sw128(a0 + kk * UMMA_K * 2), bd, idesc, acc);
+                        if (GATED) umma_bf16(d0 + BN, sdesc_sw128(a1 + kk * UMMA_K * 2), bd, idesc, acc);
+                    }
+                    umma_commit(&empty[s]);
+                    if (++s == C::kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[buf]);
+            }
+            // every MMA issued above has completed once `drain` flips
+            umma_commit(drain);
+            mbar_drain(drain, 0);
+        }
+    } else {
+        // ---- epilogue (warps 2..5) ----------------------------------------
+        const int q = warp & 3;  // TMEM lanes [32q, 32q+32) belong to this warp
+        int local = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
+            const Item item = decode_item(it, item_off, ntiles, offsets, E);
+            const int buf = local & 1;
+            const uint32_t acc_ph = static_cast<uint32_t>(local >> 1) & 1u;
+            int got = 1;
+            if (lane == 0) got = mbar_wait(&acc_full[buf], acc_ph, abort_flag, err) ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int m = item.mt * BM + q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(buf * C::kAccCols);
+            for (int c0 = 0; c0 < item.rows; c0 += 32) {
+                uint32_t g[32];
+                tmem_ld32(taddr + c0, g);
+                if (GATED) {
+                    uint32_t u[32];
+                    tmem_ld32(taddr + BN + c0, u);
+                    tmem_ld_wait();
+                    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int n = c0 + j;
+                        if (n < item.rows) {
+                            const float gv = __uint_as_float(g[j]);
+                            const float hv = gv / (1.f + expf(-gv)) * __uint_as_float(u[j]);
+                            h[static_cast<size_t>(item.row0 + n) * M + m] = __float2bfloat16_rn(hv);
+                        }
+                    }
+                } else {
+                    tmem_ld_wait();
+                    float* y = static_cast<float*>(out);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int n = c0 + j;
+                        if (n < item.rows) y[static_cast<size_t>(item.row0 + n) * M + m] = __uint_as_float(g[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        // zero-fill the unused compact rows R .. cap-1
+        const int R = offsets[E];
+        if (ok && R >= 0 && R <= cap) {
+            const int vecs = M * (GATED ? 2 : 4) / 16;
+            const int gw = blockIdx.x * 4 + (warp - 2), nw = gridDim.x * 4;
+            uint4* o = static_cast<uint4*>(out);
+            for (int row = R + gw; row < cap; row += nw)
+                for (int v = lane; v < vecs; v += 32) o[static_cast<size_t>(row) * vecs + v] = make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // ---- teardown ----------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // let every TMA copy still in flight land before the CTA's shared
+        // memory is released
+        for (int s = 0; s < C::kStages; ++s)
+            if (issued[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued[s]));
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_mutex;
+bool g_attr_set[64][2];
+
+moe_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_encode == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        MOE_CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q));
+        if (q != cudaDriverEntryPointSuccess || p == nullptr) return MOE_ERR_UNSUPPORTED;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    *fn = g_encode;
+    return MOE_OK;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][K] matrix with a box of
+// 64 K-elements x box_rows rows and 128-byte swizzle.
+moe_status encode_2d(CUtensorMap* map, const void* base, int K, long long rows, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    moe_status st = get_encode(&enc);
+    if (st != MOE_OK) return st;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+template <bool GATED>
+moe_status set_smem_attr() {
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_attr_set[dev][GATED ? 1 : 0]) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(ffn_tc_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          Cfg<GATED>::kSmemBytes));
+        g_attr_set[dev][GATED ? 1 : 0] = true;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                 const void* w_gate, const void* w_up, void* h, cudaStream_t st,
+                                 const DeviceInfo& di) {
+    CUtensorMap ma0, ma1, mb;
+    moe_status s;
+    if ((s = encode_2d(&ma0, w_gate, d, static_cast<long long>(E) * f, BM)) != MOE_OK) return s;
+    if ((s = encode_2d(&ma1, w_up, d, static_cast<long long>(E) * f, BM)) != MOE_OK) return s;
+    if ((s = encode_2d(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = set_smem_attr<true>()) != MOE_OK) return s;
+    ffn_tc_kernel<true><<<di.sm_count, kThreads, Cfg<true>::kSmemBytes, st>>>(ma0, ma1, mb, offsets, cap, E, d, f,
+                                                                              h, di.error_word);
+    return cuda_status(cudaGetLastError());
+}
+
+moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                              const void* w_down, float* y, cudaStream_t st, const DeviceInfo& di) {
+    CUtensorMap ma0, mb;
+    moe_status s;
+    if ((s = encode_2d(&ma0, w_down, f, static_cast<long long>(E) * d, BM)) != MOE_OK) return s;
+    if ((s = encode_2d(&mb, h, f, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = set_smem_attr<false>()) != MOE_OK) return s;
+    ffn_tc_kernel<false><<<di.sm_count, kThreads, Cfg<false>::kSmemBytes, st>>>(ma0, ma0, mb, offsets, cap, E, f, d,
+                                                                                y, di.error_word);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moe

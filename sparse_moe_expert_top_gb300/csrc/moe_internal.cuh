@@ -1,0 +1,69 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Bits of the sticky device error word.
+enum : unsigned {
+    DEVERR_TIMEOUT = 1u,   // a bounded wait ran out
+    DEVERR_OFFSETS = 2u,   // offsets failed the device-side consistency check
+};
+
+// Routes handled by one CTA of the histogram kernel (8 warps x 8 steps x 32 lanes).
+constexpr int kHistChunk = 2048;
+constexpr int kMaxExperts = 256;
+constexpr int kMaxK = 16;
+
+// Workspace layout (int32 words): [0] completion counter, [1..31] reserved,
+// then chunk_counts[n_chunks][256], then local_rank[T*k].
+constexpr int kWsHeaderWords = 32;
+inline int ws_chunks(int T, int k) { return (T * k + kHistChunk - 1) / kHistChunk; }
+
+struct DeviceInfo {
+    int sm_count;
+    int cc_major, cc_minor;
+    unsigned* error_word;   // device address of the sticky error word
+};
+
+// Per-device cache; returns MOE_OK and fills *info for the current device.
+moe_status device_info(DeviceInfo* info);
+
+// Records `err` as this thread's last CUDA error and returns MOE_ERR_CUDA
+// (or MOE_OK when err == cudaSuccess).
+moe_status cuda_status(cudaError_t err);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int dtype_size(int dtype) { return dtype == MOE_BF16 ? 2 : (dtype == MOE_F32 ? 4 : 0); }
+
+// Kernel launchers implemented in the other translation units.
+moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                 const void* w_gate, const void* w_up, void* h, cudaStream_t st,
+                                 const DeviceInfo& di);
+moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                              const void* w_down, float* y, cudaStream_t st, const DeviceInfo& di);
+moe_status launch_ffn_simt_gate_up(const float* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                   const float* w_gate, const float* w_up, float* h, cudaStream_t st,
+                                   const DeviceInfo& di);
+moe_status launch_ffn_simt_down(const float* h, const int32_t* offsets, int cap, int E, int d, int f,
+                                const float* w_down, float* y, cudaStream_t st, const DeviceInfo& di);
+
+}  // namespace moe
+
+// Host-side argument check helper: returns MOE_ERR_INVALID_ARG from the
+// enclosing function when `cond` is false.
+#define MOE_REQUIRE(cond)                          \
+    do {                                           \
+        if (!(cond)) return MOE_ERR_INVALID_ARG;   \
+    } while (0)
+
+#define MOE_CUDA_TRY(expr)                                      \
+    do {                                                        \
+        cudaError_t e_ = (expr);                                \
+        if (e_ != cudaSuccess) return ::moe::cuda_status(e_);   \
+    } while (0)

@@ -1,0 +1,251 @@
+"""Python binding of the C-ABI in include/moe.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does
+nothing but check tensor dtypes/shapes/devices, pass raw device pointers and
+the current CUDA stream, and turn a non-zero status into ``MoEError``.  All
+arithmetic of the path runs in the library's CUDA kernels; PyTorch only owns
+the device memory and the stream.  If the shared library is missing the
+import of this module fails: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libmoe_gb300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(5)
+MOE_F32, MOE_BF16 = 0, 1
+
+# (name, argtypes) of every exported entry point; the ABI test checks this
+# list against include/moe.h.
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)
+SIGNATURES = {
+    "moe_version": ([], _I),
+    "moe_status_string": ([_I], ctypes.c_char_p),
+    "moe_last_cuda_error": ([], _I),
+    "moe_check_device_error": ([_P], _I),
+    "moe_workspace_size": ([_I, _I, _SZ], _I),
+    "moe_route_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_route_histogram": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_prefix_offsets": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_scatter_rows": ([_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_gate_up": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P], _I),
+    "moe_grouped_down": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _P], _I),
+    "moe_grouped_ffn": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P], _I),
+    "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "moe_forward": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I,
+                     _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        lib = load()
+        msg = lib.moe_status_string(status).decode()
+        if status == MOE_ERR_CUDA:
+            msg += f" (cudaError {lib.moe_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg}")
+        self.status = status
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the shared library (raises OSError if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: build it with `python -m sparse_moe_expert_top_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MOE_OK:
+        raise MoEError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    if t.dtype == torch.float32:
+        return MOE_F32
+    raise ValueError(f"unsupported operand dtype {t.dtype}")
+
+
+def _expect(t, dtype, shape, name):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def moe_version() -> int:
+    return load().moe_version()
+
+
+def moe_check_device_error(stream=None) -> None:
+    _check("moe_check_device_error", load().moe_check_device_error(_stream(stream)))
+
+
+def moe_workspace_size(T: int, k: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_workspace_size", load().moe_workspace_size(T, k, ctypes.byref(n)))
+    return n.value
+
+
+def moe_route_topk(logits, k, ids, w, stream=None):
+    T, E = logits.shape
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(ids, torch.int32, (T, k), "ids")
+    _expect(w, torch.float32, (T, k), "w")
+    _check("moe_route_topk", load().moe_route_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(w), _stream(stream)))
+
+
+def moe_route_histogram(ids, mask, E, counts, ws, stream=None):
+    T, k = ids.shape
+    _expect(ids, torch.int32, (T, k), "ids")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect(counts, torch.int32, (E,), "counts")
+    _check("moe_route_histogram", load().moe_route_histogram(_ptr(ids), _ptr(mask), T, k, E, _ptr(counts), _ptr(ws),
+                                                             _stream(stream)))
+
+
+def moe_prefix_offsets(counts, T, k, offsets, ws, stream=None):
+    E = counts.shape[0]
+    _expect(counts, torch.int32, (E,), "counts")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _check("moe_prefix_offsets", load().moe_prefix_offsets(_ptr(counts), T, k, E, _ptr(offsets), _ptr(ws),
+                                                           _stream(stream)))
+
+
+def moe_scatter_rows(x, ids, mask, offsets, xs, row_of_route, route_of_row, ws, stream=None):
+    T, d = x.shape
+    k = ids.shape[1]
+    E = offsets.shape[0] - 1
+    _expect(ids, torch.int32, (T, k), "ids")
+    _expect(xs, x.dtype, (T * k, d), "xs")
+    _expect(row_of_route, torch.int32, (T * k,), "row_of_route")
+    _expect(route_of_row, torch.int32, (T * k,), "route_of_row")
+    _check("moe_scatter_rows", load().moe_scatter_rows(_ptr(x), _dtype_code(x), _ptr(ids), _ptr(mask), _ptr(offsets),
+                                                       T, k, d, E, _ptr(xs), _ptr(row_of_route), _ptr(route_of_row),
+                                                       _ptr(ws), _stream(stream)))
+
+
+def moe_grouped_gate_up(xs, offsets, w_gate, w_up, h, stream=None):
+    cap, d = xs.shape
+    E, f, _ = w_gate.shape
+    _expect(w_gate, xs.dtype, (E, f, d), "w_gate")
+    _expect(w_up, xs.dtype, (E, f, d), "w_up")
+    _expect(h, xs.dtype, (cap, f), "h")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _check("moe_grouped_gate_up", load().moe_grouped_gate_up(_ptr(xs), _ptr(offsets), cap, E, d, f, _ptr(w_gate),
+                                                             _ptr(w_up), _dtype_code(xs), _ptr(h), _stream(stream)))
+
+
+def moe_grouped_down(h, offsets, w_down, y, stream=None):
+    cap, f = h.shape
+    E, d, _ = w_down.shape
+    _expect(w_down, h.dtype, (E, d, f), "w_down")
+    _expect(y, torch.float32, (cap, d), "y")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _check("moe_grouped_down", load().moe_grouped_down(_ptr(h), _ptr(offsets), cap, E, d, f, _ptr(w_down),
+                                                       _dtype_code(h), _ptr(y), _stream(stream)))
+
+
+def moe_grouped_ffn(xs, offsets, w_gate, w_up, w_down, h, y, stream=None):
+    cap, d = xs.shape
+    E, f, _ = w_gate.shape
+    _expect(w_gate, xs.dtype, (E, f, d), "w_gate")
+    _expect(w_up, xs.dtype, (E, f, d), "w_up")
+    _expect(w_down, xs.dtype, (E, d, f), "w_down")
+    _expect(h, xs.dtype, (cap, f), "h")
+    _expect(y, torch.float32, (cap, d), "y")
+    _check("moe_grouped_ffn", load().moe_grouped_ffn(_ptr(xs), _ptr(offsets), cap, E, d, f, _ptr(w_gate), _ptr(w_up),
+                                                     _ptr(w_down), _dtype_code(xs), _ptr(h), _ptr(y), _stream(stream)))
+
+
+def moe_combine(y, row_of_route, w, out, stream=None):
+    T, k = w.shape
+    d = out.shape[1]
+    _expect(y, torch.float32, (y.shape[0], d), "y")
+    _expect(row_of_route, torch.int32, (T * k,), "row_of_route")
+    _expect(out, torch.float32, (T, d), "out")
+    _check("moe_combine", load().moe_combine(_ptr(y), _ptr(row_of_route), _ptr(w), T, k, d, _ptr(out),
+                                             _stream(stream)))
+
+
+class MoEBuffers:
+    """Caller-owned device buffers for one chunk shape (T, E, k, d, f, dtype).
+
+    The library never allocates; this helper allocates every intermediate
+    of the path once with PyTorch so that repeated calls reuse them.
+    """
+
+    def __init__(self, T: int, E: int, k: int, d: int, f: int, dtype: torch.dtype, device="cuda"):
+        self.T, self.E, self.k, self.d, self.f, self.dtype = T, E, k, d, f, dtype
+        cap = T * k
+        i32 = dict(dtype=torch.int32, device=device)
+        self.ids = torch.empty(T, k, **i32)
+        self.w = torch.empty(T, k, dtype=torch.float32, device=device)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.xs = torch.empty(cap, d, dtype=dtype, device=device)
+        self.row_of_route = torch.empty(cap, **i32)
+        self.route_of_row = torch.empty(cap, **i32)
+        self.h = torch.empty(cap, f, dtype=dtype, device=device)
+        self.y = torch.empty(cap, d, dtype=torch.float32, device=device)
+        self.out = torch.empty(T, d, dtype=torch.float32, device=device)
+        # the workspace must start zero-filled (it keeps a completion counter)
+        self.ws = torch.zeros(max(moe_workspace_size(T, k), 16) // 4 + 4, dtype=torch.int32, device=device)
+
+
+def moe_forward(logits, x, mask, w_gate, w_up, w_down, k: int, bufs: MoEBuffers, stream=None) -> torch.Tensor:
+    """The whole path on the current stream; returns ``bufs.out`` ([T][d] fp32)."""
+    T, E = logits.shape
+    d = x.shape[1]
+    f = w_gate.shape[1]
+    if (bufs.T, bufs.E, bufs.k, bufs.d, bufs.f, bufs.dtype) != (T, E, k, d, f, x.dtype):
+        raise ValueError("buffers were allocated for another shape")
+    _expect(logits, torch.float32, (T, E), "logits")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect(w_gate, x.dtype, (E, f, d), "w_gate")
+    _expect(w_up, x.dtype, (E, f, d), "w_up")
+    _expect(w_down, x.dtype, (E, d, f), "w_down")
+    b = bufs
+    _check("moe_forward", load().moe_forward(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, f, _ptr(w_gate), _ptr(w_up), _ptr(w_down), _dtype_code(x),
+        _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
+        _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
+    return b.out

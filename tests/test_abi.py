@@ -1,0 +1,78 @@
+"""The C-ABI library loads and exports every entry point that include/moe.h declares.
+
+Runs without a GPU: the library is loaded and inspected, no compute call is
+made.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def _declarations():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    decls = {}
+    for m in re.finditer(r"(?:moe_status|int|const char\s*\*)\s+(moe_\w+)\s*\(([^;]*?)\)\s*;", text, flags=re.S):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        decls[m.group(1)] = params
+    return decls
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_moe_expert_top_gb300 import build, moe
+    build.build()
+    return moe.load()
+
+
+def test_header_declares_the_path_entry_points():
+    names = set(_declarations())
+    for required in ("moe_route_topk", "moe_route_histogram", "moe_prefix_offsets", "moe_scatter_rows",
+                     "moe_grouped_ffn", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_forward",
+                     "moe_workspace_size", "moe_check_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from sparse_moe_expert_top_gb300 import moe
+    decls = _declarations()
+    for name, params in decls.items():
+        assert hasattr(lib, name), name
+        # the binding's argument list has the header's arity
+        assert name in moe.SIGNATURES, name
+        assert len(moe.SIGNATURES[name][0]) == len(params), (name, params)
+    assert set(moe.SIGNATURES) == set(decls)
+
+
+def test_host_only_calls(lib):
+    """Calls that need no device: version, status strings, workspace sizing, argument rejection."""
+    assert lib.moe_version() >= 100
+    assert lib.moe_status_string(0) == b"ok"
+    assert lib.moe_status_string(99) == b"unknown status"
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(2048, 6, ctypes.byref(n)) == 0
+    # header (32 words) + 6 chunks of 256 counts + 12288 ranks, int32
+    assert n.value == 4 * (32 + 6 * 256 + 2048 * 6)
+    assert lib.moe_workspace_size(10, 17, ctypes.byref(n)) == 1      # k > 16
+    assert lib.moe_workspace_size(-1, 2, ctypes.byref(n)) == 1       # T < 0
+    # argument checks reject before touching the device
+    assert lib.moe_route_topk(None, 4, 300, 2, None, None, None) == 1   # E > 256
+    assert lib.moe_route_topk(None, 4, 8, 9, None, None, None) == 1     # k > E
+    assert lib.moe_combine(None, None, None, 4, 2, 6, None, None) == 1  # d not a multiple of 4
+    assert lib.moe_grouped_ffn(None, None, 8, 4, 100, 128, None, None, None, 1, None, None, None) == 1  # bf16 d % 128
+    assert lib.moe_grouped_ffn(None, None, 8, 4, 128, 128, None, None, None, 7, None, None, None) == 2  # dtype
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "sparse_moe_expert_top_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in src.lower().replace("oracle-free", ""), fn

@@ -1,0 +1,199 @@
+"""GPU parity of the grouped expert FFN and of the whole path (through the C-ABI).
+
+Sizes here run in seconds on the oracle and still span several 128-row
+weight tiles, several 128-row compact slices of one expert, ragged tails
+and empty experts.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as mo
+from sparse_moe_expert_top_gb300 import moe as M
+from tests.helpers import assert_close, assert_close_bf16_rounded, oracle_weights, to_np
+from workloads import CONFIGS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _routing(T, E, k, seed, p_mask=0.0, dead_experts=()):
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn(T, E, generator=g)
+    # a skew makes a few experts heavy (> 128 rows: several compact slices)
+    logits += 1.5 * torch.linspace(0, 1, E)[None, :]
+    for e in dead_experts:
+        logits[:, e] = -50.0
+    mask = (torch.rand(T, k, generator=g) < p_mask).to(torch.uint8) if p_mask > 0 else None
+    return logits, mask
+
+
+def _weights(E, d, f, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    wg = (torch.randn(E, f, d, generator=g) / d ** 0.5).to(dtype)
+    wu = (torch.randn(E, f, d, generator=g) / d ** 0.5).to(dtype)
+    wd = (torch.randn(E, d, f, generator=g) / f ** 0.5).to(dtype)
+    return wg, wu, wd
+
+
+FFN_CASES = [
+    # E, d, f, T, k, p_mask, dtype
+    (8, 256, 384, 300, 2, 0.0, torch.bfloat16),
+    (4, 128, 128, 77, 2, 0.2, torch.bfloat16),
+    (16, 512, 256, 600, 4, 0.1, torch.bfloat16),
+    (1, 128, 256, 200, 1, 0.0, torch.bfloat16),
+    (8, 64, 128, 32, 2, 0.0, torch.float32),
+    (5, 96, 160, 50, 3, 0.3, torch.float32),
+]
+
+
+@pytest.mark.parametrize("E,d,f,T,k,p,dtype", FFN_CASES)
+def test_grouped_ffn_matches_oracle(E, d, f, T, k, p, dtype):
+    logits, mask = _routing(T, E, k, seed=E * 31 + T, p_mask=p, dead_experts=(1,) if E > 3 else ())
+    x = torch.randn(T, d).to(dtype)
+    wg, wu, wd = _weights(E, d, f, dtype, seed=d + f)
+    bufs = M.MoEBuffers(T, E, k, d, f, dtype)
+    for b in (bufs.h, bufs.y):
+        b.fill_(float("nan"))
+    out = M.moe_forward(logits.cuda(), x.cuda(), None if mask is None else mask.cuda(), wg.cuda(), wu.cuda(),
+                        wd.cuda(), k, bufs)
+    M.moe_check_device_error()
+    ref = mo.moe_forward(logits.numpy(), to_np(x), (to_np(wg), to_np(wu), to_np(wd)), k,
+                         None if mask is None else mask.numpy())
+    tol = "bf16" if dtype == torch.bfloat16 else "f32"
+    R = int(ref["offsets"][-1])
+    assert np.array_equal(to_np(bufs.offsets), ref["offsets"])
+    h_ref = mo.grouped_swiglu(ref["xs"], ref["offsets"], (to_np(wg), to_np(wu), to_np(wd)))
+    if dtype == torch.bfloat16:
+        assert_close_bf16_rounded(bufs.h[:R], h_ref)
+    else:
+        assert_close(bufs.h[:R], h_ref, tol)
+    # the down step is checked against the oracle applied to the GPU's own h,
+    # so that h's bf16 rounding is not counted twice
+    y_ref_from_h = np.zeros((R, d))
+    off = ref["offsets"]
+    h_gpu = to_np(bufs.h[:R]).astype(np.float64)
+    for e in range(E):
+        if off[e + 1] > off[e]:
+            y_ref_from_h[off[e]:off[e + 1]] = mo.expert_down(h_gpu[off[e]:off[e + 1]], to_np(wd[e]))
+    assert_close(bufs.y[:R], y_ref_from_h, tol)
+    assert_close(out, ref["out"], tol)
+    # unused compact rows are zero-filled
+    assert torch.all(bufs.h[R:].float() == 0) and torch.all(bufs.y[R:] == 0)
+
+
+def test_expert_with_many_compact_slices():
+    """One expert owns all routes: ~5 compact slices of 128 rows plus a ragged one."""
+    E, d, f, T, k = 2, 128, 256, 700, 1
+    logits = torch.zeros(T, E)
+    logits[:, 1] = 1.0
+    x = torch.randn(T, d).to(torch.bfloat16)
+    wg, wu, wd = _weights(E, d, f, torch.bfloat16, seed=3)
+    bufs = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    out = M.moe_forward(logits.cuda(), x.cuda(), None, wg.cuda(), wu.cuda(), wd.cuda(), k, bufs)
+    M.moe_check_device_error()
+    ref = mo.moe_forward(logits.numpy(), to_np(x), (to_np(wg), to_np(wu), to_np(wd)), k)
+    assert to_np(bufs.counts).tolist() == [0, 700]
+    assert_close(out, ref["out"], "bf16")
+
+
+def test_tiny_fp32_workload():
+    cfg = CONFIGS["tiny_fp32"]
+    inp = make_inputs(cfg)
+    bufs = M.MoEBuffers(cfg.T, cfg.E, cfg.k, cfg.d, cfg.f, torch.float32)
+    out = M.moe_forward(inp["logits"].cuda(), inp["x"].cuda(), None, inp["w_gate"].cuda(), inp["w_up"].cuda(),
+                        inp["w_down"].cuda(), cfg.k, bufs)
+    M.moe_check_device_error()
+    ref = mo.moe_forward(inp["logits"].numpy(), inp["x"].numpy(),
+                         (inp["w_gate"].numpy(), inp["w_up"].numpy(), inp["w_down"].numpy()), cfg.k)
+    assert np.array_equal(to_np(bufs.ids), ref["ids"])
+    assert np.array_equal(to_np(bufs.route_of_row), ref["route_of_row"])
+    assert_close(out, ref["out"], "f32")
+
+
+def test_nan_sentinel_and_determinism():
+    """Stale NaN in every compact buffer cannot reach the output; two runs are byte-identical."""
+    E, d, f, T, k = 8, 256, 256, 257, 3
+    logits, mask = _routing(T, E, k, seed=77, p_mask=0.25)
+    x = torch.randn(T, d).to(torch.bfloat16).cuda()
+    wg, wu, wd = (w.cuda() for w in _weights(E, d, f, torch.bfloat16, seed=9))
+    bufs = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    for b in (bufs.xs, bufs.h, bufs.y, bufs.out):
+        b.fill_(float("nan"))
+    out1 = M.moe_forward(logits.cuda(), x, mask.cuda(), wg, wu, wd, k, bufs).clone()
+    assert torch.all(torch.isfinite(out1))
+    R = int(bufs.offsets[-1])
+    assert R < T * k
+    for b in (bufs.xs, bufs.h, bufs.y):
+        assert torch.all(b[R:].float() == 0)
+    out2 = M.moe_forward(logits.cuda(), x, mask.cuda(), wg, wu, wd, k, bufs).clone()
+    assert torch.equal(out1.view(torch.int32), out2.view(torch.int32))
+    M.moe_check_device_error()
+
+
+def test_all_masked_output_is_plus_zero():
+    E, d, f, T, k = 4, 128, 128, 20, 2
+    logits, _ = _routing(T, E, k, seed=5)
+    mask = torch.ones(T, k, dtype=torch.uint8).cuda()
+    x = torch.randn(T, d).to(torch.bfloat16).cuda()
+    wg, wu, wd = (w.cuda() for w in _weights(E, d, f, torch.bfloat16, seed=2))
+    bufs = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    bufs.out.fill_(float("nan"))
+    out = M.moe_forward(logits.cuda(), x, mask, wg, wu, wd, k, bufs)
+    M.moe_check_device_error()
+    assert torch.all(out.view(torch.int32) == 0)  # +0.0 bit pattern everywhere
+
+
+def test_inconsistent_offsets_are_rejected_on_the_device():
+    """offsets[E] beyond the buffer capacity: the kernels skip their work and flag it; nothing hangs."""
+    E, d, f, cap = 4, 128, 128, 16
+    xs = torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda")
+    wg = torch.zeros(E, f, d, dtype=torch.bfloat16, device="cuda")
+    h = torch.zeros(cap, f, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(cap, d, dtype=torch.float32, device="cuda")
+    offsets = torch.tensor([0, 4, 8, 12, 40], dtype=torch.int32, device="cuda")
+    M.moe_grouped_ffn(xs, offsets, wg, wg, wg.transpose(1, 2).contiguous(), h, y)
+    with pytest.raises(M.MoEError) as exc:
+        M.moe_check_device_error()
+    assert exc.value.status == M.MOE_ERR_INVALID_ARG
+    M.moe_check_device_error()  # the error word was cleared
+
+
+def test_empty_chunk():
+    bufs = M.MoEBuffers(0, 8, 2, 128, 128, torch.bfloat16)
+    z = torch.empty(0, 8, device="cuda")
+    w = torch.zeros(8, 128, 128, dtype=torch.bfloat16, device="cuda")
+    out = M.moe_forward(z, torch.empty(0, 128, dtype=torch.bfloat16, device="cuda"), None, w, w, w, 2, bufs)
+    assert out.shape == (0, 128)
+    M.moe_check_device_error()
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: integer outputs checked completely, the output on a
+# sample of tokens recomputed by the oracle one token at a time
+# ---------------------------------------------------------------------------
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["verify_t4", "prefill_t401", "prefill_t2048", "prefill_t8192"])
+def test_full_size_workload(name):
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg, device="cuda")
+    bufs = M.MoEBuffers(cfg.T, cfg.E, cfg.k, cfg.d, cfg.f, torch.bfloat16)
+    out = M.moe_forward(inp["logits"], inp["x"], inp["mask"], inp["w_gate"], inp["w_up"], inp["w_down"], cfg.k,
+                        bufs)
+    M.moe_check_device_error()
+    mask = None if inp["mask"] is None else to_np(inp["mask"])
+    ids, w = mo.route_topk(to_np(inp["logits"]), cfg.k)
+    assert np.array_equal(to_np(bufs.ids), ids)
+    np.testing.assert_allclose(to_np(bufs.w), w, rtol=1e-6, atol=0)
+    counts = mo.route_histogram(ids, mask, cfg.E)
+    assert np.array_equal(to_np(bufs.counts), counts)
+    assert np.array_equal(to_np(bufs.offsets), mo.prefix_offsets(counts))
+    ror, rro = mo.scatter_permutation(ids, mask)
+    assert np.array_equal(to_np(bufs.row_of_route), ror)
+    assert np.array_equal(to_np(bufs.route_of_row), rro)
+    rng = np.random.default_rng(cfg.seed)
+    tokens = sorted(set([0, cfg.T - 1] + rng.choice(cfg.T, size=min(cfg.T, 6), replace=False).tolist()))
+    ref = mo.token_outputs(tokens, ids, w, mask, to_np(inp["x"]),
+                           oracle_weights(inp["w_gate"], inp["w_up"], inp["w_down"]))
+    assert_close(out[tokens], ref, "bf16")

@@ -1,0 +1,170 @@
+"""GPU parity of the routing-side kernels against the oracle (through the C-ABI).
+
+Top-k ids, counts, offsets and the permutation must match bit for bit; the
+gate weights within 1e-6 relative; the scattered rows byte for byte; the
+combine within the floating-point tolerance of its operand type.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as mo
+from sparse_moe_expert_top_gb300 import moe as M
+from tests.helpers import WEIGHT_REL, assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _topk(logits, k):
+    T, E = logits.shape
+    ids = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
+    M.moe_route_topk(logits.cuda().contiguous(), k, ids, w)
+    torch.cuda.synchronize()
+    return to_np(ids), to_np(w)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (4, 8, 2), (31, 64, 6), (33, 255, 8), (401, 256, 6), (2048, 256, 6),
+                                   (7, 256, 16), (100, 32, 4), (64, 2, 2), (50, 100, 16), (3, 17, 17 - 1)])
+def test_topk_matches_oracle(T, E, k):
+    g = torch.Generator().manual_seed(T * 7 + E)
+    logits = torch.randn(T, E, generator=g)
+    ids, w = _topk(logits, k)
+    ref_ids, ref_w = mo.route_topk(logits.numpy(), k)
+    assert np.array_equal(ids, ref_ids)
+    np.testing.assert_allclose(w, ref_w, rtol=WEIGHT_REL, atol=0)
+
+
+def test_topk_ties_and_signed_zeros():
+    """Integer-grid logits manufacture ties; half of the zeros are -0.0."""
+    g = torch.Generator().manual_seed(5)
+    logits = torch.randint(-3, 4, (512, 256), generator=g).float()
+    zeros = logits == 0
+    flip = torch.rand(logits.shape, generator=g) < 0.5
+    logits[zeros & flip] = -0.0
+    for k in (1, 6, 16):
+        ids, w = _topk(logits, k)
+        ref_ids, ref_w = mo.route_topk(logits.numpy(), k)
+        assert np.array_equal(ids, ref_ids)
+        np.testing.assert_allclose(w, ref_w, rtol=WEIGHT_REL, atol=0)
+
+
+def test_topk_golden_fixtures():
+    with open(os.path.join(GOLDEN, "topk_cases.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for c in cases:
+        ids, _ = _topk(torch.tensor([c["logits"]], dtype=torch.float32), c["k"])
+        assert ids[0].tolist() == c["ids"], c["name"]
+
+
+def _routing_case(T, E, k, p_mask, seed, skew=0.0):
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn(T, E, generator=g)
+    if skew:
+        logits += skew * torch.linspace(0, 1, E)[None, :]
+    mask = (torch.rand(T, k, generator=g) < p_mask).to(torch.uint8) if p_mask > 0 else None
+    return logits, mask
+
+
+def _run_index_path(logits, mask, k, x):
+    T, E = logits.shape
+    cap = T * k
+    dev = "cuda"
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts = torch.full((E,), -5, dtype=torch.int32, device=dev)
+    offsets = torch.full((E + 1,), -5, dtype=torch.int32, device=dev)
+    ws = torch.zeros(M.moe_workspace_size(T, k) // 4 + 4, dtype=torch.int32, device=dev)
+    xs = torch.full((cap, x.shape[1]), float("nan"), dtype=x.dtype, device=dev)
+    ror = torch.full((cap,), -9, dtype=torch.int32, device=dev)
+    rro = torch.full((cap,), -9, dtype=torch.int32, device=dev)
+    lg, xd = logits.cuda(), x.cuda()
+    md = None if mask is None else mask.cuda()
+    M.moe_route_topk(lg, k, ids, w)
+    M.moe_route_histogram(ids, md, E, counts, ws)
+    M.moe_prefix_offsets(counts, T, k, offsets, ws)
+    M.moe_scatter_rows(xd, ids, md, offsets, xs, ror, rro, ws)
+    M.moe_check_device_error()
+    return dict(ids=ids, w=w, counts=counts, offsets=offsets, xs=xs, row_of_route=ror, route_of_row=rro, ws=ws)
+
+
+@pytest.mark.parametrize("T,E,k,p,d,dtype", [
+    (1, 1, 1, 0.0, 8, torch.bfloat16),
+    (5, 4, 2, 0.5, 64, torch.float32),
+    (33, 8, 2, 0.0, 64, torch.float32),
+    (300, 16, 4, 0.1, 256, torch.bfloat16),
+    (401, 256, 6, 0.0, 4096, torch.bfloat16),
+    (2048, 256, 6, 0.1, 512, torch.bfloat16),
+    (3000, 256, 16, 0.3, 128, torch.bfloat16),   # several histogram chunks, ragged last chunk
+    (700, 3, 3, 0.0, 16, torch.bfloat16),        # heavy experts
+])
+def test_histogram_prefix_scatter(T, E, k, p, d, dtype):
+    logits, mask = _routing_case(T, E, k, p, seed=T + E)
+    x = torch.randn(T, d).to(dtype)
+    res = _run_index_path(logits, mask, k, x)
+    ref = mo.moe_forward(logits.numpy(), to_np(x), (np.zeros((E, 1, d)), np.zeros((E, 1, d)), np.zeros((E, d, 1))),
+                         k, None if mask is None else mask.numpy())
+    assert np.array_equal(to_np(res["ids"]), ref["ids"])
+    assert np.array_equal(to_np(res["counts"]), ref["counts"])
+    assert np.array_equal(to_np(res["offsets"]), ref["offsets"])
+    assert np.array_equal(to_np(res["row_of_route"]), ref["row_of_route"])
+    assert np.array_equal(to_np(res["route_of_row"]), ref["route_of_row"])
+    R = int(ref["offsets"][-1])
+    xs = res["xs"].cpu()
+    assert torch.equal(xs[:R], x[torch.as_tensor(ref["route_of_row"][:R] // k, dtype=torch.long)])
+    # unused compact rows are zero-filled (+0.0 bit patterns)
+    assert torch.all(xs[R:].view(torch.int16 if dtype == torch.bfloat16 else torch.int32) == 0)
+    # the workspace is reusable: a second pass gives the same permutation
+    res2 = _run_index_path(logits, mask, k, x)
+    assert torch.equal(res2["route_of_row"], res["route_of_row"])
+    assert torch.equal(res2["counts"], res["counts"])
+
+
+def test_all_masked_routes():
+    T, E, k = 40, 8, 2
+    logits, _ = _routing_case(T, E, k, 0.0, seed=1)
+    mask = torch.ones(T, k, dtype=torch.uint8)
+    x = torch.randn(T, 16)
+    res = _run_index_path(logits, mask, k, x)
+    assert torch.all(res["counts"] == 0) and torch.all(res["offsets"] == 0)
+    assert torch.all(res["row_of_route"] == -1) and torch.all(res["route_of_row"] == -1)
+    assert torch.all(res["xs"].cpu().view(torch.int32) == 0)
+
+
+def _combine(y, ror, w, T, k, d):
+    out = torch.full((T, d), float("nan"), dtype=torch.float32, device="cuda")
+    M.moe_combine(y.cuda(), ror.cuda(), w.cuda(), out)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def test_combine_golden_fixtures():
+    with open(os.path.join(GOLDEN, "combine_cases.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for c in cases:
+        y = torch.tensor(np.array(c["y"], dtype=np.float64), dtype=torch.float32)
+        y = torch.nn.functional.pad(y, (0, 4 - y.shape[1]))  # rows padded to a 16-byte multiple
+        out = _combine(y, torch.tensor(c["row_of_route"], dtype=torch.int32),
+                       torch.tensor(c["w"], dtype=torch.float32).reshape(c["T"], c["k"]), c["T"], c["k"], 4)
+        expect = torch.nn.functional.pad(torch.tensor(c["out"], dtype=torch.float32), (0, 4 - len(c["out"][0])))
+        assert torch.equal(out, expect), c["name"]
+        assert torch.equal(torch.signbit(out), torch.signbit(expect)), c["name"]
+
+
+@pytest.mark.parametrize("T,k,d,p", [(1, 1, 4, 0.0), (77, 2, 64, 0.3), (401, 6, 4096, 0.0), (2048, 6, 1024, 0.1)])
+def test_combine_matches_oracle(T, k, d, p):
+    g = torch.Generator().manual_seed(T)
+    cap = T * k
+    y = torch.randn(cap, d, generator=g)
+    perm = torch.randperm(cap, generator=g).to(torch.int32)
+    masked = torch.rand(cap, generator=g) < p
+    ror = torch.where(masked, torch.full_like(perm, -1), perm)
+    w = torch.rand(T, k, generator=g)
+    out = _combine(y, ror, w, T, k, d)
+    ref = mo.combine(y.numpy(), ror.numpy(), w.numpy(), T, k)
+    assert_close(out, ref, "f32")
