@@ -123,9 +123,39 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
-def _workload(name: str, rank: int):
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); identity on one rank."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int) -> dict:
+    """Algorithmic bytes and FLOPs of one step, from the realised expert counts.
+
+    Only touched experts' weights count; activations are counted once per
+    read or write.  es = operand bytes (2 for bf16, 4 for fp32); y and out are fp32.
+    """
+    counts = np.asarray(counts)
+    R = int(counts.sum())
+    touched = int(np.count_nonzero(counts))
+    gate_up = touched * 2 * f * d * es + R * d * es + R * f * es
+    down = touched * d * f * es + R * f * es + R * d * 4
+    routing = T * E * 4 + T * k * 8
+    scatter = T * d * es + R * d * es
+    combine = R * d * 4 + T * d * 4
+    return {"R": R, "touched": touched, "gate_up_bytes": gate_up, "down_bytes": down,
+            "path_bytes": routing + scatter + gate_up + down + combine, "flops": 6.0 * R * d * f}
+
+
+def _workload(name: str, rank: int, tokens: int = 0, experts: int = 0):
     from workloads import CONFIGS
     cfg = CONFIGS[name]
+    if tokens or experts:
+        cfg = cfg.replace(name=f"{name}[T={tokens or cfg.T},E={experts or cfg.E}]", T=tokens or cfg.T,
+                          E=experts or cfg.E)
     if rank:
         cfg = cfg.replace(seed=cfg.seed + 1000 * rank)
     return cfg
@@ -199,7 +229,7 @@ def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
     from workloads import make_inputs
-    cfg = _workload(args.workload, 0)
+    cfg = _workload(args.workload, 0, args.tokens, args.experts)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(cfg, device="cpu", weights_device=dev)
     per_step_budget = max(0.05, args.reference_budget_s / max(1, args.steps + args.warmup))
@@ -245,6 +275,41 @@ def _profiled_traffic(kernel: str, workload: str, units: float):
     return ent["dram_bytes_per_launch"]
 
 
+def _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k, bufs, T, d):
+    """End to end through the public API: pinned host inputs in, the output back to pinned host memory."""
+    h_logits = logits.cpu().pin_memory()
+    h_x = x.cpu().pin_memory()
+    h_mask = None if mask is None else mask.cpu().pin_memory()
+    h_out = torch.empty(T, d, dtype=torch.float32).pin_memory()
+    d_logits, d_x = torch.empty_like(logits), torch.empty_like(x)
+    d_mask = None if mask is None else torch.empty_like(mask)
+    h2d = h_logits.numel() * 4 + h_x.numel() * h_x.element_size() + (0 if h_mask is None else h_mask.numel())
+    d2h = h_out.numel() * 4
+
+    def e2e_step():
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        if d_mask is not None:
+            d_mask.copy_(h_mask, non_blocking=True)
+        out = M.moe_forward(d_logits, d_x, d_mask, wg, wu, wd, k, bufs)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    assert torch.equal(h_out, bufs.out.cpu()), "end-to-end output differs from the device-resident run"
+
+    return {"value": world * T * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
 def run_ours(args, rank: int, world: int):
     from sparse_moe_expert_top_gb300 import build as _build
     _build.build()
@@ -253,7 +318,7 @@ def run_ours(args, rank: int, world: int):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    cfg = _workload(args.workload, rank)
+    cfg = _workload(args.workload, rank, args.tokens, args.experts)
     inp = make_inputs(cfg, device=dev)
     T, E, k, d, f = cfg.T, cfg.E, cfg.k, cfg.d, cfg.f
     dtype = inp["x"].dtype
@@ -303,60 +368,22 @@ def run_ours(args, rank: int, world: int):
     clocks.mark(False)
     if world > 1:
         torch.distributed.barrier()
-    elapsed_ms = start.elapsed_time(end)
     clk = clocks.stop()
     M.moe_check_device_error()
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     per_kernel = {n: statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
                   for i, n in enumerate(names)}
 
-    # ---- end to end through the public API: pinned host inputs in, output out
-    h_logits = logits.cpu().pin_memory()
-    h_x = x.cpu().pin_memory()
-    h_mask = None if mask is None else mask.cpu().pin_memory()
-    h_out = torch.empty(T, d, dtype=torch.float32).pin_memory()
-    d_logits, d_x = torch.empty_like(logits), torch.empty_like(x)
-    d_mask = None if mask is None else torch.empty_like(mask)
-    h2d = h_logits.numel() * 4 + h_x.numel() * h_x.element_size() + (0 if h_mask is None else h_mask.numel())
-    d2h = h_out.numel() * 4
-
-    def e2e_step():
-        d_logits.copy_(h_logits, non_blocking=True)
-        d_x.copy_(h_x, non_blocking=True)
-        if d_mask is not None:
-            d_mask.copy_(h_mask, non_blocking=True)
-        out = M.moe_forward(d_logits, d_x, d_mask, wg, wu, wd, k, bufs)
-        h_out.copy_(out, non_blocking=True)
-
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_s = float(te.item())
-    assert torch.equal(h_out, bufs.out.cpu()), "end-to-end output differs from the device-resident run"
+    e2e = None if args.no_e2e else _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k, bufs, T, d)
 
     if rank != 0:
         return
 
     # ---- roofline of the dominant kernel (grouped gate/up + SwiGLU)
-    counts = bufs.counts.cpu().numpy()
-    R = int(counts.sum())
-    touched = int(np.count_nonzero(counts))
     es = 2 if dtype == torch.bfloat16 else 4
-    gate_up_bytes = touched * 2 * f * d * es + R * d * es + R * f * es
-    down_bytes = touched * d * f * es + R * f * es + R * d * 4
+    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es)
+    R, touched = work["R"], work["touched"]
+    gate_up_bytes = work["gate_up_bytes"]
     peaks = _peaks()
     gu_ms = per_kernel["gate_up"]
     achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
@@ -367,11 +394,7 @@ def run_ours(args, rank: int, world: int):
                 "algorithmic_bytes_per_launch": gate_up_bytes, "avg_launch_ms": gu_ms}
     # whole-path roofline: the slower of FLOPs at the dense bf16 tensor peak
     # and the path's algorithmic bytes at HBM bandwidth
-    flops = 6.0 * R * d * f
-    path_bytes = (T * E * 4 + T * k * 8                      # routing
-                  + T * d * es + R * d * es                  # scatter
-                  + gate_up_bytes + down_bytes               # grouped FFN
-                  + R * d * 4 + T * d * 4)                   # combine
+    flops, path_bytes = work["flops"], work["path_bytes"]
     t_roof = max(flops / (peaks["bf16_tflops_sustained"] * 1e12), path_bytes / (peaks["hbm_gbs"] * 1e9))
     ms_per_step = elapsed_ms / args.steps
     value = world * T * args.steps / (elapsed_ms * 1e-3)
@@ -394,8 +417,7 @@ def run_ours(args, rank: int, world: int):
                    "l2": f"inputs larger than L2: {touched * 3 * d * f * es / 1e9:.1f} GB of touched expert "
                          "weights streamed per step (L2 129 MB), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "e2e": {"value": world * T * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": args.steps * (7 if dtype == torch.bfloat16 else 9),
         "roofline": roofline,
         "path_roofline": {"flops": flops, "bytes": path_bytes, "t_roof_ms": t_roof * 1e3,
@@ -418,6 +440,9 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
