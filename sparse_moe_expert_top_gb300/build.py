@@ -32,10 +32,10 @@ def _nvcc() -> str:
     return cand
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, verbose_ptxas: bool, build_dir: str = BUILD, defines=()) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
     cmd = [_nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
-           "-c", os.path.join(CSRC, src), "-o", obj]
+           *[f"-D{d}" for d in defines], "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -46,25 +46,30 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False, force: bool = False) -> str:
-    """Compile and link the library; returns its path.  Skips work when up to date."""
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+def build(verbose_ptxas: bool = False, force: bool = False, out: str = LIB, defines=()) -> str:
+    """Compile and link the library; returns its path.  Skips work when up to date.
+
+    `out` and `defines` build a variant of the library elsewhere (tile-size
+    sweeps pass -D overrides of the kernels' compile-time constants).
+    """
+    build_dir = BUILD if out == LIB else out + ".objs"
+    os.makedirs(build_dir, exist_ok=True)
+    os.makedirs(os.path.dirname(out), exist_ok=True)
     inputs = [os.path.join(CSRC, s) for s in SOURCES] + [
         os.path.join(CSRC, "moe_internal.cuh"), os.path.join(ROOT, "include", "moe.h"), os.path.abspath(__file__)]
-    if not force and not verbose_ptxas and os.path.exists(LIB):
-        lib_mtime = os.path.getmtime(LIB)
+    if not force and not verbose_ptxas and not defines and os.path.exists(out):
+        lib_mtime = os.path.getmtime(out)
         if all(os.path.getmtime(p) <= lib_mtime for p in inputs):
-            return LIB
+            return out
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, build_dir, defines), SOURCES))
+    tmp = out + ".tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -45,8 +45,18 @@
 namespace moe {
 namespace {
 
+#ifndef MOE_TC_BN
+#define MOE_TC_BN 128
+#endif
+#ifndef MOE_TC_GATED_STAGES
+#define MOE_TC_GATED_STAGES 4
+#endif
+#ifndef MOE_TC_DOWN_STAGES
+#define MOE_TC_DOWN_STAGES 6
+#endif
+
 constexpr int BM = 128;        // MMA M: weight rows per tile
-constexpr int BN = 128;        // compact rows per work item (MMA N <= BN)
+constexpr int BN = MOE_TC_BN;  // compact rows per work item (MMA N <= BN, a multiple of 32)
 constexpr int BK = 64;         // K elements per stage (one 128-byte swizzle atom of bf16)
 constexpr int UMMA_K = 16;     // K per tcgen05.mma of kind::f16
 constexpr int kBoxRows = 16;   // compact rows per TMA box
@@ -56,14 +66,20 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 template <bool GATED>
 struct Cfg {
     static constexpr int kA = GATED ? 2 : 1;  // weight operands per stage
-    static constexpr int kStages = GATED ? 4 : 6;
+    static constexpr int kStages = GATED ? MOE_TC_GATED_STAGES : MOE_TC_DOWN_STAGES;
     static constexpr int kATileBytes = BM * BK * 2;
     static constexpr int kBTileBytes = BN * BK * 2;
     static constexpr int kStageBytes = kA * kATileBytes + kBTileBytes;
     static constexpr int kAccCols = kA * BN;
-    static constexpr int kTmemCols = 2 * kAccCols;  // two accumulator buffers
-    static constexpr int kCtrlBytes = 4096;
+    static constexpr int kTmemUsed = 2 * kAccCols;  // two accumulator buffers
+    // tcgen05.alloc takes a power of two >= 32 columns
+    static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                     : kTmemUsed <= 256 ? 256 : 512;
+    static constexpr int kCtrlBytes = 3072;  // barriers, TMEM slot, flags, item table (<= 2.3 KB)
     static constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+    static_assert(kTmemUsed <= 512, "TMEM has 512 columns");
+    static_assert(BN % 32 == 0 && BN <= 256, "rows per work item");
 };
 
 // ---------------------------------------------------------------------------
