@@ -114,6 +114,29 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k,
 moe_status moe_route_histogram(const int32_t* ids, const uint8_t* mask, int T, int k, int E,
                                int32_t* counts, void* ws, void* stream);
 
+/* Allocation-free variant of moe_route_histogram.  The pages have no
+ * counterpart of this entry point: it serves callers that cannot allocate
+ * device memory, such as code plugged into a host framework that owns every
+ * device allocation and hands its kernels no workspace, or runtimes that
+ * forbid allocation once they have started.  Such a caller passes only
+ * inputs and outputs:
+ *   ids, mask, T, k, E, counts  as for moe_route_histogram (same counts).
+ * The scratch (per-chunk counts, in-chunk ranks and a completion counter,
+ * 295 KB) is a static device array inside the library; every GPU that loads
+ * the library keeps it until the process exits.
+ *   Limit: T*k <= 65536 routes; a larger chunk returns MOE_ERR_INVALID_ARG
+ *   without enqueuing anything.
+ *   The first call on a device looks up the array's device address (once
+ *   per device, with that device current): make that first call before any
+ *   stream capture.
+ *   Every call on a device shares the one array and it keeps the previous
+ *   call's contents; the call clears what must start at zero itself.  Calls
+ *   that can overlap on the GPU (other streams, other host threads) race and
+ *   give wrong counts: serialise them.
+ *   Nothing is allocated: no cudaMalloc, no cudaFree. */
+moe_status moe_route_histogram_noalloc(const int32_t* ids, const uint8_t* mask, int T, int k, int E,
+                                       int32_t* counts, void* stream);
+
 /* A3 -- exclusive prefix over expert counts.  Same page, Summary
  * (GPU-native prefix).
  *   counts  [E] int32 from moe_route_histogram with the same T, k, E, ws.

@@ -13,6 +13,8 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -298,10 +300,46 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
 
 moe_status launch_status() { return cuda_status(cudaGetLastError()); }
 
+// Largest chunk the allocation-free histogram accepts, and its scratch size:
+// header + per-chunk counts + one in-chunk rank per route (295 KB).
+constexpr int kNoAllocMaxRoutes = 65536;
+constexpr int kNoAllocWords =
+    kWsHeaderWords + ((kNoAllocMaxRoutes + kHistChunk - 1) / kHistChunk) * kMaxExperts + kNoAllocMaxRoutes;
+
 }  // namespace
 }  // namespace moe
 
+// Scratch of moe_route_histogram_noalloc.  Every GPU that loads the library
+// holds this array until the process exits, and every call of that entry
+// point on a device uses the same copy.
+static __device__ __align__(256) int32_t g_noalloc_hist_scratch[moe::kNoAllocWords];
+
 using namespace moe;
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+int32_t* g_noalloc_scratch[64];
+
+// Device address of g_noalloc_hist_scratch on the current device.  In host
+// code the array's name is only a host-side stand-in, so the address is
+// looked up once per device (with that device current) and cached.
+moe_status noalloc_scratch(int32_t** out) {
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_scratch[dev] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_hist_scratch);
+        if (e != cudaSuccess) return cuda_status(e);
+        g_noalloc_scratch[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_noalloc_scratch[dev];
+    return MOE_OK;
+}
+
+}  // namespace
 
 extern "C" moe_status moe_workspace_size(int T, int k, size_t* bytes) {
     MOE_REQUIRE(bytes != nullptr && T >= 0 && k >= 1 && k <= kMaxK);
@@ -394,5 +432,28 @@ extern "C" moe_status moe_combine(const float* y, const int32_t* row_of_route, c
     if (st != MOE_OK) return st;
     combine_kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4*>(y), row_of_route, w, k, d / 4, reinterpret_cast<float4*>(out));
+    return launch_status();
+}
+
+// Allocation-free route histogram: the counts of moe_route_histogram, with
+// the scratch taken from g_noalloc_hist_scratch instead of a caller
+// workspace.  It allocates nothing; it clears the scratch's completion
+// counter before the launch because the array keeps the previous call's
+// contents.
+extern "C" moe_status moe_route_histogram_noalloc(const int32_t* ids, const uint8_t* mask, int T, int k, int E,
+                                                  int32_t* counts, void* stream) {
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E);
+    MOE_REQUIRE(counts != nullptr);
+    MOE_REQUIRE(static_cast<long long>(T) * k <= kNoAllocMaxRoutes);
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    int32_t* scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) return cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s));
+    MOE_REQUIRE(ids != nullptr);
+    MOE_CUDA_TRY(cudaMemsetAsync(scratch, 0, sizeof(int32_t), s));
+    route_histogram_kernel<<<ws_chunks(T, k), 256, 0, s>>>(ids, mask, T * k, E, scratch, counts, di.error_word);
     return launch_status();
 }

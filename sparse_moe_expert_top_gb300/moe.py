@@ -33,6 +33,7 @@ SIGNATURES = {
     "moe_workspace_size": ([_I, _I, _SZ], _I),
     "moe_route_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_route_histogram": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_route_histogram_noalloc": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_prefix_offsets": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_scatter_rows": ([_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gate_up": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P], _I),
@@ -139,6 +140,21 @@ def moe_route_histogram(ids, mask, E, counts, ws, stream=None):
     _expect(counts, torch.int32, (E,), "counts")
     _check("moe_route_histogram", load().moe_route_histogram(_ptr(ids), _ptr(mask), T, k, E, _ptr(counts), _ptr(ws),
                                                              _stream(stream)))
+
+
+def moe_route_histogram_noalloc(ids, mask, E, counts, stream=None):
+    """moe_route_histogram without a workspace: for callers that cannot allocate device memory.
+
+    The scratch is a static device array in the library (T*k <= 65536);
+    calls that overlap on the GPU race, so serialise them.
+    """
+    T, k = ids.shape
+    _expect(ids, torch.int32, (T, k), "ids")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect(counts, torch.int32, (E,), "counts")
+    _check("moe_route_histogram_noalloc", load().moe_route_histogram_noalloc(_ptr(ids), _ptr(mask), T, k, E,
+                                                                             _ptr(counts), _stream(stream)))
 
 
 def moe_prefix_offsets(counts, T, k, offsets, ws, stream=None):
