@@ -54,6 +54,16 @@ namespace {
 #ifndef MOE_TC_DOWN_STAGES
 #define MOE_TC_DOWN_STAGES 6
 #endif
+// L2 eviction priority of the TMA loads: 0 normal, 1 evict_first, 2 evict_last.
+// Weight tiles read by one work item only are streamed with evict_first;
+// tiles of experts with several row slices (read once per slice, by CTAs
+// that run at about the same time) are kept with MOE_TC_SHARED_W_POLICY.
+#ifndef MOE_TC_SHARED_W_POLICY
+#define MOE_TC_SHARED_W_POLICY 2
+#endif
+#ifndef MOE_TC_X_POLICY
+#define MOE_TC_X_POLICY 2
+#endif
 
 constexpr int BM = 128;        // MMA M: weight rows per tile
 constexpr int BN = MOE_TC_BN;  // compact rows per work item (MMA N <= BN, a multiple of 32)
@@ -150,15 +160,15 @@ __device__ __noinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     }
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+// L2 cache policy for TMA loads: 0 evict_normal, 1 evict_first, 2 evict_last.
+__device__ __forceinline__ uint64_t l2_policy(int kind) {
     uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    if (kind == 1)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    else if (kind == 2)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
@@ -356,8 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---- TMA producer -------------------------------------------------
         if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();
+            const uint64_t pol_once = l2_policy(1);
+            const uint64_t pol_shared = l2_policy(MOE_TC_SHARED_W_POLICY);
+            const uint64_t pol_x = l2_policy(MOE_TC_X_POLICY);
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -366,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
                 const uint32_t bytes = C::kA * C::kATileBytes + n16 * kBoxRows * BK * 2;
                 const int wy = item.e * M + item.mt * BM;
+                const uint64_t pol_w = ntiles[item.e] > 1 ? pol_shared : pol_once;
                 for (int kb = 0; kb < n_kb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
                         ok = false;
