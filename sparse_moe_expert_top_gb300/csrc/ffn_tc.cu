@@ -17,8 +17,9 @@
 // padding 9 rows up to an M = 128 tile.  (The pages' adaptive tile width on
 // RDNA is the same idea.)
 //
-// Work item = (expert e, 128-row slice mt of the output features, 128-row
-// slice nt of the expert's compact rows).  Items are numbered expert-major,
+// Work item = (expert e, a slice mt of the output features -- 128 for
+// gate/up, 256 (two tiles) for down -- and a 128-row slice nt of the
+// expert's compact rows).  Items are numbered expert-major,
 // then mt, then nt, so CTAs working at the same time on the nt slices of one
 // expert share its weight tile through L2.  The kernel is persistent: one
 // CTA per SM takes items blockIdx.x, blockIdx.x + gridDim.x, ...; every CTA
@@ -52,7 +53,7 @@ namespace {
 #define MOE_TC_GATED_STAGES 4
 #endif
 #ifndef MOE_TC_DOWN_STAGES
-#define MOE_TC_DOWN_STAGES 6
+#define MOE_TC_DOWN_STAGES 4
 #endif
 // L2 eviction priority of the TMA loads: 0 normal, 1 evict_first, 2 evict_last.
 // Weight tiles read by one work item only are streamed with evict_first;
@@ -75,7 +76,11 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 template <bool GATED>
 struct Cfg {
-    static constexpr int kA = GATED ? 2 : 1;  // weight operands per stage
+    // Two 128-row weight tiles per stage in both kernels: gate and up tiles of
+    // the same features (gated), or two consecutive 128-feature tiles of
+    // w_down (down).  Each stage's compact rows then feed two MMAs, which
+    // halves the row loads per weight byte of the down projection.
+    static constexpr int kA = 2;
     static constexpr int kStages = GATED ? MOE_TC_GATED_STAGES : MOE_TC_DOWN_STAGES;
     static constexpr int kATileBytes = BM * BK * 2;
     static constexpr int kBTileBytes = BN * BK * 2;
@@ -296,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_kb = K / BK;
-    const int n_mt = M / BM;
+    // feature tiles per expert: 128 features (gated) or 256 (down: two tiles)
+    const int n_mt = GATED ? M / BM : (M + 2 * BM - 1) / (2 * BM);
 
     // ---- prologue: barriers, TMEM, item table --------------------------------
     if (threadIdx.x == 0) {
@@ -376,7 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Item item = decode_item(it, item_off, ntiles, offsets, E);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
                 const uint32_t bytes = C::kA * C::kATileBytes + n16 * kBoxRows * BK * 2;
-                const int wy = item.e * M + item.mt * BM;
+                // w_down tiles past the expert's last feature (M not a multiple
+                // of 256) read the next expert's rows, or zero fill past the
+                // end of the bank; the epilogue stores none of their results
+                const int wy = item.e * M + item.mt * (GATED ? BM : 2 * BM);
+                const int wy1 = GATED ? wy : wy + BM;
                 const uint64_t pol_w = ntiles[item.e] > 1 ? pol_shared : pol_once;
                 for (int kb = 0; kb < n_kb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
@@ -387,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&full[s], bytes);
                     issued[s] = static_cast<int>(ph);
                     tma_load_2d(st, &map_a0, &full[s], kb * BK, wy, pol_w);
-                    if (GATED) tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * BK, wy, pol_w);
+                    tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * BK, wy1, pol_w);
                     uint8_t* bdst = st + C::kA * C::kATileBytes;
                     for (int j = 0; j < n16; ++j)
                         tma_load_2d(bdst + j * kBoxRows * 128, &map_b, &full[s], kb * BK, item.row0 + j * kBoxRows,
@@ -429,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
                         const uint64_t bd = sdesc_sw128(b + kk * UMMA_K * 2);
                         umma_bf16(d0, sdesc_sw128(a0 + kk * UMMA_K * 2), bd, idesc, acc);
-                        if (GATED) umma_bf16(d0 + BN, sdesc_sw128(a1 + kk * UMMA_K * 2), bd, idesc, acc);
+                        umma_bf16(d0 + BN, sdesc_sw128(a1 + kk * UMMA_K * 2), bd, idesc, acc);
                     }
                     umma_commit(&empty[s]);
                     if (++s == C::kStages) {
@@ -461,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int m = item.mt * BM + q * 32 + lane;
+            // output feature of this lane: gated -> one 128-feature tile;
+            // down -> tile 0 at m, tile 1 at m + 128
+            const int m = item.mt * (GATED ? BM : 2 * BM) + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(buf * C::kAccCols);
             for (int c0 = 0; c0 < item.rows; c0 += 32) {
@@ -482,12 +494,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
+                    uint32_t g1[32];
+                    tmem_ld32(taddr + BN + c0, g1);
                     tmem_ld_wait();
                     float* y = static_cast<float*>(out);
+                    const bool has1 = m + BM < M;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int n = c0 + j;
-                        if (n < item.rows) y[static_cast<size_t>(item.row0 + n) * M + m] = __uint_as_float(g[j]);
+                        if (n < item.rows) {
+                            float* yr = y + static_cast<size_t>(item.row0 + n) * M;
+                            yr[m] = __uint_as_float(g[j]);
+                            if (has1) yr[m + BM] = __uint_as_float(g1[j]);
+                        }
                     }
                 }
             }

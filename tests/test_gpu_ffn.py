@@ -42,6 +42,7 @@ FFN_CASES = [
     (4, 128, 128, 77, 2, 0.2, torch.bfloat16),
     (16, 512, 256, 600, 4, 0.1, torch.bfloat16),
     (1, 128, 256, 200, 1, 0.0, torch.bfloat16),
+    (3, 384, 256, 150, 2, 0.0, torch.bfloat16),   # d = 384: the down projection's last feature pair is half a pair
     (8, 64, 128, 32, 2, 0.0, torch.float32),
     (5, 96, 160, 50, 3, 0.3, torch.float32),
 ]
