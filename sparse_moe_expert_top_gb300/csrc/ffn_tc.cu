@@ -91,7 +91,9 @@ struct Cfg {
     static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                      : kTmemUsed <= 256 ? 256 : 512;
     static constexpr int kCtrlBytes = 3072;  // barriers, TMEM slot, flags, item table (<= 2.3 KB)
-    static constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + 1024;
+    // gate/up: a 32-row x 128-feature bf16 tile of h staged for row-contiguous stores
+    static constexpr int kOutStageBytes = GATED ? 32 * BM * 2 : 0;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + kOutStageBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
     static_assert(kTmemUsed <= 512, "TMEM has 512 columns");
     static_assert(BN % 32 == 0 && BN <= 256, "rows per work item");
@@ -242,6 +244,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Barrier 1 among the 128 epilogue threads (warps 2-5).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Work-item table
 // ---------------------------------------------------------------------------
@@ -298,6 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* issued = reinterpret_cast<int*>(tmem_slot + 2);  // last phase issued per stage, -1 = none
     int* item_off = issued + C::kStages;                  // E + 1 entries
     int* ntiles = item_off + kMaxExperts + 1;             // E entries
+    // outcome of the epilogue's accumulator wait, double-buffered by item
+    // parity (the four epilogue warps are never more than one item apart)
+    volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
+    __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + C::kCtrlBytes);  // gate/up only
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_kb = K / BK;
@@ -456,17 +465,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---- epilogue (warps 2..5) ----------------------------------------
-        const int q = warp & 3;  // TMEM lanes [32q, 32q+32) belong to this warp
+        // One thread waits (bounded) for the accumulator and publishes the
+        // outcome; every epilogue barrier below is reached by all four warps
+        // in every iteration, so an abandoned wait cannot leave a warp behind
+        // at a barrier.
+        const int q = warp & 3;               // TMEM lanes [32q, 32q+32) belong to this warp
+        const int et = threadIdx.x - 64;      // 0..127
         int local = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
             const Item item = decode_item(it, item_off, ntiles, offsets, E);
             const int buf = local & 1;
             const uint32_t acc_ph = static_cast<uint32_t>(local >> 1) & 1u;
-            int got = 1;
-            if (lane == 0) got = mbar_wait(&acc_full[buf], acc_ph, abort_flag, err) ? 1 : 0;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) {
+            if (et == 0) epi_flag[buf] = mbar_wait(&acc_full[buf], acc_ph, abort_flag, err) ? 1 : 0;
+            epilogue_sync();
+            if (!epi_flag[buf]) {
                 ok = false;
                 break;
             }
@@ -477,26 +490,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(buf * C::kAccCols);
             for (int c0 = 0; c0 < item.rows; c0 += 32) {
-                uint32_t g[32];
+                uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
+                tmem_ld32(taddr + BN + c0, g1);
+                tmem_ld_wait();
                 if (GATED) {
-                    uint32_t u[32];
-                    tmem_ld32(taddr + BN + c0, u);
-                    tmem_ld_wait();
-                    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
+                    // SwiGLU into the staged tile: row j, feature q*32 + lane
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
+                        const float gv = __uint_as_float(g[j]);
+                        const float hv = gv / (1.f + expf(-gv)) * __uint_as_float(g1[j]);
+                        out_stage[j * BM + q * 32 + lane] = __float2bfloat16_rn(hv);
+                    }
+                    epilogue_sync();
+                    // each row's 128 features (256 bytes) leave as 16 x 16-byte stores
+                    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
+                    const int chunk = et & 15;
+#pragma unroll
+                    for (int pass = 0; pass < 4; ++pass) {
+                        const int j = pass * 8 + (et >> 4);
                         const int n = c0 + j;
                         if (n < item.rows) {
-                            const float gv = __uint_as_float(g[j]);
-                            const float hv = gv / (1.f + expf(-gv)) * __uint_as_float(u[j]);
-                            h[static_cast<size_t>(item.row0 + n) * M + m] = __float2bfloat16_rn(hv);
+                            const uint4 v = *reinterpret_cast<const uint4*>(out_stage + j * BM + chunk * 8);
+                            *reinterpret_cast<uint4*>(h + static_cast<size_t>(item.row0 + n) * M + item.mt * BM +
+                                                      chunk * 8) = v;
                         }
                     }
+                    epilogue_sync();
                 } else {
-                    uint32_t g1[32];
-                    tmem_ld32(taddr + BN + c0, g1);
-                    tmem_ld_wait();
                     float* y = static_cast<float*>(out);
                     const bool has1 = m + BM < M;
 #pragma unroll
