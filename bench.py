@@ -199,12 +199,19 @@ def _time_oracle(inp, n_tokens: int):
     return time.perf_counter() - t0
 
 
-MAX_ORACLE_TOKENS = 16  # bounds the host copy of the sampled experts (<= 96 experts, fp32)
-
-
 def _size_oracle_sample(inp, budget_s: float):
+    """Tokens of the oracle sample: sized from a 1-token run, then corrected once.
+
+    The host copy of the sampled experts is bounded by the bank itself
+    (at most E experts, 3*d*f fp32 values each).
+    """
+    T = inp["cfg"].T
     t1 = _time_oracle(inp, 1)
-    n = int(max(1, min(inp["cfg"].T, MAX_ORACLE_TOKENS, budget_s / max(t1, 1e-3))))
+    n = int(max(1, min(T, budget_s / max(t1, 1e-3))))
+    if n < T:
+        tn = _time_oracle(inp, n)
+        if tn < 0.5 * budget_s:  # the per-token cost falls as experts are shared
+            n = int(max(1, min(T, n * budget_s / max(tn, 1e-3))))
     return n, t1
 
 
@@ -262,7 +269,7 @@ def _src_hash(*names):
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(kernel: str, workload: str, units: float):
+def _profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -387,7 +394,7 @@ def run_ours(args, rank: int, world: int):
     peaks = _peaks()
     gu_ms = per_kernel["gate_up"]
     achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic("gate_up", cfg.name, R)
+    traffic = _profiled_traffic("gate_up", cfg.name)
     roofline = {"kernel": "moe_grouped_gate_up (ffn_tc_kernel<gated>)", "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic, "peak_source": peaks["source"],

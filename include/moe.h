@@ -142,12 +142,17 @@ moe_status moe_route_histogram_noalloc(const int32_t* ids, const uint8_t* mask, 
  *   counts  [E] int32 from moe_route_histogram with the same T, k, E, ws.
  *   offsets [E+1] int32 out: offsets[0] = 0, offsets[e+1] = offsets[e] +
  *           counts[e]; offsets[E] = R.
- *   ws      the workspace moe_route_histogram filled; per-chunk counts are
- *           turned into per-chunk row bases for the scatter. */
+ *   ws      the workspace moe_route_histogram filled; the per-chunk counts
+ *           are read (not modified) and per-chunk row bases for the scatter
+ *           are written to another part of it, so the call may be repeated. */
 moe_status moe_prefix_offsets(const int32_t* counts, int T, int k, int E,
                               int32_t* offsets, void* ws, void* stream);
 
-/* A4 -- scatter to expert-major order.  Same page, Summary (GPU-native
+/* A4 -- scatter to expert-major order (every expert id, compact row and R is
+ * range-checked on the device before a write; a workspace that was not
+ * prepared by moe_route_histogram + moe_prefix_offsets for these ids makes
+ * moe_check_device_error() report MOE_ERR_INVALID_ARG, with no write outside
+ * xs, row_of_route and route_of_row).  Same page, Summary (GPU-native
  * scatter) and "Correctness and validation" (compact destinations are
  * zero-initialised).
  *   x            [T][d] operand type `dtype`.
@@ -198,7 +203,9 @@ moe_status moe_grouped_ffn(const void* xs, const int32_t* offsets, int cap, int 
  * route combine) and page "perf(ds4): batch heterogeneous MoE prefill by
  * expert", Summary (masked owner routes are exact zero contributions).
  *   y            [cap][d] fp32 expert outputs.
- *   row_of_route [T*k] int32, -1 = masked (skipped, never multiplied).
+ *   row_of_route [T*k] int32, -1 = masked (skipped, never multiplied); an
+ *                entry >= T*k is not a row of y: it is skipped and makes
+ *                moe_check_device_error() report MOE_ERR_INVALID_ARG.
  *   w            [T][k] fp32 gate weights.
  *   out          [T][d] fp32 out: out[t] = +0.0 + sum over ascending
  *                unmasked s of w[t][s] * y[row_of_route[t*k+s]], fp32

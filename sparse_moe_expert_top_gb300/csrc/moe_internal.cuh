@@ -20,9 +20,18 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxK = 16;
 
 // Workspace layout (int32 words): [0] completion counter, [1..31] reserved,
-// then chunk_counts[n_chunks][256], then local_rank[T*k].
+// then chunk_counts[n_chunks][256] (written by the histogram), local_rank[T*k]
+// (histogram), chunk_bases[n_chunks][256] (prefix).  The prefix reads the
+// counts and writes the bases elsewhere, so it can be repeated.
 constexpr int kWsHeaderWords = 32;
 inline int ws_chunks(int T, int k) { return (T * k + kHistChunk - 1) / kHistChunk; }
+inline size_t ws_rank_offset(int T, int k) {
+    return kWsHeaderWords + static_cast<size_t>(ws_chunks(T, k)) * kMaxExperts;
+}
+inline size_t ws_bases_offset(int T, int k) { return ws_rank_offset(T, k) + static_cast<size_t>(T) * k; }
+inline size_t ws_words(int T, int k) {
+    return ws_bases_offset(T, k) + static_cast<size_t>(ws_chunks(T, k)) * kMaxExperts;
+}
 
 struct DeviceInfo {
     int sm_count;

@@ -187,11 +187,13 @@ __global__ void __launch_bounds__(256) route_histogram_kernel(const int32_t* __r
 // ---------------------------------------------------------------------------
 // A3: exclusive prefix over expert counts (one CTA of 256 threads), and the
 // per-chunk row bases: base[c][e] = offsets[e] + sum of chunk counts c' < c.
+// The chunk counts are only read, so the call can be repeated.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(256) prefix_offsets_kernel(const int32_t* __restrict__ counts, int E,
                                                              int n_chunks, int32_t* __restrict__ offsets,
-                                                             int32_t* __restrict__ ws) {
+                                                             const int32_t* __restrict__ chunk_counts,
+                                                             int32_t* __restrict__ chunk_bases) {
     __shared__ int warp_sum[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = tid < E ? counts[tid] : 0;
@@ -210,12 +212,10 @@ __global__ void __launch_bounds__(256) prefix_offsets_kernel(const int32_t* __re
     if (tid == E - 1) offsets[E] = excl + c;
 
     if (tid < E) {
-        int32_t* cc = ws + kWsHeaderWords;
         int run = excl;
         for (int ch = 0; ch < n_chunks; ++ch) {
-            const int v = cc[static_cast<size_t>(ch) * kMaxExperts + tid];
-            cc[static_cast<size_t>(ch) * kMaxExperts + tid] = run;
-            run += v;
+            chunk_bases[static_cast<size_t>(ch) * kMaxExperts + tid] = run;
+            run += chunk_counts[static_cast<size_t>(ch) * kMaxExperts + tid];
         }
     }
 }
@@ -223,33 +223,47 @@ __global__ void __launch_bounds__(256) prefix_offsets_kernel(const int32_t* __re
 // ---------------------------------------------------------------------------
 // A4: scatter, one CTA per token.  The token row is read once with 128-bit
 // loads and written to each of its unmasked compact rows; the CTA also
-// zero-fills k of the unused tail rows R .. T*k-1.
+// zero-fills k of the unused tail rows R .. T*k-1.  Expert ids, compact rows
+// and R are checked against their ranges before any write: a workspace that
+// the histogram and prefix did not prepare for these ids sets
+// DEVERR_OFFSETS instead of writing outside xs.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restrict__ x,
                                                            const int32_t* __restrict__ ids,
                                                            const int32_t* __restrict__ offsets, int T, int k,
-                                                           int E, int row_vecs, const int32_t* __restrict__ ws,
-                                                           int n_chunks, uint4* __restrict__ xs,
+                                                           int E, int row_vecs, const int32_t* __restrict__ lrank,
+                                                           const int32_t* __restrict__ bases,
+                                                           uint4* __restrict__ xs,
                                                            int32_t* __restrict__ row_of_route,
-                                                           int32_t* __restrict__ route_of_row) {
+                                                           int32_t* __restrict__ route_of_row, unsigned* err) {
     __shared__ int rows[kMaxK];
     __shared__ int tails[kMaxK];
     const int t = blockIdx.x, tid = threadIdx.x;
     const int n_routes = T * k;
     if (tid < k) {
-        const int32_t* bases = ws + kWsHeaderWords;
-        const int32_t* lrank = bases + static_cast<size_t>(n_chunks) * kMaxExperts;
         const int r = t * k + tid;
         const int lr = lrank[r];
         int row = -1;
-        if (lr >= 0) row = bases[static_cast<size_t>(r / kHistChunk) * kMaxExperts + ids[r]] + lr;
+        bool bad = false;
+        if (lr >= 0) {
+            const int e = ids[r];
+            if (e >= 0 && e < E) row = bases[static_cast<size_t>(r / kHistChunk) * kMaxExperts + e] + lr;
+            if (row < 0 || row >= n_routes) {
+                bad = true;
+                row = -1;
+            }
+        }
         rows[tid] = row;
         row_of_route[r] = row;
         if (row >= 0) route_of_row[row] = r;
-        const int tail = __ldg(offsets + E) + r;
-        tails[tid] = tail < n_routes ? tail : -1;
-        if (tail < n_routes) route_of_row[tail] = -1;
+        const int R = __ldg(offsets + E);
+        int tail = -1;
+        if (R < 0 || R > n_routes) bad = true;
+        else if (R + r < n_routes) tail = R + r;
+        tails[tid] = tail;
+        if (tail >= 0) route_of_row[tail] = -1;
+        if (bad) atomicOr(err, DEVERR_OFFSETS);
     }
     __syncthreads();
     const uint4* src = x + static_cast<size_t>(t) * row_vecs;
@@ -271,13 +285,18 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
 
 __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__ y,
                                                       const int32_t* __restrict__ row_of_route,
-                                                      const float* __restrict__ w, int k, int d4,
-                                                      float4* __restrict__ out) {
+                                                      const float* __restrict__ w, int k, int d4, int cap,
+                                                      float4* __restrict__ out, unsigned* err) {
     __shared__ int rows[kMaxK];
     __shared__ float wt[kMaxK];
     const int t = blockIdx.x, tid = threadIdx.x;
     if (tid < k) {
-        rows[tid] = row_of_route[static_cast<size_t>(t) * k + tid];
+        int row = row_of_route[static_cast<size_t>(t) * k + tid];
+        if (row >= cap) {  // not a row of y: flagged, treated as masked
+            atomicOr(err, DEVERR_OFFSETS);
+            row = -1;
+        }
+        rows[tid] = row;
         wt[tid] = w[static_cast<size_t>(t) * k + tid];
     }
     __syncthreads();
@@ -344,9 +363,7 @@ moe_status noalloc_scratch(int32_t** out) {
 extern "C" moe_status moe_workspace_size(int T, int k, size_t* bytes) {
     MOE_REQUIRE(bytes != nullptr && T >= 0 && k >= 1 && k <= kMaxK);
     MOE_REQUIRE(static_cast<long long>(T) * k < (1ll << 30));
-    const size_t words = kWsHeaderWords + static_cast<size_t>(ws_chunks(T, k)) * kMaxExperts +
-                         static_cast<size_t>(T) * k;
-    *bytes = words * sizeof(int32_t);
+    *bytes = ws_words(T, k) * sizeof(int32_t);
     return MOE_OK;
 }
 
@@ -396,8 +413,9 @@ extern "C" moe_status moe_prefix_offsets(const int32_t* counts, int T, int k, in
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    prefix_offsets_kernel<<<1, 256, 0, s>>>(counts, E, T == 0 ? 0 : ws_chunks(T, k), offsets,
-                                            static_cast<int32_t*>(ws));
+    int32_t* w32 = static_cast<int32_t*>(ws);
+    prefix_offsets_kernel<<<1, 256, 0, s>>>(counts, E, T == 0 ? 0 : ws_chunks(T, k), offsets, w32 + kWsHeaderWords,
+                                            w32 + ws_bases_offset(T, k));
     return launch_status();
 }
 
@@ -416,9 +434,10 @@ extern "C" moe_status moe_scatter_rows(const void* x, int dtype, const int32_t* 
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
     const int row_vecs = static_cast<int>(static_cast<size_t>(d) * es / 16);
+    const int32_t* w32 = static_cast<const int32_t*>(ws);
     scatter_rows_kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(x), ids, offsets, T, k, E, row_vecs, static_cast<const int32_t*>(ws),
-        ws_chunks(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row);
+        static_cast<const uint4*>(x), ids, offsets, T, k, E, row_vecs, w32 + ws_rank_offset(T, k),
+        w32 + ws_bases_offset(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word);
     return launch_status();
 }
 
@@ -431,7 +450,8 @@ extern "C" moe_status moe_combine(const float* y, const int32_t* row_of_route, c
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
     combine_kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const float4*>(y), row_of_route, w, k, d / 4, reinterpret_cast<float4*>(out));
+        reinterpret_cast<const float4*>(y), row_of_route, w, k, d / 4, T * k, reinterpret_cast<float4*>(out),
+        di.error_word);
     return launch_status();
 }
 

@@ -57,8 +57,8 @@ def test_host_only_calls(lib):
     assert lib.moe_status_string(99) == b"unknown status"
     n = ctypes.c_size_t(0)
     assert lib.moe_workspace_size(2048, 6, ctypes.byref(n)) == 0
-    # header (32 words) + 6 chunks of 256 counts + 12288 ranks, int32
-    assert n.value == 4 * (32 + 6 * 256 + 2048 * 6)
+    # header (32 words) + 6 chunks of 256 counts + 12288 ranks + 6 chunks of 256 bases, int32
+    assert n.value == 4 * (32 + 6 * 256 + 2048 * 6 + 6 * 256)
     assert lib.moe_workspace_size(10, 17, ctypes.byref(n)) == 1      # k > 16
     assert lib.moe_workspace_size(-1, 2, ctypes.byref(n)) == 1       # T < 0
     # argument checks reject before touching the device

@@ -168,3 +168,53 @@ def test_combine_matches_oracle(T, k, d, p):
     out = _combine(y, ror, w, T, k, d)
     ref = mo.combine(y.numpy(), ror.numpy(), w.numpy(), T, k)
     assert_close(out, ref, "f32")
+
+
+def test_prefix_can_be_repeated():
+    """The prefix reads the histogram's chunk counts without changing them."""
+    T, E, k = 3000, 256, 6
+    logits, mask = _routing_case(T, E, k, 0.1, seed=4)
+    x = torch.randn(T, 64).to(torch.bfloat16)
+    once = _run_index_path(logits, mask, k, x)
+    again = _run_index_path(logits, mask, k, x)
+    M.moe_prefix_offsets(again["counts"], T, k, again["offsets"], again["ws"])
+    M.moe_prefix_offsets(again["counts"], T, k, again["offsets"], again["ws"])
+    M.moe_scatter_rows(x.cuda(), again["ids"], None if mask is None else mask.cuda(), again["offsets"],
+                       again["xs"], again["row_of_route"], again["route_of_row"], again["ws"])
+    M.moe_check_device_error()
+    for key in ("offsets", "row_of_route", "route_of_row", "xs"):
+        assert torch.equal(again[key], once[key]), key
+
+
+def test_scatter_rejects_an_unprepared_workspace():
+    """Ranks and bases that do not belong to these ids are caught before any write outside xs."""
+    T, E, k, d = 64, 8, 2, 64
+    logits, _ = _routing_case(T, E, k, 0.0, seed=6)
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    M.moe_route_topk(logits.cuda(), k, ids, w)
+    offsets = torch.tensor([0] + [T * k] * E, dtype=torch.int32, device="cuda")
+    ws = torch.full((M.moe_workspace_size(T, k) // 4 + 4,), 1_000_000, dtype=torch.int32, device="cuda")
+    xs = torch.zeros(T * k, d, dtype=torch.float32, device="cuda")
+    ror = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+    rro = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+    M.moe_scatter_rows(torch.randn(T, d, device="cuda"), ids, None, offsets, xs, ror, rro, ws)
+    with pytest.raises(M.MoEError) as exc:
+        M.moe_check_device_error()
+    assert exc.value.status == M.MOE_ERR_INVALID_ARG
+    assert torch.all(ror == -1) and torch.all(xs == 0)
+
+
+def test_combine_rejects_rows_beyond_the_buffer():
+    T, k, d = 16, 2, 8
+    y = torch.randn(T * k, d)
+    ror = torch.arange(T * k, dtype=torch.int32)
+    ror[5] = T * k + 7          # not a row of y
+    w = torch.rand(T, k)
+    out = _combine(y, ror, w, T, k, d)
+    with pytest.raises(M.MoEError) as exc:
+        M.moe_check_device_error()
+    assert exc.value.status == M.MOE_ERR_INVALID_ARG
+    ror_ref = ror.clone()
+    ror_ref[5] = -1             # the bad slot is skipped like a masked one
+    assert_close(out, mo.combine(y.numpy(), ror_ref.numpy(), w.numpy(), T, k), "f32")
