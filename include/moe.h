@@ -86,6 +86,19 @@ int moe_last_cuda_error(void);
  * work). */
 moe_status moe_check_device_error(void* stream);
 
+/* Diagnostic of the failure detection.  Every wait of the tensor-core
+ * kernels on a copy or an MMA is bounded (2 s); when one runs out the kernel
+ * abandons its work, drains what it has in flight, frees its tensor memory
+ * and records MOE_ERR_TIMEOUT in the device error word (the runs on the page
+ * "perf(ds4): extend sparse prefill scheduling to 10K" are likewise bounded
+ * by a guard and a timeout, and an aborted run counts as failed).  This call
+ * runs that same bounded wait on a barrier that nothing completes, giving up
+ * after limit_ms (1..5000) milliseconds, so that a caller can check the
+ * detection end to end: the following moe_check_device_error() returns
+ * MOE_ERR_TIMEOUT and clears the word.  It faults nothing and leaves the
+ * context usable. */
+moe_status moe_selftest_bounded_wait(int limit_ms, void* stream);
+
 /* Bytes of scratch workspace `ws` needed by moe_route_histogram,
  * moe_prefix_offsets, moe_scatter_rows and moe_forward for T tokens and
  * k slots.  The workspace must be zero-filled once before its first use

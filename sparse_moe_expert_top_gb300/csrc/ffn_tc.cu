@@ -141,7 +141,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Bounded wait for the phase of `bar` with parity `parity` to complete.
 // Returns false (after flagging the CTA and the device error word on a
 // time-out) when the wait is abandoned.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* err) {
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* err,
+                                       unsigned long long limit_ns = kWaitLimitNs) {
     const uint32_t addr = smem_u32(bar);
     if (mbar_try_wait(addr, parity)) return true;
     const unsigned long long t0 = global_ns();
@@ -149,7 +150,7 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile 
         if (mbar_try_wait(addr, parity)) return true;
         if ((i & 63u) == 0u) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(err, DEVERR_TIMEOUT);
                 return false;
@@ -563,6 +564,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Diagnostic of the bounded waits: one thread waits, through mbar_wait, for
+// an mbarrier phase that nothing completes, and gives up after limit_ns.
+__global__ void bounded_wait_probe_kernel(unsigned long long limit_ns, unsigned* err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, err, limit_ns);
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -643,3 +658,14 @@ moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, in
 }
 
 }  // namespace moe
+
+extern "C" moe_status moe_selftest_bounded_wait(int limit_ms, void* stream) {
+    using namespace moe;
+    MOE_REQUIRE(limit_ms >= 1 && limit_ms <= 5000);
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    bounded_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<unsigned long long>(limit_ms) * 1000000ull, di.error_word);
+    return cuda_status(cudaGetLastError());
+}

@@ -30,6 +30,7 @@ SIGNATURES = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_last_cuda_error": ([], _I),
     "moe_check_device_error": ([_P], _I),
+    "moe_selftest_bounded_wait": ([_I, _P], _I),
     "moe_workspace_size": ([_I, _I, _SZ], _I),
     "moe_route_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_route_histogram": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
@@ -116,6 +117,11 @@ def moe_version() -> int:
 
 def moe_check_device_error(stream=None) -> None:
     _check("moe_check_device_error", load().moe_check_device_error(_stream(stream)))
+
+
+def moe_selftest_bounded_wait(limit_ms: int, stream=None) -> None:
+    """Run one bounded wait that is bound to run out (see include/moe.h)."""
+    _check("moe_selftest_bounded_wait", load().moe_selftest_bounded_wait(limit_ms, _stream(stream)))
 
 
 def moe_workspace_size(T: int, k: int) -> int:
