@@ -200,7 +200,8 @@ def _time_oracle(inp, n_tokens: int):
 
 
 def _size_oracle_sample(inp, budget_s: float):
-    """Tokens of the oracle sample: sized from a 1-token run, then corrected once.
+    """Tokens of the oracle sample: sized from a 1-token run, then refined (the
+    per-token cost falls as the sampled tokens share experts).
 
     The host copy of the sampled experts is bounded by the bank itself
     (at most E experts, 3*d*f fp32 values each).
@@ -208,10 +209,13 @@ def _size_oracle_sample(inp, budget_s: float):
     T = inp["cfg"].T
     t1 = _time_oracle(inp, 1)
     n = int(max(1, min(T, budget_s / max(t1, 1e-3))))
-    if n < T:
+    for _ in range(3):
+        if n >= T:
+            break
         tn = _time_oracle(inp, n)
-        if tn < 0.5 * budget_s:  # the per-token cost falls as experts are shared
-            n = int(max(1, min(T, n * budget_s / max(tn, 1e-3))))
+        if tn >= 0.5 * budget_s:
+            break
+        n = int(max(1, min(T, n * budget_s / max(tn, 1e-3))))
     return n, t1
 
 

@@ -92,6 +92,261 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 }
 
 // ---------------------------------------------------------------------------
+// A1, streaming form (E a multiple of 4, E <= 256): four lanes per token,
+// eight tokens per warp.  Lane q of a token's quad holds float4 columns
+// q, q+4, ..., q+60 of the logit row (a quad load covers 64 contiguous bytes).
+//   1. Lower bound: every lane sorts the maxima of its float4 groups; two
+//      shuffle rounds merge the quad's sorted lists (the top of two sorted
+//      lists is the pairwise maximum of one with the other reversed), and
+//      tau = the k-th largest group maximum.  k group maxima are distinct
+//      logits >= tau, so every top-k logit is >= tau.
+//   2. Candidates: the logits >= tau (typically k plus a few) are appended
+//      to a per-token list in shared memory.
+//   3. Selection: a candidate's rank is the number of candidates that beat
+//      it under (logit descending, expert id ascending) -- a strict total
+//      order with -0.0 == +0.0 in the float comparisons -- and the ranks
+//      below k are the result, exactly.
+// A token whose candidates overflow the list (many ties at tau) is solved by
+// an exact insertion scan instead.  Few instructions per logit, no
+// divergent insertions on the common path: large chunks stream.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ bool topk_beats(float a, int ia, float b, int ib) {
+    return a > b || (a == b && ia < ib);
+}
+
+// Offers (x, e) to a sorted top-k list (v, id) whose last entry is thr: a
+// strictly larger x shifts the smaller entries down and lands after every
+// entry >= x.
+template <int KMAX>
+__device__ __forceinline__ void topk_offer(float (&v)[KMAX], int (&id)[KMAX], float& thr, int k, float x, int e) {
+    if (!(x > thr)) return;
+    bool placed = false;
+#pragma unroll
+    for (int i = KMAX - 1; i >= 0; --i) {
+        if (i < k && !placed) {
+            if (i > 0 && x > v[i - 1]) {
+                v[i] = v[i - 1];
+                id[i] = id[i - 1];
+            } else {
+                v[i] = x;
+                id[i] = e;
+                placed = true;
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i)
+        if (i == k - 1) thr = v[i];
+}
+
+// Sorts g[0..N) into descending order (bitonic network, branch-free).
+template <int N>
+__device__ __forceinline__ void sort_desc(float (&g)[N]) {
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const float hi = fmaxf(g[i], g[j]), lo = fminf(g[i], g[j]);
+                    const bool desc = (i & size) == 0;
+                    g[i] = desc ? hi : lo;
+                    g[j] = desc ? lo : hi;
+                }
+            }
+        }
+    }
+}
+
+// Sorts a bitonic sequence g[0..N) into descending order.
+template <int N>
+__device__ __forceinline__ void bitonic_merge_desc(float (&g)[N]) {
+#pragma unroll
+    for (int stride = N >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if ((i & stride) == 0) {
+                const float hi = fmaxf(g[i], g[i + stride]), lo = fminf(g[i], g[i + stride]);
+                g[i] = hi;
+                g[i + stride] = lo;
+            }
+        }
+    }
+}
+
+constexpr int kTopkCand = 32;  // candidate slots per token
+
+template <int KMAX>
+__global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                              int32_t* __restrict__ ids, float* __restrict__ w) {
+    constexpr int kNone = 0x7fffffff;
+    __shared__ float cand_v[4][8][kTopkCand];
+    __shared__ int cand_e[4][8][kTopkCand];
+    __shared__ float sel_v[4][8][KMAX];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3, tw = lane >> 2;
+    const unsigned quad = 0xfu << (lane & ~3);
+    const int t = blockIdx.x * 32 + warp * 8 + tw;
+    const bool valid = t < T;
+    const int nvec = E >> 2;
+
+    // this lane's 16 float4 groups (experts 4c .. 4c+3 for c = q + 4i)
+    float4 f[16];
+    const float4* row = reinterpret_cast<const float4*>(logits + static_cast<size_t>(valid ? t : 0) * E);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int c = q + 4 * i;
+        f[i] = (valid && c < nvec) ? __ldg(row + c) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+
+    // 1. tau: the k-th largest group maximum of the quad
+    float g[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[i] = fmaxf(fmaxf(f[i].x, f[i].y), fmaxf(f[i].z, f[i].w));
+    sort_desc<16>(g);
+    float top[KMAX];
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) top[i] = g[i];
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+        float other[KMAX];
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) other[i] = __shfl_xor_sync(quad, top[i], m);
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) top[i] = fmaxf(top[i], other[KMAX - 1 - i]);
+        bitonic_merge_desc<KMAX>(top);
+    }
+    float tau = top[0];
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i)
+        if (i == k - 1) tau = top[i];
+
+    // 2. candidates: logits >= tau, appended in (lane, group) order
+    int mine = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        mine += (f[i].x >= tau) + (f[i].y >= tau) + (f[i].z >= tau) + (f[i].w >= tau);
+    int incl = mine;
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        const int o = __shfl_up_sync(quad, incl, off, 4);
+        if (q >= off) incl += o;
+    }
+    const int n_cand = __shfl_sync(quad, incl, 3, 4);
+    float* cv = cand_v[warp][tw];
+    int* ce = cand_e[warp][tw];
+    float* sv = sel_v[warp][tw];
+    if (n_cand <= kTopkCand) {
+        int pos = incl - mine;
+        auto append = [&](float x, int e) {
+            if (x >= tau) {
+                cv[pos] = x;
+                ce[pos] = e;
+                ++pos;
+            }
+        };
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int e0 = 4 * (q + 4 * i);
+            append(f[i].x, e0);
+            append(f[i].y, e0 + 1);
+            append(f[i].z, e0 + 2);
+            append(f[i].w, e0 + 3);
+        }
+        __syncwarp(quad);
+        // 3. exact ranks among the candidates
+        for (int j = q; j < n_cand; j += 4) {
+            const float vj = cv[j];
+            const int ej = ce[j];
+            int rank = 0;
+            for (int i = 0; i < n_cand; ++i) rank += topk_beats(cv[i], ce[i], vj, ej) ? 1 : 0;
+            if (rank < k && valid) {
+                ids[static_cast<size_t>(t) * k + rank] = ej;
+                sv[rank] = vj;
+            }
+        }
+    } else {
+        // many ties at tau: exact insertion scan of all logits, then a merge
+        float v[KMAX];
+        int id[KMAX];
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) {
+            v[i] = -INFINITY;
+            id[i] = kNone;
+        }
+        float thr = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int e0 = 4 * (q + 4 * i);
+            topk_offer<KMAX>(v, id, thr, k, f[i].x, e0);
+            topk_offer<KMAX>(v, id, thr, k, f[i].y, e0 + 1);
+            topk_offer<KMAX>(v, id, thr, k, f[i].z, e0 + 2);
+            topk_offer<KMAX>(v, id, thr, k, f[i].w, e0 + 3);
+        }
+#pragma unroll
+        for (int m = 1; m <= 2; m <<= 1) {
+            float pv[KMAX];
+            int pid[KMAX];
+#pragma unroll
+            for (int i = 0; i < KMAX; ++i) {
+                pv[i] = __shfl_xor_sync(quad, v[i], m);
+                pid[i] = __shfl_xor_sync(quad, id[i], m);
+            }
+            float nv[KMAX];
+            int nid[KMAX];
+#pragma unroll
+            for (int r = 0; r < KMAX; ++r) {
+                nv[r] = -INFINITY;
+                nid[r] = kNone;
+                if (r < k) {
+                    const bool take_a = topk_beats(v[0], id[0], pv[0], pid[0]);
+                    nv[r] = take_a ? v[0] : pv[0];
+                    nid[r] = take_a ? id[0] : pid[0];
+#pragma unroll
+                    for (int i = 0; i < KMAX - 1; ++i) {
+                        v[i] = take_a ? v[i + 1] : v[i];
+                        id[i] = take_a ? id[i + 1] : id[i];
+                        pv[i] = take_a ? pv[i] : pv[i + 1];
+                        pid[i] = take_a ? pid[i] : pid[i + 1];
+                    }
+                    if (take_a) {
+                        v[KMAX - 1] = -INFINITY;
+                        id[KMAX - 1] = kNone;
+                    } else {
+                        pv[KMAX - 1] = -INFINITY;
+                        pid[KMAX - 1] = kNone;
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < KMAX; ++i) {
+                v[i] = nv[i];
+                id[i] = nid[i];
+            }
+        }
+        if (q == 0 && valid) {
+#pragma unroll
+            for (int r = 0; r < KMAX; ++r)
+                if (r < k) {
+                    ids[static_cast<size_t>(t) * k + r] = id[r];
+                    sv[r] = v[r];
+                }
+        }
+    }
+    __syncwarp(quad);
+    if (valid && q == 0) {
+        // softmax over the k selected logits, summed in slot order
+        float sum = 0.f;
+        for (int r = 0; r < k; ++r) sum += expf(sv[r] - sv[0]);
+        const float inv = 1.f / sum;
+        float* w_t = w + static_cast<size_t>(t) * k;
+        for (int r = 0; r < k; ++r) w_t[r] = expf(sv[r] - sv[0]) * inv;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // A2: route histogram with stable in-chunk ranks.
 //
 // CTA c owns routes [c*2048, (c+1)*2048); warp w of the CTA owns 256 of them
@@ -375,9 +630,17 @@ extern "C" moe_status moe_route_topk(const float* logits, int T, int E, int k, i
     DeviceInfo di;
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (E % 4 == 0 && aligned16(logits)) {  // E <= 256: 16 float4 groups per lane at most
+        const int blocks = (T + 31) / 32;  // 4 warps x 8 tokens
+        if (k <= 8)
+            route_topk_quad_kernel<8><<<blocks, 128, 0, s>>>(logits, T, E, k, ids, w);
+        else
+            route_topk_quad_kernel<16><<<blocks, 128, 0, s>>>(logits, T, E, k, ids, w);
+        return launch_status();
+    }
     const int threads = 256, warps_per_block = threads / 32;
     const int blocks = (T + warps_per_block - 1) / warps_per_block;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (E <= 32)
         route_topk_kernel<1><<<blocks, threads, 0, s>>>(logits, T, E, k, ids, w);
     else if (E <= 64)

@@ -218,3 +218,27 @@ def test_combine_rejects_rows_beyond_the_buffer():
     ror_ref = ror.clone()
     ror_ref[5] = -1             # the bad slot is skipped like a masked one
     assert_close(out, mo.combine(y.numpy(), ror_ref.numpy(), w.numpy(), T, k), "f32")
+
+
+@pytest.mark.parametrize("k", [1, 6, 8, 9, 16])
+def test_topk_streaming_and_warp_kernels_agree(k):
+    """E = 256 with 16-byte-aligned logits takes the streaming kernel; a 4-byte offset view takes the warp kernel."""
+    T, E = 777, 256
+    g = torch.Generator().manual_seed(k)
+    logits = torch.randint(-4, 5, (T, E), generator=g).float()   # many ties
+    logits[logits == 0] = -0.0
+    flat = torch.empty(T * E + 1, device="cuda")
+    shifted = flat[1:].view(T, E)
+    shifted.copy_(logits.cuda())
+    assert shifted.data_ptr() % 16 != 0
+    ids_a = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    ids_b = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w_a = torch.empty(T, k, device="cuda")
+    w_b = torch.empty(T, k, device="cuda")
+    M.moe_route_topk(logits.cuda(), k, ids_a, w_a)
+    M.moe_route_topk(shifted, k, ids_b, w_b)
+    ref_ids, ref_w = mo.route_topk(logits.numpy(), k)
+    assert np.array_equal(to_np(ids_a), ref_ids)
+    assert np.array_equal(to_np(ids_b), ref_ids)
+    np.testing.assert_allclose(to_np(w_a), ref_w, rtol=WEIGHT_REL, atol=0)
+    np.testing.assert_allclose(to_np(w_b), ref_w, rtol=WEIGHT_REL, atol=0)
