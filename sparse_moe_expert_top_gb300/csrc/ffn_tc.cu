@@ -46,14 +46,11 @@
 namespace moe {
 namespace {
 
-#ifndef MOE_TC_BN
-#define MOE_TC_BN 128
-#endif
-#ifndef MOE_TC_GATED_STAGES
-#define MOE_TC_GATED_STAGES 4
-#endif
-#ifndef MOE_TC_DOWN_STAGES
-#define MOE_TC_DOWN_STAGES 4
+// Big-item mode (row slices of up to 256 rows, 3 stages of 64 KB) is taken
+// when the rows beyond the first 128 of each expert reach this percentage
+// of all rows; otherwise row slices of 128 rows and 4 stages of 48 KB.
+#ifndef MOE_TC_BIG_MODE_PCT
+#define MOE_TC_BIG_MODE_PCT 50
 #endif
 // L2 eviction priority of the TMA loads: 0 normal, 1 evict_first, 2 evict_last.
 // Weight tiles read by one work item only are streamed with evict_first;
@@ -67,36 +64,37 @@ namespace {
 #endif
 
 constexpr int BM = 128;        // MMA M: weight rows per tile
-constexpr int BN = MOE_TC_BN;  // compact rows per work item (MMA N <= BN, a multiple of 32)
+constexpr int BN = 128;        // rows of a light work item / of one accumulator slot
 constexpr int BK = 64;         // K elements per stage (one 128-byte swizzle atom of bf16)
 constexpr int UMMA_K = 16;     // K per tcgen05.mma of kind::f16
-constexpr int kBoxRows = 16;   // compact rows per TMA box
+constexpr int kBoxRows = 16;   // compact rows per small TMA box (the granule of N)
+#ifndef MOE_TC_BIG_BOX_ROWS
+#define MOE_TC_BIG_BOX_ROWS 64
+#endif
+constexpr int kBigBoxRows = MOE_TC_BIG_BOX_ROWS;  // compact rows per large TMA box
 constexpr int kThreads = 192;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Shared memory: a 192 KB ring, carved per launch into 4 stages of 48 KB
+// (two 16 KB weight tiles + up to 128 rows) or, in big-item mode, 3 stages
+// of 64 KB (two weight tiles + up to 256 rows).  TMEM: 512 columns, region r
+// (weight tile r) at columns 256r, each region in two 128-column slots; a
+// light item uses slot s of both regions (consecutive light items alternate
+// slots, so one item's epilogue overlaps the next item's MMAs), a big item
+// uses both slots, i.e. 256 contiguous columns per region.
 template <bool GATED>
 struct Cfg {
-    // Two 128-row weight tiles per stage in both kernels: gate and up tiles of
-    // the same features (gated), or two consecutive 128-feature tiles of
-    // w_down (down).  Each stage's compact rows then feed two MMAs, which
-    // halves the row loads per weight byte of the down projection.
-    static constexpr int kA = 2;
-    static constexpr int kStages = GATED ? MOE_TC_GATED_STAGES : MOE_TC_DOWN_STAGES;
+    static constexpr int kA = 2;  // weight tiles per stage (gate+up, or two w_down feature tiles)
     static constexpr int kATileBytes = BM * BK * 2;
-    static constexpr int kBTileBytes = BN * BK * 2;
-    static constexpr int kStageBytes = kA * kATileBytes + kBTileBytes;
-    static constexpr int kAccCols = kA * BN;
-    static constexpr int kTmemUsed = 2 * kAccCols;  // two accumulator buffers
-    // tcgen05.alloc takes a power of two >= 32 columns
-    static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
-                                     : kTmemUsed <= 256 ? 256 : 512;
+    static constexpr int kMaxStages = 4;
+    static constexpr int kRingBytes = 4 * (kA * kATileBytes + BN * BK * 2);  // = 3 x 64 KB
+    static constexpr int kTmemCols = 512;
     static constexpr int kCtrlBytes = 3072;  // barriers, TMEM slot, flags, item table (<= 2.3 KB)
     // gate/up: a 32-row x 128-feature bf16 tile of h staged for row-contiguous stores
     static constexpr int kOutStageBytes = GATED ? 32 * BM * 2 : 0;
-    static constexpr int kSmemBytes = kStages * kStageBytes + kCtrlBytes + kOutStageBytes + 1024;
+    static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kOutStageBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
-    static_assert(kTmemUsed <= 512, "TMEM has 512 columns");
-    static_assert(BN % 32 == 0 && BN <= 256, "rows per work item");
+    static_assert(kRingBytes == 3 * (kA * kATileBytes + 2 * BN * BK * 2), "both carve-ups fill the ring");
 };
 
 // ---------------------------------------------------------------------------
@@ -259,7 +257,7 @@ struct Item {
 // item_off[e] = first item of expert e (exclusive scan), ntiles[e] = compact
 // row slices of expert e.  Items of one expert are ordered mt-major, nt-minor.
 __device__ __forceinline__ Item decode_item(int it, const int* item_off, const int* ntiles, const int32_t* offsets,
-                                            int E) {
+                                            int E, int slice) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -273,8 +271,8 @@ __device__ __forceinline__ Item decode_item(int it, const int* item_off, const i
     r.mt = local / n;
     const int nt = local - r.mt * n;
     const int seg_lo = __ldg(offsets + lo), seg_hi = __ldg(offsets + lo + 1);
-    r.row0 = seg_lo + nt * BN;
-    r.rows = min(BN, seg_hi - r.row0);
+    r.row0 = seg_lo + nt * slice;
+    r.rows = min(slice, seg_hi - r.row0);
     return r;
 }
 
@@ -287,26 +285,28 @@ __device__ __forceinline__ Item decode_item(int it, const int* item_off, const i
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-                  const __grid_constant__ CUtensorMap map_b, const int32_t* __restrict__ offsets, int cap, int E,
+                  const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
+                  const int32_t* __restrict__ offsets, int cap, int E,
                   int K, int M, void* __restrict__ out, unsigned* err) {
     using C = Cfg<GATED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* ctrl = smem + C::kStages * C::kStageBytes;
+    uint8_t* ctrl = smem + C::kRingBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-    uint64_t* empty = full + C::kStages;
-    uint64_t* acc_full = empty + C::kStages;
+    uint64_t* empty = full + C::kMaxStages;
+    uint64_t* acc_full = empty + C::kMaxStages;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* issued = reinterpret_cast<int*>(tmem_slot + 2);  // last phase issued per stage, -1 = none
-    int* item_off = issued + C::kStages;                  // E + 1 entries
+    int* item_off = issued + C::kMaxStages;               // E + 1 entries
     int* ntiles = item_off + kMaxExperts + 1;             // E entries
     // outcome of the epilogue's accumulator wait, double-buffered by item
     // parity (the four epilogue warps are never more than one item apart)
     volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
+    int* mode_big = const_cast<int*>(reinterpret_cast<volatile int*>(epi_flag + 2));   // launch-wide carve-up
     __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + C::kCtrlBytes);  // gate/up only
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- prologue: barriers, TMEM, item table --------------------------------
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kMaxStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             issued[s] = -1;
@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&map_a0);
         if (GATED) prefetch_tmap(&map_a1);
         prefetch_tmap(&map_b);
+        prefetch_tmap(&map_b_big);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -339,15 +340,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (warp == 2) {
-        // validate the segments and count the compact-row slices of every expert
+        // validate the segments, pick the carve-up, count the row slices of every expert
         bool bad = false;
+        long long rows = 0, excess = 0;
         for (int e = lane; e < E; e += 32) {
             const int lo = offsets[e], hi = offsets[e + 1];
-            const bool seg_bad = lo < 0 || hi < lo || hi > cap;
-            bad |= seg_bad;
-            ntiles[e] = seg_bad ? 0 : (hi - lo + BN - 1) / BN;
+            bad |= lo < 0 || hi < lo || hi > cap;
+            const int n = hi - lo;
+            rows += n > 0 ? n : 0;
+            excess += n > BN ? n - BN : 0;
         }
         bad = __any_sync(0xffffffffu, bad);
+        for (int off = 16; off > 0; off >>= 1) {
+            rows += __shfl_xor_sync(0xffffffffu, rows, off);
+            excess += __shfl_xor_sync(0xffffffffu, excess, off);
+        }
+        const bool big = rows > 0 && excess * 100 >= static_cast<long long>(MOE_TC_BIG_MODE_PCT) * rows;
+        if (lane == 0) *mode_big = big ? 1 : 0;
+        for (int e = lane; e < E; e += 32) {
+            const int n = offsets[e + 1] - offsets[e];
+            ntiles[e] = bad || n <= 0 ? 0 : (big && n > BN ? (n + 2 * BN - 1) / (2 * BN) : (n + BN - 1) / BN);
+        }
         __syncwarp();
         // exclusive scan of the item counts ntiles[e] * n_mt: lane j owns
         // experts [j*per, (j+1)*per)
@@ -378,6 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int n_items = item_off[E];
+    const bool big = *mode_big != 0;
+    const int S = big ? 3 : 4;                                     // stages
+    const int stage_bytes = C::kRingBytes / S;                     // 64 KB or 48 KB
+    const int slice = big ? 2 * BN : BN;                           // rows per work item at most
 
     if (warp == 0) {
         // ---- TMA producer -------------------------------------------------
@@ -389,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const Item item = decode_item(it, item_off, ntiles, offsets, E);
+                const Item item = decode_item(it, item_off, ntiles, offsets, E, slice);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
                 const uint32_t bytes = C::kA * C::kATileBytes + n16 * kBoxRows * BK * 2;
                 // w_down tiles past the expert's last feature (M not a multiple
@@ -403,16 +420,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* st = smem + s * C::kStageBytes;
+                    uint8_t* st = smem + s * stage_bytes;
                     mbar_arrive_expect_tx(&full[s], bytes);
                     issued[s] = static_cast<int>(ph);
                     tma_load_2d(st, &map_a0, &full[s], kb * BK, wy, pol_w);
                     tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * BK, wy1, pol_w);
                     uint8_t* bdst = st + C::kA * C::kATileBytes;
-                    for (int j = 0; j < n16; ++j)
-                        tma_load_2d(bdst + j * kBoxRows * 128, &map_b, &full[s], kb * BK, item.row0 + j * kBoxRows,
-                                    pol_x);
-                    if (++s == C::kStages) {
+                    // the rows in as few boxes as possible: 64-row boxes, then 16-row ones
+                    int r = 0;
+                    for (; r + kBigBoxRows <= n16 * kBoxRows; r += kBigBoxRows)
+                        tma_load_2d(bdst + r * 128, &map_b_big, &full[s], kb * BK, item.row0 + r, pol_x);
+                    for (; r < n16 * kBoxRows; r += kBoxRows)
+                        tma_load_2d(bdst + r * 128, &map_b, &full[s], kb * BK, item.row0 + r, pol_x);
+                    if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -424,24 +444,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            int local = 0;
+            int toggle = 0;            // slot of the next light item
+            uint32_t use0 = 0, use1 = 0;  // uses of each accumulator slot so far
             bool ok = true;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++local) {
-                const Item item = decode_item(it, item_off, ntiles, offsets, E);
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const Item item = decode_item(it, item_off, ntiles, offsets, E, slice);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
                 const uint32_t idesc = idesc_bf16(BM, n16 * kBoxRows);
-                const int buf = local & 1;
-                const uint32_t acc_ph = static_cast<uint32_t>(local >> 1) & 1u;
-                if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, abort_flag, err)) break;
+                const bool both = item.rows > BN;
+                const int slot = both ? 0 : toggle;
+                const uint32_t use_s = slot ? use1 : use0;
+                if (!mbar_wait(&acc_empty[slot], (use_s & 1u) ^ 1u, abort_flag, err)) break;
+                if (both && !mbar_wait(&acc_empty[1], (use1 & 1u) ^ 1u, abort_flag, err)) break;
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::kAccCols);
+                const uint32_t d0 = tmem_base + static_cast<uint32_t>(slot * BN);
                 for (int kb = 0; kb < n_kb; ++kb) {
                     if (!mbar_wait(&full[s], ph, abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smem + s * C::kStageBytes);
+                    const uint32_t a0 = smem_u32(smem + s * stage_bytes);
                     const uint32_t a1 = a0 + C::kATileBytes;
                     const uint32_t b = a0 + C::kA * C::kATileBytes;
 #pragma unroll
@@ -449,16 +472,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
                         const uint64_t bd = sdesc_sw128(b + kk * UMMA_K * 2);
                         umma_bf16(d0, sdesc_sw128(a0 + kk * UMMA_K * 2), bd, idesc, acc);
-                        umma_bf16(d0 + BN, sdesc_sw128(a1 + kk * UMMA_K * 2), bd, idesc, acc);
+                        umma_bf16(d0 + 2 * BN, sdesc_sw128(a1 + kk * UMMA_K * 2), bd, idesc, acc);
                     }
                     umma_commit(&empty[s]);
-                    if (++s == C::kStages) {
+                    if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(&acc_full[buf]);
+                umma_commit(&acc_full[slot]);
+                if (slot) ++use1;
+                else ++use0;
+                if (both) {
+                    umma_commit(&acc_full[1]);
+                    ++use1;
+                    toggle = 0;
+                } else {
+                    toggle ^= 1;
+                }
             }
             // every MMA issued above has completed once `drain` flips
             umma_commit(drain);
@@ -473,12 +505,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;               // TMEM lanes [32q, 32q+32) belong to this warp
         const int et = threadIdx.x - 64;      // 0..127
         int local = 0;
+        int toggle = 0;
+        uint32_t use0 = 0, use1 = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
-            const Item item = decode_item(it, item_off, ntiles, offsets, E);
-            const int buf = local & 1;
-            const uint32_t acc_ph = static_cast<uint32_t>(local >> 1) & 1u;
-            if (et == 0) epi_flag[buf] = mbar_wait(&acc_full[buf], acc_ph, abort_flag, err) ? 1 : 0;
+            const Item item = decode_item(it, item_off, ntiles, offsets, E, slice);
+            const bool both = item.rows > BN;
+            const int slot = both ? 0 : toggle;
+            const int buf = local & 1;  // flag parity
+            if (et == 0) {
+                bool got = mbar_wait(&acc_full[slot], (slot ? use1 : use0) & 1u, abort_flag, err);
+                if (got && both) got = mbar_wait(&acc_full[1], use1 & 1u, abort_flag, err);
+                epi_flag[buf] = got ? 1 : 0;
+            }
             epilogue_sync();
             if (!epi_flag[buf]) {
                 ok = false;
@@ -489,11 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // down -> tile 0 at m, tile 1 at m + 128
             const int m = item.mt * (GATED ? BM : 2 * BM) + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(buf * C::kAccCols);
+                                   static_cast<uint32_t>(slot * BN);
             for (int c0 = 0; c0 < item.rows; c0 += 32) {
                 uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
-                tmem_ld32(taddr + BN + c0, g1);
+                tmem_ld32(taddr + 2 * BN + c0, g1);
                 tmem_ld_wait();
                 if (GATED) {
                     // SwiGLU into the staged tile: row j, feature q*32 + lane
@@ -534,7 +573,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[slot]);
+                if (both) mbar_arrive(&acc_empty[1]);
+            }
+            if (slot) ++use1;
+            else ++use0;
+            if (both) {
+                ++use1;
+                toggle = 0;
+            } else {
+                toggle ^= 1;
+            }
         }
         // zero-fill the unused compact rows R .. cap-1
         const int R = offsets[E];
@@ -553,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort_flag && threadIdx.x == 0) {
         // let every TMA copy still in flight land before the CTA's shared
         // memory is released
-        for (int s = 0; s < C::kStages; ++s)
+        for (int s = 0; s < S; ++s)
             if (issued[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued[s]));
     }
     __syncthreads();
@@ -634,26 +684,28 @@ moe_status set_smem_attr() {
 moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
                                  const void* w_gate, const void* w_up, void* h, cudaStream_t st,
                                  const DeviceInfo& di) {
-    CUtensorMap ma0, ma1, mb;
+    CUtensorMap ma0, ma1, mb, mbb;
     moe_status s;
     if ((s = encode_2d(&ma0, w_gate, d, static_cast<long long>(E) * f, BM)) != MOE_OK) return s;
     if ((s = encode_2d(&ma1, w_up, d, static_cast<long long>(E) * f, BM)) != MOE_OK) return s;
     if ((s = encode_2d(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_2d(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
     if ((s = set_smem_attr<true>()) != MOE_OK) return s;
-    ffn_tc_kernel<true><<<di.sm_count, kThreads, Cfg<true>::kSmemBytes, st>>>(ma0, ma1, mb, offsets, cap, E, d, f,
-                                                                              h, di.error_word);
+    ffn_tc_kernel<true><<<di.sm_count, kThreads, Cfg<true>::kSmemBytes, st>>>(ma0, ma1, mb, mbb, offsets, cap, E, d,
+                                                                              f, h, di.error_word);
     return cuda_status(cudaGetLastError());
 }
 
 moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
                               const void* w_down, float* y, cudaStream_t st, const DeviceInfo& di) {
-    CUtensorMap ma0, mb;
+    CUtensorMap ma0, mb, mbb;
     moe_status s;
     if ((s = encode_2d(&ma0, w_down, f, static_cast<long long>(E) * d, BM)) != MOE_OK) return s;
     if ((s = encode_2d(&mb, h, f, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_2d(&mbb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
     if ((s = set_smem_attr<false>()) != MOE_OK) return s;
-    ffn_tc_kernel<false><<<di.sm_count, kThreads, Cfg<false>::kSmemBytes, st>>>(ma0, ma0, mb, offsets, cap, E, f, d,
-                                                                                y, di.error_word);
+    ffn_tc_kernel<false><<<di.sm_count, kThreads, Cfg<false>::kSmemBytes, st>>>(ma0, ma0, mb, mbb, offsets, cap, E, f,
+                                                                                d, y, di.error_word);
     return cuda_status(cudaGetLastError());
 }
 

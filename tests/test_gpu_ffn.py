@@ -198,3 +198,26 @@ def test_full_size_workload(name):
     ref = mo.token_outputs(tokens, ids, w, mask, to_np(inp["x"]),
                            oracle_weights(inp["w_gate"], inp["w_up"], inp["w_down"]))
     assert_close(out[tokens], ref, "bf16")
+
+
+@pytest.mark.parametrize("d,f", [(256, 256), (384, 256)])
+def test_big_item_mode_with_light_and_big_items(d, f):
+    """Most rows go to two experts (slices of up to 256 rows, the big-item carve-up); the rest stay light."""
+    E, T, k = 8, 700, 2
+    g = torch.Generator().manual_seed(d)
+    logits = torch.randn(T, E, generator=g)
+    logits[:, 6] += 3.0
+    logits[:, 7] += 2.5
+    x = torch.randn(T, d).to(torch.bfloat16)
+    wg, wu, wd = _weights(E, d, f, torch.bfloat16, seed=f)
+    bufs = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    out = M.moe_forward(logits.cuda(), x.cuda(), None, wg.cuda(), wu.cuda(), wd.cuda(), k, bufs)
+    M.moe_check_device_error()
+    ref = mo.moe_forward(logits.numpy(), to_np(x), (to_np(wg), to_np(wu), to_np(wd)), k)
+    counts = ref["counts"]
+    assert np.maximum(counts - 128, 0).sum() * 2 >= counts.sum()      # the big-item carve-up applies
+    assert (counts > 256).sum() >= 2 and ((counts > 0) & (counts <= 128)).sum() >= 2
+    h_ref = mo.grouped_swiglu(ref["xs"], ref["offsets"], (to_np(wg), to_np(wu), to_np(wd)))
+    R = int(ref["offsets"][-1])
+    assert_close_bf16_rounded(bufs.h[:R], h_ref)
+    assert_close(out, ref["out"], "bf16")
