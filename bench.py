@@ -441,6 +441,77 @@ def run_ours(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+def run_routing_sweep(args):
+    """Routing-side kernels (top-k, histogram, prefix, scatter, combine) over a T-sweep.
+
+    E = 256, k = 6, 10 % of routes masked; the row width d shrinks as T grows
+    so that every case fits a few GB.  Prints one JSON line per T with each
+    kernel's time and its achieved bandwidth (algorithmic bytes / time).
+    """
+    from sparse_moe_expert_top_gb300 import build as _build
+    _build.build()
+    from sparse_moe_expert_top_gb300 import moe as M
+
+    def timeit(fn, n=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n * 1e-3
+
+    E, k, dev = 256, 6, "cuda"
+    peak = _peaks()["hbm_gbs"]
+    for T, d in [(2048, 4096), (8192, 4096), (32768, 2048), (131072, 512), (262144, 256)]:
+        g = torch.Generator(device=dev).manual_seed(T)
+        logits = torch.randn(T, E, device=dev, generator=g)
+        x = torch.randn(T, d, device=dev, generator=g).to(torch.bfloat16)
+        mask = (torch.rand(T, k, device=dev, generator=g) < 0.1).to(torch.uint8)
+        cap = T * k
+        i32 = dict(dtype=torch.int32, device=dev)
+        ids, w = torch.empty(T, k, **i32), torch.empty(T, k, device=dev)
+        counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+        ws = torch.zeros(M.moe_workspace_size(T, k) // 4 + 4, **i32)
+        xs = torch.empty(cap, d, dtype=torch.bfloat16, device=dev)
+        ror, rro = torch.empty(cap, **i32), torch.empty(cap, **i32)
+        y = torch.randn(cap, d, device=dev, generator=g)
+        out = torch.empty(T, d, device=dev)
+        M.moe_route_topk(logits, k, ids, w)
+        M.moe_route_histogram(ids, mask, E, counts, ws)
+        M.moe_prefix_offsets(counts, T, k, offsets, ws)
+        M.moe_scatter_rows(x, ids, mask, offsets, xs, ror, rro, ws)
+        M.moe_check_device_error()
+        R = int(counts.sum())
+        times = {
+            "topk": timeit(lambda: M.moe_route_topk(logits, k, ids, w)),
+            "histogram": timeit(lambda: M.moe_route_histogram(ids, mask, E, counts, ws)),
+            "prefix": timeit(lambda: M.moe_prefix_offsets(counts, T, k, offsets, ws)),
+            "scatter": timeit(lambda: M.moe_scatter_rows(x, ids, mask, offsets, xs, ror, rro, ws)),
+            "combine": timeit(lambda: M.moe_combine(y, ror, w, out)),
+        }
+        M.moe_check_device_error()
+        nbytes = {
+            "topk": T * E * 4 + T * k * 8,
+            "histogram": T * k * 9,
+            "scatter": T * d * 2 + cap * d * 2 + T * k * 12,
+            "combine": R * d * 4 + T * d * 4 + T * k * 8,
+        }
+        line = {"routing_sweep": True, "T": T, "E": E, "k": k, "d": d, "R": R}
+        for name, t in times.items():
+            line[name + "_us"] = round(t * 1e6, 2)
+            if name in nbytes:
+                gbs = nbytes[name] / t / 1e9
+                line[name + "_GBs"] = round(gbs)
+                line[name + "_frac_of_hbm"] = round(gbs / peak, 3)
+        print(json.dumps(line), flush=True)
+        del logits, x, xs, y, out, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,6 +525,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
+    ap.add_argument("--routing-sweep", action="store_true",
+                    help="time the routing-side kernels over a T-sweep instead (JSON line per T)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -465,7 +538,9 @@ def main():
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group(backend)
     try:
-        if args.impl == "reference":
+        if args.routing_sweep:
+            run_routing_sweep(args)
+        elif args.impl == "reference":
             run_reference(args, rank, world)
         else:
             run_ours(args, rank, world)
