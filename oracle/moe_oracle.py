@@ -47,7 +47,9 @@ than itself): hand-derived golden fixtures, brute-force top-k over all
 orderings on tiny inputs, a closed-form two-expert softmax, counting and
 permutation invariants, the E=1/k=1 reduction to a dense SwiGLU FFN, the k=E
 reduction to a full softmax mixture, and the all-masked exact +0.0 case.
-No function here is unpinned.
+The FP8 E4M3 weight quantization at the end of the module is pinned against
+PyTorch's float8_e4m3fn cast (an independent implementation of the format),
+the format's bit layout and hand-worked ties.  No function here is unpinned.
 """
 
 from __future__ import annotations
@@ -299,3 +301,75 @@ def token_outputs(tokens, ids, w, mask, x, weights):
                 y = expert_ffn(x[t][None, :], *_expert(weights, int(ids[t, s])))[0]
                 out[i] += w[t, s] * y
     return out
+
+
+# ---------------------------------------------------------------------------
+# Low-bit expert weights: FP8 E4M3 codes with one scale per output channel
+# ---------------------------------------------------------------------------
+#
+# The pages run their experts on quantized weights (page "perf(ds4): batch
+# heterogeneous MoE prefill by expert", "Fresh main-snapshot requalification":
+# a ROCmFP2 model; page "perf(ggml): reuse ROCmFP4 weights across q=4
+# columns": ROCmFP4/FPX formats).  The GB300 counterpart here is the OCP FP8
+# E4M3 format (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; no
+# infinities; the all-ones code is NaN, so the largest finite value is 448;
+# subnormals down to 2^-9) with one float32 scale per output channel:
+#   s[e][m] = max_k |w[e][m][k]| / 448  (1 when the row is all zero),
+#   q[e][m][k] = E4M3 round-to-nearest-even of the float32 quotient
+#                w[e][m][k] / s[e][m], saturating at +-448,
+# and the dequantized weight is s * q.  Both divisions are float32 (IEEE),
+# so the codes are a function of the float32 inputs alone.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x):
+    """Nearest E4M3 value (ties to even), saturating at +-448, as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    # exponent of a: a = frac * 2^E with frac in [0.5, 1)  ->  binade 2^(E-1)
+    _, E = np.frexp(np.where(a > 0, a, 1.0))
+    binade = np.maximum(E - 1, -6)                  # subnormals share the 2^-6 binade's spacing
+    quantum = np.ldexp(1.0, binade - 3)             # 3 mantissa bits
+    r = np.round(a / quantum) * quantum             # np.round: half to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(x < 0, -r, r)
+
+
+def e4m3_encode(v):
+    """Byte code of E4M3 values (as produced by e4m3_round)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    sign = (v < 0) | ((v == 0) & np.signbit(v))
+    _, E = np.frexp(np.where(a > 0, a, 1.0))
+    e_field = np.where(a >= 2.0 ** -6, E - 1 + 7, 0)
+    mant = np.where(e_field > 0, a / np.ldexp(1.0, E - 1) * 8 - 8, a / 2.0 ** -9)
+    code = (sign.astype(np.int64) << 7) | (e_field.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
+    return np.where(a == 0, sign.astype(np.int64) << 7, code).astype(np.uint8)
+
+
+def e4m3_decode(code):
+    """Values of E4M3 byte codes (NaN code excluded)."""
+    c = np.asarray(code, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e > 0, np.ldexp(1.0 + m / 8.0, e - 7), np.ldexp(m / 8.0, -6))
+    return sign * val
+
+
+def quantize_weights_fp8(w):
+    """Per-output-channel FP8 E4M3 quantization of a weight bank [..., M, K].
+
+    Returns (codes uint8 [..., M, K], scales float32 [..., M]).  The
+    dequantized weights are scales[..., None] * e4m3_decode(codes).
+    """
+    w32 = np.asarray(w, dtype=np.float32)
+    amax = np.max(np.abs(w32), axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    quotient = (w32 / scale[..., None]).astype(np.float32)
+    return e4m3_encode(e4m3_round(quotient)), scale
+
+
+def dequantize_weights_fp8(codes, scales):
+    return np.asarray(scales, dtype=np.float64)[..., None] * e4m3_decode(codes)

@@ -1,0 +1,70 @@
+"""Pins of the oracle's FP8 E4M3 weight quantization.
+
+The rounding is checked against PyTorch's float8_e4m3fn cast (an independent
+implementation of the same OCP format), the codes against the format's bit
+layout, and the per-channel scaling against its defining properties.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as mo
+
+
+def test_e4m3_round_matches_torch_cast():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 100,                    # normals
+        rng.standard_normal(5000) * 2.0 ** -8,               # subnormal range
+        np.array([0.0, -0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11]),
+    ]).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(mo.e4m3_round(x), ref)
+
+
+def test_e4m3_ties_go_to_even_and_saturate():
+    # 1 + 1/16 lies halfway between 1 and 1.125: even mantissa (1.0) wins
+    assert mo.e4m3_round(1.0 + 1 / 16) == 1.0
+    # 1.125 + 1/16 lies between 1.125 (odd) and 1.25 (even): 1.25 wins
+    assert mo.e4m3_round(1.125 + 1 / 16) == 1.25
+    assert mo.e4m3_round(460.0) == 448.0 and mo.e4m3_round(1e6) == 448.0 and mo.e4m3_round(-1e6) == -448.0
+    assert mo.e4m3_round(2.0 ** -10) == 0.0            # half of the smallest subnormal -> even (0)
+    assert mo.e4m3_round(3 * 2.0 ** -10) == 2.0 ** -8  # 1.5 quanta -> 2 quanta (even)
+
+
+def test_code_layout_and_round_trip():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)  # all but NaN
+    vals = mo.e4m3_decode(codes)
+    assert vals.max() == 448.0 and vals.min() == -448.0
+    assert mo.e4m3_decode(np.array([0x38]))[0] == 1.0         # 0 0111 000
+    assert mo.e4m3_decode(np.array([0x01]))[0] == 2.0 ** -9   # smallest subnormal
+    np.testing.assert_array_equal(mo.e4m3_encode(vals), codes)
+    torch_vals = torch.from_numpy(codes.view(np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(vals, torch_vals)
+
+
+def test_per_channel_scaling_properties():
+    rng = np.random.default_rng(1)
+    w = (rng.standard_normal((3, 16, 64)) * 0.02).astype(np.float32)
+    w[1, 5] = 0.0                                       # an all-zero channel
+    codes, scales = mo.quantize_weights_fp8(w)
+    assert codes.dtype == np.uint8 and scales.dtype == np.float32 and scales.shape == (3, 16)
+    q = mo.e4m3_decode(codes)
+    assert scales[1, 5] == 1.0 and np.all(q[1, 5] == 0)
+    amax_q = np.abs(q).max(axis=-1)
+    nz = np.abs(w).max(axis=-1) > 0
+    assert np.all(amax_q[nz] == 448.0)                  # the largest element lands on the largest code
+    deq = mo.dequantize_weights_fp8(codes, scales)
+    # RNE error bound: half a quantum of the element's binade, at most 2^-4 of |w| for normals
+    err = np.abs(deq - w.astype(np.float64))
+    assert np.all(err <= np.abs(w) * 2.0 ** -4 + scales[..., None].astype(np.float64) * 2.0 ** -10 + 1e-30)
+
+
+def test_quantize_reads_float32_quotients():
+    """The quotient is rounded to float32 before the E4M3 rounding (both sides compute it in float32)."""
+    w = np.array([[0.1, 0.3, -0.7]], dtype=np.float32)
+    codes, scales = mo.quantize_weights_fp8(w)
+    expect_q = mo.e4m3_round((w / scales[:, None]).astype(np.float32))
+    np.testing.assert_array_equal(mo.e4m3_decode(codes), expect_q)
