@@ -333,7 +333,7 @@ def e4m3_round(x):
     quantum = np.ldexp(1.0, binade - 3)             # 3 mantissa bits
     r = np.round(a / quantum) * quantum             # np.round: half to even
     r = np.minimum(r, E4M3_MAX)
-    return np.where(x < 0, -r, r)
+    return np.copysign(r, x)                        # the format has a signed zero: -tiny -> -0
 
 
 def e4m3_encode(v):

@@ -20,8 +20,16 @@ def test_e4m3_round_matches_torch_cast():
         np.array([0.0, -0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11]),
     ]).astype(np.float32)
     x = np.clip(x, -448, 448)
-    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
-    np.testing.assert_array_equal(mo.e4m3_round(x), ref)
+    ref_t = torch.from_numpy(x).to(torch.float8_e4m3fn)
+    np.testing.assert_array_equal(mo.e4m3_round(x), ref_t.to(torch.float64).numpy())
+    # byte codes too, so that the sign of zero results is compared as well
+    np.testing.assert_array_equal(mo.e4m3_encode(mo.e4m3_round(x)), ref_t.view(torch.uint8).numpy())
+
+
+def test_negative_values_that_round_to_zero_keep_their_sign():
+    x = np.array([-0.0, -1e-9, -2.0 ** -11, 0.0, 1e-9], dtype=np.float32)
+    codes = mo.e4m3_encode(mo.e4m3_round(x))
+    assert codes.tolist() == [0x80, 0x80, 0x80, 0x00, 0x00]
 
 
 def test_e4m3_ties_go_to_even_and_saturate():
