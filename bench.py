@@ -132,17 +132,21 @@ def max_over_ranks(value: float, world: int, device) -> float:
     return float(t.item())
 
 
-def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int) -> dict:
+def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp8: bool = False) -> dict:
     """Algorithmic bytes and FLOPs of one step, from the realised expert counts.
 
     Only touched experts' weights count; activations are counted once per
-    read or write.  es = operand bytes (2 for bf16, 4 for fp32); y and out are fp32.
+    read or write.  es = operand bytes (2 for bf16, 4 for fp32); y and out are
+    fp32.  fp8: the expert weights are 1-byte codes plus one fp32 scale per
+    output channel (activations stay bf16).
     """
     counts = np.asarray(counts)
     R = int(counts.sum())
     touched = int(np.count_nonzero(counts))
-    gate_up = touched * 2 * f * d * es + R * d * es + R * f * es
-    down = touched * d * f * es + R * f * es + R * d * 4
+    wgu = touched * 2 * f * (d + 4) if fp8 else touched * 2 * f * d * es
+    wdn = touched * d * (f + 4) if fp8 else touched * d * f * es
+    gate_up = wgu + R * d * es + R * f * es
+    down = wdn + R * f * es + R * d * 4
     routing = T * E * 4 + T * k * 8
     scatter = T * d * es + R * d * es
     combine = R * d * 4 + T * d * 4
@@ -162,7 +166,11 @@ def _workload(name: str, rank: int, tokens: int = 0, experts: int = 0):
 
 
 def _oracle_inputs(inp, tokens):
-    """Host (float64) copies of the inputs a token sample needs: its logits, rows, mask and experts."""
+    """Host (float64) copies of the inputs a token sample needs: its logits, rows, mask and experts.
+
+    With FP8 weights (inp["fp8"]) the oracle quantizes each sampled expert
+    itself and works on the dequantized values.
+    """
     from oracle import moe_oracle as mo
     cfg = inp["cfg"]
     logits = inp["logits"].float().cpu().numpy()[tokens]
@@ -170,9 +178,14 @@ def _oracle_inputs(inp, tokens):
     mask = None if inp["mask"] is None else inp["mask"].cpu().numpy()[tokens]
     ids, _ = mo.route_topk(logits, cfg.k)
     experts = sorted(set(ids.ravel().tolist()))
+
+    def host(t):
+        a = t.float().cpu().numpy()
+        return mo.dequantize_weights_fp8(*mo.quantize_weights_fp8(a)) if inp.get("fp8") else a
+
     bank = {}
     for e in experts:
-        bank[e] = tuple(t[e].float().cpu().numpy() for t in (inp["w_gate"], inp["w_up"], inp["w_down"]))
+        bank[e] = tuple(host(t[e]) for t in (inp["w_gate"], inp["w_up"], inp["w_down"]))
     zero = None
     def get(e):
         nonlocal zero
@@ -243,6 +256,7 @@ def run_reference(args, rank: int, world: int):
     cfg = _workload(args.workload, 0, args.tokens, args.experts)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(cfg, device="cpu", weights_device=dev)
+    inp["fp8"] = args.weights == "fp8"
     per_step_budget = max(0.05, args.reference_budget_s / max(1, args.steps + args.warmup))
     n, _ = _size_oracle_sample(inp, per_step_budget)
     for _ in range(args.warmup):
@@ -256,7 +270,9 @@ def run_reference(args, rank: int, world: int):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k},
+        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k,
+                   "weights": "fp8_e4m3 codes + fp32 per-channel scales (quantized by the oracle)"
+                   if inp["fp8"] else "as drawn"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"first {n} tokens of the {cfg.T}-token chunk per step (numpy float64)",
                          "cpu": _cpu_desc()},
@@ -286,7 +302,7 @@ def _profiled_traffic(kernel: str, workload: str):
     return ent["dram_bytes_per_launch"]
 
 
-def _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k, bufs, T, d):
+def _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k, bufs, T, d, forward):
     """End to end through the public API: pinned host inputs in, the output back to pinned host memory."""
     h_logits = logits.cpu().pin_memory()
     h_x = x.cpu().pin_memory()
@@ -302,7 +318,7 @@ def _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k, bufs, T, d):
         d_x.copy_(h_x, non_blocking=True)
         if d_mask is not None:
             d_mask.copy_(h_mask, non_blocking=True)
-        out = M.moe_forward(d_logits, d_x, d_mask, wg, wu, wd, k, bufs)
+        out = forward(d_logits, d_x, d_mask, wg, wu, wd, k, bufs)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -333,9 +349,23 @@ def run_ours(args, rank: int, world: int):
     inp = make_inputs(cfg, device=dev)
     T, E, k, d, f = cfg.T, cfg.E, cfg.k, cfg.d, cfg.f
     dtype = inp["x"].dtype
-    bufs = M.MoEBuffers(T, E, k, d, f, dtype, device=dev)
+    fp8 = args.weights == "fp8"
+    # the FP8-weight path keeps its compact activations (xs, h) in fp16
+    bufs = M.MoEBuffers(T, E, k, d, f, torch.float16 if fp8 else dtype, device=dev)
     logits, x, mask = inp["logits"], inp["x"], inp["mask"]
-    wg, wu, wd = inp["w_gate"], inp["w_up"], inp["w_down"]
+    if fp8:
+        if dtype != torch.bfloat16:
+            raise SystemExit("--weights fp8 needs a bf16 workload")
+        # load-time step, outside the timed region: FP8 E4M3 codes + per-channel scales
+        inp["fp8"] = True
+        wg, wu, wd = (M.moe_quantize_weights_fp8(inp[n]) for n in ("w_gate", "w_up", "w_down"))
+        torch.cuda.synchronize()
+        gate_up_call, down_call, forward = M.moe_grouped_gate_up_fp8, M.moe_grouped_down_fp8, M.moe_forward_fp8
+        scatter_call = M.moe_scatter_rows_f16
+    else:
+        wg, wu, wd = inp["w_gate"], inp["w_up"], inp["w_down"]
+        gate_up_call, down_call, forward = M.moe_grouped_gate_up, M.moe_grouped_down, M.moe_forward
+        scatter_call = M.moe_scatter_rows
 
     names = ("topk", "histogram", "prefix", "scatter", "gate_up", "down", "combine")
 
@@ -345,9 +375,9 @@ def run_ours(args, rank: int, world: int):
             lambda: M.moe_route_topk(logits, k, b.ids, b.w),
             lambda: M.moe_route_histogram(b.ids, mask, E, b.counts, b.ws),
             lambda: M.moe_prefix_offsets(b.counts, T, k, b.offsets, b.ws),
-            lambda: M.moe_scatter_rows(x, b.ids, mask, b.offsets, b.xs, b.row_of_route, b.route_of_row, b.ws),
-            lambda: M.moe_grouped_gate_up(b.xs, b.offsets, wg, wu, b.h),
-            lambda: M.moe_grouped_down(b.h, b.offsets, wd, b.y),
+            lambda: scatter_call(x, b.ids, mask, b.offsets, b.xs, b.row_of_route, b.route_of_row, b.ws),
+            lambda: gate_up_call(b.xs, b.offsets, wg, wu, b.h),
+            lambda: down_call(b.h, b.offsets, wd, b.y),
             lambda: M.moe_combine(b.y, b.row_of_route, b.w, b.out),
         )
         for i, c in enumerate(calls):
@@ -385,21 +415,24 @@ def run_ours(args, rank: int, world: int):
     per_kernel = {n: statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
                   for i, n in enumerate(names)}
 
-    e2e = None if args.no_e2e else _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k, bufs, T, d)
+    e2e = None if args.no_e2e else _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k, bufs, T, d,
+                                            forward)
 
     if rank != 0:
         return
 
     # ---- roofline of the dominant kernel (grouped gate/up + SwiGLU)
     es = 2 if dtype == torch.bfloat16 else 4
-    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es)
+    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8)
     R, touched = work["R"], work["touched"]
     gate_up_bytes = work["gate_up_bytes"]
     peaks = _peaks()
     gu_ms = per_kernel["gate_up"]
     achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic("gate_up", cfg.name)
-    roofline = {"kernel": "moe_grouped_gate_up (ffn_tc_kernel<gated>)", "bound": "hbm", "achieved": achieved,
+    traffic = _profiled_traffic("gate_up_fp8" if fp8 else "gate_up", cfg.name)
+    kname = "moe_grouped_gate_up_fp8 (ffn_fp8_kernel<gated>)" if fp8 else \
+        "moe_grouped_gate_up (ffn_tc_kernel<gated>)"
+    roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic, "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": gate_up_bytes, "avg_launch_ms": gu_ms}
@@ -425,8 +458,10 @@ def run_ours(args, rank: int, world: int):
         "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32", "data": "synthetic",
         "config": {"workload": cfg.name, "T": T, "d": d, "f": f, "E": E, "k": k, "mask_p": cfg.mask_p,
                    "routes_unmasked": R, "experts_touched": touched,
-                   "l2": f"inputs larger than L2: {touched * 3 * d * f * es / 1e9:.1f} GB of touched expert "
-                         "weights streamed per step (L2 129 MB), no flush",
+                   "weights": "fp8_e4m3 codes + fp32 per-channel scales" if fp8 else
+                              ("bf16" if dtype == torch.bfloat16 else "f32"),
+                   "l2": f"inputs larger than L2: {touched * 3 * d * f * (1 if fp8 else es) / 1e9:.1f} GB of "
+                         "touched expert weights streamed per step (L2 129 MB), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "e2e": e2e,
         "gpu_launches": args.steps * (7 if dtype == torch.bfloat16 else 9),
@@ -525,6 +560,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
+    ap.add_argument("--weights", choices=("bf16", "fp8"), default="bf16",
+                    help="expert weight format: the workload's own (bf16), or FP8 E4M3 codes with per-channel "
+                         "scales quantized at load time")
     ap.add_argument("--routing-sweep", action="store_true",
                     help="time the routing-side kernels over a T-sweep instead (JSON line per T)")
     args = ap.parse_args()

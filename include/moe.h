@@ -61,7 +61,8 @@ typedef enum moe_status {
     MOE_ERR_INVALID_ARG = 1,  /* bad size, null pointer or misalignment (host check), or bad offsets (device check) */
     MOE_ERR_UNSUPPORTED = 2,  /* not an sm_103 device, or an unknown operand type */
     MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed; see moe_last_cuda_error() */
-    MOE_ERR_TIMEOUT = 4       /* a bounded wait inside a kernel ran out (device error word) */
+    MOE_ERR_TIMEOUT = 4,      /* a bounded wait inside a kernel ran out (device error word) */
+    MOE_ERR_RANGE = 5         /* a value did not fit the fp16 operands of the FP8-weight path (device error word) */
 } moe_status;
 
 typedef enum moe_dtype {
@@ -81,9 +82,10 @@ int moe_last_cuda_error(void);
 
 /* Synchronises `stream`, then reads and clears the sticky device error word
  * of the current device.  Returns MOE_OK, MOE_ERR_TIMEOUT (a bounded wait in
- * a kernel ran out; that kernel's outputs are undefined) or
+ * a kernel ran out; that kernel's outputs are undefined),
  * MOE_ERR_INVALID_ARG (a kernel found inconsistent offsets and skipped its
- * work). */
+ * work) or MOE_ERR_RANGE (the FP8-weight path met an activation beyond the
+ * fp16 range; the affected outputs hold infinities). */
 moe_status moe_check_device_error(void* stream);
 
 /* Diagnostic of the failure detection.  Every wait of the tensor-core
@@ -234,6 +236,81 @@ moe_status moe_forward(const float* logits, const void* x, const uint8_t* mask,
                        int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
                        void* xs, int32_t* row_of_route, int32_t* route_of_row,
                        void* h, float* y, float* out, void* ws, void* stream);
+
+/* A4 for the FP8-weight path: moe_scatter_rows with bf16 x, writing the
+ * compact rows xs as fp16 ([T*k][d], same layout).  The conversion is exact
+ * for |x| <= 65504 down to 2^-17 (smaller magnitudes round to fp16
+ * subnormals); a finite |x| > 65504 is written as an infinity and makes
+ * moe_check_device_error() report MOE_ERR_RANGE. */
+moe_status moe_scatter_rows_f16(const void* x, const int32_t* ids, const uint8_t* mask,
+                                const int32_t* offsets, int T, int k, int d, int E,
+                                void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                                void* ws, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Low-bit expert weights: FP8 E4M3 with one scale per output channel.
+ * The pages run their routed experts on low-bit weights (page "perf(ds4):
+ * batch heterogeneous MoE prefill by expert", "Fresh main-snapshot
+ * requalification": a ROCmFP2 expert model; page "perf(ggml): reuse ROCmFP4
+ * weights across q=4 columns": ROCmFP4/FPX weights).  Here a weight row
+ * (one output channel, K values) is stored as K OCP FP8 E4M3 codes (sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448) and one
+ * fp32 scale; the weight the FFN uses is scale * value(code), exactly.
+ * The codes are widened inside the SM to fp16 (exact: every E4M3 value is an
+ * fp16 value), so the compact activations xs and h of this path are fp16
+ * (tcgen05 kind::f16 takes both operands in one type), the products
+ * accumulate in fp32 and y and out are fp32.
+ * ------------------------------------------------------------------------ */
+
+/* Quantizes `rows` weight rows of K values (load-time step, not part of the
+ * per-chunk path).
+ *   w       [rows][K] operand type `dtype` (MOE_BF16 or MOE_F32), finite.
+ *   codes   [rows][K] uint8 out: E4M3 code of w / scale (fp32 division,
+ *           round to nearest even, saturating at +-448).
+ *   scales  [rows] fp32 out: max over the row of |w|, divided by 448 in
+ *           fp32; 1 for an all-zero row.
+ * K must be a multiple of 16; w and codes 16-byte aligned.  For expert
+ * banks pass rows = E*f (w_gate, w_up; K = d) or E*d (w_down; K = f). */
+moe_status moe_quantize_weights_fp8(const void* w, int dtype, long long rows, int K,
+                                    uint8_t* codes, float* scales, void* stream);
+
+/* A5 with FP8 weights: h[i] = silu(g) * u with g = s_gate[e][j] *
+ * (xs[i] . value(w_gate_q[e][j])) and u likewise from w_up_q, s_up.
+ *   xs       [cap][d] fp16 compact rows (moe_scatter_rows_f16); offsets as
+ *            for moe_grouped_gate_up.
+ *   w_gate_q, w_up_q [E][f][d] uint8 codes; s_gate, s_up [E][f] fp32.
+ *   h        [cap][f] fp16 out (round to nearest even); rows R .. cap-1
+ *            zero-filled; |h| > 65504 is written as an infinity and makes
+ *            moe_check_device_error() report MOE_ERR_RANGE.
+ * d and f multiples of 128. */
+moe_status moe_grouped_gate_up_fp8(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                   const uint8_t* w_gate_q, const float* s_gate,
+                                   const uint8_t* w_up_q, const float* s_up, void* h, void* stream);
+
+/* A6 with FP8 weights: y[i][j] = s_down[e][j] * (h[i] . value(w_down_q[e][j])).
+ *   h        [cap][f] fp16; w_down_q [E][d][f] uint8; s_down [E][d] fp32.
+ *   y        [cap][d] fp32 out; rows R .. cap-1 zero-filled. */
+moe_status moe_grouped_down_fp8(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                                const uint8_t* w_down_q, const float* s_down, float* y, void* stream);
+
+/* A5 + A6 with FP8 weights (two kernels on `stream`). */
+moe_status moe_grouped_ffn_fp8(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                               const uint8_t* w_gate_q, const float* s_gate,
+                               const uint8_t* w_up_q, const float* s_up,
+                               const uint8_t* w_down_q, const float* s_down,
+                               void* h, float* y, void* stream);
+
+/* The whole path (A1..A7) with FP8 expert weights: x is bf16, xs and h are
+ * fp16 (moe_scatter_rows_f16 is the scatter), every other argument as for
+ * moe_forward. */
+moe_status moe_forward_fp8(const float* logits, const void* x, const uint8_t* mask,
+                           int T, int E, int k, int d, int f,
+                           const uint8_t* w_gate_q, const float* s_gate,
+                           const uint8_t* w_up_q, const float* s_up,
+                           const uint8_t* w_down_q, const float* s_down,
+                           int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                           void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                           void* h, float* y, float* out, void* ws, void* stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmoe_gb300.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "routing.cu", "ffn_simt.cu", "ffn_tc.cu"]
+SOURCES = ["api.cu", "routing.cu", "ffn_simt.cu", "ffn_tc.cu", "ffn_fp8.cu"]
 
 
 def _nvcc() -> str:
@@ -56,7 +56,7 @@ def build(verbose_ptxas: bool = False, force: bool = False, out: str = LIB, defi
     os.makedirs(build_dir, exist_ok=True)
     os.makedirs(os.path.dirname(out), exist_ok=True)
     inputs = [os.path.join(CSRC, s) for s in SOURCES] + [
-        os.path.join(CSRC, "moe_internal.cuh"), os.path.join(ROOT, "include", "moe.h"), os.path.abspath(__file__)]
+        os.path.join(CSRC, "moe_internal.cuh"), os.path.join(CSRC, "tc_common.cuh"), os.path.join(ROOT, "include", "moe.h"), os.path.abspath(__file__)]
     if not force and not verbose_ptxas and not defines and os.path.exists(out):
         lib_mtime = os.path.getmtime(out)
         if all(os.path.getmtime(p) <= lib_mtime for p in inputs):

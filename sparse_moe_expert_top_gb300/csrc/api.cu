@@ -62,6 +62,7 @@ extern "C" const char* moe_status_string(int status) {
         case MOE_ERR_UNSUPPORTED: return "unsupported device or operand type";
         case MOE_ERR_CUDA: return "CUDA call failed";
         case MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case MOE_ERR_RANGE: return "a value out of the fp16 operand range";
         default: return "unknown status";
     }
 }
@@ -79,7 +80,9 @@ extern "C" moe_status moe_check_device_error(void* stream) {
     if (word == 0) return MOE_OK;
     const unsigned zero = 0;
     MOE_CUDA_TRY(cudaMemcpy(di.error_word, &zero, sizeof(zero), cudaMemcpyHostToDevice));
-    return (word & DEVERR_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_INVALID_ARG;
+    if (word & DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (word & DEVERR_OFFSETS) return MOE_ERR_INVALID_ARG;
+    return MOE_ERR_RANGE;
 }
 
 namespace {
@@ -160,6 +163,86 @@ extern "C" moe_status moe_forward(const float* logits, const void* x, const uint
                                stream)) != MOE_OK)
         return st;
     if ((st = moe_grouped_ffn(xs, offsets, cap, E, d, f, w_gate, w_up, w_down, dtype, h, y, stream)) != MOE_OK)
+        return st;
+    return moe_combine(y, row_of_route, w, T, k, d, out, stream);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 expert weights
+// ---------------------------------------------------------------------------
+
+extern "C" moe_status moe_quantize_weights_fp8(const void* w, int dtype, long long rows, int K, uint8_t* codes,
+                                               float* scales, void* stream) {
+    if (dtype_size(dtype) == 0) return MOE_ERR_UNSUPPORTED;
+    MOE_REQUIRE(rows >= 0 && K >= 16 && K % 16 == 0);
+    if (rows == 0) return MOE_OK;
+    MOE_REQUIRE(w && codes && scales && aligned16(w) && aligned16(codes));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_quantize_fp8(w, dtype, rows, K, codes, scales, static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_grouped_gate_up_fp8(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                              const uint8_t* w_gate_q, const float* s_gate, const uint8_t* w_up_q,
+                                              const float* s_up, void* h, void* stream) {
+    moe_status st = check_ffn_args(offsets, cap, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(xs && w_gate_q && s_gate && w_up_q && s_up && h);
+    MOE_REQUIRE(aligned16(xs) && aligned16(w_gate_q) && aligned16(w_up_q) && aligned16(h));
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_ffn_fp8_gate_up(xs, offsets, cap, E, d, f, w_gate_q, s_gate, w_up_q, s_up, h,
+                                  static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_grouped_down_fp8(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                                           const uint8_t* w_down_q, const float* s_down, float* y, void* stream) {
+    moe_status st = check_ffn_args(offsets, cap, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(h && w_down_q && s_down && y);
+    MOE_REQUIRE(aligned16(h) && aligned16(w_down_q) && aligned16(y));
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_ffn_fp8_down(h, offsets, cap, E, d, f, w_down_q, s_down, y, static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_grouped_ffn_fp8(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                          const uint8_t* w_gate_q, const float* s_gate, const uint8_t* w_up_q,
+                                          const float* s_up, const uint8_t* w_down_q, const float* s_down, void* h,
+                                          float* y, void* stream) {
+    moe_status st = moe_grouped_gate_up_fp8(xs, offsets, cap, E, d, f, w_gate_q, s_gate, w_up_q, s_up, h, stream);
+    if (st != MOE_OK) return st;
+    return moe_grouped_down_fp8(h, offsets, cap, E, d, f, w_down_q, s_down, y, stream);
+}
+
+extern "C" moe_status moe_forward_fp8(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k,
+                                      int d, int f, const uint8_t* w_gate_q, const float* s_gate,
+                                      const uint8_t* w_up_q, const float* s_up, const uint8_t* w_down_q,
+                                      const float* s_down, int32_t* ids, float* w, int32_t* counts,
+                                      int32_t* offsets, void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                                      void* h, float* y, float* out, void* ws, void* stream) {
+    moe_status st = check_ffn_args(offsets, T * k, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && k <= E);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && w_gate_q && s_gate && w_up_q && s_up && w_down_q && s_down && ids && w && counts &&
+                xs && row_of_route && route_of_row && h && y && out && ws);
+    MOE_REQUIRE(aligned16(x) && aligned16(xs) && aligned16(h) && aligned16(y) && aligned16(out) &&
+                aligned16(ws) && aligned16(w_gate_q) && aligned16(w_up_q) && aligned16(w_down_q));
+    const int cap = T * k;
+    if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
+    if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
+    if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+    if ((st = moe_scatter_rows_f16(x, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
+                                   stream)) != MOE_OK)
+        return st;
+    if ((st = moe_grouped_ffn_fp8(xs, offsets, cap, E, d, f, w_gate_q, s_gate, w_up_q, s_up, w_down_q, s_down, h, y,
+                                  stream)) != MOE_OK)
         return st;
     return moe_combine(y, row_of_route, w, T, k, d, out, stream);
 }

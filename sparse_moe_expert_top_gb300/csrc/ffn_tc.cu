@@ -34,14 +34,9 @@
 // Every mbarrier wait is bounded: when it runs out the kernel records
 // DEVERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and returns.
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
-#include <cuda_runtime.h>
 
-#include <mutex>
-
-#include "moe_internal.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
@@ -73,7 +68,6 @@ constexpr int kBoxRows = 16;   // compact rows per small TMA box (the granule of
 #endif
 constexpr int kBigBoxRows = MOE_TC_BIG_BOX_ROWS;  // compact rows per large TMA box
 constexpr int kThreads = 192;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Shared memory: a 192 KB ring, carved per launch into 4 stages of 48 KB
 // (two 16 KB weight tiles + up to 128 rows) or, in big-item mode, 3 stages
@@ -96,185 +90,6 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
     static_assert(kRingBytes == 3 * (kA * kATileBytes + 2 * BN * BK * 2), "both carve-ups fill the ring");
 };
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait for the phase of `bar` with parity `parity` to complete.
-// Returns false (after flagging the CTA and the device error word on a
-// time-out) when the wait is abandoned.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* err,
-                                       unsigned long long limit_ns = kWaitLimitNs) {
-    const uint32_t addr = smem_u32(bar);
-    if (mbar_try_wait(addr, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(addr, parity)) return true;
-        if ((i & 63u) == 0u) {
-            if (*abort_flag) return false;
-            if (global_ns() - t0 > limit_ns) {
-                *abort_flag = 1;
-                atomicOr(err, DEVERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
-// Bounded wait that ignores the abort flag: used while draining copies and
-// MMAs that are already in flight.
-__device__ __noinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
-    const uint32_t addr = smem_u32(bar);
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(addr, parity) && global_ns() - t0 < kWaitLimitNs) {
-    }
-}
-
-// L2 cache policy for TMA loads: 0 evict_normal, 1 evict_first, 2 evict_last.
-__device__ __forceinline__ uint64_t l2_policy(int kind) {
-    uint64_t p;
-    if (kind == 1)
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    else if (kind == 2)
-        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    else
-        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major, 128B-swizzled operand tile:
-// rows of 128 bytes, 8-row core groups 1024 bytes apart (stride byte
-// offset), descriptor version 1, swizzle mode 2 (128B).  The leading byte
-// offset is unused for this layout.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(1) << 16;
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
-
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
-// and B, both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Barrier 1 among the 128 epilogue threads (warps 2-5).
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// ---------------------------------------------------------------------------
-// Work-item table
-// ---------------------------------------------------------------------------
-
-struct Item {
-    int e, mt, row0, rows;
-};
-
-// item_off[e] = first item of expert e (exclusive scan), ntiles[e] = compact
-// row slices of expert e.  Items of one expert are ordered mt-major, nt-minor.
-__device__ __forceinline__ Item decode_item(int it, const int* item_off, const int* ntiles, const int32_t* offsets,
-                                            int E, int slice) {
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (item_off[mid] <= it) lo = mid;
-        else hi = mid - 1;
-    }
-    Item r;
-    r.e = lo;
-    const int local = it - item_off[lo];
-    const int n = ntiles[lo];
-    r.mt = local / n;
-    const int nt = local - r.mt * n;
-    const int seg_lo = __ldg(offsets + lo), seg_hi = __ldg(offsets + lo + 1);
-    r.row0 = seg_lo + nt * slice;
-    r.rows = min(slice, seg_hi - r.row0);
-    return r;
-}
 
 // ---------------------------------------------------------------------------
 // The kernel.  GATED: out = h (bf16 [cap][M]) = silu(A0 . xs) * (A1 . xs) with
@@ -464,15 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smem + s * stage_bytes);
-                    const uint32_t a1 = a0 + C::kATileBytes;
-                    const uint32_t b = a0 + C::kA * C::kATileBytes;
+                    // descriptors advance by 32 bytes of K (2 in the low half) per MMA
+                    const uint32_t a0 = sdesc_lo(smem_u32(smem + s * stage_bytes));
+                    const uint32_t a1 = a0 + (C::kATileBytes >> 4);
+                    const uint32_t b = a0 + ((C::kA * C::kATileBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-                        const uint64_t bd = sdesc_sw128(b + kk * UMMA_K * 2);
-                        umma_bf16(d0, sdesc_sw128(a0 + kk * UMMA_K * 2), bd, idesc, acc);
-                        umma_bf16(d0 + 2 * BN, sdesc_sw128(a1 + kk * UMMA_K * 2), bd, idesc, acc);
+                        const uint64_t bd = sdesc_from_lo(b + 2 * kk);
+                        umma_bf16(d0, sdesc_from_lo(a0 + 2 * kk), bd, idesc, acc);
+                        umma_bf16(d0 + 2 * BN, sdesc_from_lo(a1 + 2 * kk), bd, idesc, acc);
                     }
                     umma_commit(&empty[s]);
                     if (++s == S) {
@@ -632,37 +448,14 @@ __global__ void bounded_wait_probe_kernel(unsigned long long limit_ns, unsigned*
 // Host side
 // ---------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_mutex;
 bool g_attr_set[64][2];
-
-moe_status get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_encode == nullptr) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        MOE_CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q));
-        if (q != cudaDriverEntryPointSuccess || p == nullptr) return MOE_ERR_UNSUPPORTED;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    *fn = g_encode;
-    return MOE_OK;
-}
 
 // 2-D bf16 tensor map over a row-major [rows][K] matrix with a box of
 // 64 K-elements x box_rows rows and 128-byte swizzle.
 moe_status encode_2d(CUtensorMap* map, const void* base, int K, long long rows, int box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
-    moe_status st = get_encode(&enc);
-    if (st != MOE_OK) return st;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
-                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+    return encode_2d_map(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, rows, BK, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <bool GATED>

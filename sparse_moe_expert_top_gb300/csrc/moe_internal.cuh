@@ -12,6 +12,7 @@ namespace moe {
 enum : unsigned {
     DEVERR_TIMEOUT = 1u,   // a bounded wait ran out
     DEVERR_OFFSETS = 2u,   // offsets failed the device-side consistency check
+    DEVERR_RANGE = 4u,     // a value did not fit the fp16 operands of the FP8-weight path
 };
 
 // Routes handled by one CTA of the histogram kernel (8 warps x 8 steps x 32 lanes).
@@ -61,6 +62,15 @@ moe_status launch_ffn_simt_gate_up(const float* xs, const int32_t* offsets, int 
                                    const DeviceInfo& di);
 moe_status launch_ffn_simt_down(const float* h, const int32_t* offsets, int cap, int E, int d, int f,
                                 const float* w_down, float* y, cudaStream_t st, const DeviceInfo& di);
+
+moe_status launch_ffn_fp8_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                  const uint8_t* q_gate, const float* s_gate, const uint8_t* q_up, const float* s_up,
+                                  void* h, cudaStream_t st, const DeviceInfo& di);
+moe_status launch_ffn_fp8_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                               const uint8_t* q_down, const float* s_down, float* y, cudaStream_t st,
+                               const DeviceInfo& di);
+moe_status launch_quantize_fp8(const void* w, int dtype, long long rows, int K, uint8_t* codes, float* scales,
+                               cudaStream_t st, const DeviceInfo& di);
 
 }  // namespace moe
 

@@ -484,6 +484,17 @@ __global__ void __launch_bounds__(256) prefix_offsets_kernel(const int32_t* __re
 // DEVERR_OFFSETS instead of writing outside xs.
 // ---------------------------------------------------------------------------
 
+// bf16x2 -> f16x2 (exact for |v| <= 65504 down to 2^-17; smaller values
+// round to fp16 subnormals).  Sets `range` when a value is beyond 65504.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool& range) {
+    const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
+    range |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <bool TO_F16>
 __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restrict__ x,
                                                            const int32_t* __restrict__ ids,
                                                            const int32_t* __restrict__ offsets, int T, int k,
@@ -522,8 +533,15 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
     }
     __syncthreads();
     const uint4* src = x + static_cast<size_t>(t) * row_vecs;
+    bool range = false;
     for (int v = tid; v < row_vecs; v += blockDim.x) {
-        const uint4 val = __ldg(src + v);
+        uint4 val = __ldg(src + v);
+        if (TO_F16) {
+            val.x = bf16x2_to_f16x2(val.x, range);
+            val.y = bf16x2_to_f16x2(val.y, range);
+            val.z = bf16x2_to_f16x2(val.z, range);
+            val.w = bf16x2_to_f16x2(val.w, range);
+        }
         for (int s = 0; s < k; ++s) {
             const int row = rows[s];
             if (row >= 0) xs[static_cast<size_t>(row) * row_vecs + v] = val;
@@ -531,6 +549,7 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
             if (tail >= 0) xs[static_cast<size_t>(tail) * row_vecs + v] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
+    if (TO_F16 && __syncthreads_or(range) && tid == 0) atomicOr(err, DEVERR_RANGE);
 }
 
 // ---------------------------------------------------------------------------
@@ -682,12 +701,11 @@ extern "C" moe_status moe_prefix_offsets(const int32_t* counts, int T, int k, in
     return launch_status();
 }
 
-extern "C" moe_status moe_scatter_rows(const void* x, int dtype, const int32_t* ids, const uint8_t* mask,
-                                       const int32_t* offsets, int T, int k, int d, int E, void* xs,
-                                       int32_t* row_of_route, int32_t* route_of_row, void* ws, void* stream) {
-    (void)mask;  // the histogram already folded the mask into the workspace ranks
-    const int es = dtype_size(dtype);
-    if (es == 0) return MOE_ERR_UNSUPPORTED;
+namespace {
+
+moe_status scatter_rows(const void* x, int es, bool to_f16, const int32_t* ids, const int32_t* offsets, int T,
+                        int k, int d, int E, void* xs, int32_t* row_of_route, int32_t* route_of_row, void* ws,
+                        void* stream) {
     MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 1);
     MOE_REQUIRE((static_cast<size_t>(d) * es) % 16 == 0);
     if (T == 0) return MOE_OK;
@@ -698,10 +716,29 @@ extern "C" moe_status moe_scatter_rows(const void* x, int dtype, const int32_t* 
     if (st != MOE_OK) return st;
     const int row_vecs = static_cast<int>(static_cast<size_t>(d) * es / 16);
     const int32_t* w32 = static_cast<const int32_t*>(ws);
-    scatter_rows_kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+    auto kernel = to_f16 ? scatter_rows_kernel<true> : scatter_rows_kernel<false>;
+    kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(x), ids, offsets, T, k, E, row_vecs, w32 + ws_rank_offset(T, k),
         w32 + ws_bases_offset(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word);
     return launch_status();
+}
+
+}  // namespace
+
+extern "C" moe_status moe_scatter_rows(const void* x, int dtype, const int32_t* ids, const uint8_t* mask,
+                                       const int32_t* offsets, int T, int k, int d, int E, void* xs,
+                                       int32_t* row_of_route, int32_t* route_of_row, void* ws, void* stream) {
+    (void)mask;  // the histogram already folded the mask into the workspace ranks
+    const int es = dtype_size(dtype);
+    if (es == 0) return MOE_ERR_UNSUPPORTED;
+    return scatter_rows(x, es, false, ids, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws, stream);
+}
+
+extern "C" moe_status moe_scatter_rows_f16(const void* x, const int32_t* ids, const uint8_t* mask,
+                                           const int32_t* offsets, int T, int k, int d, int E, void* xs,
+                                           int32_t* row_of_route, int32_t* route_of_row, void* ws, void* stream) {
+    (void)mask;
+    return scatter_rows(x, 2, true, ids, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws, stream);
 }
 
 extern "C" moe_status moe_combine(const float* y, const int32_t* row_of_route, const float* w, int T, int k, int d,

@@ -19,12 +19,12 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libmoe_gb300.so")
 
-MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(5)
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_RANGE = range(6)
 MOE_F32, MOE_BF16 = 0, 1
 
 # (name, argtypes) of every exported entry point; the ABI test checks this
 # list against include/moe.h.
-_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)
+_P, _I, _L, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.POINTER(ctypes.c_size_t)
 SIGNATURES = {
     "moe_version": ([], _I),
     "moe_status_string": ([_I], ctypes.c_char_p),
@@ -37,12 +37,19 @@ SIGNATURES = {
     "moe_route_histogram_noalloc": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_prefix_offsets": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_scatter_rows": ([_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "moe_scatter_rows_f16": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gate_up": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P], _I),
     "moe_grouped_down": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _P], _I),
     "moe_grouped_ffn": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_forward": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I,
                      _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_quantize_weights_fp8": ([_P, _I, _L, _I, _P, _P, _P], _I),
+    "moe_grouped_gate_up_fp8": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_down_fp8": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_grouped_ffn_fp8": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_forward_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                         _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
 }
 
 
@@ -184,6 +191,21 @@ def moe_scatter_rows(x, ids, mask, offsets, xs, row_of_route, route_of_row, ws, 
                                                        _ptr(ws), _stream(stream)))
 
 
+def moe_scatter_rows_f16(x, ids, mask, offsets, xs, row_of_route, route_of_row, ws, stream=None):
+    """moe_scatter_rows for the FP8-weight path: bf16 x in, fp16 compact rows out."""
+    T, d = x.shape
+    k = ids.shape[1]
+    E = offsets.shape[0] - 1
+    _expect(x, torch.bfloat16, (T, d), "x")
+    _expect(ids, torch.int32, (T, k), "ids")
+    _expect(xs, torch.float16, (T * k, d), "xs")
+    _expect(row_of_route, torch.int32, (T * k,), "row_of_route")
+    _expect(route_of_row, torch.int32, (T * k,), "route_of_row")
+    _check("moe_scatter_rows_f16", load().moe_scatter_rows_f16(
+        _ptr(x), _ptr(ids), _ptr(mask), _ptr(offsets), T, k, d, E, _ptr(xs), _ptr(row_of_route),
+        _ptr(route_of_row), _ptr(ws), _stream(stream)))
+
+
 def moe_grouped_gate_up(xs, offsets, w_gate, w_up, h, stream=None):
     cap, d = xs.shape
     E, f, _ = w_gate.shape
@@ -268,6 +290,113 @@ def moe_forward(logits, x, mask, w_gate, w_up, w_down, k: int, bufs: MoEBuffers,
     b = bufs
     _check("moe_forward", load().moe_forward(
         _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, f, _ptr(w_gate), _ptr(w_up), _ptr(w_down), _dtype_code(x),
+        _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
+        _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
+    return b.out
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 expert weights (one fp32 scale per output channel)
+# ---------------------------------------------------------------------------
+
+class FP8Weights:
+    """One expert bank in FP8 E4M3: ``codes`` uint8 [E][rows][K], ``scales`` fp32 [E][rows]."""
+
+    def __init__(self, codes: torch.Tensor, scales: torch.Tensor):
+        if codes.dtype != torch.uint8 or scales.dtype != torch.float32 or codes.dim() != 3:
+            raise ValueError("expected uint8 codes [E][rows][K] and fp32 scales [E][rows]")
+        if tuple(scales.shape) != tuple(codes.shape[:2]):
+            raise ValueError(f"scales {tuple(scales.shape)} do not match codes {tuple(codes.shape)}")
+        self.codes, self.scales = codes, scales
+
+    @property
+    def shape(self):
+        return self.codes.shape
+
+
+def moe_quantize_weights_fp8(w, codes=None, scales=None, stream=None) -> FP8Weights:
+    """Quantize a bank [E][rows][K] (bf16 or fp32) to FP8 E4M3 codes and per-row scales."""
+    if w.dim() != 3:
+        raise ValueError("expected a weight bank [E][rows][K]")
+    E, rows, K = w.shape
+    if codes is None:
+        codes = torch.empty(E, rows, K, dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty(E, rows, dtype=torch.float32, device=w.device)
+    _expect(codes, torch.uint8, (E, rows, K), "codes")
+    _expect(scales, torch.float32, (E, rows), "scales")
+    _check("moe_quantize_weights_fp8", load().moe_quantize_weights_fp8(
+        _ptr(w), _dtype_code(w), E * rows, K, _ptr(codes), _ptr(scales), _stream(stream)))
+    return FP8Weights(codes, scales)
+
+
+def _expect_fp8(q, shape, name):
+    if not isinstance(q, FP8Weights):
+        raise ValueError(f"{name}: expected FP8Weights")
+    _expect(q.codes, torch.uint8, shape, name + ".codes")
+    _expect(q.scales, torch.float32, shape[:2], name + ".scales")
+
+
+def moe_grouped_gate_up_fp8(xs, offsets, q_gate: FP8Weights, q_up: FP8Weights, h, stream=None):
+    cap, d = xs.shape
+    E, f, _ = q_gate.shape
+    _expect(xs, torch.float16, (cap, d), "xs")
+    _expect_fp8(q_gate, (E, f, d), "q_gate")
+    _expect_fp8(q_up, (E, f, d), "q_up")
+    _expect(h, torch.float16, (cap, f), "h")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _check("moe_grouped_gate_up_fp8", load().moe_grouped_gate_up_fp8(
+        _ptr(xs), _ptr(offsets), cap, E, d, f, _ptr(q_gate.codes), _ptr(q_gate.scales), _ptr(q_up.codes),
+        _ptr(q_up.scales), _ptr(h), _stream(stream)))
+
+
+def moe_grouped_down_fp8(h, offsets, q_down: FP8Weights, y, stream=None):
+    cap, f = h.shape
+    E, d, _ = q_down.shape
+    _expect(h, torch.float16, (cap, f), "h")
+    _expect_fp8(q_down, (E, d, f), "q_down")
+    _expect(y, torch.float32, (cap, d), "y")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _check("moe_grouped_down_fp8", load().moe_grouped_down_fp8(
+        _ptr(h), _ptr(offsets), cap, E, d, f, _ptr(q_down.codes), _ptr(q_down.scales), _ptr(y), _stream(stream)))
+
+
+def moe_grouped_ffn_fp8(xs, offsets, q_gate: FP8Weights, q_up: FP8Weights, q_down: FP8Weights, h, y, stream=None):
+    cap, d = xs.shape
+    E, f, _ = q_gate.shape
+    _expect(xs, torch.float16, (cap, d), "xs")
+    _expect_fp8(q_gate, (E, f, d), "q_gate")
+    _expect_fp8(q_up, (E, f, d), "q_up")
+    _expect_fp8(q_down, (E, d, f), "q_down")
+    _expect(h, torch.float16, (cap, f), "h")
+    _expect(y, torch.float32, (cap, d), "y")
+    _check("moe_grouped_ffn_fp8", load().moe_grouped_ffn_fp8(
+        _ptr(xs), _ptr(offsets), cap, E, d, f, _ptr(q_gate.codes), _ptr(q_gate.scales), _ptr(q_up.codes),
+        _ptr(q_up.scales), _ptr(q_down.codes), _ptr(q_down.scales), _ptr(h), _ptr(y), _stream(stream)))
+
+
+def moe_forward_fp8(logits, x, mask, q_gate: FP8Weights, q_up: FP8Weights, q_down: FP8Weights, k: int,
+                    bufs: MoEBuffers, stream=None) -> torch.Tensor:
+    """The whole path with FP8 expert weights; returns ``bufs.out`` ([T][d] fp32).
+
+    x is bf16; ``bufs`` holds fp16 compact activations (``MoEBuffers(..., torch.float16)``).
+    """
+    T, E = logits.shape
+    d = x.shape[1]
+    f = q_gate.shape[1]
+    if (bufs.T, bufs.E, bufs.k, bufs.d, bufs.f, bufs.dtype) != (T, E, k, d, f, torch.float16):
+        raise ValueError("buffers were allocated for another shape (the FP8 path keeps xs and h in fp16)")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect_fp8(q_gate, (E, f, d), "q_gate")
+    _expect_fp8(q_up, (E, f, d), "q_up")
+    _expect_fp8(q_down, (E, d, f), "q_down")
+    b = bufs
+    _check("moe_forward_fp8", load().moe_forward_fp8(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, f, _ptr(q_gate.codes), _ptr(q_gate.scales),
+        _ptr(q_up.codes), _ptr(q_up.scales), _ptr(q_down.codes), _ptr(q_down.scales),
         _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
         _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
     return b.out

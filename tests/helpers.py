@@ -19,7 +19,7 @@ WEIGHT_REL = 1e-6
 def to_np(t) -> np.ndarray:
     if isinstance(t, torch.Tensor):
         t = t.detach().cpu()
-        if t.dtype == torch.bfloat16:
+        if t.dtype in (torch.bfloat16, torch.float16):
             t = t.float()
         return t.numpy()
     return np.asarray(t)
@@ -72,6 +72,22 @@ def assert_close_bf16_rounded(got, ref):
     return st
 
 
+def assert_close_f16_rounded(got, ref):
+    """An intermediate stored in fp16 (h of the FP8-weight path): each element
+    within its fp16 rounding bound, 2^-11 of its magnitude, plus 1e-3 * rms(ref)
+    for the fp32-versus-fp64 accumulation difference of elements near zero."""
+    g = to_np(got).astype(np.float64)
+    r = to_np(ref).astype(np.float64)
+    assert g.shape == r.shape
+    st = error_stats(g, r)
+    assert st["finite"], st
+    bound = 2.0 ** -11 * np.abs(r) + 1e-3 * st["rms_ref"]
+    worst = float(np.max(np.abs(g - r) - bound)) if g.size else -1.0
+    assert worst <= 0.0, (worst, st)
+    assert st["rel_fro"] <= BF16_REL_FRO, st
+    return st
+
+
 def oracle_weights(w_gate, w_up, w_down):
     """Oracle view of (possibly bf16, possibly CUDA) weight banks: fetch one expert at a time."""
     cache = {}
@@ -80,6 +96,25 @@ def oracle_weights(w_gate, w_up, w_down):
         if e not in cache:
             cache.clear()
             cache[e] = (to_np(w_gate[e]), to_np(w_up[e]), to_np(w_down[e]))
+        return cache[e]
+
+    return get
+
+
+def oracle_weights_fp8(w_gate, w_up, w_down):
+    """Oracle view of FP8 expert weights: the oracle quantizes each expert of
+    the (bf16 or fp32) banks itself and hands back the dequantized values."""
+    from oracle import moe_oracle as mo
+    cache = {}
+
+    def deq(w):
+        codes, scales = mo.quantize_weights_fp8(to_np(w).astype(np.float32))
+        return mo.dequantize_weights_fp8(codes, scales)
+
+    def get(e):
+        if e not in cache:
+            cache.clear()
+            cache[e] = (deq(w_gate[e]), deq(w_up[e]), deq(w_down[e]))
         return cache[e]
 
     return get

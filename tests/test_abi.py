@@ -35,6 +35,7 @@ def test_header_declares_the_path_entry_points():
     names = set(_declarations())
     for required in ("moe_route_topk", "moe_route_histogram", "moe_prefix_offsets", "moe_scatter_rows",
                      "moe_grouped_ffn", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_forward",
+                     "moe_quantize_weights_fp8", "moe_grouped_ffn_fp8", "moe_forward_fp8", "moe_scatter_rows_f16",
                      "moe_workspace_size", "moe_check_device_error"):
         assert required in names
 
@@ -55,6 +56,7 @@ def test_host_only_calls(lib):
     assert lib.moe_version() >= 100
     assert lib.moe_status_string(0) == b"ok"
     assert lib.moe_status_string(99) == b"unknown status"
+    assert lib.moe_status_string(5) == b"a value out of the fp16 operand range"
     n = ctypes.c_size_t(0)
     assert lib.moe_workspace_size(2048, 6, ctypes.byref(n)) == 0
     # header (32 words) + 6 chunks of 256 counts + 12288 ranks + 6 chunks of 256 bases, int32
@@ -67,6 +69,10 @@ def test_host_only_calls(lib):
     assert lib.moe_combine(None, None, None, 4, 2, 6, None, None) == 1  # d not a multiple of 4
     assert lib.moe_grouped_ffn(None, None, 8, 4, 100, 128, None, None, None, 1, None, None, None) == 1  # bf16 d % 128
     assert lib.moe_grouped_ffn(None, None, 8, 4, 128, 128, None, None, None, 7, None, None, None) == 2  # dtype
+    assert lib.moe_quantize_weights_fp8(None, 1, 4, 24, None, None, None) == 1      # K not a multiple of 16
+    assert lib.moe_quantize_weights_fp8(None, 9, 4, 32, None, None, None) == 2      # dtype
+    assert lib.moe_grouped_gate_up_fp8(None, None, 8, 4, 100, 128, None, None, None, None, None, None) == 1
+    assert lib.moe_scatter_rows_f16(None, None, None, None, 4, 17, 128, 8, None, None, None, None, None) == 1  # k
 
 
 def test_product_path_does_not_import_the_oracle():
