@@ -54,8 +54,13 @@
 namespace moe {
 namespace {
 
+// Compact rows per work item at most (MMA N): 64 leaves tensor memory for
+// six widened stages, 128 for four.
+#ifndef MOE_FP8_BN
+#define MOE_FP8_BN 128
+#endif
 constexpr int BM = 128;          // weight rows per tile (MMA M)
-constexpr int BN = 128;          // compact rows per work item at most (MMA N)
+constexpr int BN = MOE_FP8_BN;
 constexpr int BK = 64;           // K per stage
 constexpr int UMMA_K = 16;
 constexpr int kBoxRows = 16;
@@ -63,7 +68,7 @@ constexpr int kBigBoxRows = 64;
 // Converter warps: groups of 4 (one warp per tensor-memory lane quarter);
 // group g widens both weight tiles of the stages j with j % groups == g.
 #ifndef MOE_FP8_CONV_WARPS
-#define MOE_FP8_CONV_WARPS 8
+#define MOE_FP8_CONV_WARPS 4
 #endif
 constexpr int kConvWarps = MOE_FP8_CONV_WARPS;
 constexpr int kConvGroups = kConvWarps / 4;
@@ -76,8 +81,8 @@ constexpr int kQStages = 8;      // ring of code tiles (TMA -> converters)
 // (converters -> MMA) advance together: stage j of both is freed by one
 // tcgen05.commit (a commit costs the issuing thread about as much as two
 // MMAs at these N, so there is one per stage, not one per ring).
-constexpr int kBStages = 4;
-constexpr int kAStages = 4;
+constexpr int kAStages = (512 - 2 * BN) / 64;
+constexpr int kBStages = kAStages;
 static_assert(kBStages == kAStages, "one release barrier per stage of both rings");
 constexpr int kQTileBytes = BM * BK;          // 8 KB of codes per weight tile
 constexpr int kQStageBytes = 2 * kQTileBytes;
