@@ -81,6 +81,51 @@ def load() -> ctypes.CDLL:
     return _lib
 
 
+class _Recorder:
+    """Stands in for the library while `bind` marshals a call: records the C calls instead of making them."""
+
+    def __init__(self, lib):
+        self._real = lib
+        self.calls = []
+
+    def __getattr__(self, name):
+        real = getattr(self._real, name)
+
+        def record(*args):
+            self.calls.append((name, real, args))
+            return MOE_OK
+
+        return record
+
+
+def bind(fn, *args, **kwargs):
+    """Marshal one call of a binding function now and return a zero-argument
+    callable that makes the same C call(s) again (same pointers, sizes and
+    stream) without repeating the Python-side checks.  Meant for timed loops
+    of tiny batches, where the checks would cost more than the kernels.  The
+    callable keeps references to the arguments, so the tensors behind the
+    recorded pointers stay allocated as long as it lives."""
+    global _lib
+    lib = load()
+    rec = _Recorder(lib)
+    _lib = rec
+    try:
+        fn(*args, **kwargs)
+    finally:
+        _lib = lib
+    calls = rec.calls
+    keep = (args, kwargs)   # the recorded pointers stay valid while the callable lives
+
+    def run():
+        assert keep is not None
+        for name, f, a in calls:
+            status = f(*a)
+            if status != MOE_OK:
+                raise MoEError(name, status)
+
+    return run
+
+
 def _check(fn: str, status: int) -> None:
     if status != MOE_OK:
         raise MoEError(fn, status)
