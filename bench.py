@@ -33,6 +33,8 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
+# chunks up to this size take the fused A1-A4 launch (moe_route_scatter_small)
+SMALL_TOKENS, SMALL_ROUTES = 128, 512
 METRIC = "grouped MoE prefill tokens/s (T=401/2048/8192, E=256, top-6); % of roofline"
 UNIT = "tokens/s"
 
@@ -367,15 +369,23 @@ def run_ours(args, rank: int, world: int):
         gate_up_call, down_call, forward = M.moe_grouped_gate_up, M.moe_grouped_down, M.moe_forward
         scatter_call = M.moe_scatter_rows
 
-    names = ("topk", "histogram", "prefix", "scatter", "gate_up", "down", "combine")
-    GU = names.index("gate_up")
     b = bufs
-    # every call is marshalled once (M.bind); the timed loop replays the C calls
-    calls = [
-        M.bind(M.moe_route_topk, logits, k, b.ids, b.w),
-        M.bind(M.moe_route_histogram, b.ids, mask, E, b.counts, b.ws),
-        M.bind(M.moe_prefix_offsets, b.counts, T, k, b.offsets, b.ws),
-        M.bind(scatter_call, x, b.ids, mask, b.offsets, b.xs, b.row_of_route, b.route_of_row, b.ws),
+    # every call is marshalled once (M.bind); the timed loop replays the C calls.
+    # Small chunks take A1-A4 in one launch, as moe_forward does.
+    small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES
+    if small:
+        names = ("route_scatter_small", "gate_up", "down", "combine")
+        routing = [M.bind(M.moe_route_scatter_small, logits, x, mask, k, b)]
+    else:
+        names = ("topk", "histogram", "prefix", "scatter", "gate_up", "down", "combine")
+        routing = [
+            M.bind(M.moe_route_topk, logits, k, b.ids, b.w),
+            M.bind(M.moe_route_histogram, b.ids, mask, E, b.counts, b.ws),
+            M.bind(M.moe_prefix_offsets, b.counts, T, k, b.offsets, b.ws),
+            M.bind(scatter_call, x, b.ids, mask, b.offsets, b.xs, b.row_of_route, b.route_of_row, b.ws),
+        ]
+    GU = names.index("gate_up")
+    calls = routing + [
         M.bind(gate_up_call, b.xs, b.offsets, wg, wu, b.h),
         M.bind(down_call, b.h, b.offsets, wd, b.y),
         M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
@@ -436,6 +446,9 @@ def run_ours(args, rank: int, world: int):
     if rank != 0:
         return
 
+    # kernels per step: one per call; the fp32 SIMT FFN launches two kernels per projection
+    launches_per_step = len(calls) + (2 if dtype == torch.float32 else 0)
+
     # ---- roofline of the dominant kernel (grouped gate/up + SwiGLU)
     es = 2 if dtype == torch.bfloat16 else 4
     work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8)
@@ -478,7 +491,7 @@ def run_ours(args, rank: int, world: int):
                          "touched expert weights streamed per step (L2 129 MB), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "e2e": e2e,
-        "gpu_launches": args.steps * (7 if dtype == torch.bfloat16 else 9),
+        "gpu_launches": args.steps * launches_per_step,
         "roofline": roofline,
         "path_roofline": {"flops": flops, "bytes": path_bytes, "t_roof_ms": t_roof * 1e3,
                           "frac": t_roof * 1e3 / ms_per_step,

@@ -184,6 +184,24 @@ moe_status moe_scatter_rows(const void* x, int dtype, const int32_t* ids, const 
                             void* xs, int32_t* row_of_route, int32_t* route_of_row,
                             void* ws, void* stream);
 
+/* A1-A4 in one launch for small chunks -- the verification-width batches of
+ * the page "perf(ds4): accelerate ROCm decode and long-context selection"
+ * (q=4 verification) and any chunk with T <= 128 and T*k <= 512.  Every CTA
+ * recomputes the routing of the whole chunk (cheaper than three more
+ * launches at these sizes) and copies its share of the token rows.
+ * Outputs are those of moe_route_topk + moe_route_histogram +
+ * moe_prefix_offsets + moe_scatter_rows (or moe_scatter_rows_f16 when
+ * xs_f16 != 0, x bf16), bit for bit when E is a multiple of 4 (for other E
+ * the gate weights sum the softmax in slot order, which may differ from
+ * moe_route_topk in the last bit).  No workspace.
+ *   logits [T][E], x [T][d] (dtype), mask [T][k] or NULL: as above.
+ *   ids, w, counts, offsets, xs, row_of_route, route_of_row: out, as above.
+ * moe_forward and moe_forward_fp8 use this call for such chunks. */
+moe_status moe_route_scatter_small(const float* logits, const void* x, int dtype, int xs_f16,
+                                   const uint8_t* mask, int T, int E, int k, int d,
+                                   int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                   void* xs, int32_t* row_of_route, int32_t* route_of_row, void* stream);
+
 /* A5 -- grouped gate/up projection with SwiGLU.  Same page, Summary
  * (grouped gate/up MMID graphs instead of a serial graph per active expert);
  * the SwiGLU is the "DS4 SwiGLU split op" of the page "perf(ggml): reuse

@@ -156,12 +156,18 @@ extern "C" moe_status moe_forward(const float* logits, const void* x, const uint
     MOE_REQUIRE(aligned16(x) && aligned16(xs) && aligned16(h) && aligned16(y) && aligned16(out) &&
                 aligned16(ws) && aligned16(w_gate) && aligned16(w_up) && aligned16(w_down));
     const int cap = T * k;
-    if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
-    if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
-    if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
-    if ((st = moe_scatter_rows(x, dtype, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
-                               stream)) != MOE_OK)
-        return st;
+    if (T <= kSmallTokens && cap <= kSmallRoutes) {
+        if ((st = moe_route_scatter_small(logits, x, dtype, 0, mask, T, E, k, d, ids, w, counts, offsets, xs,
+                                          row_of_route, route_of_row, stream)) != MOE_OK)
+            return st;
+    } else {
+        if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
+        if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_scatter_rows(x, dtype, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
+                                   stream)) != MOE_OK)
+            return st;
+    }
     if ((st = moe_grouped_ffn(xs, offsets, cap, E, d, f, w_gate, w_up, w_down, dtype, h, y, stream)) != MOE_OK)
         return st;
     return moe_combine(y, row_of_route, w, T, k, d, out, stream);
@@ -235,12 +241,18 @@ extern "C" moe_status moe_forward_fp8(const float* logits, const void* x, const 
     MOE_REQUIRE(aligned16(x) && aligned16(xs) && aligned16(h) && aligned16(y) && aligned16(out) &&
                 aligned16(ws) && aligned16(w_gate_q) && aligned16(w_up_q) && aligned16(w_down_q));
     const int cap = T * k;
-    if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
-    if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
-    if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
-    if ((st = moe_scatter_rows_f16(x, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
-                                   stream)) != MOE_OK)
-        return st;
+    if (T <= kSmallTokens && cap <= kSmallRoutes) {
+        if ((st = moe_route_scatter_small(logits, x, MOE_BF16, 1, mask, T, E, k, d, ids, w, counts, offsets, xs,
+                                          row_of_route, route_of_row, stream)) != MOE_OK)
+            return st;
+    } else {
+        if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
+        if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_scatter_rows_f16(x, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
+                                       stream)) != MOE_OK)
+            return st;
+    }
     if ((st = moe_grouped_ffn_fp8(xs, offsets, cap, E, d, f, w_gate_q, s_gate, w_up_q, s_up, w_down_q, s_down, h, y,
                                   stream)) != MOE_OK)
         return st;

@@ -70,8 +70,9 @@ constexpr int kBigBoxRows = MOE_TC_BIG_BOX_ROWS;  // compact rows per large TMA 
 constexpr int kThreads = 192;
 
 // Shared memory: a 192 KB ring, carved per launch into 4 stages of 48 KB
-// (two 16 KB weight tiles + up to 128 rows) or, in big-item mode, 3 stages
-// of 64 KB (two weight tiles + up to 256 rows).  TMEM: 512 columns, region r
+// (two 16 KB weight tiles + up to 128 rows; narrow items: two k-blocks of one
+// weight tile + up to 64 rows each) or, in big-item mode, 3 stages of 64 KB
+// (two weight tiles + up to 256 rows).  TMEM: 512 columns, region r
 // (weight tile r) at columns 256r, each region in two 128-column slots; a
 // light item uses slot s of both regions (consecutive light items alternate
 // slots, so one item's epilogue overlaps the next item's MMAs), a big item
@@ -84,11 +85,14 @@ struct Cfg {
     static constexpr int kRingBytes = 4 * (kA * kATileBytes + BN * BK * 2);  // = 3 x 64 KB
     static constexpr int kTmemCols = 512;
     static constexpr int kCtrlBytes = 3072;  // barriers, TMEM slot, flags, item table (<= 2.3 KB)
-    // gate/up: a 32-row x 128-feature bf16 tile of h staged for row-contiguous stores
-    static constexpr int kOutStageBytes = GATED ? 32 * BM * 2 : 0;
+    // gate/up: a 32-row x 128-feature bf16 tile of h staged for row-contiguous
+    // stores, then (narrow items) the up half of a stacked tile, 64 features x 32
+    // rows of fp32 padded to 33 columns
+    static constexpr int kOutStageBytes = GATED ? 32 * BM * 2 + 64 * 33 * 4 : 0;
     static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kOutStageBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
     static_assert(kRingBytes == 3 * (kA * kATileBytes + 2 * BN * BK * 2), "both carve-ups fill the ring");
+    static_assert(kRingBytes / 4 >= kA * kATileBytes + 2 * 64 * BK * 2, "narrow carve-up: two k-blocks per stage");
 };
 
 // ---------------------------------------------------------------------------
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                   const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
                   const int32_t* __restrict__ offsets, int cap, int E,
-                  int K, int M, void* __restrict__ out, unsigned* err) {
+                  int K, int M, int narrow, void* __restrict__ out, unsigned* err) {
     using C = Cfg<GATED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
@@ -123,11 +127,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
     int* mode_big = const_cast<int*>(reinterpret_cast<volatile int*>(epi_flag + 2));   // launch-wide carve-up
     __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + C::kCtrlBytes);  // gate/up only
+    float* up_stage = reinterpret_cast<float*>(ctrl + C::kCtrlBytes + 32 * BM * 2);     // narrow gate/up only
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_kb = K / BK;
-    // feature tiles per expert: 128 features (gated) or 256 (down: two tiles)
-    const int n_mt = GATED ? M / BM : (M + 2 * BM - 1) / (2 * BM);
+    // Output features per work item.  Normal items: 128 (gate/up: a gate tile
+    // and an up tile, two MMAs) or 256 (down: two tiles).  Narrow items (small
+    // chunks, chosen on the host so that there are more items than waves of
+    // SMs): 64 for gate/up -- 64 gate rows stacked on 64 up rows in one 128-row
+    // A tile, one MMA -- or 128 for down (one tile).
+    const int fw = GATED ? (narrow ? BM / 2 : BM) : (narrow ? BM : 2 * BM);
+    const int n_mt = (M + fw - 1) / fw;
 
     // ---- prologue: barriers, TMEM, item table --------------------------------
     if (threadIdx.x == 0) {
@@ -170,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             rows += __shfl_xor_sync(0xffffffffu, rows, off);
             excess += __shfl_xor_sync(0xffffffffu, excess, off);
         }
-        const bool big = rows > 0 && excess * 100 >= static_cast<long long>(MOE_TC_BIG_MODE_PCT) * rows;
+        const bool big = !narrow && rows > 0 && excess * 100 >= static_cast<long long>(MOE_TC_BIG_MODE_PCT) * rows;
         if (lane == 0) *mode_big = big ? 1 : 0;
         for (int e = lane; e < E; e += 32) {
             const int n = offsets[e + 1] - offsets[e];
@@ -207,8 +217,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int n_items = item_off[E];
     const bool big = *mode_big != 0;
-    const int S = big ? 3 : 4;                                     // stages
-    const int stage_bytes = C::kRingBytes / S;                     // 64 KB or 48 KB
+    // stages: 3 x 64 KB (big items), else 4 x 48 KB.  A narrow stage holds two
+    // consecutive k-blocks (two 16 KB A tiles and their rows, at most 64), so
+    // that it carries as many weight bytes as a normal one.
+    const int S = big ? 3 : 4;
+    const int stage_bytes = C::kRingBytes / S;
+    const int kpb = narrow ? 2 : 1;          // k-blocks per stage
+    const int n_st = n_kb / kpb;             // stages per item (K is a multiple of 128)
     const int slice = big ? 2 * BN : BN;                           // rows per work item at most
 
     if (warp == 0) {
@@ -223,14 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const Item item = decode_item(it, item_off, ntiles, offsets, E, slice);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
-                const uint32_t bytes = C::kA * C::kATileBytes + n16 * kBoxRows * BK * 2;
+                const int row_bytes = n16 * kBoxRows * BK * 2;   // one k-block of the item's rows
+                const uint32_t bytes = C::kA * C::kATileBytes + kpb * row_bytes;
                 // w_down tiles past the expert's last feature (M not a multiple
                 // of 256) read the next expert's rows, or zero fill past the
                 // end of the bank; the epilogue stores none of their results
-                const int wy = item.e * M + item.mt * (GATED ? BM : 2 * BM);
+                const int wy = item.e * M + item.mt * fw;
                 const int wy1 = GATED ? wy : wy + BM;
                 const uint64_t pol_w = ntiles[item.e] > 1 ? pol_shared : pol_once;
-                for (int kb = 0; kb < n_kb; ++kb) {
+                for (int js = 0; js < n_st; ++js) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
                         ok = false;
                         break;
@@ -238,15 +254,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* st = smem + s * stage_bytes;
                     mbar_arrive_expect_tx(&full[s], bytes);
                     issued[s] = static_cast<int>(ph);
-                    tma_load_2d(st, &map_a0, &full[s], kb * BK, wy, pol_w);
-                    tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * BK, wy1, pol_w);
-                    uint8_t* bdst = st + C::kA * C::kATileBytes;
-                    // the rows in as few boxes as possible: 64-row boxes, then 16-row ones
-                    int r = 0;
-                    for (; r + kBigBoxRows <= n16 * kBoxRows; r += kBigBoxRows)
-                        tma_load_2d(bdst + r * 128, &map_b_big, &full[s], kb * BK, item.row0 + r, pol_x);
-                    for (; r < n16 * kBoxRows; r += kBoxRows)
-                        tma_load_2d(bdst + r * 128, &map_b, &full[s], kb * BK, item.row0 + r, pol_x);
+                    for (int hk = 0; hk < kpb; ++hk) {
+                        const int kb = js * kpb + hk;
+                        if (narrow) {
+                            // k-block hk: A tile at hk * 16 KB (gate/up: 64 gate rows, then 64 up rows)
+                            uint8_t* at = st + hk * C::kATileBytes;
+                            tma_load_2d(at, &map_a0, &full[s], kb * BK, wy, pol_w);
+                            if (GATED) tma_load_2d(at + C::kATileBytes / 2, &map_a1, &full[s], kb * BK, wy, pol_w);
+                        } else {
+                            tma_load_2d(st, &map_a0, &full[s], kb * BK, wy, pol_w);
+                            tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * BK, wy1, pol_w);
+                        }
+                        uint8_t* bdst = st + C::kA * C::kATileBytes + hk * row_bytes;
+                        // the rows in as few boxes as possible: 64-row boxes, then 16-row ones
+                        int r = 0;
+                        for (; r + kBigBoxRows <= n16 * kBoxRows; r += kBigBoxRows)
+                            tma_load_2d(bdst + r * 128, &map_b_big, &full[s], kb * BK, item.row0 + r, pol_x);
+                        for (; r < n16 * kBoxRows; r += kBoxRows)
+                            tma_load_2d(bdst + r * 128, &map_b, &full[s], kb * BK, item.row0 + r, pol_x);
+                    }
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -273,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (both && !mbar_wait(&acc_empty[1], (use1 & 1u) ^ 1u, abort_flag, err)) break;
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(slot * BN);
-                for (int kb = 0; kb < n_kb; ++kb) {
+                const int row_bytes = n16 * kBoxRows * BK * 2;
+                for (int js = 0; js < n_st; ++js) {
                     if (!mbar_wait(&full[s], ph, abort_flag, err)) {
                         ok = false;
                         break;
@@ -283,12 +310,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a0 = sdesc_lo(smem_u32(smem + s * stage_bytes));
                     const uint32_t a1 = a0 + (C::kATileBytes >> 4);
                     const uint32_t b = a0 + ((C::kA * C::kATileBytes) >> 4);
+                    if (narrow) {
+                        // two k-blocks, each one MMA per 16 K on its own A tile and rows
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-                        const uint64_t bd = sdesc_from_lo(b + 2 * kk);
-                        umma_bf16(d0, sdesc_from_lo(a0 + 2 * kk), bd, idesc, acc);
-                        umma_bf16(d0 + 2 * BN, sdesc_from_lo(a1 + 2 * kk), bd, idesc, acc);
+                        for (int hk = 0; hk < 2; ++hk) {
+                            const uint32_t ah = hk ? a1 : a0;
+                            const uint32_t bh = b + static_cast<uint32_t>((hk * row_bytes) >> 4);
+#pragma unroll
+                            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                                const uint32_t acc = (js | hk | kk) != 0 ? 1u : 0u;
+                                umma_bf16(d0, sdesc_from_lo(ah + 2 * kk), sdesc_from_lo(bh + 2 * kk), idesc, acc);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            const uint32_t acc = (js | kk) != 0 ? 1u : 0u;
+                            const uint64_t bd = sdesc_from_lo(b + 2 * kk);
+                            umma_bf16(d0, sdesc_from_lo(a0 + 2 * kk), bd, idesc, acc);
+                            umma_bf16(d0 + 2 * BN, sdesc_from_lo(a1 + 2 * kk), bd, idesc, acc);
+                        }
                     }
                     umma_commit(&empty[s]);
                     if (++s == S) {
@@ -340,17 +381,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // output feature of this lane: gated -> one 128-feature tile;
-            // down -> tile 0 at m, tile 1 at m + 128
-            const int m = item.mt * (GATED ? BM : 2 * BM) + q * 32 + lane;
+            // output feature of this lane: gated -> one 128-feature tile (narrow:
+            // lanes 0-63 gate, 64-127 up of a 64-feature tile); down -> tile 0 at
+            // m, tile 1 at m + 128
+            const int m = item.mt * fw + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(slot * BN);
             for (int c0 = 0; c0 < item.rows; c0 += 32) {
                 uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
-                tmem_ld32(taddr + 2 * BN + c0, g1);
+                if (!narrow) tmem_ld32(taddr + 2 * BN + c0, g1);
                 tmem_ld_wait();
-                if (GATED) {
+                if (GATED && narrow) {
+                    // the up half (warps of lane quarters 2, 3) goes through shared memory
+                    if (q >= 2) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) up_stage[((q - 2) * 32 + lane) * 33 + j] = __uint_as_float(g[j]);
+                    }
+                    epilogue_sync();
+                    if (q < 2) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float gv = __uint_as_float(g[j]);
+                            const float hv = gv / (1.f + expf(-gv)) * up_stage[(q * 32 + lane) * 33 + j];
+                            out_stage[j * (BM / 2) + q * 32 + lane] = __float2bfloat16_rn(hv);
+                        }
+                    }
+                    epilogue_sync();
+                    // each row's 64 features (128 bytes) leave as 8 x 16-byte stores
+                    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
+                    const int chunk = et & 7;
+#pragma unroll
+                    for (int pass = 0; pass < 2; ++pass) {
+                        const int j = pass * 16 + (et >> 3);
+                        const int n = c0 + j;
+                        if (n < item.rows) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(out_stage + j * (BM / 2) + chunk * 8);
+                            *reinterpret_cast<uint4*>(h + static_cast<size_t>(item.row0 + n) * M + item.mt * fw +
+                                                      chunk * 8) = v;
+                        }
+                    }
+                    epilogue_sync();
+                } else if (GATED) {
                     // SwiGLU into the staged tile: row j, feature q*32 + lane
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -375,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     epilogue_sync();
                 } else {
                     float* y = static_cast<float*>(out);
-                    const bool has1 = m + BM < M;
+                    const bool has1 = !narrow && m + BM < M;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int n = c0 + j;
@@ -474,18 +546,30 @@ moe_status set_smem_attr() {
 
 }  // namespace
 
+// Narrow items for chunks of at most 64 routes (no expert can have more than
+// 64 rows, so two k-blocks of rows fit a stage and the big-item carve-up
+// never applies) when even
+// an upper bound on the normal items -- min(E, cap) touched experts times
+// the feature tiles per expert -- stays under four waves of CTAs.
+bool use_narrow(int cap, int E, int tiles_per_expert, const DeviceInfo& di) {
+    const long long experts = E < cap ? E : cap;
+    return cap <= BN / 2 && experts * tiles_per_expert < 4LL * di.sm_count;
+}
+
 moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
                                  const void* w_gate, const void* w_up, void* h, cudaStream_t st,
                                  const DeviceInfo& di) {
     CUtensorMap ma0, ma1, mb, mbb;
     moe_status s;
-    if ((s = encode_2d(&ma0, w_gate, d, static_cast<long long>(E) * f, BM)) != MOE_OK) return s;
-    if ((s = encode_2d(&ma1, w_up, d, static_cast<long long>(E) * f, BM)) != MOE_OK) return s;
+    const bool narrow = use_narrow(cap, E, f / BM, di);
+    const int wbox = narrow ? BM / 2 : BM;
+    if ((s = encode_2d(&ma0, w_gate, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
+    if ((s = encode_2d(&ma1, w_up, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
     if ((s = encode_2d(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
     if ((s = encode_2d(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
     if ((s = set_smem_attr<true>()) != MOE_OK) return s;
     ffn_tc_kernel<true><<<di.sm_count, kThreads, Cfg<true>::kSmemBytes, st>>>(ma0, ma1, mb, mbb, offsets, cap, E, d,
-                                                                              f, h, di.error_word);
+                                                                              f, narrow ? 1 : 0, h, di.error_word);
     return cuda_status(cudaGetLastError());
 }
 
@@ -497,8 +581,9 @@ moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, in
     if ((s = encode_2d(&mb, h, f, cap, kBoxRows)) != MOE_OK) return s;
     if ((s = encode_2d(&mbb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
     if ((s = set_smem_attr<false>()) != MOE_OK) return s;
+    const bool narrow = use_narrow(cap, E, (d + 2 * BM - 1) / (2 * BM), di);
     ffn_tc_kernel<false><<<di.sm_count, kThreads, Cfg<false>::kSmemBytes, st>>>(ma0, ma0, mb, mbb, offsets, cap, E, f,
-                                                                                d, y, di.error_word);
+                                                                                d, narrow ? 1 : 0, y, di.error_word);
     return cuda_status(cudaGetLastError());
 }
 

@@ -19,6 +19,10 @@ enum : unsigned {
 constexpr int kHistChunk = 2048;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxK = 16;
+// Chunks with T*k <= kSmallRoutes and T <= kSmallTokens can take A1-A4 in one
+// launch (moe_route_scatter_small); moe_forward does so.
+constexpr int kSmallRoutes = 512;
+constexpr int kSmallTokens = 128;
 
 // Workspace layout (int32 words): [0] completion counter, [1..31] reserved,
 // then chunk_counts[n_chunks][256] (written by the histogram), local_rank[T*k]

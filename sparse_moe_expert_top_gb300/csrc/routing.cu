@@ -557,10 +557,12 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
 // fp32 FMAs starting from +0.0, masked slots are skipped.
 // ---------------------------------------------------------------------------
 
+// CTA (t, c) combines float4 columns [c * chunk4, (c + 1) * chunk4) of token
+// t (one chunk spanning the row unless the chunk is small).
 __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__ y,
                                                       const int32_t* __restrict__ row_of_route,
-                                                      const float* __restrict__ w, int k, int d4, int cap,
-                                                      float4* __restrict__ out, unsigned* err) {
+                                                      const float* __restrict__ w, int k, int d4, int chunk4,
+                                                      int cap, float4* __restrict__ out, unsigned* err) {
     __shared__ int rows[kMaxK];
     __shared__ float wt[kMaxK];
     const int t = blockIdx.x, tid = threadIdx.x;
@@ -575,7 +577,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
     }
     __syncthreads();
     float4* dst = out + static_cast<size_t>(t) * d4;
-    for (int v = tid; v < d4; v += blockDim.x) {
+    const int v_end = min(d4, static_cast<int>(blockIdx.y + 1) * chunk4);
+    for (int v = static_cast<int>(blockIdx.y) * chunk4 + tid; v < v_end; v += blockDim.x) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < k; ++s) {
             const int row = rows[s];
@@ -589,6 +592,160 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
         }
         dst[v] = acc;
     }
+}
+
+// ---------------------------------------------------------------------------
+// A1-A4 in one launch for small chunks (T*k <= kSmallRoutes, T <= kSmallTokens):
+// every CTA recomputes the routing of the whole chunk (a few tokens: cheaper
+// than a launch) and copies its share of the token rows; CTA 0 alone writes
+// ids, w, counts, offsets, row_of_route and route_of_row.  The results are
+// those of moe_route_topk (streaming form: slot-order softmax sum) +
+// moe_route_histogram + moe_prefix_offsets + moe_scatter_rows, bit for bit.
+// ---------------------------------------------------------------------------
+
+constexpr int kSmallThreads = 512;
+
+template <bool TO_F16>
+__global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
+    const float* __restrict__ logits, const uint4* __restrict__ x, const uint8_t* __restrict__ mask, int T, int E,
+    int k, int row_vecs, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, uint4* __restrict__ xs, int32_t* __restrict__ row_of_route,
+    int32_t* __restrict__ route_of_row, unsigned* err) {
+    __shared__ int s_e[kSmallRoutes];     // expert of route r, -1 when masked
+    __shared__ int s_row[kSmallRoutes];   // rank, then compact row (-1 masked)
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarps = kSmallThreads / 32;
+    const int n_routes = T * k;
+    const bool writer = blockIdx.x == 0;
+    for (int e = tid; e < kMaxExperts; e += kSmallThreads) s_cnt[e] = 0;
+
+    // A1: warp per token, k rounds of a warp arg-max over order keys
+    for (int t = warp; t < T; t += kWarps) {
+        const float* row = logits + static_cast<size_t>(t) * E;
+        unsigned long long key[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane + 32 * j;
+            key[j] = (e < E) ? topk_key(__ldg(row + e), e) : 0ull;
+        }
+        float sel_val = 0.f;
+        int sel_id = 0;
+        for (int sl = 0; sl < k; ++sl) {
+            unsigned long long best = key[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) best = key[j] > best ? key[j] : best;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const unsigned long long o = __shfl_xor_sync(kFull, best, off);
+                best = o > best ? o : best;
+            }
+            const int e = 0xFFFF - static_cast<int>(best & 0xFFFFu);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (lane + 32 * j == e) key[j] = 0ull;
+            if (lane == sl) {
+                sel_val = key_value(best);
+                sel_id = e;
+            }
+        }
+        // softmax over the k selected logits, summed in slot order
+        const float top = __shfl_sync(kFull, sel_val, 0);
+        float sum = 0.f;
+        for (int r = 0; r < k; ++r) sum += expf(__shfl_sync(kFull, sel_val, r) - top);
+        const float inv = 1.f / sum;
+        if (lane < k) {
+            const int r = t * k + lane;
+            const bool masked = mask != nullptr && __ldg(mask + r) != 0;
+            s_e[r] = masked ? -1 : sel_id;
+            if (writer) {
+                ids[r] = sel_id;
+                w[r] = expf(sel_val - top) * inv;
+            }
+        }
+    }
+    __syncthreads();
+
+    // A2: stable ranks in route order (one warp, 32 routes at a time)
+    if (warp == 0) {
+        const unsigned lt_mask = (1u << lane) - 1u;
+        for (int base = 0; base < n_routes; base += 32) {
+            const int r = base + lane;
+            const int e = r < n_routes ? s_e[r] : -1;
+            const unsigned peers = __match_any_sync(kFull, e);
+            const int rank = e >= 0 ? s_cnt[e] + __popc(peers & lt_mask) : -1;
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(peers) - 1) s_cnt[e] += __popc(peers);
+            __syncwarp();
+            if (r < n_routes) s_row[r] = rank;
+        }
+        // A3: exclusive prefix over the experts (8 consecutive experts per lane)
+        int c[8], local = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            c[i] = e < E ? s_cnt[e] : 0;
+            local += c[i];
+        }
+        int incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - local;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            if (e < E) s_off[e] = run;
+            run += c[i];
+        }
+        if (lane == 31) s_off[E] = incl;
+    }
+    __syncthreads();
+    const int R = s_off[E];
+    for (int r = tid; r < n_routes; r += kSmallThreads) {
+        const int e = s_e[r], rank = s_row[r];
+        const int row = e >= 0 ? s_off[e] + rank : -1;
+        s_row[r] = row;
+        if (writer) {
+            row_of_route[r] = row;
+            if (row >= 0) route_of_row[row] = r;
+        }
+    }
+    if (writer) {
+        for (int e = tid; e < E; e += kSmallThreads) {
+            counts[e] = s_cnt[e];
+            offsets[e] = s_off[e];
+        }
+        if (tid == 0) offsets[E] = R;
+        for (int j = R + tid; j < n_routes; j += kSmallThreads) route_of_row[j] = -1;
+    }
+    __syncthreads();
+
+    // A4: this CTA's share of the compact rows, and of the zero-filled tail
+    bool range = false;
+    for (int r = blockIdx.x; r < n_routes; r += gridDim.x) {
+        const int row = s_row[r];
+        if (row < 0) continue;
+        const uint4* src = x + static_cast<size_t>(r / k) * row_vecs;
+        uint4* dst = xs + static_cast<size_t>(row) * row_vecs;
+        for (int v = tid; v < row_vecs; v += kSmallThreads) {
+            uint4 val = __ldg(src + v);
+            if (TO_F16) {
+                val.x = bf16x2_to_f16x2(val.x, range);
+                val.y = bf16x2_to_f16x2(val.y, range);
+                val.z = bf16x2_to_f16x2(val.z, range);
+                val.w = bf16x2_to_f16x2(val.w, range);
+            }
+            dst[v] = val;
+        }
+    }
+    for (int j = R + static_cast<int>(blockIdx.x); j < n_routes; j += gridDim.x)
+        for (int v = tid; v < row_vecs; v += kSmallThreads)
+            xs[static_cast<size_t>(j) * row_vecs + v] = make_uint4(0u, 0u, 0u, 0u);
+    if (TO_F16 && __syncthreads_or(range) && tid == 0) atomicOr(err, DEVERR_RANGE);
 }
 
 moe_status launch_status() { return cuda_status(cudaGetLastError()); }
@@ -741,6 +898,31 @@ extern "C" moe_status moe_scatter_rows_f16(const void* x, const int32_t* ids, co
     return scatter_rows(x, 2, true, ids, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws, stream);
 }
 
+extern "C" moe_status moe_route_scatter_small(const float* logits, const void* x, int dtype, int xs_f16,
+                                              const uint8_t* mask, int T, int E, int k, int d, int32_t* ids,
+                                              float* w, int32_t* counts, int32_t* offsets, void* xs,
+                                              int32_t* row_of_route, int32_t* route_of_row, void* stream) {
+    const int es = dtype_size(dtype);
+    if (es == 0) return MOE_ERR_UNSUPPORTED;
+    MOE_REQUIRE(T >= 0 && T <= kSmallTokens && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E &&
+                T * k <= kSmallRoutes && d >= 1);
+    MOE_REQUIRE(!xs_f16 || dtype == MOE_BF16);
+    MOE_REQUIRE((static_cast<size_t>(d) * es) % 16 == 0);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && ids && w && counts && offsets && xs && row_of_route && route_of_row);
+    MOE_REQUIRE(aligned16(x) && aligned16(xs));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    const int row_vecs = static_cast<int>(static_cast<size_t>(d) * es / 16);
+    const int grid = T * k < 2 * di.sm_count ? T * k : 2 * di.sm_count;
+    auto kernel = xs_f16 ? route_scatter_small_kernel<true> : route_scatter_small_kernel<false>;
+    kernel<<<grid, kSmallThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        logits, static_cast<const uint4*>(x), mask, T, E, k, row_vecs, ids, w, counts, offsets,
+        static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word);
+    return launch_status();
+}
+
 extern "C" moe_status moe_combine(const float* y, const int32_t* row_of_route, const float* w, int T, int k, int d,
                                   float* out, void* stream) {
     MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && d >= 1 && d % 4 == 0);
@@ -749,8 +931,12 @@ extern "C" moe_status moe_combine(const float* y, const int32_t* row_of_route, c
     DeviceInfo di;
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
-    combine_kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const float4*>(y), row_of_route, w, k, d / 4, T * k, reinterpret_cast<float4*>(out),
+    // a small chunk splits every row over CTAs of 128 float4 columns so that all SMs take part
+    const int d4 = d / 4;
+    const int chunk4 = T < 2 * di.sm_count ? 128 : d4;
+    const dim3 grid(T, (d4 + chunk4 - 1) / chunk4);
+    combine_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const float4*>(y), row_of_route, w, k, d4, chunk4, T * k, reinterpret_cast<float4*>(out),
         di.error_word);
     return launch_status();
 }

@@ -38,6 +38,7 @@ SIGNATURES = {
     "moe_prefix_offsets": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_scatter_rows": ([_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_scatter_rows_f16": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "moe_route_scatter_small": ([_P, _P, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gate_up": ([_P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P], _I),
     "moe_grouped_down": ([_P, _P, _I, _I, _I, _I, _P, _I, _P, _P], _I),
     "moe_grouped_ffn": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P], _I),
@@ -249,6 +250,25 @@ def moe_scatter_rows_f16(x, ids, mask, offsets, xs, row_of_route, route_of_row, 
     _check("moe_scatter_rows_f16", load().moe_scatter_rows_f16(
         _ptr(x), _ptr(ids), _ptr(mask), _ptr(offsets), T, k, d, E, _ptr(xs), _ptr(row_of_route),
         _ptr(route_of_row), _ptr(ws), _stream(stream)))
+
+
+def moe_route_scatter_small(logits, x, mask, k, bufs, stream=None):
+    """A1-A4 in one launch for a small chunk (T <= 128, T*k <= 512) into ``bufs``.
+
+    ``bufs.xs`` is fp16 (FP8-weight path, x bf16) or of x's type."""
+    T, E = logits.shape
+    d = x.shape[1]
+    b = bufs
+    _expect(logits, torch.float32, (T, E), "logits")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    xs_f16 = b.xs.dtype == torch.float16 and x.dtype == torch.bfloat16
+    if not xs_f16:
+        _expect(b.xs, x.dtype, (T * k, d), "xs")
+    _check("moe_route_scatter_small", load().moe_route_scatter_small(
+        _ptr(logits), _ptr(x), _dtype_code(x), 1 if xs_f16 else 0, _ptr(mask), T, E, k, d, _ptr(b.ids), _ptr(b.w),
+        _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route), _ptr(b.route_of_row),
+        _stream(stream)))
 
 
 def moe_grouped_gate_up(xs, offsets, w_gate, w_up, h, stream=None):

@@ -43,6 +43,10 @@ FFN_CASES = [
     (16, 512, 256, 600, 4, 0.1, torch.bfloat16),
     (1, 128, 256, 200, 1, 0.0, torch.bfloat16),
     (3, 384, 256, 150, 2, 0.0, torch.bfloat16),   # d = 384: the down projection's last feature pair is half a pair
+    # T*k <= 128: narrow work items (64-feature gate/up items, single-tile down items)
+    (16, 512, 384, 20, 4, 0.1, torch.bfloat16),
+    (3, 384, 256, 30, 2, 0.0, torch.bfloat16),    # d = 384: three single-tile down items per expert
+    (256, 256, 256, 4, 6, 0.0, torch.bfloat16),   # a 4-token verification batch
     (8, 64, 128, 32, 2, 0.0, torch.float32),
     (5, 96, 160, 50, 3, 0.3, torch.float32),
 ]

@@ -79,6 +79,7 @@ FP8_CASES = [
     (1, 128, 256, 200, 1, 0.0),
     (3, 384, 256, 150, 2, 0.0),    # d = 384: the down projection's last 256-feature item is half full
     (2, 128, 256, 700, 1, 0.0),    # one heavy expert: several 128-row slices
+    (256, 256, 256, 4, 6, 0.0),    # a 4-token verification batch
 ]
 
 

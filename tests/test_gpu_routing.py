@@ -242,3 +242,65 @@ def test_topk_streaming_and_warp_kernels_agree(k):
     assert np.array_equal(to_np(ids_b), ref_ids)
     np.testing.assert_allclose(to_np(w_a), ref_w, rtol=WEIGHT_REL, atol=0)
     np.testing.assert_allclose(to_np(w_b), ref_w, rtol=WEIGHT_REL, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# A1-A4 in one launch for small chunks: the same outputs as the four steps
+# ---------------------------------------------------------------------------
+
+class _Bufs:
+    def __init__(self, T, E, k, d, xs_dtype):
+        cap, dev = T * k, "cuda"
+        self.ids = torch.full((T, k), -7, dtype=torch.int32, device=dev)
+        self.w = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev)
+        self.counts = torch.full((E,), -5, dtype=torch.int32, device=dev)
+        self.offsets = torch.full((E + 1,), -5, dtype=torch.int32, device=dev)
+        self.xs = torch.full((cap, d), float("nan"), dtype=xs_dtype, device=dev)
+        self.row_of_route = torch.full((cap,), -9, dtype=torch.int32, device=dev)
+        self.route_of_row = torch.full((cap,), -9, dtype=torch.int32, device=dev)
+
+
+@pytest.mark.parametrize("T,E,k,p,d,dtype,xs_f16", [
+    (1, 256, 6, 0.0, 4096, torch.bfloat16, False),
+    (4, 256, 6, 0.0, 4096, torch.bfloat16, False),
+    (4, 256, 6, 0.0, 4096, torch.bfloat16, True),
+    (7, 64, 4, 0.3, 128, torch.float32, False),
+    (85, 256, 6, 0.2, 256, torch.bfloat16, False),
+    (128, 256, 4, 0.0, 128, torch.bfloat16, True),   # T*k = 512, the largest small chunk
+    (128, 8, 2, 0.5, 64, torch.float32, False),      # heavy experts, half the routes masked
+    (33, 60, 3, 0.1, 64, torch.bfloat16, False),     # E not a multiple of 4
+    (16, 4, 4, 1.0, 64, torch.bfloat16, False),      # every route masked
+])
+def test_small_chunk_routing_equals_the_four_steps(T, E, k, p, d, dtype, xs_f16):
+    logits, mask = _routing_case(T, E, k, p, seed=3 * T + E, skew=1.0)
+    if p == 1.0:
+        mask = torch.ones(T, k, dtype=torch.uint8)
+    x = torch.randn(T, d).to(dtype)
+    ref = _run_index_path(logits, mask, k, x)
+    b = _Bufs(T, E, k, d, torch.float16 if xs_f16 else dtype)
+    M.moe_route_scatter_small(logits.cuda(), x.cuda(), None if mask is None else mask.cuda(), k, b)
+    M.moe_check_device_error()
+    for name in ("ids", "counts", "offsets", "row_of_route", "route_of_row"):
+        assert torch.equal(getattr(b, name), ref[name]), name
+    if E % 4 == 0:
+        assert torch.equal(b.w, ref["w"])
+    else:
+        torch.testing.assert_close(b.w, ref["w"], rtol=WEIGHT_REL, atol=0)
+    want = ref["xs"].to(torch.float16) if xs_f16 else ref["xs"]
+    bits = torch.int16 if want.element_size() == 2 else torch.int32
+    assert torch.equal(b.xs.view(bits), want.view(bits))
+    # and against the oracle's definition
+    oref = mo.moe_forward(logits.numpy(), to_np(x), (np.zeros((E, 1, d)), np.zeros((E, 1, d)), np.zeros((E, d, 1))),
+                          k, None if mask is None else mask.numpy())
+    assert np.array_equal(to_np(b.ids), oref["ids"])
+    assert np.array_equal(to_np(b.route_of_row), oref["route_of_row"])
+    np.testing.assert_allclose(to_np(b.w), oref["w"], rtol=WEIGHT_REL, atol=0)
+
+
+def test_small_chunk_routing_rejects_large_chunks():
+    T, E, k, d = 129, 8, 2, 64
+    logits, _ = _routing_case(T, E, k, 0.0, seed=1)
+    x = torch.randn(T, d)
+    b = _Bufs(T, E, k, d, torch.float32)
+    with pytest.raises(M.MoEError):
+        M.moe_route_scatter_small(logits.cuda(), x.cuda(), None, k, b)
