@@ -49,7 +49,9 @@ permutation invariants, the E=1/k=1 reduction to a dense SwiGLU FFN, the k=E
 reduction to a full softmax mixture, and the all-masked exact +0.0 case.
 The FP8 E4M3 weight quantization at the end of the module is pinned against
 PyTorch's float8_e4m3fn cast (an independent implementation of the format),
-the format's bit layout and hand-worked ties.  No function here is unpinned.
+the format's bit layout and hand-worked ties.  The router projection is
+pinned by a hand-worked case, one-hot router rows and linearity/permutation
+properties.  No function here is unpinned.
 """
 
 from __future__ import annotations
@@ -373,3 +375,25 @@ def quantize_weights_fp8(w):
 
 def dequantize_weights_fp8(codes, scales):
     return np.asarray(scales, dtype=np.float64)[..., None] * e4m3_decode(codes)
+
+
+# ---------------------------------------------------------------------------
+# The router projection in front of A1
+# ---------------------------------------------------------------------------
+#
+# The pages route every token to its top-6 of 256 routed experts from router
+# logits (page "perf(ds4): extend sparse prefill scheduling to 10K", Summary:
+# native top-6 routing); the logits are the token row times the router
+# matrix.  Here the router matrix is stored like the expert weights,
+# K-contiguous: wr [E][d], logits[t][e] = sum_j x[t][j] * wr[e][j].
+
+def router_logits(x, wr):
+    """Router logits [T][E] = x [T][d] . wr[E][d]^T, in float64."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(wr, dtype=np.float64).T
+
+
+def route_from_router(x, wr, k: int):
+    """Logits, ids and gate weights of the router step followed by A1."""
+    logits = router_logits(x, wr)
+    ids, w = route_topk(logits, k)
+    return logits, ids, w
