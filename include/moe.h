@@ -108,6 +108,19 @@ moe_status moe_selftest_bounded_wait(int limit_ms, void* stream);
  * workspace serves one stream at a time.  T >= 0, 1 <= k <= 16. */
 moe_status moe_workspace_size(int T, int k, size_t* bytes);
 
+/* The router projection in front of A1, with A1 in its epilogue.  Page
+ * "perf(ds4): extend sparse prefill scheduling to 10K", Summary (native
+ * top-6 routing over the routed experts, from the router logits).
+ *   x      [T][d] bf16 token rows; d a multiple of 64.
+ *   wr     [E][d] bf16 router matrix (K-contiguous, like the expert weights).
+ *   logits [T][E] fp32 out, or NULL: logits[t][e] = x[t] . wr[e], bf16
+ *          products accumulated in fp32 on the tensor cores.
+ *   ids, w [T][k] out: as moe_route_topk applied to those logits (the k
+ *          largest in descending order, ties to the lower expert id; softmax
+ *          over the k selected, summed in slot order). */
+moe_status moe_router_topk(const void* x, const void* wr, int T, int E, int d, int k,
+                           float* logits, int32_t* ids, float* w, void* stream);
+
 /* A1 -- top-k routing.  Page "perf(ds4): batch heterogeneous MoE prefill by
  * expert", Summary (routed experts, up to 256) and page "perf(ds4): extend
  * sparse prefill scheduling to 10K", Summary (native top-6 routing).

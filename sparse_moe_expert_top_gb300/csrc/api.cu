@@ -258,3 +258,18 @@ extern "C" moe_status moe_forward_fp8(const float* logits, const void* x, const 
         return st;
     return moe_combine(y, row_of_route, w, T, k, d, out, stream);
 }
+
+// ---------------------------------------------------------------------------
+// Router projection + top-k
+// ---------------------------------------------------------------------------
+
+extern "C" moe_status moe_router_topk(const void* x, const void* wr, int T, int E, int d, int k, float* logits,
+                                      int32_t* ids, float* w, void* stream) {
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 64 && d % 64 == 0);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(x && wr && ids && w && aligned16(x) && aligned16(wr));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_router_topk(x, wr, T, E, d, k, logits, ids, w, static_cast<cudaStream_t>(stream), di);
+}

@@ -38,6 +38,25 @@ inline size_t ws_words(int T, int k) {
     return ws_bases_offset(T, k) + static_cast<size_t>(ws_chunks(T, k)) * kMaxExperts;
 }
 
+#ifdef __CUDACC__
+// Order-preserving 64-bit top-k key: high word = the logit's bits mapped so
+// that unsigned order equals float order (with -0.0 folded onto +0.0), low
+// word = 0xFFFF - expert so that equal logits rank the lower expert first.
+// Key 0 is below every real key and marks "taken" or "no expert".
+__device__ __forceinline__ unsigned long long topk_order_key(float v, int e) {
+    unsigned u = __float_as_uint(v);
+    if ((u << 1) == 0u) u = 0u;
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<unsigned long long>(u) << 32) | static_cast<unsigned>(0xFFFF - e);
+}
+
+__device__ __forceinline__ float topk_key_value(unsigned long long key) {
+    unsigned u = static_cast<unsigned>(key >> 32);
+    u = (u & 0x80000000u) ? (u & 0x7fffffffu) : ~u;
+    return __uint_as_float(u);
+}
+#endif
+
 struct DeviceInfo {
     int sm_count;
     int cc_major, cc_minor;
@@ -73,6 +92,8 @@ moe_status launch_ffn_fp8_gate_up(const void* xs, const int32_t* offsets, int ca
 moe_status launch_ffn_fp8_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
                                const uint8_t* q_down, const float* s_down, float* y, cudaStream_t st,
                                const DeviceInfo& di);
+moe_status launch_router_topk(const void* x, const void* wr, int T, int E, int d, int k, float* logits,
+                              int32_t* ids, float* w, cudaStream_t st, const DeviceInfo& di);
 moe_status launch_quantize_fp8(const void* w, int dtype, long long rows, int K, uint8_t* codes, float* scales,
                                cudaStream_t st, const DeviceInfo& di);
 

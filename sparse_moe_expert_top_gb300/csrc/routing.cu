@@ -26,22 +26,6 @@ constexpr unsigned kFull = 0xffffffffu;
 // A1: top-k routing, one warp per token.
 // ---------------------------------------------------------------------------
 
-// Order-preserving 64-bit key: high word = the logit's bits mapped so that
-// unsigned order equals float order (with -0.0 folded onto +0.0), low word =
-// 0xFFFF - expert so that equal logits rank the lower expert first.  Key 0 is
-// below every real key and marks "taken" or "no expert".
-__device__ __forceinline__ unsigned long long topk_key(float v, int e) {
-    unsigned u = __float_as_uint(v);
-    if ((u << 1) == 0u) u = 0u;
-    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return (static_cast<unsigned long long>(u) << 32) | static_cast<unsigned>(0xFFFF - e);
-}
-
-__device__ __forceinline__ float key_value(unsigned long long key) {
-    unsigned u = static_cast<unsigned>(key >> 32);
-    u = (u & 0x80000000u) ? (u & 0x7fffffffu) : ~u;
-    return __uint_as_float(u);
-}
 
 template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
@@ -55,7 +39,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
         const int e = lane + 32 * j;
-        key[j] = (e < E) ? topk_key(__ldg(row + e), e) : 0ull;
+        key[j] = (e < E) ? topk_order_key(__ldg(row + e), e) : 0ull;
     }
 
     float sel_val = 0.f;
@@ -74,7 +58,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
         for (int j = 0; j < EPL; ++j)
             if (lane + 32 * j == e) key[j] = 0ull;
         if (lane == s) {
-            sel_val = key_value(best);
+            sel_val = topk_key_value(best);
             sel_id = e;
         }
     }
@@ -628,7 +612,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int e = lane + 32 * j;
-            key[j] = (e < E) ? topk_key(__ldg(row + e), e) : 0ull;
+            key[j] = (e < E) ? topk_order_key(__ldg(row + e), e) : 0ull;
         }
         float sel_val = 0.f;
         int sel_id = 0;
@@ -646,7 +630,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
             for (int j = 0; j < 8; ++j)
                 if (lane + 32 * j == e) key[j] = 0ull;
             if (lane == sl) {
-                sel_val = key_value(best);
+                sel_val = topk_key_value(best);
                 sel_id = e;
             }
         }

@@ -33,6 +33,7 @@ SIGNATURES = {
     "moe_selftest_bounded_wait": ([_I, _P], _I),
     "moe_workspace_size": ([_I, _I, _SZ], _I),
     "moe_route_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_router_topk": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_route_histogram": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
     "moe_route_histogram_noalloc": ([_P, _P, _I, _I, _I, _P, _P], _I),
     "moe_prefix_offsets": ([_P, _I, _I, _I, _P, _P, _P], _I),
@@ -189,6 +190,20 @@ def moe_route_topk(logits, k, ids, w, stream=None):
     _expect(ids, torch.int32, (T, k), "ids")
     _expect(w, torch.float32, (T, k), "w")
     _check("moe_route_topk", load().moe_route_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(w), _stream(stream)))
+
+
+def moe_router_topk(x, wr, k, ids, w, logits=None, stream=None):
+    """Router logits x . wr^T (bf16, fp32 accumulation) and their top-k routing; logits optional."""
+    T, d = x.shape
+    E = wr.shape[0]
+    _expect(x, torch.bfloat16, (T, d), "x")
+    _expect(wr, torch.bfloat16, (E, d), "wr")
+    _expect(ids, torch.int32, (T, k), "ids")
+    _expect(w, torch.float32, (T, k), "w")
+    if logits is not None:
+        _expect(logits, torch.float32, (T, E), "logits")
+    _check("moe_router_topk", load().moe_router_topk(_ptr(x), _ptr(wr), T, E, d, k, _ptr(logits), _ptr(ids), _ptr(w),
+                                                     _stream(stream)))
 
 
 def moe_route_histogram(ids, mask, E, counts, ws, stream=None):
