@@ -402,8 +402,21 @@ def run_ours(args, rank: int, world: int):
     b = bufs
     # every call is marshalled once (M.bind); the timed loop replays the C calls.
     # Small chunks take A1-A4 in one launch, as moe_forward does.
-    small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES
-    if small:
+    small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES and not args.router
+    if args.router:
+        # the router projection on the tensor cores replaces the given logits
+        if dtype != torch.bfloat16:
+            raise SystemExit("--router needs a bf16 workload")
+        from workloads.synthetic import make_router_matrix
+        wr = make_router_matrix(cfg, dev)
+        names = ("router_topk", "histogram", "prefix", "scatter", "gate_up", "down", "combine")
+        routing = [
+            M.bind(M.moe_router_topk, x, wr, k, b.ids, b.w),
+            M.bind(M.moe_route_histogram, b.ids, mask, E, b.counts, b.ws),
+            M.bind(M.moe_prefix_offsets, b.counts, T, k, b.offsets, b.ws),
+            M.bind(scatter_call, x, b.ids, mask, b.offsets, b.xs, b.row_of_route, b.route_of_row, b.ws),
+        ]
+    elif small:
         names = ("route_scatter_small", "gate_up", "down", "combine")
         routing = [M.bind(M.moe_route_scatter_small, logits, x, mask, k, b)]
     else:
@@ -470,8 +483,9 @@ def run_ours(args, rank: int, world: int):
     per_kernel = {n: statistics.mean(evk[s][i][0].elapsed_time(evk[s][i][1]) for s in range(n_bd))
                   for i, n in enumerate(names)}
 
-    e2e = None if args.no_e2e else _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k, bufs, T, d,
-                                            forward)
+    # the end-to-end leg runs moe_forward, which takes the logits as input: not with --router
+    e2e = None if (args.no_e2e or args.router) else _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k,
+                                                             bufs, T, d, forward)
 
     if rank != 0:
         return
@@ -496,13 +510,16 @@ def run_ours(args, rank: int, world: int):
     # whole-path roofline: the slower of FLOPs at the dense bf16 tensor peak
     # and the path's algorithmic bytes at HBM bandwidth
     flops, path_bytes = work["flops"], work["path_bytes"]
+    if args.router:
+        flops += 2.0 * T * E * d
+        path_bytes += T * d * 2 + E * d * 2 - T * E * 4   # x and wr read instead of the logits
     t_roof = max(flops / (peaks["bf16_tflops_sustained"] * 1e12), path_bytes / (peaks["hbm_gbs"] * 1e9))
     ms_per_step = elapsed_ms / args.steps
     value = world * T * args.steps / (elapsed_ms * 1e-3)
 
     # ---- CPU baseline: the oracle on the host cores, bounded sample
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not args.router:
         n, _ = _size_oracle_sample(inp, args.cpu_budget_s)
         secs = _time_oracle(inp, n)
         cpu = {"value": n / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
@@ -517,6 +534,8 @@ def run_ours(args, rank: int, world: int):
                    "routes_unmasked": R, "experts_touched": touched,
                    "weights": "fp8_e4m3 codes + fp32 per-channel scales" if fp8 else
                               ("bf16" if dtype == torch.bfloat16 else "f32"),
+                   "router": "x . Wr^T on the tensor cores (moe_router_topk, Wr ~ N(0, 1/d) bf16) in front of "
+                             "the histogram; the workload's own logits unused" if args.router else None,
                    "l2": f"inputs larger than L2: {touched * 3 * d * f * (1 if fp8 else es) / 1e9:.1f} GB of "
                          "touched expert weights streamed per step (L2 129 MB), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -622,6 +641,8 @@ def main():
     ap.add_argument("--weights", choices=("bf16", "fp8"), default="bf16",
                     help="expert weight format: the workload's own (bf16), or FP8 E4M3 codes with per-channel "
                          "scales quantized at load time")
+    ap.add_argument("--router", action="store_true",
+                    help="compute the router projection x . Wr^T on the GPU in front of the path (moe_router_topk)")
     ap.add_argument("--routing-sweep", action="store_true",
                     help="time the routing-side kernels over a T-sweep instead (JSON line per T)")
     args = ap.parse_args()

@@ -51,6 +51,7 @@ _TAG_MASK = 6
 _TAG_BIAS = 7
 _TAG_PERM = 8
 _TAG_ROUTER = 9
+_TAG_ROUTER_ROWS = 10
 
 
 @dataclasses.dataclass(frozen=True)
@@ -164,6 +165,14 @@ def make_weights(cfg: MoEConfig, device="cpu", chunk: int = 8):
     wu = _randn_scaled((E, f, d), 1.0 / math.sqrt(d), dt, _gen(cfg.seed, _TAG_UP, device), device, chunk)
     wd = _randn_scaled((E, d, f), 1.0 / math.sqrt(f), dt, _gen(cfg.seed, _TAG_DOWN, device), device, chunk)
     return wg, wu, wd
+
+
+def make_router_matrix(cfg: MoEConfig, device="cpu") -> torch.Tensor:
+    """Router matrix Wr [E][d] ~ N(0, 1/d) in the workload's operand dtype, stored
+    K-contiguous like the expert weights, for runs that compute the router
+    projection X . Wr^T themselves (unit-variance logits for unit-variance X)."""
+    g = _gen(cfg.seed, _TAG_ROUTER_ROWS, device)
+    return _randn_scaled((cfg.E, cfg.d), 1.0 / math.sqrt(cfg.d), _torch_dtype(cfg.dtype), g, device, 64)
 
 
 def make_inputs(cfg: MoEConfig, device="cpu", weights_device=None) -> dict:
