@@ -8,15 +8,20 @@
 // token rows times the router matrix (stored K-contiguous, wr [E][d], like
 // the expert weights).
 //
-// GB300 design: one CTA per 64-token tile.  The router matrix (E <= 256 rows,
-// at most two 128-row tiles) is the A operand of tcgen05.mma (M = 128), the
-// token rows the B operand (N = 64); K = d streams through a 4-stage TMA ring
-// of 40 KB stages.  The whole router matrix is read by every CTA, from L2
-// after the first.  After the last MMA the accumulators (one 64-column region
-// per expert tile) are read with tcgen05.ld and written transposed into
-// shared memory (the ring is free by then), [token][expert]; one warp per
-// token then selects the top-k with order keys and writes ids, weights and,
-// when asked, the logits row.  Bounded waits as in the FFN kernels.
+// GB300 design: a cluster of 4 CTAs per 64-token tile, each CTA one quarter
+// of K.  The router matrix (E <= 256 rows, at most two 128-row tiles) is the
+// A operand of tcgen05.mma (M = 128), the token rows the B operand (N = 64);
+// a CTA's K range streams through a 4-stage TMA ring of 40 KB stages.  After
+// its last MMA each CTA reads its accumulators (one 64-column region per
+// expert tile) with tcgen05.ld and writes them transposed into shared memory
+// (the ring is free by then), [token][expert].  After a cluster barrier, CTA
+// r sums the four partial tiles for tokens 16r .. 16r+15 over distributed
+// shared memory in rank order (fixed, so the logits are reproducible) and
+// one warp per token selects the top-k with order keys and writes ids,
+// weights and, when asked, the logits row.  A second cluster barrier keeps
+// every CTA's tile alive until its neighbours have read it.  Bounded waits as
+// in the FFN kernels; every thread reaches both cluster barriers, also after
+// an abandoned wait.
 
 #include <cuda_bf16.h>
 
@@ -37,6 +42,7 @@ constexpr int kRRing = kRStages * kRStage;           // 160 KB
 constexpr int kRLogitPitch = kMaxExperts + 1;        // floats per token row in shared memory
 constexpr int kRCtrl = 256;
 constexpr int kRSmem = kRRing + kRCtrl + 1024;
+constexpr int kRCluster = 4;                          // CTAs per token tile (K split)
 static_assert(RT * kRLogitPitch * 4 <= kRRing, "the logit tile fits the ring");
 
 __global__ void __launch_bounds__(kRThreads, 1)
@@ -58,8 +64,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
     float* tile = reinterpret_cast<float*>(smem);          // [RT][kRLogitPitch], after the MMAs
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.x * RT;
-    const int n_kb = d / RK;
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int t0 = (blockIdx.x / kRCluster) * RT;
+    // this CTA's k-blocks: [kb_lo, kb_hi) of d / RK, split as evenly as possible
+    const int n_all = d / RK;
+    const int kb_lo = (n_all * static_cast<int>(rank)) / kRCluster;
+    const int kb_hi = (n_all * (static_cast<int>(rank) + 1)) / kRCluster;
+    const int n_kb = kb_hi - kb_lo;
     const bool two = E > RM;                                // a second expert tile
     const uint32_t stage_tx = (two ? 2 : 1) * kRATile + kRBTile;
 
@@ -93,7 +105,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
             const uint64_t pol_x = l2_policy(1);
             int s = 0;
             uint32_t ph = 0;
-            for (int kb = 0; kb < n_kb; ++kb) {
+            for (int j = 0; j < n_kb; ++j) {
+                const int kb = kb_lo + j;
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) break;
                 uint8_t* st = smem + s * kRStage;
                 mbar_arrive_expect_tx(&full[s], stage_tx);
@@ -137,7 +150,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                     ph ^= 1u;
                 }
             }
-            if (ok) umma_commit(acc_full);
+            if (ok) umma_commit(acc_full);   // (with no k-blocks it arrives at once; the epilogue writes zeros)
             umma_commit(drain);
             mbar_drain(drain, 0);
         }
@@ -155,27 +168,55 @@ __global__ void __launch_bounds__(kRThreads, 1)
 #pragma unroll
                 for (int c0 = 0; c0 < RT; c0 += 32) {
                     uint32_t v[32];
-                    tmem_ld32(lane_addr + static_cast<uint32_t>(r * RT + c0), v);
-                    tmem_ld_wait();
+                    if (n_kb > 0) {
+                        tmem_ld32(lane_addr + static_cast<uint32_t>(r * RT + c0), v);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0u;
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) tile[(c0 + j) * kRLogitPitch + e] = __uint_as_float(v[j]);
                 }
             }
         }
         tc_fence_before();
-        epilogue_sync();
-        if (*epi_ok) {
-            // warp per token: k rounds of a warp arg-max over order keys
-            for (int tt = q; tt < RT; tt += 4) {
+    }
+
+    // every CTA's partial tile is complete: CTA `rank` reduces tokens
+    // [16 rank, 16 rank + 16) over the four tiles and routes them
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (warp >= 2) {
+        const int q = warp & 3;
+        if (*epi_ok && *abort_flag == 0) {
+            uint32_t peer[kRCluster];
+            const uint32_t tile_addr = smem_u32(tile);
+#pragma unroll
+            for (int c = 0; c < kRCluster; ++c)
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(peer[c]) : "r"(tile_addr), "r"(c));
+            // warp per token: sum the partials in rank order, then k rounds of a warp arg-max
+            for (int tt = static_cast<int>(rank) * (RT / kRCluster) + q; tt < (static_cast<int>(rank) + 1) * (RT / kRCluster);
+                 tt += 4) {
                 const int t = t0 + tt;
                 if (t >= T) break;
-                const float* lrow = tile + tt * kRLogitPitch;
                 unsigned long long key[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int e = lane + 32 * j;
-                    key[j] = e < E ? topk_order_key(lrow[e], e) : 0ull;
-                    if (logits != nullptr && e < E) logits[static_cast<size_t>(t) * E + e] = lrow[e];
+                    float acc = 0.f;
+                    if (e < E) {
+#pragma unroll
+                        for (int c = 0; c < kRCluster; ++c) {
+                            float pv;
+                            asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                                         : "=f"(pv)
+                                         : "r"(peer[c] + static_cast<uint32_t>((tt * kRLogitPitch + e) * 4)));
+                            acc = c == 0 ? pv : acc + pv;
+                        }
+                    }
+                    key[j] = e < E ? topk_order_key(acc, e) : 0ull;
+                    if (logits != nullptr && e < E) logits[static_cast<size_t>(t) * E + e] = acc;
                 }
                 float sel_val = 0.f;
                 int sel_id = 0;
@@ -209,6 +250,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
             }
         }
     }
+    // keep this CTA's tile until every neighbour has read it
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 
     tc_fence_before();
     __syncthreads();
@@ -249,9 +293,21 @@ moe_status launch_router_topk(const void* x, const void* wr, int T, int E, int d
             g_router_attr[dev] = true;
         }
     }
-    router_topk_kernel<<<(T + RT - 1) / RT, kRThreads, kRSmem, st>>>(mw, mx, T, E, d, k, logits, ids, w,
-                                                                    di.error_word);
-    return cuda_status(cudaGetLastError());
+    // clusters of kRCluster CTAs, one cluster per 64-token tile
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(((T + RT - 1) / RT) * kRCluster));
+    cfg.blockDim = dim3(kRThreads);
+    cfg.dynamicSmemBytes = kRSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kRCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, router_topk_kernel, mw, mx, T, E, d, k, logits, ids, w,
+                                          di.error_word));
 }
 
 }  // namespace moe
