@@ -19,7 +19,10 @@
 //
 // Work item = (expert e, a slice mt of the output features -- 128 for
 // gate/up, 256 (two tiles) for down -- and a 128-row slice nt of the
-// expert's compact rows).  Items are numbered expert-major,
+// expert's compact rows).  Chunks of at most 64 routes use narrow items
+// instead -- 64 features for gate/up (gate and up rows stacked in one MMA
+// tile), one 128-row tile for down -- so that a handful of tokens still gives
+// several waves of items.  Items are numbered expert-major,
 // then mt, then nt, so CTAs working at the same time on the nt slices of one
 // expert share its weight tile through L2.  The kernel is persistent: one
 // CTA per SM takes items blockIdx.x, blockIdx.x + gridDim.x, ...; every CTA

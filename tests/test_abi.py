@@ -36,6 +36,7 @@ def test_header_declares_the_path_entry_points():
     for required in ("moe_route_topk", "moe_route_histogram", "moe_prefix_offsets", "moe_scatter_rows",
                      "moe_grouped_ffn", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_forward",
                      "moe_quantize_weights_fp8", "moe_grouped_ffn_fp8", "moe_forward_fp8", "moe_scatter_rows_f16",
+                     "moe_route_scatter_small", "moe_router_topk",
                      "moe_workspace_size", "moe_check_device_error"):
         assert required in names
 
@@ -73,6 +74,9 @@ def test_host_only_calls(lib):
     assert lib.moe_quantize_weights_fp8(None, 9, 4, 32, None, None, None) == 2      # dtype
     assert lib.moe_grouped_gate_up_fp8(None, None, 8, 4, 100, 128, None, None, None, None, None, None) == 1
     assert lib.moe_scatter_rows_f16(None, None, None, None, 4, 17, 128, 8, None, None, None, None, None) == 1  # k
+    assert lib.moe_route_scatter_small(None, None, 1, 0, None, 129, 8, 2, 64, None, None, None, None, None, None,
+                                       None, None) == 1                                    # T > 128
+    assert lib.moe_router_topk(None, None, 4, 8, 96, 2, None, None, None, None) == 1     # d % 64
 
 
 def test_product_path_does_not_import_the_oracle():
