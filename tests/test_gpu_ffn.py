@@ -245,3 +245,24 @@ def test_bound_calls_replay_the_same_path():
     run()
     M.moe_check_device_error()
     assert torch.equal(bufs.out, direct)
+
+
+def test_swiglu_of_large_negative_gates_is_zero_not_nan():
+    """Gate pre-activations far below -88 overflow e^-g to infinity: silu must give -0, not NaN."""
+    E, d, f, T, k = 2, 128, 128, 40, 1
+    logits, _ = _routing(T, E, k, seed=21)
+    x = (torch.randn(T, d) * 100.0).to(torch.bfloat16)       # |gate| up to several hundred
+    wg, wu, wd = _weights(E, d, f, torch.bfloat16, seed=22)
+    bufs = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    out = M.moe_forward(logits.cuda(), x.cuda(), None, wg.cuda(), wu.cuda(), wd.cuda(), k, bufs)
+    M.moe_check_device_error()
+    ref = mo.moe_forward(logits.numpy(), to_np(x), (to_np(wg), to_np(wu), to_np(wd)), k)
+    h_ref = mo.grouped_swiglu(ref["xs"], ref["offsets"], (to_np(wg), to_np(wu), to_np(wd)))
+    assert (h_ref < -1e-30).sum() + (np.abs(h_ref) < 1e-30).sum() > 0
+    xs = ref["xs"]
+    g = np.concatenate([xs[ref["offsets"][e]:ref["offsets"][e + 1]] @ to_np(wg[e]).astype(np.float64).T
+                        for e in range(E) if ref["offsets"][e + 1] > ref["offsets"][e]])
+    assert (g < -88).sum() > 100                               # the overflow case is exercised
+    assert torch.isfinite(bufs.h[:T].float()).all()
+    assert_close_bf16_rounded(bufs.h[:T], h_ref)
+    assert_close(out, ref["out"], "bf16")
