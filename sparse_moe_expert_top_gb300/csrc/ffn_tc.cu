@@ -75,7 +75,18 @@ constexpr int kBoxRows = 16;   // compact rows per small TMA box (the granule of
 #define MOE_TC_BIG_BOX_ROWS 64
 #endif
 constexpr int kBigBoxRows = MOE_TC_BIG_BOX_ROWS;  // compact rows per large TMA box
-constexpr int kThreads = 192;
+// Warps 0 (TMA) and 1 (MMA), then the epilogue: 4 warps for gate/up, 8 for
+// down (two per tensor-memory lane quarter taking alternate 32-row chunks:
+// its fp32 stores made the down epilogue, not the MMAs, the pace of heavy
+// experts' 256-row items).
+template <bool GATED>
+struct Roles {
+    static constexpr int kEpiWarps = GATED ? 4 : 8;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+};
+__device__ __forceinline__ void epilogue_sync_n(int threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
 
 // Shared memory: a 192 KB ring, carved per launch into 4 stages of 48 KB
 // (two 16 KB weight tiles + up to 128 rows; narrow items: two k-blocks of one
@@ -110,7 +121,7 @@ struct Cfg {
 // ---------------------------------------------------------------------------
 
 template <bool GATED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                   const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
                   const int32_t* __restrict__ offsets, int cap, int E,
@@ -156,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+            mbar_init(&acc_empty[b], Roles<GATED>::kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -362,13 +373,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(drain, 0);
         }
     } else {
-        // ---- epilogue (warps 2..5) ----------------------------------------
+        // ---- epilogue (warps 2..) ----------------------------------------
         // One thread waits (bounded) for the accumulator and publishes the
-        // outcome; every epilogue barrier below is reached by all four warps
+        // outcome; every epilogue barrier below is reached by all epilogue warps
         // in every iteration, so an abandoned wait cannot leave a warp behind
         // at a barrier.
         const int q = warp & 3;               // TMEM lanes [32q, 32q+32) belong to this warp
-        const int et = threadIdx.x - 64;      // 0..127
+        const int et = threadIdx.x - 64;      // 0 .. 32 * epilogue warps - 1
+        constexpr int kEpiThreads = 32 * Roles<GATED>::kEpiWarps;
+        const int grp = (warp - 2) >> 2;      // down: chunk group (alternate 32-row chunks)
+        constexpr int kGroups = Roles<GATED>::kEpiWarps / 4;
         int local = 0;
         int toggle = 0;
         uint32_t use0 = 0, use1 = 0;
@@ -383,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (got && both) got = mbar_wait(&acc_full[1], use1 & 1u, abort_flag, err);
                 epi_flag[buf] = got ? 1 : 0;
             }
-            epilogue_sync();
+            epilogue_sync_n(kEpiThreads);
             if (!epi_flag[buf]) {
                 ok = false;
                 break;
@@ -395,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int m = item.mt * fw + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(slot * BN);
-            for (int c0 = 0; c0 < item.rows; c0 += 32) {
+            for (int c0 = 32 * grp; c0 < item.rows; c0 += 32 * kGroups) {
                 uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
                 if (!narrow) tmem_ld32(taddr + 2 * BN + c0, g1);
@@ -406,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) up_stage[((q - 2) * 32 + lane) * 33 + j] = __uint_as_float(g[j]);
                     }
-                    epilogue_sync();
+                    epilogue_sync_n(kEpiThreads);
                     if (q < 2) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             out_stage[j * (BM / 2) + q * 32 + lane] = __float2bfloat16_rn(hv);
                         }
                     }
-                    epilogue_sync();
+                    epilogue_sync_n(kEpiThreads);
                     // each row's 64 features (128 bytes) leave as 8 x 16-byte stores
                     __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
                     const int chunk = et & 7;
@@ -429,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       chunk * 8) = v;
                         }
                     }
-                    epilogue_sync();
+                    epilogue_sync_n(kEpiThreads);
                 } else if (GATED) {
                     // SwiGLU into the staged tile: row j, feature q*32 + lane
 #pragma unroll
@@ -438,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float hv = silu_fast(gv) * __uint_as_float(g1[j]);
                         out_stage[j * BM + q * 32 + lane] = __float2bfloat16_rn(hv);
                     }
-                    epilogue_sync();
+                    epilogue_sync_n(kEpiThreads);
                     // each row's 128 features (256 bytes) leave as 16 x 16-byte stores
                     __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
                     const int chunk = et & 15;
@@ -452,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       chunk * 8) = v;
                         }
                     }
-                    epilogue_sync();
+                    epilogue_sync_n(kEpiThreads);
                 } else {
                     float* y = static_cast<float*>(out);
                     const bool has1 = !narrow && m + BM < M;
@@ -486,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int R = offsets[E];
         if (ok && R >= 0 && R <= cap) {
             const int vecs = M * (GATED ? 2 : 4) / 16;
-            const int gw = blockIdx.x * 4 + (warp - 2), nw = gridDim.x * 4;
+            const int gw = blockIdx.x * Roles<GATED>::kEpiWarps + (warp - 2);
+            const int nw = gridDim.x * Roles<GATED>::kEpiWarps;
             uint4* o = static_cast<uint4*>(out);
             for (int row = R + gw; row < cap; row += nw)
                 for (int v = lane; v < vecs; v += 32) o[static_cast<size_t>(row) * vecs + v] = make_uint4(0, 0, 0, 0);
@@ -576,7 +591,7 @@ moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap
     if ((s = encode_2d(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
     if ((s = encode_2d(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
     if ((s = set_smem_attr<true>()) != MOE_OK) return s;
-    ffn_tc_kernel<true><<<di.sm_count, kThreads, Cfg<true>::kSmemBytes, st>>>(ma0, ma1, mb, mbb, offsets, cap, E, d,
+    ffn_tc_kernel<true><<<di.sm_count, Roles<true>::kThreads, Cfg<true>::kSmemBytes, st>>>(ma0, ma1, mb, mbb, offsets, cap, E, d,
                                                                               f, narrow ? 1 : 0, h, di.error_word);
     return cuda_status(cudaGetLastError());
 }
@@ -590,7 +605,7 @@ moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, in
     if ((s = encode_2d(&mbb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
     if ((s = set_smem_attr<false>()) != MOE_OK) return s;
     const bool narrow = use_narrow(cap, E, (d + 2 * BM - 1) / (2 * BM), di);
-    ffn_tc_kernel<false><<<di.sm_count, kThreads, Cfg<false>::kSmemBytes, st>>>(ma0, ma0, mb, mbb, offsets, cap, E, f,
+    ffn_tc_kernel<false><<<di.sm_count, Roles<false>::kThreads, Cfg<false>::kSmemBytes, st>>>(ma0, ma0, mb, mbb, offsets, cap, E, f,
                                                                                 d, narrow ? 1 : 0, y, di.error_word);
     return cuda_status(cudaGetLastError());
 }
