@@ -76,12 +76,17 @@ constexpr int kBoxRows = 16;   // compact rows per small TMA box (the granule of
 #endif
 constexpr int kBigBoxRows = MOE_TC_BIG_BOX_ROWS;  // compact rows per large TMA box
 // Warps 0 (TMA) and 1 (MMA), then the epilogue: 4 warps for gate/up, 8 for
-// down (two per tensor-memory lane quarter taking alternate 32-row chunks:
-// its fp32 stores made the down epilogue, not the MMAs, the pace of heavy
-// experts' 256-row items).
+// down.  In big-item mode the down kernel's 8 epilogue warps work as two
+// groups, two warps per tensor-memory lane quarter taking alternate 32-row
+// chunks: the fp32 stores of 256-row items otherwise set the pace instead of
+// the MMAs.  In the other modes the second group only takes part in the
+// barriers (a second group there was measured slower).
+#ifndef MOE_TC_DOWN_EPI_WARPS
+#define MOE_TC_DOWN_EPI_WARPS 8
+#endif
 template <bool GATED>
 struct Roles {
-    static constexpr int kEpiWarps = GATED ? 4 : 8;
+    static constexpr int kEpiWarps = GATED ? 4 : MOE_TC_DOWN_EPI_WARPS;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
 };
 __device__ __forceinline__ void epilogue_sync_n(int threads) {
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
         const int et = threadIdx.x - 64;      // 0 .. 32 * epilogue warps - 1
         constexpr int kEpiThreads = 32 * Roles<GATED>::kEpiWarps;
         const int grp = (warp - 2) >> 2;      // down: chunk group (alternate 32-row chunks)
-        constexpr int kGroups = Roles<GATED>::kEpiWarps / 4;
+        const int n_groups = big ? Roles<GATED>::kEpiWarps / 4 : 1;
         int local = 0;
         int toggle = 0;
         uint32_t use0 = 0, use1 = 0;
@@ -409,7 +414,7 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
             const int m = item.mt * fw + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(slot * BN);
-            for (int c0 = 32 * grp; c0 < item.rows; c0 += 32 * kGroups) {
+            for (int c0 = 32 * grp; grp < n_groups && c0 < item.rows; c0 += 32 * n_groups) {
                 uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
                 if (!narrow) tmem_ld32(taddr + 2 * BN + c0, g1);
