@@ -134,13 +134,16 @@ def max_over_ranks(value: float, world: int, device) -> float:
     return float(t.item())
 
 
-def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp8: bool = False) -> dict:
+def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp8: bool = False,
+                     fused: bool = False, gather: bool = False) -> dict:
     """Algorithmic bytes and FLOPs of one step, from the realised expert counts.
 
     Only touched experts' weights count; activations are counted once per
     read or write.  es = operand bytes (2 for bf16, 4 for fp32); y and out are
     fp32.  fp8: the expert weights are 1-byte codes plus one fp32 scale per
-    output channel (activations stay bf16).
+    output channel (activations stay bf16).  fused: the down kernel writes
+    out directly (the combine's y round trip is not counted); with gather the
+    gate/up kernel also reads the token rows x itself (no compact copy).
     """
     counts = np.asarray(counts)
     R = int(counts.sum())
@@ -152,6 +155,13 @@ def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp
     routing = T * E * 4 + T * k * 8
     scatter = T * d * es + R * d * es
     combine = R * d * 4 + T * d * 4
+    if fused:
+        down = wdn + R * f * es + T * d * 4
+        if gather:
+            gate_up = wgu + T * d * es + R * f * es
+            scatter = T * k * 8
+        return {"R": R, "touched": touched, "gate_up_bytes": gate_up, "down_bytes": down,
+                "path_bytes": routing + scatter + gate_up + down, "flops": 6.0 * R * d * f}
     return {"R": R, "touched": touched, "gate_up_bytes": gate_up, "down_bytes": down,
             "path_bytes": routing + scatter + gate_up + down + combine, "flops": 6.0 * R * d * f}
 
@@ -382,6 +392,9 @@ def run_ours(args, rank: int, world: int):
     T, E, k, d, f = cfg.T, cfg.E, cfg.k, cfg.d, cfg.f
     dtype = inp["x"].dtype
     fp8 = args.weights == "fp8"
+    fused = args.fused
+    if fused and (fp8 or args.router or dtype != torch.bfloat16):
+        raise SystemExit("--fused runs the bf16 path with the workload's logits")
     # the FP8-weight path keeps its compact activations (xs, h) in fp16
     bufs = M.MoEBuffers(T, E, k, d, f, torch.float16 if fp8 else dtype, device=dev)
     logits, x, mask = inp["logits"], inp["x"], inp["mask"]
@@ -403,7 +416,20 @@ def run_ours(args, rank: int, world: int):
     # every call is marshalled once (M.bind); the timed loop replays the C calls.
     # Small chunks take A1-A4 in one launch, as moe_forward does.
     small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES and not args.router
-    if args.router:
+    # fused: the gate/up kernel gathers the token rows while experts get few
+    # rows (moe_forward_fused's automatic choice), else the compact copy
+    gather = fused and (args.fused_mode == "gather" or (args.fused_mode == "auto" and T * k <= 16 * E))
+    if fused:
+        # the combine runs inside the down kernel
+        names = ("topk", "histogram", "prefix", "scatter_index", "gate_up", "down_combine")
+        routing = [
+            M.bind(M.moe_route_topk, logits, k, b.ids, b.w),
+            M.bind(M.moe_route_histogram, b.ids, mask, E, b.counts, b.ws),
+            M.bind(M.moe_prefix_offsets, b.counts, T, k, b.offsets, b.ws),
+            M.bind(M.moe_scatter_index, b.ids, mask, b.offsets, d, b.row_of_route, b.route_of_row, b.tile_counts,
+                   b.out, b.ws, None if gather else x, None if gather else b.xs),
+        ]
+    elif args.router:
         # the router projection on the tensor cores replaces the given logits
         if dtype != torch.bfloat16:
             raise SystemExit("--router needs a bf16 workload")
@@ -428,11 +454,24 @@ def run_ours(args, rank: int, world: int):
             M.bind(scatter_call, x, b.ids, mask, b.offsets, b.xs, b.row_of_route, b.route_of_row, b.ws),
         ]
     GU = names.index("gate_up")
-    calls = routing + [
-        M.bind(gate_up_call, b.xs, b.offsets, wg, wu, b.h),
-        M.bind(down_call, b.h, b.offsets, wd, b.y),
-        M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
-    ]
+    if fused:
+        fmode = M.MOE_FUSED_GATHER if gather else M.MOE_FUSED_COMPACT
+
+        def forward(*a):
+            return M.moe_forward_fused(*a, mode=fmode)
+
+        calls = routing + [
+            M.bind(M.moe_grouped_gate_up_gather, x, k, b.route_of_row, b.offsets, wg, wu, b.h) if gather else
+            M.bind(M.moe_grouped_gate_up, b.xs, b.offsets, wg, wu, b.h),
+            M.bind(M.moe_grouped_down_combine, b.h, b.offsets, wd, b.route_of_row, b.row_of_route, b.w, b.y,
+                   b.tile_counts, b.out),
+        ]
+    else:
+        calls = routing + [
+            M.bind(gate_up_call, b.xs, b.offsets, wg, wu, b.h),
+            M.bind(down_call, b.h, b.offsets, wd, b.y),
+            M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
+        ]
 
     def step(gu_events=None):
         for i, c in enumerate(calls):
@@ -495,14 +534,15 @@ def run_ours(args, rank: int, world: int):
 
     # ---- roofline of the dominant kernel (grouped gate/up + SwiGLU)
     es = 2 if dtype == torch.bfloat16 else 4
-    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8)
+    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8, fused, gather)
     R, touched = work["R"], work["touched"]
     gate_up_bytes = work["gate_up_bytes"]
     peaks = _peaks()
     achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic("gate_up_fp8" if fp8 else "gate_up", cfg.name)
+    traffic = _profiled_traffic("gate_up_fp8" if fp8 else ("gate_up_gather" if gather else "gate_up"), cfg.name)
     kname = "moe_grouped_gate_up_fp8 (ffn_fp8_kernel<gated>)" if fp8 else \
-        "moe_grouped_gate_up (ffn_tc_kernel<gated>)"
+        ("moe_grouped_gate_up_gather (ffn_tc_kernel<gated, fused>)" if gather else
+         "moe_grouped_gate_up (ffn_tc_kernel<gated>)")
     roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic, "peak_source": peaks["source"],
@@ -534,6 +574,9 @@ def run_ours(args, rank: int, world: int):
                    "routes_unmasked": R, "experts_touched": touched,
                    "weights": "fp8_e4m3 codes + fp32 per-channel scales" if fp8 else
                               ("bf16" if dtype == torch.bfloat16 else "f32"),
+                   "permutation": ("fused: token rows gathered by the gate/up kernel, weighted combine in the "
+                                   "down kernel" if gather else "compact copy xs, weighted combine in the down "
+                                   "kernel") if fused else "compact copy xs + separate combine",
                    "router": "x . Wr^T on the tensor cores (moe_router_topk, Wr ~ N(0, 1/d) bf16) in front of "
                              "the histogram; the workload's own logits unused" if args.router else None,
                    "l2": f"inputs larger than L2: {touched * 3 * d * f * (1 if fp8 else es) / 1e9:.1f} GB of "
@@ -641,6 +684,12 @@ def main():
     ap.add_argument("--weights", choices=("bf16", "fp8"), default="bf16",
                     help="expert weight format: the workload's own (bf16), or FP8 E4M3 codes with per-channel "
                          "scales quantized at load time")
+    ap.add_argument("--fused", action="store_true",
+                    help="the fused permutation (bf16): rows gathered in the gate/up kernel, combine in the down "
+                         "kernel (moe_forward_fused)")
+    ap.add_argument("--fused-mode", choices=("auto", "gather", "compact"), default="auto",
+                    help="with --fused: rows gathered in the gate/up kernel, or the compact copy (auto: gather "
+                         "while T*k <= 16*E)")
     ap.add_argument("--router", action="store_true",
                     help="compute the router projection x . Wr^T on the GPU in front of the path (moe_router_topk)")
     ap.add_argument("--routing-sweep", action="store_true",

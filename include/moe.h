@@ -343,6 +343,92 @@ moe_status moe_forward_fp8(const float* logits, const void* x, const uint8_t* ma
                            void* xs, int32_t* row_of_route, int32_t* route_of_row,
                            void* h, float* y, float* out, void* ws, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Fused permutation (bf16 operands only).  The pages fuse the combine into
+ * one expert-major kernel (page "perf(ds4): accelerate ROCm decode and
+ * long-context selection", lucebox8 gfx1151 A/B; page "perf(ds4): extend
+ * sparse prefill scheduling to 10K", historical fused-combine
+ * discriminator).  Here the permutation moves into the GEMMs themselves:
+ * the gate/up kernel gathers token rows from x (no compact copy xs), and the
+ * down kernel adds each token's slots into out as soon as the last of them
+ * is stored (no separate combine).  out is bit-identical to the unfused
+ * path's (same values of h and y, same fixed-order fp32 combine).
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of the slot counters `tile_counts` of the fused combine for T
+ * tokens of width d: T * ceil(d/128) int32. */
+moe_status moe_tile_counts_size(int T, int d, size_t* bytes);
+
+/* A4 with the fused combine's preparation.  Writes row_of_route and
+ * route_of_row exactly as moe_scatter_rows does (same checks), sets
+ * tile_counts to zero, and sets out[t] to +0.0 for every token whose k slots
+ * are all masked (no down item reaches such a token).  With x and xs given
+ * it also writes the compact rows xs as moe_scatter_rows does; with both
+ * NULL it copies no rows (for moe_grouped_gate_up_gather).
+ *   ids, mask, offsets, ws: as for moe_scatter_rows.
+ *   x, xs        [T][d], [T*k][d] bf16, both or neither.
+ *   tile_counts  [T][ceil(d/128)] int32 out, zeroed.
+ *   out          [T][d] fp32; only the rows of all-masked tokens are written.
+ * d a multiple of 8; out, x and xs 16-byte aligned. */
+moe_status moe_scatter_index(const int32_t* ids, const uint8_t* mask, const int32_t* offsets,
+                             int T, int k, int d, int E, const void* x, void* xs,
+                             int32_t* row_of_route, int32_t* route_of_row,
+                             int32_t* tile_counts, float* out, void* ws, void* stream);
+
+/* A5 reading the token rows directly: h[i] = silu(x[t].Wg_e) * (x[t].Wu_e)
+ * with t = route_of_row[i] / k, for every compact row i < offsets[E] (the
+ * expert e whose segment holds i); rows R .. T*k-1 of h are zero-filled.
+ * Bit-identical to moe_scatter_rows + moe_grouped_gate_up.
+ *   x             [T][d] bf16, 16-byte aligned.
+ *   route_of_row  [T*k] from moe_scatter_index / moe_scatter_rows; an entry
+ *                 outside [0, T*k) for a row below R makes
+ *                 moe_check_device_error() report MOE_ERR_INVALID_ARG.
+ *   offsets, w_gate, w_up, h: as for moe_grouped_gate_up with cap = T*k.
+ * d and f multiples of 128. */
+moe_status moe_grouped_gate_up_gather(const void* x, int T, int k, const int32_t* route_of_row,
+                                      const int32_t* offsets, int E, int d, int f,
+                                      const void* w_gate, const void* w_up, void* h, void* stream);
+
+/* A6 + A7: the down projection with the weighted combine in the same kernel.
+ * out[t] for every token with at least one unmasked slot is written exactly
+ * as moe_combine writes it (+0.0, then w[t][s] * y_s by fp32 FMAs in
+ * ascending unmasked slot order); rows of all-masked tokens are left to
+ * moe_scatter_index.
+ *   h, offsets, w_down: as for moe_grouped_down with cap = T*k (bf16).
+ *   route_of_row, row_of_route  [T*k] from moe_scatter_index.
+ *   w            [T][k] fp32 gate weights.
+ *   y            [T*k][d] fp32 scratch (the exchange buffer between the CTAs
+ *                that own a token's slots); its contents are undefined after
+ *                the call.  128-byte aligned.
+ *   tile_counts  [T][ceil(d/128)] int32, zero on entry (moe_scatter_index
+ *                zeroes them); left nonzero.
+ *   out          [T][d] fp32 out, 16-byte aligned.
+ * d and f multiples of 128. */
+moe_status moe_grouped_down_combine(const void* h, const int32_t* offsets, int T, int k, int E, int d, int f,
+                                    const void* w_down, const int32_t* route_of_row,
+                                    const int32_t* row_of_route, const float* w, float* y,
+                                    int32_t* tile_counts, float* out, void* stream);
+
+/* Modes of moe_forward_fused. */
+enum {
+    MOE_FUSED_AUTO = 0,     /* gather while T*k <= 16*E (few rows per expert), else compact */
+    MOE_FUSED_GATHER = 1,   /* rows gathered by the gate/up kernel; xs unused (may be NULL) */
+    MOE_FUSED_COMPACT = 2   /* compact copy xs, then the plain gate/up kernel */
+};
+
+/* The whole path with the fused combine (bf16): moe_route_topk,
+ * moe_route_histogram, moe_prefix_offsets, moe_scatter_index, the gate/up
+ * projection (moe_grouped_gate_up_gather, or moe_grouped_gate_up on the
+ * compact rows), moe_grouped_down_combine.  Arguments as for moe_forward
+ * without dtype; xs may be NULL (then the gather mode is used); y is scratch;
+ * tile_counts as above.  Every mode gives the same out, bit for bit. */
+moe_status moe_forward_fused(const float* logits, const void* x, const uint8_t* mask,
+                             int T, int E, int k, int d, int f,
+                             const void* w_gate, const void* w_up, const void* w_down, int mode,
+                             int32_t* ids, float* w, int32_t* counts, int32_t* offsets, void* xs,
+                             int32_t* row_of_route, int32_t* route_of_row,
+                             void* h, float* y, int32_t* tile_counts, float* out, void* ws, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

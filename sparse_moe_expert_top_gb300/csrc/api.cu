@@ -260,6 +260,84 @@ extern "C" moe_status moe_forward_fp8(const float* logits, const void* x, const 
 }
 
 // ---------------------------------------------------------------------------
+// Fused permutation (bf16)
+// ---------------------------------------------------------------------------
+
+extern "C" moe_status moe_grouped_gate_up_gather(const void* x, int T, int k, const int32_t* route_of_row,
+                                                 const int32_t* offsets, int E, int d, int f, const void* w_gate,
+                                                 const void* w_up, void* h, void* stream) {
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && static_cast<long long>(T) * k < (1ll << 30));
+    moe_status st = check_ffn_args(offsets, T * k, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(x && route_of_row && w_gate && w_up && h);
+    MOE_REQUIRE(aligned16(x) && aligned16(w_gate) && aligned16(w_up) && aligned16(h));
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_ffn_tc_gate_up_gather(x, T, k, route_of_row, offsets, E, d, f, w_gate, w_up, h,
+                                        static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_grouped_down_combine(const void* h, const int32_t* offsets, int T, int k, int E, int d,
+                                               int f, const void* w_down, const int32_t* route_of_row,
+                                               const int32_t* row_of_route, const float* w, float* y,
+                                               int32_t* tile_counts, float* out, void* stream) {
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && static_cast<long long>(T) * k < (1ll << 30));
+    moe_status st = check_ffn_args(offsets, T * k, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(h && w_down && route_of_row && row_of_route && w && y && tile_counts && out);
+    MOE_REQUIRE(aligned16(h) && aligned16(w_down) && aligned128(y) && aligned16(out));
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_ffn_tc_down_combine(h, offsets, T, k, E, d, f, w_down, route_of_row, row_of_route, w, y,
+                                      tile_counts, out, static_cast<cudaStream_t>(stream), di);
+}
+
+// Average routes per expert up to which moe_forward_fused's automatic mode
+// gathers the token rows inside the gate/up kernel (above it the compact
+// copy's large TMA boxes are cheaper than per-row gathers).
+#ifndef MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT
+#define MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT 16
+#endif
+
+extern "C" moe_status moe_forward_fused(const float* logits, const void* x, const uint8_t* mask, int T, int E,
+                                        int k, int d, int f, const void* w_gate, const void* w_up,
+                                        const void* w_down, int mode, int32_t* ids, float* w, int32_t* counts,
+                                        int32_t* offsets, void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                                        void* h, float* y, int32_t* tile_counts, float* out, void* ws,
+                                        void* stream) {
+    moe_status st = check_ffn_args(offsets, T * k, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && k <= E);
+    MOE_REQUIRE(mode == MOE_FUSED_AUTO || mode == MOE_FUSED_GATHER || mode == MOE_FUSED_COMPACT);
+    MOE_REQUIRE(mode != MOE_FUSED_COMPACT || xs != nullptr);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && w_gate && w_up && w_down && ids && w && counts && row_of_route && route_of_row && h &&
+                y && tile_counts && out && ws);
+    MOE_REQUIRE(aligned16(x) && aligned16(h) && aligned128(y) && aligned16(out) && aligned16(ws) &&
+                aligned16(w_gate) && aligned16(w_up) && aligned16(w_down) && (xs == nullptr || aligned16(xs)));
+    const bool gather = mode == MOE_FUSED_GATHER || xs == nullptr ||
+                        (mode == MOE_FUSED_AUTO &&
+                         static_cast<long long>(T) * k <= static_cast<long long>(E) * MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT);
+    if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
+    if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
+    if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+    if ((st = moe_scatter_index(ids, mask, offsets, T, k, d, E, gather ? nullptr : x, gather ? nullptr : xs,
+                                row_of_route, route_of_row, tile_counts, out, ws, stream)) != MOE_OK)
+        return st;
+    if (gather)
+        st = moe_grouped_gate_up_gather(x, T, k, route_of_row, offsets, E, d, f, w_gate, w_up, h, stream);
+    else
+        st = moe_grouped_gate_up(xs, offsets, T * k, E, d, f, w_gate, w_up, MOE_BF16, h, stream);
+    if (st != MOE_OK) return st;
+    return moe_grouped_down_combine(h, offsets, T, k, E, d, f, w_down, route_of_row, row_of_route, w, y,
+                                    tile_counts, out, stream);
+}
+
+// ---------------------------------------------------------------------------
 // Router projection + top-k
 // ---------------------------------------------------------------------------
 

@@ -36,6 +36,30 @@
 // accumulator with tcgen05.ld, apply SwiGLU (gate/up) and store rows.
 // Every mbarrier wait is bounded: when it runs out the kernel records
 // DEVERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and returns.
+//
+// Fused permutation (the FUSED instantiations)
+// --------------------------------------------
+// Pages "perf(ds4): accelerate ROCm decode and long-context selection"
+// (PR #667), its gfx1151 fused-combine A/B, and "perf(ds4): extend sparse
+// prefill scheduling to 10K" (PR #684), its historical fused-combine
+// discriminator: the combine is a fused expert-major kernel there; here the
+// whole row permutation moves into the GEMMs.
+// * Gate/up: no compact copy xs.  A gather warp (next to the TMA warp, which
+//   keeps streaming the weight tiles) copies the item's token rows from x
+//   with 16-byte cp.async copies (token = route_of_row[row] / k) into the
+//   128B-swizzled layout of the MMA operand; each lane's copies arrive on the
+//   stage's full barrier when they land (cp.async.mbarrier.arrive), and the
+//   MMA thread fences the generic proxy against the async proxy before it
+//   reads them.  (TMA row gathers, four rows per copy, were measured slower:
+//   their per-copy cost exceeds what the compact copy costs.)
+// * Down: four combine warps follow the epilogue.  After an item's y rows
+//   are stored they count, per (token, feature slice), the slots stored so
+//   far (one global counter each); the CTA that stores a token's last slot
+//   adds its slots in ascending slot order from +0.0 (the unfused combine's
+//   arithmetic, so out is bit-identical) and drops the y lines it read from
+//   L2 without write-back.  y is scratch here and laid out slice-major
+//   ([feature slice][row][slice width]), so that the items running at the
+//   same time write contiguous memory.
 
 #include <cuda_bf16.h>
 
@@ -84,14 +108,33 @@ constexpr int kBigBoxRows = MOE_TC_BIG_BOX_ROWS;  // compact rows per large TMA 
 #ifndef MOE_TC_DOWN_EPI_WARPS
 #define MOE_TC_DOWN_EPI_WARPS 8
 #endif
-template <bool GATED>
+// The fused kernels add warps after the epilogue warps: one row-gather warp
+// (gate/up) or four combine warps (down).
+template <bool GATED, bool FUSED>
 struct Roles {
     static constexpr int kEpiWarps = GATED ? 4 : MOE_TC_DOWN_EPI_WARPS;
-    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kCombWarps = (!GATED && FUSED) ? 4 : 0;
+    static constexpr int kGatherWarps = (GATED && FUSED) ? 1 : 0;
+    static constexpr int kThreads = 64 + 32 * (kEpiWarps + kCombWarps + kGatherWarps);
 };
 __device__ __forceinline__ void epilogue_sync_n(int threads) {
     asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
+__device__ __forceinline__ void combine_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// Slots whose loads the combine warps keep in flight together (top-6 routing
+// takes one group).
+constexpr int kSlotGroup = 6;
+
+// Arguments of the fused permutation (unused by the plain instantiations).
+struct FusedArgs {
+    const uint8_t* x;             // gate/up: token rows, bf16 [T][d]
+    const int32_t* route_of_row;  // compact row -> route t*k+s
+    const int32_t* row_of_route;  // down: route -> compact row, -1 if masked
+    const float* w;               // down: gate weights [T][k]
+    float* out;                   // down: [T][d]
+    int32_t* tile_counts;         // down: [T][cstride] slot counters, zero on entry
+    int T, k, cstride;
+};
 
 // Shared memory: a 192 KB ring, carved per launch into 4 stages of 48 KB
 // (two 16 KB weight tiles + up to 128 rows; narrow items: two k-blocks of one
@@ -113,8 +156,13 @@ struct Cfg {
     // stores, then (narrow items) the up half of a stacked tile, 64 features x 32
     // rows of fp32 padded to 33 columns
     static constexpr int kOutStageBytes = GATED ? 32 * BM * 2 + 64 * 33 * 4 : 0;
+    // fused kernels only: the token of each row of the current item (gate/up),
+    // or the combine warps' barriers, list of completed tokens and their
+    // compact rows (down)
+    static constexpr int kFusedBytes = GATED ? 2048 : 1024 + 2 * BN * 4 + 2 * BN * kMaxK * 4;
     static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kOutStageBytes + 1024;
-    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+    static constexpr int smem_bytes(bool fused) { return kSmemBytes + (fused ? kFusedBytes : 0); }
+    static_assert(kSmemBytes + kFusedBytes <= 232448, "shared memory budget of one CTA");
     static_assert(kRingBytes == 3 * (kA * kATileBytes + 2 * BN * BK * 2), "both carve-ups fill the ring");
     static_assert(kRingBytes / 4 >= kA * kATileBytes + 2 * 64 * BK * 2, "narrow carve-up: two k-blocks per stage");
 };
@@ -125,13 +173,14 @@ struct Cfg {
 // A0 . h with A0 = w_down, M = d, K = f.
 // ---------------------------------------------------------------------------
 
-template <bool GATED>
-__global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
+template <bool GATED, bool FUSED>
+__global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                   const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
                   const int32_t* __restrict__ offsets, int cap, int E,
-                  int K, int M, int narrow, void* __restrict__ out, unsigned* err) {
+                  int K, int M, int narrow, void* __restrict__ out, unsigned* err, const FusedArgs fa) {
     using C = Cfg<GATED>;
+    using Ro = Roles<GATED, FUSED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -152,6 +201,14 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
     int* mode_big = const_cast<int*>(reinterpret_cast<volatile int*>(epi_flag + 2));   // launch-wide carve-up
     __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + C::kCtrlBytes);  // gate/up only
     float* up_stage = reinterpret_cast<float*>(ctrl + C::kCtrlBytes + 32 * BM * 2);     // narrow gate/up only
+    uint8_t* fused_smem = ctrl + C::kCtrlBytes + C::kOutStageBytes;
+    int* tok_s = reinterpret_cast<int*>(fused_smem);                  // gather: token of each row of the item
+    uint64_t* comb_done = reinterpret_cast<uint64_t*>(fused_smem);    // combine: an item's y rows are stored (2)
+    uint64_t* comb_free = comb_done + 2;                               // combine: that barrier phase was consumed (2)
+    volatile int* comb_flag = reinterpret_cast<volatile int*>(comb_free + 2);
+    volatile int* list_n = comb_flag + 1;                              // tokens completed by this CTA's item
+    int* list = reinterpret_cast<int*>(fused_smem + 1024);             // up to 2 * BN of them
+    int* list_rows = list + 2 * BN;                                    // their compact rows, kMaxK per token
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_kb = K / BK;
@@ -166,14 +223,20 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
     // ---- prologue: barriers, TMEM, item table --------------------------------
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kMaxStages; ++s) {
-            mbar_init(&full[s], 1);
+            // gather: one arrival with the weight bytes, one per gather-warp lane when its rows have landed
+            mbar_init(&full[s], GATED && FUSED ? 33 : 1);
             mbar_init(&empty[s], 1);
             issued[s] = -1;
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], Roles<GATED>::kEpiWarps);
+            mbar_init(&acc_empty[b], Ro::kEpiWarps);
+            if (!GATED && FUSED) {
+                mbar_init(&comb_done[b], Ro::kEpiWarps);
+                mbar_init(&comb_free[b], Ro::kCombWarps);
+            }
         }
+        if (!GATED && FUSED) *list_n = 0;
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -249,6 +312,7 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
     const int kpb = narrow ? 2 : 1;          // k-blocks per stage
     const int n_st = n_kb / kpb;             // stages per item (K is a multiple of 128)
     const int slice = big ? 2 * BN : BN;                           // rows per work item at most
+    auto item_at = [&](int it) { return decode_item(it, item_off, ntiles, offsets, E, slice); };
 
     if (warp == 0) {
         // ---- TMA producer -------------------------------------------------
@@ -260,10 +324,11 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const Item item = decode_item(it, item_off, ntiles, offsets, E, slice);
+                const Item item = item_at(it);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
                 const int row_bytes = n16 * kBoxRows * BK * 2;   // one k-block of the item's rows
-                const uint32_t bytes = C::kA * C::kATileBytes + kpb * row_bytes;
+                // (the fused gate/up kernel's rows come from the gather warp)
+                const uint32_t bytes = C::kA * C::kATileBytes + (GATED && FUSED ? 0 : kpb * row_bytes);
                 // w_down tiles past the expert's last feature (M not a multiple
                 // of 256) read the next expert's rows, or zero fill past the
                 // end of the bank; the epilogue stores none of their results
@@ -289,6 +354,7 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
                             tma_load_2d(st, &map_a0, &full[s], kb * BK, wy, pol_w);
                             tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * BK, wy1, pol_w);
                         }
+                        if (GATED && FUSED) continue;
                         uint8_t* bdst = st + C::kA * C::kATileBytes + hk * row_bytes;
                         // the rows in as few boxes as possible: 64-row boxes, then 16-row ones
                         int r = 0;
@@ -313,7 +379,7 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
             uint32_t use0 = 0, use1 = 0;  // uses of each accumulator slot so far
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const Item item = decode_item(it, item_off, ntiles, offsets, E, slice);
+                const Item item = item_at(it);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
                 const uint32_t idesc = idesc_bf16(BM, n16 * kBoxRows);
                 const bool both = item.rows > BN;
@@ -329,6 +395,8 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
                         ok = false;
                         break;
                     }
+                    // gathered rows were written by the generic proxy (cp.async)
+                    if (GATED && FUSED) fence_proxy_async_smem();
                     tc_fence_after();
                     // descriptors advance by 32 bytes of K (2 in the low half) per MMA
                     const uint32_t a0 = sdesc_lo(smem_u32(smem + s * stage_bytes));
@@ -377,7 +445,7 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
             umma_commit(drain);
             mbar_drain(drain, 0);
         }
-    } else {
+    } else if (warp < 2 + Ro::kEpiWarps) {
         // ---- epilogue (warps 2..) ----------------------------------------
         // One thread waits (bounded) for the accumulator and publishes the
         // outcome; every epilogue barrier below is reached by all epilogue warps
@@ -385,15 +453,15 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
         // at a barrier.
         const int q = warp & 3;               // TMEM lanes [32q, 32q+32) belong to this warp
         const int et = threadIdx.x - 64;      // 0 .. 32 * epilogue warps - 1
-        constexpr int kEpiThreads = 32 * Roles<GATED>::kEpiWarps;
+        constexpr int kEpiThreads = 32 * Ro::kEpiWarps;
         const int grp = (warp - 2) >> 2;      // down: chunk group (alternate 32-row chunks)
-        const int n_groups = big ? Roles<GATED>::kEpiWarps / 4 : 1;
+        const int n_groups = big ? Ro::kEpiWarps / 4 : 1;
         int local = 0;
         int toggle = 0;
         uint32_t use0 = 0, use1 = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
-            const Item item = decode_item(it, item_off, ntiles, offsets, E, slice);
+            const Item item = item_at(it);
             const bool both = item.rows > BN;
             const int slot = both ? 0 : toggle;
             const int buf = local & 1;  // flag parity
@@ -473,15 +541,21 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
                     }
                     epilogue_sync_n(kEpiThreads);
                 } else {
-                    float* y = static_cast<float*>(out);
                     const bool has1 = !narrow && m + BM < M;
+                    // y row-major [cap][M]; the fused kernel's scratch y is
+                    // slice-major instead: slice mt is [cap][its width] at
+                    // mt * fw * cap, so concurrent items of one slice write
+                    // contiguous memory
+                    const int ystride = FUSED ? min(fw, M - item.mt * fw) : M;
+                    float* y = static_cast<float*>(out) + (FUSED ? static_cast<size_t>(item.mt) * fw * cap : 0);
+                    const int mo = FUSED ? m - item.mt * fw : m;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int n = c0 + j;
                         if (n < item.rows) {
-                            float* yr = y + static_cast<size_t>(item.row0 + n) * M;
-                            yr[m] = __uint_as_float(g[j]);
-                            if (has1) yr[m + BM] = __uint_as_float(g1[j]);
+                            float* yr = y + static_cast<size_t>(item.row0 + n) * ystride;
+                            yr[mo] = __uint_as_float(g[j]);
+                            if (has1) yr[mo + BM] = __uint_as_float(g1[j]);
                         }
                     }
                 }
@@ -491,6 +565,10 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
             if (lane == 0) {
                 mbar_arrive(&acc_empty[slot]);
                 if (both) mbar_arrive(&acc_empty[1]);
+                // fused down: hand the stored item to the combine warps (at most
+                // two items ahead of them; a failed wait has raised the abort flag)
+                if (!GATED && FUSED && mbar_wait(&comb_free[buf], ((local >> 1) & 1) ^ 1u, abort_flag, err))
+                    mbar_arrive(&comb_done[buf]);
             }
             if (slot) ++use1;
             else ++use0;
@@ -501,15 +579,179 @@ __global__ void __launch_bounds__(Roles<GATED>::kThreads, 1)
                 toggle ^= 1;
             }
         }
-        // zero-fill the unused compact rows R .. cap-1
+        // zero-fill the unused compact rows R .. cap-1 (the fused down kernel's
+        // y is scratch)
         const int R = offsets[E];
-        if (ok && R >= 0 && R <= cap) {
+        if (ok && !(FUSED && !GATED) && R >= 0 && R <= cap) {
             const int vecs = M * (GATED ? 2 : 4) / 16;
-            const int gw = blockIdx.x * Roles<GATED>::kEpiWarps + (warp - 2);
-            const int nw = gridDim.x * Roles<GATED>::kEpiWarps;
+            const int gw = blockIdx.x * Ro::kEpiWarps + (warp - 2);
+            const int nw = gridDim.x * Ro::kEpiWarps;
             uint4* o = static_cast<uint4*>(out);
             for (int row = R + gw; row < cap; row += nw)
                 for (int v = lane; v < vecs; v += 32) o[static_cast<size_t>(row) * vecs + v] = make_uint4(0, 0, 0, 0);
+        }
+    } else if (GATED && FUSED) {
+        // ---- row-gather warp (fused gate/up) -------------------------------
+        // Waits for each stage's slot like the TMA warp and copies 16-byte
+        // chunks of token rows -- lane l takes chunk l % 8 of rows l / 8,
+        // l / 8 + 4, ... -- then arrives on the stage's full barrier when its
+        // copies have landed.
+        const uint64_t pol_x = l2_policy(MOE_TC_X_POLICY);
+        const size_t xrow = static_cast<size_t>(K) * 2;   // bytes per token row
+        const int n_routes = fa.T * fa.k;
+        const int chunk = lane & 7;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+            const Item item = item_at(it);
+            const int N = (item.rows + kBoxRows - 1) / kBoxRows * kBoxRows;
+            const int row_bytes = N * BK * 2;
+            // the token of every row; padding rows repeat the first row
+            __syncwarp();
+            for (int n = lane; n < N; n += 32) {
+                const int r = fa.route_of_row[item.row0 + (n < item.rows ? n : 0)];
+                const bool good = r >= 0 && r < n_routes;
+                if (!good) atomicOr(err, DEVERR_OFFSETS);
+                tok_s[n] = good ? r / fa.k : 0;
+            }
+            __syncwarp();
+            for (int js = 0; js < n_st; ++js) {
+                int got = 1;
+                if (lane == 0) got = mbar_wait(&empty[s], ph ^ 1u, abort_flag, err) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + s * stage_bytes;
+                for (int hk = 0; hk < kpb; ++hk) {
+                    const int kb = js * kpb + hk;
+                    const uint32_t bdst = smem_u32(st + C::kA * C::kATileBytes + hk * row_bytes);
+                    const uint8_t* src = fa.x + kb * (BK * 2) + chunk * 16;
+                    // 128B swizzle: chunk c of row n sits at chunk position c ^ (n % 8)
+                    for (int n = lane >> 3; n < N; n += 4)
+                        cp_async16(bdst + n * 128 + ((chunk ^ (n & 7)) << 4), src + tok_s[n] * xrow, pol_x);
+                }
+                cp_async_arrive_noinc(&full[s]);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        // every copy lands before the CTA ends (also after an abandoned wait)
+        cp_async_wait_all();
+    } else if (!GATED && FUSED) {
+        // ---- combine warps (fused down) -----------------------------------
+        // For each item, once the epilogue has stored its y rows: count every
+        // row's slot on its (token, feature slice) counter; the CTA whose count
+        // completes the token's unmasked slots adds them into out.  The
+        // epilogue's stores reach the counters through its mbarrier arrive (CTA
+        // scope) and a gpu-scope release fence here; the completing CTA fences
+        // again (acquire) before it reads the other CTAs' rows.
+        const int ct = threadIdx.x - 32 * (2 + Ro::kEpiWarps);
+        constexpr int kCombThreads = 32 * Ro::kCombWarps;
+        const int k = fa.k;
+        const int n_routes = fa.T * k;
+        const int d4 = M / 4;
+        const int per = fw / 4;                 // float4 columns of a token's slice (64 or 32)
+        const int tpp = kCombThreads / per;     // tokens per pass
+        const int c = ct % per, jt = ct / per;
+        const float4* y4 = static_cast<const float4*>(out);
+        float4* out4 = reinterpret_cast<float4*>(fa.out);
+        int local = 0;
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
+            const Item item = item_at(it);
+            const int b = local & 1;
+            if (ct == 0) *comb_flag = mbar_wait(&comb_done[b], (local >> 1) & 1u, abort_flag, err) ? 1 : 0;
+            combine_sync();
+            if (!*comb_flag) break;
+            if (lane == 0) mbar_arrive(&comb_free[b]);
+            fence_acq_rel_gpu();
+            for (int n = ct; n < item.rows; n += kCombThreads) {
+                const int r = fa.route_of_row[item.row0 + n];
+                if (r < 0 || r >= n_routes) {
+                    atomicOr(err, DEVERR_OFFSETS);
+                    continue;
+                }
+                const int t = r / k;
+                const int32_t* rows_t = fa.row_of_route + static_cast<size_t>(t) * k;
+                int rows[kMaxK];
+                int nv = 0;
+#pragma unroll
+                for (int sl = 0; sl < kMaxK; ++sl) {
+                    rows[sl] = sl < k ? __ldg(rows_t + sl) : -1;
+                    if (rows[sl] >= cap) rows[sl] = -1;
+                    nv += rows[sl] >= 0 ? 1 : 0;
+                }
+                const int old = atomicAdd(fa.tile_counts + static_cast<size_t>(t) * fa.cstride + item.mt, 1);
+                if (old == nv - 1) {
+                    const int p = atomicAdd(const_cast<int*>(list_n), 1);
+                    list[p] = t;
+#pragma unroll
+                    for (int sl = 0; sl < kMaxK; ++sl) list_rows[p * kMaxK + sl] = rows[sl];
+                }
+            }
+            fence_acq_rel_gpu();
+            combine_sync();
+            const int n_list = *list_n;
+            // y is slice-major: slice mt holds rows of w4 float4 columns
+            const int w4 = min(per, d4 - item.mt * per);
+            const float4* ys = y4 + static_cast<size_t>(item.mt) * per * cap;
+            const int col = item.mt * per + c;   // float4 column of out
+            // d is a multiple of 128, so a warp's 32 columns are all in range or all out.
+            // Two tokens per thread and pass, slots in groups of kSlotGroup, every
+            // load of a group in flight before the fixed-order sum.
+            if (c < w4) {
+                for (int j0 = jt; j0 < n_list; j0 += 2 * tpp) {
+                    const bool two = j0 + tpp < n_list;
+                    const int jj[2] = {j0, two ? j0 + tpp : j0};
+                    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+                    for (int s0 = 0; s0 < k; s0 += kSlotGroup) {
+                        float4 yv[2][kSlotGroup];
+                        float ws[2][kSlotGroup];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int* rj = list_rows + jj[u] * kMaxK + s0;
+                            const float* w_t = fa.w + static_cast<size_t>(list[jj[u]]) * k + s0;
+#pragma unroll
+                            for (int sl = 0; sl < kSlotGroup; ++sl) {
+                                const int row = s0 + sl < k ? rj[sl] : -1;
+                                if (row >= 0) {
+                                    yv[u][sl] = __ldcg(ys + static_cast<size_t>(row) * w4 + c);
+                                    ws[u][sl] = __ldg(w_t + sl);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int* rj = list_rows + jj[u] * kMaxK + s0;
+#pragma unroll
+                            for (int sl = 0; sl < kSlotGroup; ++sl) {
+                                if (s0 + sl < k && rj[sl] >= 0) {
+                                    acc[u].x = fmaf(ws[u][sl], yv[u][sl].x, acc[u].x);
+                                    acc[u].y = fmaf(ws[u][sl], yv[u][sl].y, acc[u].y);
+                                    acc[u].z = fmaf(ws[u][sl], yv[u][sl].z, acc[u].z);
+                                    acc[u].w = fmaf(ws[u][sl], yv[u][sl].w, acc[u].w);
+                                }
+                            }
+                        }
+                    }
+                    out4[static_cast<size_t>(list[jj[0]]) * d4 + col] = acc[0];
+                    if (two) out4[static_cast<size_t>(list[jj[1]]) * d4 + col] = acc[1];
+                    // the y lines of these tokens' slices are dead: drop them from L2
+                    __syncwarp();
+                    if ((c & 7) == 0) {
+                        for (int u = 0; u < (two ? 2 : 1); ++u) {
+                            const int* rj = list_rows + jj[u] * kMaxK;
+                            for (int sl = 0; sl < k; ++sl)
+                                if (rj[sl] >= 0) l2_discard128(ys + static_cast<size_t>(rj[sl]) * w4 + c);
+                        }
+                    }
+                }
+            }
+            combine_sync();
+            if (ct == 0) *list_n = 0;
         }
     }
 
@@ -549,7 +791,7 @@ __global__ void bounded_wait_probe_kernel(unsigned long long limit_ns, unsigned*
 // ---------------------------------------------------------------------------
 
 std::mutex g_mutex;
-bool g_attr_set[64][2];
+bool g_attr_set[64][4];
 
 // 2-D bf16 tensor map over a row-major [rows][K] matrix with a box of
 // 64 K-elements x box_rows rows and 128-byte swizzle.
@@ -558,18 +800,30 @@ moe_status encode_2d(CUtensorMap* map, const void* base, int K, long long rows, 
                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool GATED>
+template <bool GATED, bool FUSED>
 moe_status set_smem_attr() {
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    constexpr int v = (GATED ? 1 : 0) + (FUSED ? 2 : 0);
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_attr_set[dev][GATED ? 1 : 0]) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(ffn_tc_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          Cfg<GATED>::kSmemBytes));
-        g_attr_set[dev][GATED ? 1 : 0] = true;
+    if (!g_attr_set[dev][v]) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(ffn_tc_kernel<GATED, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          Cfg<GATED>::smem_bytes(FUSED)));
+        g_attr_set[dev][v] = true;
     }
     return MOE_OK;
+}
+
+template <bool GATED, bool FUSED>
+moe_status launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& bb,
+                  const int32_t* offsets, int cap, int E, int K, int M, bool narrow, void* out, const FusedArgs& fa,
+                  cudaStream_t st, const DeviceInfo& di) {
+    moe_status s;
+    if ((s = set_smem_attr<GATED, FUSED>()) != MOE_OK) return s;
+    ffn_tc_kernel<GATED, FUSED><<<di.sm_count, Roles<GATED, FUSED>::kThreads, Cfg<GATED>::smem_bytes(FUSED), st>>>(
+        a0, a1, b, bb, offsets, cap, E, K, M, narrow ? 1 : 0, out, di.error_word, fa);
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace
@@ -595,10 +849,7 @@ moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap
     if ((s = encode_2d(&ma1, w_up, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
     if ((s = encode_2d(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
     if ((s = encode_2d(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
-    if ((s = set_smem_attr<true>()) != MOE_OK) return s;
-    ffn_tc_kernel<true><<<di.sm_count, Roles<true>::kThreads, Cfg<true>::kSmemBytes, st>>>(ma0, ma1, mb, mbb, offsets, cap, E, d,
-                                                                              f, narrow ? 1 : 0, h, di.error_word);
-    return cuda_status(cudaGetLastError());
+    return launch<true, false>(ma0, ma1, mb, mbb, offsets, cap, E, d, f, narrow, h, FusedArgs{}, st, di);
 }
 
 moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
@@ -608,11 +859,51 @@ moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, in
     if ((s = encode_2d(&ma0, w_down, f, static_cast<long long>(E) * d, BM)) != MOE_OK) return s;
     if ((s = encode_2d(&mb, h, f, cap, kBoxRows)) != MOE_OK) return s;
     if ((s = encode_2d(&mbb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
-    if ((s = set_smem_attr<false>()) != MOE_OK) return s;
     const bool narrow = use_narrow(cap, E, (d + 2 * BM - 1) / (2 * BM), di);
-    ffn_tc_kernel<false><<<di.sm_count, Roles<false>::kThreads, Cfg<false>::kSmemBytes, st>>>(ma0, ma0, mb, mbb, offsets, cap, E, f,
-                                                                                d, narrow ? 1 : 0, y, di.error_word);
-    return cuda_status(cudaGetLastError());
+    return launch<false, false>(ma0, ma0, mb, mbb, offsets, cap, E, f, d, narrow, y, FusedArgs{}, st, di);
+}
+
+moe_status launch_ffn_tc_gate_up_gather(const void* x, int T, int k, const int32_t* route_of_row,
+                                        const int32_t* offsets, int E, int d, int f, const void* w_gate,
+                                        const void* w_up, void* h, cudaStream_t st, const DeviceInfo& di) {
+    CUtensorMap ma0, ma1, mb;
+    moe_status s;
+    const int cap = T * k;
+    const bool narrow = use_narrow(cap, E, f / BM, di);
+    const int wbox = narrow ? BM / 2 : BM;
+    if ((s = encode_2d(&ma0, w_gate, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
+    if ((s = encode_2d(&ma1, w_up, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
+    // the row maps are not used by the gather warp; a valid map over x stands in
+    if ((s = encode_2d(&mb, x, d, T, 1)) != MOE_OK) return s;
+    FusedArgs fa{};
+    fa.x = static_cast<const uint8_t*>(x);
+    fa.route_of_row = route_of_row;
+    fa.T = T;
+    fa.k = k;
+    return launch<true, true>(ma0, ma1, mb, mb, offsets, cap, E, d, f, narrow, h, fa, st, di);
+}
+
+moe_status launch_ffn_tc_down_combine(const void* h, const int32_t* offsets, int T, int k, int E, int d, int f,
+                                      const void* w_down, const int32_t* route_of_row,
+                                      const int32_t* row_of_route, const float* w, float* y,
+                                      int32_t* tile_counts, float* out, cudaStream_t st, const DeviceInfo& di) {
+    CUtensorMap ma0, mb, mbb;
+    moe_status s;
+    const int cap = T * k;
+    if ((s = encode_2d(&ma0, w_down, f, static_cast<long long>(E) * d, BM)) != MOE_OK) return s;
+    if ((s = encode_2d(&mb, h, f, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_2d(&mbb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
+    const bool narrow = use_narrow(cap, E, (d + 2 * BM - 1) / (2 * BM), di);
+    FusedArgs fa{};
+    fa.route_of_row = route_of_row;
+    fa.row_of_route = row_of_route;
+    fa.w = w;
+    fa.out = out;
+    fa.tile_counts = tile_counts;
+    fa.T = T;
+    fa.k = k;
+    fa.cstride = tile_counts_per_token(d);
+    return launch<false, true>(ma0, ma0, mb, mbb, offsets, cap, E, f, d, narrow, y, fa, st, di);
 }
 
 }  // namespace moe

@@ -71,6 +71,10 @@ moe_status device_info(DeviceInfo* info);
 moe_status cuda_status(cudaError_t err);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned128(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 127u) == 0; }
+
+// Slot counters of the fused combine: one per token and 128-feature slice.
+inline int tile_counts_per_token(int d) { return (d + 127) / 128; }
 
 inline int dtype_size(int dtype) { return dtype == MOE_BF16 ? 2 : (dtype == MOE_F32 ? 4 : 0); }
 
@@ -85,6 +89,14 @@ moe_status launch_ffn_simt_gate_up(const float* xs, const int32_t* offsets, int 
                                    const DeviceInfo& di);
 moe_status launch_ffn_simt_down(const float* h, const int32_t* offsets, int cap, int E, int d, int f,
                                 const float* w_down, float* y, cudaStream_t st, const DeviceInfo& di);
+
+moe_status launch_ffn_tc_gate_up_gather(const void* x, int T, int k, const int32_t* route_of_row,
+                                        const int32_t* offsets, int E, int d, int f, const void* w_gate,
+                                        const void* w_up, void* h, cudaStream_t st, const DeviceInfo& di);
+moe_status launch_ffn_tc_down_combine(const void* h, const int32_t* offsets, int T, int k, int E, int d, int f,
+                                      const void* w_down, const int32_t* route_of_row,
+                                      const int32_t* row_of_route, const float* w, float* y,
+                                      int32_t* tile_counts, float* out, cudaStream_t st, const DeviceInfo& di);
 
 moe_status launch_ffn_fp8_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
                                   const uint8_t* q_gate, const float* s_gate, const uint8_t* q_up, const float* s_up,

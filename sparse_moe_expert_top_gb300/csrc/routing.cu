@@ -486,7 +486,9 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
                                                            const int32_t* __restrict__ bases,
                                                            uint4* __restrict__ xs,
                                                            int32_t* __restrict__ row_of_route,
-                                                           int32_t* __restrict__ route_of_row, unsigned* err) {
+                                                           int32_t* __restrict__ route_of_row, unsigned* err,
+                                                           int32_t* __restrict__ tile_counts, int n_counts,
+                                                           float4* __restrict__ out, int d4) {
     __shared__ int rows[kMaxK];
     __shared__ int tails[kMaxK];
     const int t = blockIdx.x, tid = threadIdx.x;
@@ -516,6 +518,14 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
         if (bad) atomicOr(err, DEVERR_OFFSETS);
     }
     __syncthreads();
+    if (tile_counts != nullptr) {
+        // the fused combine's preparation, as in scatter_index_kernel
+        bool any = false;
+        for (int s = 0; s < k; ++s) any |= rows[s] >= 0;
+        for (int j = tid; j < n_counts; j += blockDim.x) tile_counts[static_cast<size_t>(t) * n_counts + j] = 0;
+        if (!any)
+            for (int v = tid; v < d4; v += blockDim.x) out[static_cast<size_t>(t) * d4 + v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const uint4* src = x + static_cast<size_t>(t) * row_vecs;
     bool range = false;
     for (int v = tid; v < row_vecs; v += blockDim.x) {
@@ -534,6 +544,49 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
         }
     }
     if (TO_F16 && __syncthreads_or(range) && tid == 0) atomicOr(err, DEVERR_RANGE);
+}
+
+// A4 without the row copy, for the fused path (the gate/up kernel gathers
+// the token rows itself).  One warp per token: the compact row of each slot
+// exactly as scatter_rows_kernel computes it, both index maps, and the
+// token's preparation for the fused combine -- its slot counters cleared and,
+// when every slot is masked, its output row set to +0.0.
+__global__ void __launch_bounds__(256) scatter_index_kernel(const int32_t* __restrict__ ids,
+                                                            const int32_t* __restrict__ offsets, int T, int k,
+                                                            int E, const int32_t* __restrict__ lrank,
+                                                            const int32_t* __restrict__ bases,
+                                                            int32_t* __restrict__ row_of_route,
+                                                            int32_t* __restrict__ route_of_row,
+                                                            int32_t* __restrict__ tile_counts, int n_counts,
+                                                            float4* __restrict__ out, int d4, unsigned* err) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int n_routes = T * k;
+    int row = -1;
+    if (lane < k) {
+        const int r = t * k + lane;
+        const int lr = lrank[r];
+        bool bad = false;
+        if (lr >= 0) {
+            const int e = ids[r];
+            if (e >= 0 && e < E) row = bases[static_cast<size_t>(r / kHistChunk) * kMaxExperts + e] + lr;
+            if (row < 0 || row >= n_routes) {
+                bad = true;
+                row = -1;
+            }
+        }
+        row_of_route[r] = row;
+        if (row >= 0) route_of_row[row] = r;
+        const int R = __ldg(offsets + E);
+        if (R < 0 || R > n_routes) bad = true;
+        else if (R + r < n_routes) route_of_row[R + r] = -1;
+        if (bad) atomicOr(err, DEVERR_OFFSETS);
+    }
+    const bool any = __ballot_sync(0xffffffffu, row >= 0) != 0u;
+    for (int j = lane; j < n_counts; j += 32) tile_counts[static_cast<size_t>(t) * n_counts + j] = 0;
+    if (!any)
+        for (int v = lane; v < d4; v += 32) out[static_cast<size_t>(t) * d4 + v] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -860,7 +913,8 @@ moe_status scatter_rows(const void* x, int es, bool to_f16, const int32_t* ids, 
     auto kernel = to_f16 ? scatter_rows_kernel<true> : scatter_rows_kernel<false>;
     kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(x), ids, offsets, T, k, E, row_vecs, w32 + ws_rank_offset(T, k),
-        w32 + ws_bases_offset(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word);
+        w32 + ws_bases_offset(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word, nullptr, 0,
+        nullptr, 0);
     return launch_status();
 }
 
@@ -873,6 +927,41 @@ extern "C" moe_status moe_scatter_rows(const void* x, int dtype, const int32_t* 
     const int es = dtype_size(dtype);
     if (es == 0) return MOE_ERR_UNSUPPORTED;
     return scatter_rows(x, es, false, ids, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws, stream);
+}
+
+extern "C" moe_status moe_tile_counts_size(int T, int d, size_t* bytes) {
+    MOE_REQUIRE(bytes != nullptr && T >= 0 && d >= 1);
+    *bytes = static_cast<size_t>(T) * tile_counts_per_token(d) * sizeof(int32_t);
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_scatter_index(const int32_t* ids, const uint8_t* mask, const int32_t* offsets, int T,
+                                        int k, int d, int E, const void* x, void* xs, int32_t* row_of_route,
+                                        int32_t* route_of_row, int32_t* tile_counts, float* out, void* ws,
+                                        void* stream) {
+    (void)mask;  // folded into the workspace ranks by the histogram
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 8 && d % 8 == 0);
+    MOE_REQUIRE((x == nullptr) == (xs == nullptr));
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(ids && offsets && row_of_route && route_of_row && tile_counts && out && ws);
+    MOE_REQUIRE(aligned16(out) && aligned16(ws));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    const int32_t* w32 = static_cast<const int32_t*>(ws);
+    if (x != nullptr) {
+        // with the compact copy of the bf16 token rows
+        MOE_REQUIRE(aligned16(x) && aligned16(xs));
+        scatter_rows_kernel<false><<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+            static_cast<const uint4*>(x), ids, offsets, T, k, E, d / 8, w32 + ws_rank_offset(T, k),
+            w32 + ws_bases_offset(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word,
+            tile_counts, tile_counts_per_token(d), reinterpret_cast<float4*>(out), d / 4);
+        return launch_status();
+    }
+    scatter_index_kernel<<<(T + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        ids, offsets, T, k, E, w32 + ws_rank_offset(T, k), w32 + ws_bases_offset(T, k), row_of_route, route_of_row,
+        tile_counts, tile_counts_per_token(d), reinterpret_cast<float4*>(out), d / 4, di.error_word);
+    return launch_status();
 }
 
 extern "C" moe_status moe_scatter_rows_f16(const void* x, const int32_t* ids, const uint8_t* mask,

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_RANGE = range(6)
 MOE_F32, MOE_BF16 = 0, 1
+MOE_FUSED_AUTO, MOE_FUSED_GATHER, MOE_FUSED_COMPACT = 0, 1, 2
 
 # (name, argtypes) of every exported entry point; the ABI test checks this
 # list against include/moe.h.
@@ -52,6 +53,12 @@ SIGNATURES = {
     "moe_grouped_ffn_fp8": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_forward_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                          _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_tile_counts_size": ([_I, _I, _SZ], _I),
+    "moe_scatter_index": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_gate_up_gather": ([_P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_grouped_down_combine": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_forward_fused": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I,
+                           _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
 }
 
 
@@ -352,6 +359,8 @@ class MoEBuffers:
         self.out = torch.empty(T, d, dtype=torch.float32, device=device)
         # the workspace must start zero-filled (it keeps a completion counter)
         self.ws = torch.zeros(max(moe_workspace_size(T, k), 16) // 4 + 4, dtype=torch.int32, device=device)
+        # slot counters of the fused combine (moe_forward_fused)
+        self.tile_counts = torch.zeros(max(moe_tile_counts_size(T, d), 4) // 4, dtype=torch.int32, device=device)
 
 
 def moe_forward(logits, x, mask, w_gate, w_up, w_down, k: int, bufs: MoEBuffers, stream=None) -> torch.Tensor:
@@ -372,6 +381,99 @@ def moe_forward(logits, x, mask, w_gate, w_up, w_down, k: int, bufs: MoEBuffers,
         _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, f, _ptr(w_gate), _ptr(w_up), _ptr(w_down), _dtype_code(x),
         _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
         _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
+    return b.out
+
+
+# ---------------------------------------------------------------------------
+# Fused permutation (bf16): row gather in the gate/up kernel, combine in the
+# down kernel
+# ---------------------------------------------------------------------------
+
+def moe_tile_counts_size(T: int, d: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_tile_counts_size", load().moe_tile_counts_size(T, d, ctypes.byref(n)))
+    return n.value
+
+
+def moe_scatter_index(ids, mask, offsets, d, row_of_route, route_of_row, tile_counts, out, ws, x=None, xs=None,
+                      stream=None):
+    """A4 with the fused combine's preparation: clears ``tile_counts``, zeroes ``out`` rows of all-masked
+    tokens; copies the compact rows ``xs`` only when ``x`` and ``xs`` are given."""
+    T, k = ids.shape
+    E = offsets.shape[0] - 1
+    if (x is None) != (xs is None):
+        raise ValueError("give both x and xs, or neither")
+    if x is not None:
+        _expect(x, torch.bfloat16, (T, d), "x")
+        _expect(xs, torch.bfloat16, (T * k, d), "xs")
+    _expect(ids, torch.int32, (T, k), "ids")
+    _expect(row_of_route, torch.int32, (T * k,), "row_of_route")
+    _expect(route_of_row, torch.int32, (T * k,), "route_of_row")
+    _expect(out, torch.float32, (T, d), "out")
+    if tile_counts.dtype != torch.int32 or tile_counts.numel() * 4 < moe_tile_counts_size(T, d):
+        raise ValueError("tile_counts: expected int32 of moe_tile_counts_size(T, d) bytes")
+    _check("moe_scatter_index", load().moe_scatter_index(
+        _ptr(ids), _ptr(mask), _ptr(offsets), T, k, d, E, _ptr(x), _ptr(xs), _ptr(row_of_route),
+        _ptr(route_of_row), _ptr(tile_counts), _ptr(out), _ptr(ws), _stream(stream)))
+
+
+def moe_grouped_gate_up_gather(x, k, route_of_row, offsets, w_gate, w_up, h, stream=None):
+    """A5 reading token rows of x through route_of_row (no compact copy)."""
+    T, d = x.shape
+    E, f, _ = w_gate.shape
+    _expect(x, torch.bfloat16, (T, d), "x")
+    _expect(route_of_row, torch.int32, (T * k,), "route_of_row")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _expect(w_gate, torch.bfloat16, (E, f, d), "w_gate")
+    _expect(w_up, torch.bfloat16, (E, f, d), "w_up")
+    _expect(h, torch.bfloat16, (T * k, f), "h")
+    _check("moe_grouped_gate_up_gather", load().moe_grouped_gate_up_gather(
+        _ptr(x), T, k, _ptr(route_of_row), _ptr(offsets), E, d, f, _ptr(w_gate), _ptr(w_up), _ptr(h),
+        _stream(stream)))
+
+
+def moe_grouped_down_combine(h, offsets, w_down, route_of_row, row_of_route, w, y, tile_counts, out, stream=None):
+    """A6 + A7 in one kernel; ``y`` is scratch, ``tile_counts`` must be zero (moe_scatter_index)."""
+    T, k = w.shape
+    cap, f = h.shape
+    E, d, _ = w_down.shape
+    _expect(h, torch.bfloat16, (T * k, f), "h")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _expect(w_down, torch.bfloat16, (E, d, f), "w_down")
+    _expect(route_of_row, torch.int32, (T * k,), "route_of_row")
+    _expect(row_of_route, torch.int32, (T * k,), "row_of_route")
+    _expect(w, torch.float32, (T, k), "w")
+    _expect(y, torch.float32, (T * k, d), "y")
+    _expect(out, torch.float32, (T, d), "out")
+    if tile_counts.dtype != torch.int32 or tile_counts.numel() * 4 < moe_tile_counts_size(T, d):
+        raise ValueError("tile_counts: expected int32 of moe_tile_counts_size(T, d) bytes")
+    _check("moe_grouped_down_combine", load().moe_grouped_down_combine(
+        _ptr(h), _ptr(offsets), T, k, E, d, f, _ptr(w_down), _ptr(route_of_row), _ptr(row_of_route), _ptr(w),
+        _ptr(y), _ptr(tile_counts), _ptr(out), _stream(stream)))
+
+
+def moe_forward_fused(logits, x, mask, w_gate, w_up, w_down, k: int, bufs: MoEBuffers, mode: int = MOE_FUSED_AUTO,
+                      stream=None) -> torch.Tensor:
+    """The whole path with the fused combine (bf16); returns ``bufs.out``.  ``mode``: MOE_FUSED_AUTO,
+    MOE_FUSED_GATHER (rows gathered by the gate/up kernel, ``bufs.xs`` unused) or MOE_FUSED_COMPACT.
+    ``bufs.y`` is scratch."""
+    T, E = logits.shape
+    d = x.shape[1]
+    f = w_gate.shape[1]
+    if (bufs.T, bufs.E, bufs.k, bufs.d, bufs.f, bufs.dtype) != (T, E, k, d, f, torch.bfloat16):
+        raise ValueError("buffers were allocated for another shape")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect(w_gate, torch.bfloat16, (E, f, d), "w_gate")
+    _expect(w_up, torch.bfloat16, (E, f, d), "w_up")
+    _expect(w_down, torch.bfloat16, (E, d, f), "w_down")
+    b = bufs
+    _check("moe_forward_fused", load().moe_forward_fused(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, f, _ptr(w_gate), _ptr(w_up), _ptr(w_down), int(mode),
+        _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
+        _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.tile_counts), _ptr(b.out), _ptr(b.ws), _stream(stream)))
     return b.out
 
 

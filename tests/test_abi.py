@@ -36,7 +36,9 @@ def test_header_declares_the_path_entry_points():
     for required in ("moe_route_topk", "moe_route_histogram", "moe_prefix_offsets", "moe_scatter_rows",
                      "moe_grouped_ffn", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_forward",
                      "moe_quantize_weights_fp8", "moe_grouped_ffn_fp8", "moe_forward_fp8", "moe_scatter_rows_f16",
-                     "moe_route_scatter_small", "moe_router_topk",
+                     "moe_route_scatter_small", "moe_router_topk", "moe_scatter_index",
+                     "moe_grouped_gate_up_gather", "moe_grouped_down_combine", "moe_forward_fused",
+                     "moe_tile_counts_size",
                      "moe_workspace_size", "moe_check_device_error"):
         assert required in names
 
@@ -77,6 +79,26 @@ def test_host_only_calls(lib):
     assert lib.moe_route_scatter_small(None, None, 1, 0, None, 129, 8, 2, 64, None, None, None, None, None, None,
                                        None, None) == 1                                    # T > 128
     assert lib.moe_router_topk(None, None, 4, 8, 96, 2, None, None, None, None) == 1     # d % 64
+    # fused permutation: one counter per token and 128-feature slice
+    fake = ctypes.c_void_p(4096)
+    assert lib.moe_tile_counts_size(2048, 4096, ctypes.byref(n)) == 0 and n.value == 2048 * 32 * 4
+    assert lib.moe_tile_counts_size(3, 130, ctypes.byref(n)) == 0 and n.value == 3 * 2 * 4
+    assert lib.moe_scatter_index(None, None, None, 4, 2, 6, 8, None, None, None, None, None, None, None,
+                                 None) == 1                                                       # d % 8
+    assert lib.moe_scatter_index(fake, fake, fake, 4, 2, 8, 8, fake, None, fake, fake, fake, fake, fake,
+                                 None) == 1                                                       # x without xs
+    assert lib.moe_grouped_gate_up_gather(None, 4, 2, None, None, 8, 100, 128, None, None, None, None) == 1  # d
+    assert lib.moe_grouped_gate_up_gather(None, 4, 17, None, None, 8, 128, 128, None, None, None, None) == 1  # k
+    # y of the fused down projection must be 128-byte aligned (its L2 lines are dropped after use)
+    bad_y = ctypes.c_void_p(4096 + 16)
+    assert lib.moe_grouped_down_combine(fake, fake, 4, 2, 8, 128, 128, fake, fake, fake, fake, bad_y, fake, fake,
+                                        None) == 1
+    assert lib.moe_forward_fused(None, None, None, 4, 8, 2, 100, 128, None, None, None, 0, None, None, None,
+                                 None, None, None, None, None, None, None, None, None, None) == 1  # d % 128
+    assert lib.moe_forward_fused(None, None, None, 4, 8, 2, 128, 128, None, None, None, 2, None, None, None,
+                                 fake, None, None, None, None, None, None, None, None, None) == 1  # compact, no xs
+    assert lib.moe_forward_fused(None, None, None, 4, 8, 2, 128, 128, None, None, None, 7, None, None, None,
+                                 fake, fake, None, None, None, None, None, None, None, None) == 1  # mode
 
 
 def test_product_path_does_not_import_the_oracle():
