@@ -416,10 +416,21 @@ def run_ours(args, rank: int, world: int):
     # every call is marshalled once (M.bind); the timed loop replays the C calls.
     # Small chunks take A1-A4 in one launch, as moe_forward does.
     small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES and not args.router
-    # fused: the gate/up kernel gathers the token rows while experts get few
-    # rows (moe_forward_fused's automatic choice), else the compact copy
-    gather = fused and (args.fused_mode == "gather" or (args.fused_mode == "auto" and T * k <= 16 * E))
-    if fused:
+    # fused: moe_forward_fused's automatic choice -- gather the token rows in
+    # the gate/up kernel while experts get few rows, else the compact copy;
+    # the combine in the down kernel while y fits in twice the L2, else the
+    # unfused path
+    if fused and args.fused_mode == "auto":
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        args.fused_mode = "gather" if T * k <= 16 * E else ("compact" if T * k * d * 4 <= 2 * l2 else "none")
+    if args.fused_mode == "none":
+        fused = False
+    gather = fused and args.fused_mode == "gather"
+    small = small and not fused
+    if fused and T <= SMALL_TOKENS and T * k <= SMALL_ROUTES:
+        names = ("route_scatter_small", "gate_up", "down_combine")
+        routing = [M.bind(M.moe_route_scatter_small_fused, logits, x, mask, k, b, gather)]
+    elif fused:
         # the combine runs inside the down kernel
         names = ("topk", "histogram", "prefix", "scatter_index", "gate_up", "down_combine")
         routing = [
@@ -687,9 +698,9 @@ def main():
     ap.add_argument("--fused", action="store_true",
                     help="the fused permutation (bf16): rows gathered in the gate/up kernel, combine in the down "
                          "kernel (moe_forward_fused)")
-    ap.add_argument("--fused-mode", choices=("auto", "gather", "compact"), default="auto",
-                    help="with --fused: rows gathered in the gate/up kernel, or the compact copy (auto: gather "
-                         "while T*k <= 16*E)")
+    ap.add_argument("--fused-mode", choices=("auto", "gather", "compact", "none"), default="auto",
+                    help="with --fused: rows gathered in the gate/up kernel, the compact copy, or the unfused "
+                         "path (auto: moe_forward_fused's choice)")
     ap.add_argument("--router", action="store_true",
                     help="compute the router projection x . Wr^T on the GPU in front of the path (moe_router_topk)")
     ap.add_argument("--routing-sweep", action="store_true",

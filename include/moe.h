@@ -375,6 +375,17 @@ moe_status moe_scatter_index(const int32_t* ids, const uint8_t* mask, const int3
                              int32_t* row_of_route, int32_t* route_of_row,
                              int32_t* tile_counts, float* out, void* ws, void* stream);
 
+/* moe_route_scatter_small (bf16 x) with the preparation of moe_scatter_index:
+ * A1-A4 in one launch for a chunk with T <= 128 and T*k <= 512, tile_counts
+ * zeroed and out[t] = +0.0 for every token whose slots are all masked; xs
+ * NULL copies no rows (for moe_grouped_gate_up_gather).  d a multiple of 8;
+ * x, xs and out 16-byte aligned. */
+moe_status moe_route_scatter_small_fused(const float* logits, const void* x, const uint8_t* mask,
+                                         int T, int E, int k, int d,
+                                         int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                         void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                                         int32_t* tile_counts, float* out, void* stream);
+
 /* A5 reading the token rows directly: h[i] = silu(x[t].Wg_e) * (x[t].Wu_e)
  * with t = route_of_row[i] / k, for every compact row i < offsets[E] (the
  * expert e whose segment holds i); rows R .. T*k-1 of h are zero-filled.
@@ -411,17 +422,21 @@ moe_status moe_grouped_down_combine(const void* h, const int32_t* offsets, int T
 
 /* Modes of moe_forward_fused. */
 enum {
-    MOE_FUSED_AUTO = 0,     /* gather while T*k <= 16*E (few rows per expert), else compact */
+    MOE_FUSED_AUTO = 0,     /* GATHER while T*k <= 16*E (few rows per expert); else COMPACT while y
+                               (T*k*d*4 bytes) fits in twice the L2; else NONE */
     MOE_FUSED_GATHER = 1,   /* rows gathered by the gate/up kernel; xs unused (may be NULL) */
-    MOE_FUSED_COMPACT = 2   /* compact copy xs, then the plain gate/up kernel */
+    MOE_FUSED_COMPACT = 2,  /* compact copy xs, the plain gate/up kernel, the fused down + combine */
+    MOE_FUSED_NONE = 3      /* the unfused path (moe_forward): y is written as moe_grouped_down writes it */
 };
 
-/* The whole path with the fused combine (bf16): moe_route_topk,
- * moe_route_histogram, moe_prefix_offsets, moe_scatter_index, the gate/up
+/* The whole path with the fused combine (bf16): the routing (one launch for
+ * chunks with T <= 128 and T*k <= 512, else moe_route_topk,
+ * moe_route_histogram, moe_prefix_offsets and moe_scatter_index), the gate/up
  * projection (moe_grouped_gate_up_gather, or moe_grouped_gate_up on the
  * compact rows), moe_grouped_down_combine.  Arguments as for moe_forward
- * without dtype; xs may be NULL (then the gather mode is used); y is scratch;
- * tile_counts as above.  Every mode gives the same out, bit for bit. */
+ * without dtype; xs may be NULL (then the gather mode is used); y is scratch
+ * except in mode NONE; tile_counts as above.  Every mode gives the same out,
+ * bit for bit, as moe_forward. */
 moe_status moe_forward_fused(const float* logits, const void* x, const uint8_t* mask,
                              int T, int E, int k, int d, int f,
                              const void* w_gate, const void* w_up, const void* w_down, int mode,

@@ -38,6 +38,7 @@ moe_status device_info(DeviceInfo* info) {
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev));
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev));
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev));
         if (di.cc_major != 10 || di.cc_minor != 3) return MOE_ERR_UNSUPPORTED;
         void* p = nullptr;
         MOE_CUDA_TRY(cudaGetSymbolAddress(&p, g_moe_device_error));
@@ -296,9 +297,12 @@ extern "C" moe_status moe_grouped_down_combine(const void* h, const int32_t* off
                                       tile_counts, out, static_cast<cudaStream_t>(stream), di);
 }
 
-// Average routes per expert up to which moe_forward_fused's automatic mode
-// gathers the token rows inside the gate/up kernel (above it the compact
-// copy's large TMA boxes are cheaper than per-row gathers).
+// moe_forward_fused's automatic mode: gather the token rows inside the
+// gate/up kernel while the chunk averages at most this many routes per expert
+// (above it the compact copy's large TMA boxes are cheaper than per-row
+// copies), and fuse the combine into the down kernel while y (T*k*d fp32,
+// the exchange between the CTAs that own a token's slots) fits in twice the
+// L2; above that the separate combine kernel is faster.
 #ifndef MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT
 #define MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT 16
 #endif
@@ -312,22 +316,45 @@ extern "C" moe_status moe_forward_fused(const float* logits, const void* x, cons
     moe_status st = check_ffn_args(offsets, T * k, E, d, f, MOE_BF16);
     if (st != MOE_OK) return st;
     MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && k <= E);
-    MOE_REQUIRE(mode == MOE_FUSED_AUTO || mode == MOE_FUSED_GATHER || mode == MOE_FUSED_COMPACT);
-    MOE_REQUIRE(mode != MOE_FUSED_COMPACT || xs != nullptr);
+    MOE_REQUIRE(mode == MOE_FUSED_AUTO || mode == MOE_FUSED_GATHER || mode == MOE_FUSED_COMPACT ||
+                mode == MOE_FUSED_NONE);
+    MOE_REQUIRE((mode != MOE_FUSED_COMPACT && mode != MOE_FUSED_NONE) || xs != nullptr);
     if (T == 0) return MOE_OK;
     MOE_REQUIRE(logits && x && w_gate && w_up && w_down && ids && w && counts && row_of_route && route_of_row && h &&
                 y && tile_counts && out && ws);
     MOE_REQUIRE(aligned16(x) && aligned16(h) && aligned128(y) && aligned16(out) && aligned16(ws) &&
                 aligned16(w_gate) && aligned16(w_up) && aligned16(w_down) && (xs == nullptr || aligned16(xs)));
-    const bool gather = mode == MOE_FUSED_GATHER || xs == nullptr ||
-                        (mode == MOE_FUSED_AUTO &&
-                         static_cast<long long>(T) * k <= static_cast<long long>(E) * MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT);
-    if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
-    if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
-    if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
-    if ((st = moe_scatter_index(ids, mask, offsets, T, k, d, E, gather ? nullptr : x, gather ? nullptr : xs,
-                                row_of_route, route_of_row, tile_counts, out, ws, stream)) != MOE_OK)
-        return st;
+    DeviceInfo di;
+    st = device_info(&di);
+    if (st != MOE_OK) return st;
+    const long long cap = static_cast<long long>(T) * k;
+    if (mode == MOE_FUSED_AUTO) {
+        if (xs == nullptr || cap <= static_cast<long long>(E) * MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT)
+            mode = MOE_FUSED_GATHER;
+        else if (cap * d * 4 <= 2LL * di.l2_bytes)
+            mode = MOE_FUSED_COMPACT;
+        else
+            mode = MOE_FUSED_NONE;
+    }
+    if (mode == MOE_FUSED_NONE)
+        return moe_forward(logits, x, mask, T, E, k, d, f, w_gate, w_up, w_down, MOE_BF16, ids, w, counts, offsets, xs,
+                           row_of_route, route_of_row, h, y, out, ws, stream);
+    const bool gather = mode == MOE_FUSED_GATHER;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T <= kSmallTokens && cap <= kSmallRoutes) {
+        // A1-A4 in one launch, with the fused combine's preparation
+        if ((st = launch_route_scatter_small_fused(logits, x, mask, T, E, k, d, ids, w, counts, offsets,
+                                                   gather ? nullptr : xs, row_of_route, route_of_row, tile_counts,
+                                                   out, s, di)) != MOE_OK)
+            return st;
+    } else {
+        if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
+        if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_scatter_index(ids, mask, offsets, T, k, d, E, gather ? nullptr : x, gather ? nullptr : xs,
+                                    row_of_route, route_of_row, tile_counts, out, ws, stream)) != MOE_OK)
+            return st;
+    }
     if (gather)
         st = moe_grouped_gate_up_gather(x, T, k, route_of_row, offsets, E, d, f, w_gate, w_up, h, stream);
     else

@@ -60,6 +60,7 @@ __device__ __forceinline__ float topk_key_value(unsigned long long key) {
 struct DeviceInfo {
     int sm_count;
     int cc_major, cc_minor;
+    int l2_bytes;
     unsigned* error_word;   // device address of the sticky error word
 };
 
@@ -106,6 +107,13 @@ moe_status launch_ffn_fp8_down(const void* h, const int32_t* offsets, int cap, i
                                const DeviceInfo& di);
 moe_status launch_router_topk(const void* x, const void* wr, int T, int E, int d, int k, float* logits,
                               int32_t* ids, float* w, cudaStream_t st, const DeviceInfo& di);
+// moe_route_scatter_small for the fused path: xs may be NULL (no row copy);
+// tile_counts [T][n_counts] are zeroed and out rows of all-masked tokens set
+// to +0.0.
+moe_status launch_route_scatter_small_fused(const float* logits, const void* x, const uint8_t* mask, int T, int E,
+                                            int k, int d, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                            void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                                            int32_t* tile_counts, float* out, cudaStream_t st, const DeviceInfo& di);
 moe_status launch_quantize_fp8(const void* w, int dtype, long long rows, int K, uint8_t* codes, float* scales,
                                cudaStream_t st, const DeviceInfo& di);
 

@@ -647,7 +647,8 @@ __global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
     const float* __restrict__ logits, const uint4* __restrict__ x, const uint8_t* __restrict__ mask, int T, int E,
     int k, int row_vecs, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, uint4* __restrict__ xs, int32_t* __restrict__ row_of_route,
-    int32_t* __restrict__ route_of_row, unsigned* err) {
+    int32_t* __restrict__ route_of_row, unsigned* err, int32_t* __restrict__ tile_counts, int n_counts,
+    float4* __restrict__ out, int d4) {
     __shared__ int s_e[kSmallRoutes];     // expert of route r, -1 when masked
     __shared__ int s_row[kSmallRoutes];   // rank, then compact row (-1 masked)
     __shared__ int s_cnt[kMaxExperts];
@@ -760,6 +761,21 @@ __global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
         for (int j = R + tid; j < n_routes; j += kSmallThreads) route_of_row[j] = -1;
     }
     __syncthreads();
+
+    // the fused combine's preparation (fused path): this CTA's share of the
+    // tokens gets its slot counters cleared, and +0.0 rows when every slot is
+    // masked
+    if (tile_counts != nullptr) {
+        for (int t = blockIdx.x; t < T; t += gridDim.x) {
+            bool any = false;
+            for (int s = 0; s < k; ++s) any |= s_row[t * k + s] >= 0;
+            for (int j = tid; j < n_counts; j += kSmallThreads) tile_counts[static_cast<size_t>(t) * n_counts + j] = 0;
+            if (!any)
+                for (int v = tid; v < d4; v += kSmallThreads)
+                    out[static_cast<size_t>(t) * d4 + v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    if (xs == nullptr) return;   // the gate/up kernel gathers the rows itself
 
     // A4: this CTA's share of the compact rows, and of the zero-filled tail
     bool range = false;
@@ -992,9 +1008,43 @@ extern "C" moe_status moe_route_scatter_small(const float* logits, const void* x
     auto kernel = xs_f16 ? route_scatter_small_kernel<true> : route_scatter_small_kernel<false>;
     kernel<<<grid, kSmallThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         logits, static_cast<const uint4*>(x), mask, T, E, k, row_vecs, ids, w, counts, offsets,
-        static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word);
+        static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word, nullptr, 0, nullptr, 0);
     return launch_status();
 }
+
+extern "C" moe_status moe_route_scatter_small_fused(const float* logits, const void* x, const uint8_t* mask, int T,
+                                                    int E, int k, int d, int32_t* ids, float* w, int32_t* counts,
+                                                    int32_t* offsets, void* xs, int32_t* row_of_route,
+                                                    int32_t* route_of_row, int32_t* tile_counts, float* out,
+                                                    void* stream) {
+    MOE_REQUIRE(T >= 0 && T <= kSmallTokens && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E &&
+                T * k <= kSmallRoutes && d >= 8 && d % 8 == 0);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && ids && w && counts && offsets && row_of_route && route_of_row && tile_counts && out);
+    MOE_REQUIRE(aligned16(x) && aligned16(out) && (xs == nullptr || aligned16(xs)));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_route_scatter_small_fused(logits, x, mask, T, E, k, d, ids, w, counts, offsets, xs, row_of_route,
+                                            route_of_row, tile_counts, out, static_cast<cudaStream_t>(stream), di);
+}
+
+namespace moe {
+
+moe_status launch_route_scatter_small_fused(const float* logits, const void* x, const uint8_t* mask, int T, int E,
+                                            int k, int d, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                            void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                                            int32_t* tile_counts, float* out, cudaStream_t st, const DeviceInfo& di) {
+    const int row_vecs = d / 8;   // bf16 rows
+    const int grid = T * k < 2 * di.sm_count ? T * k : 2 * di.sm_count;
+    route_scatter_small_kernel<false><<<grid, kSmallThreads, 0, st>>>(
+        logits, static_cast<const uint4*>(x), mask, T, E, k, row_vecs, ids, w, counts, offsets,
+        static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word, tile_counts, tile_counts_per_token(d),
+        reinterpret_cast<float4*>(out), d / 4);
+    return launch_status();
+}
+
+}  // namespace moe
 
 extern "C" moe_status moe_combine(const float* y, const int32_t* row_of_route, const float* w, int T, int k, int d,
                                   float* out, void* stream) {

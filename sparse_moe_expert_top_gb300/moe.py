@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_RANGE = range(6)
 MOE_F32, MOE_BF16 = 0, 1
-MOE_FUSED_AUTO, MOE_FUSED_GATHER, MOE_FUSED_COMPACT = 0, 1, 2
+MOE_FUSED_AUTO, MOE_FUSED_GATHER, MOE_FUSED_COMPACT, MOE_FUSED_NONE = 0, 1, 2, 3
 
 # (name, argtypes) of every exported entry point; the ABI test checks this
 # list against include/moe.h.
@@ -55,6 +55,7 @@ SIGNATURES = {
                          _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_tile_counts_size": ([_I, _I, _SZ], _I),
     "moe_scatter_index": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_route_scatter_small_fused": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gate_up_gather": ([_P, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_grouped_down_combine": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_forward_fused": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I,
@@ -417,6 +418,22 @@ def moe_scatter_index(ids, mask, offsets, d, row_of_route, route_of_row, tile_co
         _ptr(route_of_row), _ptr(tile_counts), _ptr(out), _ptr(ws), _stream(stream)))
 
 
+def moe_route_scatter_small_fused(logits, x, mask, k, bufs, gather: bool = True, stream=None):
+    """A1-A4 in one launch for a small chunk, with the fused combine's preparation (bf16 x); copies the
+    compact rows into ``bufs.xs`` only when ``gather`` is False."""
+    T, E = logits.shape
+    d = x.shape[1]
+    b = bufs
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _check("moe_route_scatter_small_fused", load().moe_route_scatter_small_fused(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets),
+        None if gather else _ptr(b.xs), _ptr(b.row_of_route), _ptr(b.route_of_row), _ptr(b.tile_counts),
+        _ptr(b.out), _stream(stream)))
+
+
 def moe_grouped_gate_up_gather(x, k, route_of_row, offsets, w_gate, w_up, h, stream=None):
     """A5 reading token rows of x through route_of_row (no compact copy)."""
     T, d = x.shape
@@ -455,8 +472,8 @@ def moe_grouped_down_combine(h, offsets, w_down, route_of_row, row_of_route, w, 
 def moe_forward_fused(logits, x, mask, w_gate, w_up, w_down, k: int, bufs: MoEBuffers, mode: int = MOE_FUSED_AUTO,
                       stream=None) -> torch.Tensor:
     """The whole path with the fused combine (bf16); returns ``bufs.out``.  ``mode``: MOE_FUSED_AUTO,
-    MOE_FUSED_GATHER (rows gathered by the gate/up kernel, ``bufs.xs`` unused) or MOE_FUSED_COMPACT.
-    ``bufs.y`` is scratch."""
+    MOE_FUSED_GATHER (rows gathered by the gate/up kernel, ``bufs.xs`` unused), MOE_FUSED_COMPACT or
+    MOE_FUSED_NONE (the unfused path).  ``bufs.y`` is scratch."""
     T, E = logits.shape
     d = x.shape[1]
     f = w_gate.shape[1]

@@ -38,7 +38,7 @@ def test_header_declares_the_path_entry_points():
                      "moe_quantize_weights_fp8", "moe_grouped_ffn_fp8", "moe_forward_fp8", "moe_scatter_rows_f16",
                      "moe_route_scatter_small", "moe_router_topk", "moe_scatter_index",
                      "moe_grouped_gate_up_gather", "moe_grouped_down_combine", "moe_forward_fused",
-                     "moe_tile_counts_size",
+                     "moe_tile_counts_size", "moe_route_scatter_small_fused",
                      "moe_workspace_size", "moe_check_device_error"):
         assert required in names
 
@@ -89,6 +89,8 @@ def test_host_only_calls(lib):
                                  None) == 1                                                       # x without xs
     assert lib.moe_grouped_gate_up_gather(None, 4, 2, None, None, 8, 100, 128, None, None, None, None) == 1  # d
     assert lib.moe_grouped_gate_up_gather(None, 4, 17, None, None, 8, 128, 128, None, None, None, None) == 1  # k
+    assert lib.moe_route_scatter_small_fused(None, None, None, 129, 8, 2, 128, None, None, None, None, None, None,
+                                             None, None, None, None) == 1                        # T > 128
     # y of the fused down projection must be 128-byte aligned (its L2 lines are dropped after use)
     bad_y = ctypes.c_void_p(4096 + 16)
     assert lib.moe_grouped_down_combine(fake, fake, 4, 2, 8, 128, 128, fake, fake, fake, fake, bad_y, fake, fake,

@@ -37,7 +37,7 @@ def _routing(T, E, k, seed, p_mask=0.0, skew=1.5):
     return logits, mask
 
 
-GATHER, COMPACT = M.MOE_FUSED_GATHER, M.MOE_FUSED_COMPACT
+GATHER, COMPACT, NONE = M.MOE_FUSED_GATHER, M.MOE_FUSED_COMPACT, M.MOE_FUSED_NONE
 
 
 def _both_paths(logits, x, mask, wg, wu, wd, k, mode=M.MOE_FUSED_AUTO):
@@ -77,7 +77,7 @@ FUSED_CASES = [
 ]
 
 
-@pytest.mark.parametrize("mode", [GATHER, COMPACT])
+@pytest.mark.parametrize("mode", [GATHER, COMPACT, NONE])
 @pytest.mark.parametrize("E,d,f,T,k,p", FUSED_CASES)
 def test_fused_path_equals_unfused_and_oracle(E, d, f, T, k, p, mode):
     logits, mask = _routing(T, E, k, seed=E * 7 + T, p_mask=p)
@@ -227,7 +227,7 @@ def test_down_combine_skips_work_on_inconsistent_offsets():
 @pytest.mark.slow
 @pytest.mark.parametrize("name,mode", [("verify_t4", M.MOE_FUSED_AUTO), ("prefill_t401", M.MOE_FUSED_AUTO),
                                        ("prefill_t2048", M.MOE_FUSED_AUTO), ("prefill_t2048", GATHER),
-                                       ("prefill_t8192", M.MOE_FUSED_AUTO)])
+                                       ("prefill_t8192", M.MOE_FUSED_AUTO), ("prefill_t8192", COMPACT)])
 def test_full_size_workload_fused(name, mode):
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, device="cuda")
@@ -250,3 +250,58 @@ def test_full_size_workload_fused(name, mode):
     ref = mo.token_outputs(tokens, ids, w, mask, to_np(inp["x"]),
                            oracle_weights(inp["w_gate"], inp["w_up"], inp["w_down"]))
     assert_close(out[tokens], ref, "bf16")
+
+
+@pytest.mark.parametrize("mode", [GATHER, COMPACT])
+def test_small_chunk_fused_routing_step_by_step(mode):
+    """moe_route_scatter_small_fused + the gate/up and fused down calls equal moe_forward_fused on a small chunk."""
+    E, d, f, T, k = 32, 256, 256, 40, 6
+    logits, mask = _routing(T, E, k, seed=31, p_mask=0.2)
+    mask[3] = 1                                   # one token with every slot masked
+    x = torch.randn(T, d).to(torch.bfloat16).cuda()
+    wg, wu, wd = (w.cuda() for w in _weights(E, d, f, seed=32))
+    m = mask.cuda()
+    b = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    whole = M.moe_forward_fused(logits.cuda(), x, m, wg, wu, wd, k, b, mode=mode).clone()
+    s = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    s.out.fill_(float("nan"))
+    s.tile_counts.fill_(3)
+    M.moe_route_scatter_small_fused(logits.cuda(), x, m, k, s, gather=(mode == GATHER))
+    if mode == GATHER:
+        M.moe_grouped_gate_up_gather(x, k, s.route_of_row, s.offsets, wg, wu, s.h)
+    else:
+        M.moe_grouped_gate_up(s.xs, s.offsets, wg, wu, s.h)
+    M.moe_grouped_down_combine(s.h, s.offsets, wd, s.route_of_row, s.row_of_route, s.w, s.y, s.tile_counts, s.out)
+    M.moe_check_device_error()
+    assert torch.equal(s.out.view(torch.int32), whole.view(torch.int32))
+    assert torch.all(s.out[3].view(torch.int32) == 0)
+    a = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    M.moe_forward(logits.cuda(), x, m, wg, wu, wd, k, a)
+    assert torch.equal(a.out.view(torch.int32), whole.view(torch.int32))
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_whole_path_is_capturable_in_a_cuda_graph(fused):
+    """No allocation, synchronisation or host read inside the path: a CUDA graph of one call replays it."""
+    E, d, f, T, k = 16, 256, 256, 300, 4
+    logits, mask = _routing(T, E, k, seed=41, p_mask=0.1)
+    x = torch.randn(T, d).to(torch.bfloat16).cuda()
+    wg, wu, wd = (w.cuda() for w in _weights(E, d, f, seed=42))
+    args = (logits.cuda(), x, mask.cuda(), wg, wu, wd, k)
+    fwd = M.moe_forward_fused if fused else M.moe_forward
+    b = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ref = fwd(*args, b).clone()            # warm-up call off the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fwd(*args, b)
+    b.out.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    M.moe_check_device_error()
+    assert torch.equal(b.out.view(torch.int32), ref.view(torch.int32))
