@@ -86,6 +86,23 @@ def test_algorithmic_work_counts_touched_experts_only():
     assert w["path_bytes"] == routing + scatter + w["gate_up_bytes"] + w["down_bytes"] + combine
 
 
+def test_algorithmic_work_of_the_fused_permutation():
+    """--fused: no combine pass and no y round trip; with the gather, x is read once instead of xs."""
+    counts = np.array([0, 3, 2])
+    T, E, k, d, f, es = 3, 3, 2, 128, 256, 2
+    plain = bench.algorithmic_work(counts, T, E, k, d, f, es)
+    compact = bench.algorithmic_work(counts, T, E, k, d, f, es, fused=True)
+    gather = bench.algorithmic_work(counts, T, E, k, d, f, es, fused=True, gather=True)
+    routing = 3 * 3 * 4 + 3 * 2 * 8
+    down = 2 * (128 * 256 * 2) + 5 * 256 * 2 + 3 * 128 * 4          # out written once, y not counted
+    assert compact["down_bytes"] == gather["down_bytes"] == down
+    assert compact["gate_up_bytes"] == plain["gate_up_bytes"]
+    assert gather["gate_up_bytes"] == 2 * (2 * 256 * 128 * 2) + 3 * 128 * 2 + 5 * 256 * 2
+    assert compact["path_bytes"] == routing + (3 * 128 * 2 + 5 * 128 * 2) + plain["gate_up_bytes"] + down
+    assert gather["path_bytes"] == routing + 3 * 2 * 8 + gather["gate_up_bytes"] + down
+    assert gather["flops"] == compact["flops"] == plain["flops"]
+
+
 def test_workload_overrides_for_profiling_cases():
     cfg = bench._workload("prefill_t2048", 0, tokens=128, experts=32)
     assert (cfg.T, cfg.E, cfg.d, cfg.f, cfg.k) == (128, 32, 4096, 2048, 6)
