@@ -595,7 +595,10 @@ __global__ void __launch_bounds__(256) scatter_index_kernel(const int32_t* __res
 // ---------------------------------------------------------------------------
 
 // CTA (t, c) combines float4 columns [c * chunk4, (c + 1) * chunk4) of token
-// t (one chunk spanning the row unless the chunk is small).
+// t (one chunk spanning the row unless the chunk is small); U float4 columns
+// per thread and pass (2 for wide rows; 1 keeps the registers, and so the
+// resident CTAs, of short rows).
+template <int U>
 __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__ y,
                                                       const int32_t* __restrict__ row_of_route,
                                                       const float* __restrict__ w, int k, int d4, int chunk4,
@@ -615,19 +618,49 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
     __syncthreads();
     float4* dst = out + static_cast<size_t>(t) * d4;
     const int v_end = min(d4, static_cast<int>(blockIdx.y + 1) * chunk4);
-    for (int v = static_cast<int>(blockIdx.y) * chunk4 + tid; v < v_end; v += blockDim.x) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < k; ++s) {
-            const int row = rows[s];
-            if (row < 0) continue;
-            const float4 yy = __ldg(y + static_cast<size_t>(row) * d4 + v);
-            const float ws = wt[s];
-            acc.x = fmaf(ws, yy.x, acc.x);
-            acc.y = fmaf(ws, yy.y, acc.y);
-            acc.z = fmaf(ws, yy.z, acc.z);
-            acc.w = fmaf(ws, yy.w, acc.w);
+    // U float4 columns per thread and pass; the loads of a group of slots are
+    // all in flight before the fixed-order sum (slots ascending from +0.0,
+    // masked slots skipped, as above)
+    constexpr int kGroup = 6;
+    const int step = blockDim.x;
+    for (int v0 = static_cast<int>(blockIdx.y) * chunk4 + tid; v0 < v_end; v0 += U * step) {
+        int vv[U];
+        bool in[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            in[u] = v0 + u * step < v_end;
+            vv[u] = in[u] ? v0 + u * step : v0;
         }
-        dst[v] = acc;
+        float4 acc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < k; s0 += kGroup) {
+            float4 yv[U][kGroup];
+#pragma unroll
+            for (int sl = 0; sl < kGroup; ++sl) {
+                const int row = s0 + sl < k ? rows[s0 + sl] : -1;
+                if (row >= 0) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) yv[u][sl] = __ldg(y + static_cast<size_t>(row) * d4 + vv[u]);
+                }
+            }
+#pragma unroll
+            for (int sl = 0; sl < kGroup; ++sl) {
+                if (s0 + sl < k && rows[s0 + sl] >= 0) {
+                    const float ws = wt[s0 + sl];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        acc[u].x = fmaf(ws, yv[u][sl].x, acc[u].x);
+                        acc[u].y = fmaf(ws, yv[u][sl].y, acc[u].y);
+                        acc[u].z = fmaf(ws, yv[u][sl].z, acc[u].z);
+                        acc[u].w = fmaf(ws, yv[u][sl].w, acc[u].w);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (in[u]) dst[vv[u]] = acc[u];
     }
 }
 
@@ -1058,7 +1091,9 @@ extern "C" moe_status moe_combine(const float* y, const int32_t* row_of_route, c
     const int d4 = d / 4;
     const int chunk4 = T < 2 * di.sm_count ? 128 : d4;
     const dim3 grid(T, (d4 + chunk4 - 1) / chunk4);
-    combine_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+    // two columns per thread once a CTA's span has at least 512 float4 (2 KB per thread pass)
+    auto kernel = chunk4 >= 512 ? combine_kernel<2> : combine_kernel<1>;
+    kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4*>(y), row_of_route, w, k, d4, chunk4, T * k, reinterpret_cast<float4*>(out),
         di.error_word);
     return launch_status();
