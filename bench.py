@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -293,11 +294,19 @@ def run_reference(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines: what the kernels are compiled from."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def _src_hash(*names):
+    """Hash of the kernel sources (comments ignored) that a stored ncu traffic record belongs to."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "sparse_moe_expert_top_gb300", "csrc", n), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "sparse_moe_expert_top_gb300", "csrc", n)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

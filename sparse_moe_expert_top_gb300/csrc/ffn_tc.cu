@@ -12,28 +12,32 @@
 // 2048), so the work is streaming the touched experts' weights from HBM.
 // The kernel therefore swaps the GEMM operands: the WEIGHT tile is the
 // M = 128 operand of tcgen05.mma and the expert's compact token rows form N
-// (a multiple of 16, at most 128 per work item).  Each weight byte is loaded
-// once per 128 rows, and an expert with 9 rows issues N = 16 MMAs instead of
-// padding 9 rows up to an M = 128 tile.  (The pages' adaptive tile width on
-// RDNA is the same idea.)
+// (a multiple of 16, at most 128 per work item, 256 in big-item mode).  Each
+// weight byte is loaded once per row slice, and an expert with 9 rows issues
+// N = 16 MMAs instead of padding 9 rows up to an M = 128 tile.  (The pages'
+// adaptive tile width on RDNA is the same idea.)
 //
 // Work item = (expert e, a slice mt of the output features -- 128 for
-// gate/up, 256 (two tiles) for down -- and a 128-row slice nt of the
-// expert's compact rows).  Chunks of at most 64 routes use narrow items
-// instead -- 64 features for gate/up (gate and up rows stacked in one MMA
-// tile), one 128-row tile for down -- so that a handful of tokens still gives
-// several waves of items.  Items are numbered expert-major,
-// then mt, then nt, so CTAs working at the same time on the nt slices of one
-// expert share its weight tile through L2.  The kernel is persistent: one
-// CTA per SM takes items blockIdx.x, blockIdx.x + gridDim.x, ...; every CTA
-// derives the same item table from `offsets` in its prologue, so ragged
-// per-expert row counts (including empty experts) need no host round trip.
+// gate/up, 256 (two tiles) for down -- and a slice nt of the expert's
+// compact rows: 128 rows, or 256 when most rows belong to heavy experts).
+// Chunks of at most 64 routes use narrow items instead -- 64 features for
+// gate/up (gate and up rows stacked in one MMA tile), one 128-row tile for
+// down -- so that a handful of tokens still gives several waves of items.
+// Items are numbered expert by expert (expert-id order; heaviest expert
+// first in the fused down kernel), then mt, then nt, so CTAs working at the
+// same time on the nt slices of one expert share its weight tile through L2.
+// The kernel is persistent: one CTA per SM takes items blockIdx.x,
+// blockIdx.x + gridDim.x, ...; every CTA derives the same item table from
+// `offsets` in its prologue, so ragged per-expert row counts (including empty
+// experts) need no host round trip.
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA loads into a ring of shared-
-// memory stages (128B-swizzled, 64 K-elements per stage); warp 1 lane 0
-// issues tcgen05.mma into a double-buffered TMEM accumulator (gate and up
-// accumulators side by side for the SwiGLU stage); warps 2-5 read the
-// accumulator with tcgen05.ld, apply SwiGLU (gate/up) and store rows.
+// Roles: warp 0 lane 0 issues TMA loads into a ring of shared-memory stages
+// (128B-swizzled, 64 K-elements per stage); warp 1 lane 0 issues
+// tcgen05.mma into a double-buffered TMEM accumulator (gate and up
+// accumulators side by side for the SwiGLU stage); the epilogue warps (4 for
+// gate/up, 8 for down) read the accumulator with tcgen05.ld, apply SwiGLU
+// (gate/up) and store rows; the fused instantiations add a row-gather warp
+// (gate/up) or four combine warps (down), below.
 // Every mbarrier wait is bounded: when it runs out the kernel records
 // DEVERR_TIMEOUT, lets its copies and MMAs drain, frees TMEM and returns.
 //
