@@ -173,16 +173,19 @@ __global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3, tw = lane >> 2;
     const unsigned quad = 0xfu << (lane & ~3);
     const int t = blockIdx.x * 32 + warp * 8 + tw;
-    const bool valid = t < T;
+    // every synchronisation below is among the four lanes of one token, so
+    // the quads of padding tokens past T leave at once (their -inf logits
+    // would all tie at tau and take the slow exact path)
+    if (t >= T) return;
     const int nvec = E >> 2;
 
     // this lane's 16 float4 groups (experts 4c .. 4c+3 for c = q + 4i)
     float4 f[16];
-    const float4* row = reinterpret_cast<const float4*>(logits + static_cast<size_t>(valid ? t : 0) * E);
+    const float4* row = reinterpret_cast<const float4*>(logits + static_cast<size_t>(t) * E);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const int c = q + 4 * i;
-        f[i] = (valid && c < nvec) ? __ldg(row + c) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        f[i] = c < nvec ? __ldg(row + c) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 
     // 1. tau: the k-th largest group maximum of the quad
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __
             const int ej = ce[j];
             int rank = 0;
             for (int i = 0; i < n_cand; ++i) rank += topk_beats(cv[i], ce[i], vj, ej) ? 1 : 0;
-            if (rank < k && valid) {
+            if (rank < k) {
                 ids[static_cast<size_t>(t) * k + rank] = ej;
                 sv[rank] = vj;
             }
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __
                 id[i] = nid[i];
             }
         }
-        if (q == 0 && valid) {
+        if (q == 0) {
 #pragma unroll
             for (int r = 0; r < KMAX; ++r)
                 if (r < k) {
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __
         }
     }
     __syncwarp(quad);
-    if (valid && q == 0) {
+    if (q == 0) {
         // softmax over the k selected logits, summed in slot order
         float sum = 0.f;
         for (int r = 0; r < k; ++r) sum += expf(sv[r] - sv[0]);
