@@ -74,6 +74,8 @@ FUSED_CASES = [
     (3, 384, 256, 150, 2, 0.0),    # d = 384: the last down feature slice holds a single tile
     (16, 512, 384, 20, 4, 0.1),    # T*k <= 64: narrow items
     (256, 256, 256, 4, 6, 0.0),    # a 4-token verification batch
+    (32, 256, 256, 150, 8, 0.1),   # k = 8: two slot groups in the combine warps
+    (32, 128, 128, 70, 16, 0.2),   # k = 16 (the largest k)
 ]
 
 
