@@ -10,8 +10,8 @@ Under torchrun each rank runs an independent replica on its own GPU with its
 own seed (no data-path collective); value = tokens of all ranks / the
 slowest rank's time.
 
---impl reference times the CPU oracle (float64, numpy) on the host cores on a
-bounded sample of the same workload, as the reference arm.
+--impl reference times the CPU oracle (C++, float64, OpenMP) on the host cores
+on a bounded sample of the same workload, as the reference arm.
 """
 
 from __future__ import annotations
@@ -179,36 +179,19 @@ def _workload(name: str, rank: int, tokens: int = 0, experts: int = 0):
 
 
 def _oracle_inputs(inp, tokens):
-    """Host (float64) copies of the inputs a token sample needs: its logits, rows, mask and experts.
-
-    With FP8 weights (inp["fp8"]) the oracle quantizes each sampled expert
-    itself and works on the dequantized values.
-    """
+    """Host copies of what the oracle needs for a token sample: its logits, rows and mask, and the expert
+    banks (bf16, read exactly by the oracle; with FP8 weights (inp["fp8"]) the oracle's own E4M3 codes and
+    per-channel scales of the bank).  The bank is copied (and quantized) once per run, outside any timing."""
     from oracle import moe_oracle as mo
-    cfg = inp["cfg"]
-    logits = inp["logits"].float().cpu().numpy()[tokens]
-    x = inp["x"].float().cpu().numpy()[tokens]
-    mask = None if inp["mask"] is None else inp["mask"].cpu().numpy()[tokens]
-    ids, _ = mo.route_topk(logits, cfg.k)
-    experts = sorted(set(ids.ravel().tolist()))
-
-    def host(t):
-        a = t.float().cpu().numpy()
-        return mo.dequantize_weights_fp8(*mo.quantize_weights_fp8(a)) if inp.get("fp8") else a
-
-    bank = {}
-    for e in experts:
-        bank[e] = tuple(host(t[e]) for t in (inp["w_gate"], inp["w_up"], inp["w_down"]))
-    zero = None
-    def get(e):
-        nonlocal zero
-        if e in bank:
-            return bank[e]
-        if zero is None:
-            zero = (np.zeros((cfg.f, cfg.d), np.float32), np.zeros((cfg.f, cfg.d), np.float32),
-                    np.zeros((cfg.d, cfg.f), np.float32))
-        return zero
-    return logits, x, mask, get
+    logits = inp["logits"].cpu()[tokens]
+    x = inp["x"].cpu()[tokens]
+    mask = None if inp["mask"] is None else inp["mask"].cpu()[tokens]
+    if "_oracle_bank" not in inp:
+        bank = tuple(inp[n].cpu() for n in ("w_gate", "w_up", "w_down"))
+        if inp.get("fp8"):
+            bank = tuple(mo.quantize_bank_fp8(b) for b in bank)
+        inp["_oracle_bank"] = bank
+    return logits, x, mask, inp["_oracle_bank"]
 
 
 def _time_oracle(inp, n_tokens: int):
@@ -219,18 +202,23 @@ def _time_oracle(inp, n_tokens: int):
     if n_tokens not in cache:
         cache.clear()
         cache[n_tokens] = _oracle_inputs(inp, list(range(n_tokens)))
-    logits, x, mask, get = cache[n_tokens]
+    logits, x, mask, bank = cache[n_tokens]
     t0 = time.perf_counter()
-    mo.moe_forward(logits, x, get, cfg.k, mask)
+    mo.moe_forward(logits, x, bank, cfg.k, mask)
     return time.perf_counter() - t0
+
+
+def _oracle_threads():
+    from oracle import moe_oracle as mo
+    return mo.threads()
 
 
 def _size_oracle_sample(inp, budget_s: float):
     """Tokens of the oracle sample: sized from a 1-token run, then refined (the
     per-token cost falls as the sampled tokens share experts).
 
-    The host copy of the sampled experts is bounded by the bank itself
-    (at most E experts, 3*d*f fp32 values each).
+    The oracle reads the host copy of the bank (bf16, or its FP8 codes):
+    one copy per run.
     """
     T = inp["cfg"].T
     t1 = _time_oracle(inp, 1)
@@ -278,7 +266,7 @@ def run_reference(args, rank: int, world: int):
     for _ in range(args.steps):
         total += _time_oracle(inp, n)
     value = n * args.steps / total
-    cores = os.cpu_count()
+    cores = _oracle_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
@@ -287,7 +275,8 @@ def run_reference(args, rank: int, world: int):
                    "weights": "fp8_e4m3 codes + fp32 per-channel scales (quantized by the oracle)"
                    if inp["fp8"] else "as drawn"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"first {n} tokens of the {cfg.T}-token chunk per step (numpy float64)",
+                         "sample": f"first {n} tokens of the {cfg.T}-token chunk per step (C++ oracle, float64, "
+                                   f"OpenMP over {cores} threads)",
                          "cpu": _cpu_desc()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -512,22 +501,26 @@ def run_ours(args, rank: int, world: int):
     # timed region: the whole path per step; CUDA events around the dominant
     # kernel (grouped gate/up) on its stream give its live launch duration
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # step boundaries: bnd[s] .. bnd[s+1] is step s; bnd[0] .. bnd[-1] the whole timed region
+    bnd = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.mark(True)
-    start.record()
+    bnd[0].record()
     for s in range(args.steps):
         step(ev[s])
-    end.record()
+        bnd[s + 1].record()
     torch.cuda.synchronize()
     clocks.mark(False)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     M.moe_check_device_error()
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    elapsed_ms = max_over_ranks(bnd[0].elapsed_time(bnd[-1]), world, dev)
+    step_ms = [bnd[s].elapsed_time(bnd[s + 1]) for s in range(args.steps)]
+    step_median = statistics.median(step_ms)
+    step_mad = statistics.median(abs(t - step_median) for t in step_ms)
     gu_ms = statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps))
 
     # per-kernel breakdown: a separate loop after the timed region, with events around every call
@@ -582,13 +575,16 @@ def run_ours(args, rank: int, world: int):
     if not args.no_cpu_baseline and not args.router:
         n, _ = _size_oracle_sample(inp, args.cpu_budget_s)
         secs = _time_oracle(inp, n)
-        cpu = {"value": n / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"first {n} of {T} tokens, whole path in float64 (numpy, BLAS on all cores), "
-                         f"{secs:.1f} s", "cpu": _cpu_desc()}
+        cores = _oracle_threads()
+        cpu = {"value": n / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {n} of {T} tokens, whole path in float64 (C++ oracle, OpenMP over {cores} "
+                         f"threads), {secs:.1f} s", "cpu": _cpu_desc()}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": step_median, "ms_per_step_mad": step_mad,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32", "data": "synthetic",
         "config": {"workload": cfg.name, "T": T, "d": d, "f": f, "E": E, "k": k, "mask_p": cfg.mask_p,
                    "routes_unmasked": R, "experts_touched": touched,

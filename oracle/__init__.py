@@ -1,4 +1,4 @@
-"""CPU oracle of grouped MoE prefill (test infrastructure; see moe_oracle)."""
+"""CPU oracle of grouped MoE prefill (test infrastructure): C++ in moe_oracle.cpp, marshalled by moe_oracle."""
 
 from . import moe_oracle
 

@@ -88,33 +88,42 @@ def assert_close_f16_rounded(got, ref):
     return st
 
 
-def oracle_weights(w_gate, w_up, w_down):
-    """Oracle view of (possibly bf16, possibly CUDA) weight banks: fetch one expert at a time."""
-    cache = {}
-
-    def get(e):
-        if e not in cache:
-            cache.clear()
-            cache[e] = (to_np(w_gate[e]), to_np(w_up[e]), to_np(w_down[e]))
-        return cache[e]
-
-    return get
-
-
-def oracle_weights_fp8(w_gate, w_up, w_down):
-    """Oracle view of FP8 expert weights: the oracle quantizes each expert of
-    the (bf16 or fp32) banks itself and hands back the dequantized values."""
+def oracle_weights(w_gate, w_up, w_down, fp8=False, check_codes=None):
+    """The oracle's view of expert banks that may live on the GPU: fetch(e0, e1) copies experts e0 .. e1-1
+    to host memory (bf16 read exactly by the oracle).  With fp8 the oracle quantizes each block itself
+    (FP8 E4M3 codes + per-channel scales) and works on the values the codes stand for; check_codes, if
+    given, is called as check_codes(e0, e1, banks) with the oracle's quantized banks of the block."""
     from oracle import moe_oracle as mo
-    cache = {}
 
-    def deq(w):
-        codes, scales = mo.quantize_weights_fp8(to_np(w).astype(np.float32))
-        return mo.dequantize_weights_fp8(codes, scales)
+    def fetch(e0, e1):
+        banks = tuple(None if w is None else w[e0:e1].detach().cpu() for w in (w_gate, w_up, w_down))
+        if fp8:
+            banks = tuple(None if b is None else mo.quantize_bank_fp8(b) for b in banks)
+            if check_codes is not None:
+                check_codes(e0, e1, banks)
+        return banks
 
-    def get(e):
-        if e not in cache:
-            cache.clear()
-            cache[e] = (deq(w_gate[e]), deq(w_up[e]), deq(w_down[e]))
-        return cache[e]
+    return fetch
 
-    return get
+
+# full-size oracle results, computed once per workload and test session
+_FULL_SIZE = {}
+
+
+def full_size_reference(inp, fp8=False, check_codes=None):
+    """The oracle's moe_forward of a full-size workload (ids, w, counts, offsets, the permutation, h, out).
+
+    The weight bank is fetched 16 experts at a time from wherever it lives.  Results are cached per
+    (workload, weight format) for the session; xs and y are dropped to bound host memory.
+    """
+    from oracle import moe_oracle as mo
+    cfg = inp["cfg"]
+    key = (cfg.name, cfg.seed, fp8)
+    if key not in _FULL_SIZE:
+        mask = None if inp["mask"] is None else inp["mask"].cpu()
+        res = mo.moe_forward(inp["logits"].cpu(), inp["x"].cpu(),
+                             oracle_weights(inp["w_gate"], inp["w_up"], inp["w_down"], fp8, check_codes),
+                             cfg.k, mask)
+        del res["xs"], res["y"]
+        _FULL_SIZE[key] = res
+    return _FULL_SIZE[key]

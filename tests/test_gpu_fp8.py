@@ -14,7 +14,7 @@ import torch
 
 from oracle import moe_oracle as mo
 from sparse_moe_expert_top_gb300 import moe as M
-from tests.helpers import assert_close, assert_close_f16_rounded, oracle_weights_fp8, to_np
+from tests.helpers import assert_close, assert_close_f16_rounded, full_size_reference, to_np
 from workloads import CONFIGS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -177,25 +177,30 @@ def test_fp8_inconsistent_offsets_are_rejected_on_the_device():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["prefill_t401", "prefill_t2048"])
+@pytest.mark.parametrize("name", ["verify_t4", "prefill_t401", "prefill_t2048", "prefill_t8192"])
 def test_fp8_full_size_workload(name):
+    """Every FP8 code and scale of the bank bit for bit against the oracle's quantizer; h on every compact row
+    within its fp16 rounding bound and out on every token within the bf16 tolerance, against the oracle on
+    the values the codes stand for."""
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, device="cuda")
     qg, qu, qd = (M.moe_quantize_weights_fp8(inp[n]) for n in ("w_gate", "w_up", "w_down"))
     bufs = M.MoEBuffers(cfg.T, cfg.E, cfg.k, cfg.d, cfg.f, torch.float16)
+    bufs.h.fill_(float("nan"))
     out = M.moe_forward_fp8(inp["logits"], inp["x"], inp["mask"], qg, qu, qd, cfg.k, bufs)
     M.moe_check_device_error()
-    mask = None if inp["mask"] is None else to_np(inp["mask"])
-    ids, w = mo.route_topk(to_np(inp["logits"]), cfg.k)
-    assert np.array_equal(to_np(bufs.ids), ids)
-    rng = np.random.default_rng(cfg.seed + 1)
-    tokens = sorted(set([0, cfg.T - 1] + rng.choice(cfg.T, size=2, replace=False).tolist()))
-    # the codes of the experts these tokens use are the oracle's
-    for e in sorted(set(ids[tokens].ravel().tolist()))[:4]:
-        for name_w, q in (("w_gate", qg), ("w_down", qd)):
-            codes, scales = _oracle_quant(inp[name_w][e])
-            assert np.array_equal(to_np(q.codes[e]), codes)
-            assert np.array_equal(to_np(q.scales[e]), scales)
-    ref = mo.token_outputs(tokens, ids, w, mask, to_np(inp["x"]),
-                           oracle_weights_fp8(inp["w_gate"], inp["w_up"], inp["w_down"]))
-    assert_close(out[tokens], ref, "bf16")
+    checked = []
+
+    def check_codes(e0, e1, banks):
+        for q, ob in zip((qg, qu, qd), banks):
+            assert np.array_equal(to_np(q.codes[e0:e1]), ob.codes)
+            assert np.array_equal(to_np(q.scales[e0:e1]), ob.scales)
+        checked.append((e0, e1))
+
+    ref = full_size_reference(inp, fp8=True, check_codes=check_codes)
+    assert checked, "the oracle visited no expert block"
+    for key in ("ids", "counts", "offsets", "row_of_route", "route_of_row"):
+        assert np.array_equal(to_np(getattr(bufs, key)), ref[key]), key
+    R = int(ref["offsets"][-1])
+    assert_close_f16_rounded(bufs.h[:R], ref["h"])
+    assert_close(out, ref["out"], "bf16")

@@ -16,7 +16,7 @@ import torch
 
 from oracle import moe_oracle as mo
 from sparse_moe_expert_top_gb300 import moe as M
-from tests.helpers import assert_close, assert_close_bf16_rounded, oracle_weights, to_np
+from tests.helpers import assert_close, assert_close_bf16_rounded, full_size_reference, to_np
 from workloads import CONFIGS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -151,11 +151,9 @@ def test_wide_ffn_many_rows_per_expert():
     wg, wu, wd = _weights(E, d, f, seed=4)
     a, b = _both_paths(logits, x, mask, wg, wu, wd, k)
     _assert_fused_equals_unfused(a, b)
-    tokens = [0, 1, 777, 2048, T - 1]
-    ids, w = mo.route_topk(logits.numpy(), k)
-    assert np.array_equal(to_np(b.ids), ids)
-    ref = mo.token_outputs(tokens, ids, w, mask.numpy(), to_np(x), oracle_weights(wg, wu, wd))
-    assert_close(b.out[tokens], ref, "bf16")
+    ref = mo.moe_forward(logits.numpy(), to_np(x), (wg, wu, wd), k, mask.numpy())
+    assert np.array_equal(to_np(b.ids), ref["ids"])
+    assert_close(b.out, ref["out"], "bf16")
 
 
 @pytest.mark.parametrize("mode", [GATHER, COMPACT])
@@ -222,8 +220,9 @@ def test_down_combine_skips_work_on_inconsistent_offsets():
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads: equal to the unfused path bit for bit; index outputs
-# checked completely against the oracle, the output on sampled tokens
+# full-size workloads: equal to the unfused path bit for bit; every output
+# checked against the oracle (index outputs bit for bit, h on every compact
+# row, out on every token)
 # ---------------------------------------------------------------------------
 
 @pytest.mark.slow
@@ -241,17 +240,12 @@ def test_full_size_workload_fused(name, mode):
     out = M.moe_forward_fused(*args, b, mode=mode)
     M.moe_check_device_error()
     _assert_fused_equals_unfused(a, b)
-    mask = None if inp["mask"] is None else to_np(inp["mask"])
-    ids, w = mo.route_topk(to_np(inp["logits"]), cfg.k)
-    assert np.array_equal(to_np(b.ids), ids)
-    ror, rro = mo.scatter_permutation(ids, mask)
-    assert np.array_equal(to_np(b.row_of_route), ror)
-    assert np.array_equal(to_np(b.route_of_row), rro)
-    rng = np.random.default_rng(cfg.seed + 1)
-    tokens = sorted(set([0, cfg.T - 1] + rng.choice(cfg.T, size=min(cfg.T, 6), replace=False).tolist()))
-    ref = mo.token_outputs(tokens, ids, w, mask, to_np(inp["x"]),
-                           oracle_weights(inp["w_gate"], inp["w_up"], inp["w_down"]))
-    assert_close(out[tokens], ref, "bf16")
+    ref = full_size_reference(inp)
+    for key in ("ids", "counts", "offsets", "row_of_route", "route_of_row"):
+        assert np.array_equal(to_np(getattr(b, key)), ref[key]), key
+    R = int(ref["offsets"][-1])
+    assert_close_bf16_rounded(b.h[:R], ref["h"])
+    assert_close(out, ref["out"], "bf16")
 
 
 @pytest.mark.parametrize("mode", [GATHER, COMPACT])

@@ -76,3 +76,25 @@ def test_quantize_reads_float32_quotients():
     codes, scales = mo.quantize_weights_fp8(w)
     expect_q = mo.e4m3_round((w / scales[:, None]).astype(np.float32))
     np.testing.assert_array_equal(mo.e4m3_decode(codes), expect_q)
+
+
+def test_quantized_bank_ffn_is_the_dequantized_ffn():
+    """The FFN on a bank of E4M3 codes + row scales is the dense SwiGLU FFN on the weights those codes stand
+    for, decoded here by PyTorch's float8_e4m3fn (an implementation independent of the oracle's decoder)."""
+    rng = np.random.default_rng(2)
+    n, d, f = 5, 32, 48
+    x = rng.standard_normal((n, d))
+    banks = [(rng.standard_normal((1, f, d)) / d ** 0.5).astype(np.float32),
+             (rng.standard_normal((1, f, d)) / d ** 0.5).astype(np.float32),
+             (rng.standard_normal((1, d, f)) / f ** 0.5).astype(np.float32)]
+    q = [mo.quantize_bank_fp8(b) for b in banks]
+
+    def torch_dequant(qb):
+        vals = torch.from_numpy(qb.codes).view(torch.float8_e4m3fn).to(torch.float64)
+        return vals * torch.from_numpy(qb.scales).to(torch.float64)[..., None]
+
+    wg, wu, wd = (torch_dequant(b)[0] for b in q)
+    xt = torch.from_numpy(x)
+    ref = torch.nn.functional.linear(torch.nn.functional.silu(xt @ wg.T) * (xt @ wu.T), wd).numpy()
+    got = mo.grouped_ffn(x, np.array([0, n], dtype=np.int32), tuple(q))
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)

@@ -246,17 +246,31 @@ def test_masked_expert_never_touched():
     assert not np.allclose(clean, full["out"])
 
 
-def test_token_outputs_agree_with_forward():
+def test_expert_blocks_and_row_blocks_change_no_bit(monkeypatch):
+    """A bank fetched a block of experts at a time, and rows evaluated one at a time instead of four per
+    pass, give the same output bit for bit (every dot product is the same ascending sum)."""
     rng = np.random.default_rng(14)
-    T, d, f, E, k = 12, 5, 9, 6, 3
+    T, d, f, E, k = 23, 5, 9, 6, 3
     x = rng.standard_normal((T, d))
     w = (rng.standard_normal((E, f, d)), rng.standard_normal((E, f, d)), rng.standard_normal((E, d, f)))
     logits = rng.standard_normal((T, E)).astype(np.float32)
     mask = (rng.random((T, k)) < 0.3).astype(np.uint8)
-    res = mo.moe_forward(logits, x, w, k, mask)
-    tok = [0, 5, 11]
-    got = mo.token_outputs(tok, res["ids"], res["w"], mask, x, lambda e: (w[0][e], w[1][e], w[2][e]))
-    np.testing.assert_allclose(got, res["out"][tok], rtol=1e-13, atol=1e-13)
+    whole = mo.moe_forward(logits, x, w, k, mask)
+    monkeypatch.setattr(mo, "EXPERT_BLOCK", 4)
+    fetched = []
+
+    def fetch(e0, e1):
+        fetched.append((e0, e1))
+        return w[0][e0:e1], w[1][e0:e1], w[2][e0:e1]
+
+    blocked = mo.moe_forward(logits, x, fetch, k, mask)
+    assert set(fetched) <= {(0, 4), (4, 6)} and len(fetched) >= 2
+    assert np.array_equal(blocked["out"], whole["out"])
+    # one row at a time through the same grouped call
+    xs, off = whole["xs"], whole["offsets"]
+    rows = np.concatenate([mo.expert_ffn(xs[i:i + 1], w[0][e], w[1][e], w[2][e])
+                           for e in range(E) for i in range(off[e], off[e + 1])])
+    assert np.array_equal(rows, whole["y"])
 
 
 def test_silu_closed_forms():
