@@ -44,7 +44,10 @@
  *   reports and clears it.
  * - The calls keep no host state between calls apart from a per-device
  *   cache (SM count, kernel attributes, the address of the device error
- *   word); they are safe to call from several host threads.
+ *   word); they are safe to call from several host threads.  Device
+ *   addresses in the cache are tied to the CUDA context they were looked up
+ *   in and are looked up again when another context is current (after
+ *   cudaDeviceReset, for instance).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -154,9 +157,11 @@ moe_status moe_route_histogram(const int32_t* ids, const uint8_t* mask, int T, i
  * the library keeps it until the process exits.
  *   Limit: T*k <= 65536 routes; a larger chunk returns MOE_ERR_INVALID_ARG
  *   without enqueuing anything.
- *   The first call on a device looks up the array's device address (once
- *   per device, with that device current): make that first call before any
- *   stream capture.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current) and caches it for the CUDA context that is current;
+ *   when another context is current later (after cudaDeviceReset, say) the
+ *   next call looks it up again.  Make the first call before any stream
+ *   capture.
  *   Every call on a device shares the one array and it keeps the previous
  *   call's contents; the call clears what must start at zero itself.  Calls
  *   that can overlap on the GPU (other streams, other host threads) race and

@@ -2,6 +2,7 @@
 // grouped FFN dispatch and the whole-path convenience call.
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -17,8 +18,13 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 bool g_ready[kMaxDevices];
+unsigned long long g_context[kMaxDevices];   // context the cached device addresses belong to
 DeviceInfo g_info[kMaxDevices];
 thread_local int g_last_cuda_error = 0;
+
+std::once_flag g_ctx_fn_once;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
 
 }  // namespace
 
@@ -28,10 +34,33 @@ moe_status cuda_status(cudaError_t err) {
     return MOE_ERR_CUDA;
 }
 
+moe_status current_context_id(unsigned long long* id) {
+    std::call_once(g_ctx_fn_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return MOE_ERR_UNSUPPORTED;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return cuda_status(cudaErrorUnknown);
+    *id = 0;
+    if (ctx != nullptr && g_ctx_get_id(ctx, id) != CUDA_SUCCESS) return cuda_status(cudaErrorUnknown);
+    return MOE_OK;
+}
+
 moe_status device_info(DeviceInfo* info) {
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    unsigned long long ctx = 0;
+    moe_status st = current_context_id(&ctx);
+    if (st != MOE_OK) return st;
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_ready[dev]) {
         DeviceInfo di{};
@@ -40,11 +69,19 @@ moe_status device_info(DeviceInfo* info) {
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev));
         if (di.cc_major != 10 || di.cc_minor != 3) return MOE_ERR_UNSUPPORTED;
-        void* p = nullptr;
-        MOE_CUDA_TRY(cudaGetSymbolAddress(&p, g_moe_device_error));
-        di.error_word = static_cast<unsigned*>(p);
         g_info[dev] = di;
         g_ready[dev] = true;
+    }
+    // A device address belongs to one context: after cudaDeviceReset the
+    // runtime makes a new primary context and loads the module again, so the
+    // address is looked up again whenever the current context is another one
+    // (or none was current yet: the lookup itself makes the primary context).
+    if (ctx == 0 || g_context[dev] != ctx) {
+        void* p = nullptr;
+        MOE_CUDA_TRY(cudaGetSymbolAddress(&p, g_moe_device_error));
+        if ((st = current_context_id(&ctx)) != MOE_OK) return st;
+        g_info[dev].error_word = static_cast<unsigned*>(p);
+        g_context[dev] = ctx;
     }
     *info = g_info[dev];
     return MOE_OK;

@@ -65,7 +65,12 @@ struct DeviceInfo {
 };
 
 // Per-device cache; returns MOE_OK and fills *info for the current device.
+// The device addresses in it are those of the current CUDA context.
 moe_status device_info(DeviceInfo* info);
+
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), 0
+// when no context is current yet.
+moe_status current_context_id(unsigned long long* id);
 
 // Records `err` as this thread's last CUDA error and returns MOE_ERR_CUDA
 // (or MOE_OK when err == cudaSuccess).

@@ -859,20 +859,29 @@ namespace {
 
 std::mutex g_noalloc_mutex;
 int32_t* g_noalloc_scratch[64];
+unsigned long long g_noalloc_context[64];   // context the cached address belongs to
 
 // Device address of g_noalloc_hist_scratch on the current device.  In host
 // code the array's name is only a host-side stand-in, so the address is
-// looked up once per device (with that device current) and cached.
+// looked up (with the device current) and cached per device, together with
+// the id of the CUDA context it belongs to: when another context is current
+// (after cudaDeviceReset the runtime makes a new primary context and loads
+// the module again) the address is looked up again.
 moe_status noalloc_scratch(int32_t** out) {
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    unsigned long long ctx = 0;
+    moe_status st = current_context_id(&ctx);
+    if (st != MOE_OK) return st;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_scratch[dev] == nullptr) {
+    if (g_noalloc_scratch[dev] == nullptr || ctx == 0 || g_noalloc_context[dev] != ctx) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_hist_scratch);
         if (e != cudaSuccess) return cuda_status(e);
+        if ((st = current_context_id(&ctx)) != MOE_OK) return st;
         g_noalloc_scratch[dev] = static_cast<int32_t*>(p);
+        g_noalloc_context[dev] = ctx;
     }
     *out = g_noalloc_scratch[dev];
     return MOE_OK;

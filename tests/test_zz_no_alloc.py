@@ -5,12 +5,15 @@ memory (for instance code inside a host framework that owns every device
 allocation and passes no workspace).  Its scratch is a static device array
 inside the library, shared by every call; these tests call it through the
 C-ABI twice in a row and compare with moe_route_histogram, whose scratch is
-the caller's workspace.  Counts are integers, so the comparison is exact.
+the caller's workspace, and with the CPU oracle's histogram of the same
+routes.  Counts are integers, so the comparisons are exact.
 """
 
+import numpy as np
 import pytest
 import torch
 
+from oracle import moe_oracle as mo
 from sparse_moe_expert_top_gb300 import moe as M
 
 pytestmark = pytest.mark.gpu
@@ -33,11 +36,14 @@ def test_noalloc_histogram_matches_workspace_histogram(T, E, k, p):
     ref = torch.empty(E, dtype=torch.int32, device="cuda")
     ws = torch.zeros(M.moe_workspace_size(T, k) // 4 + 4, dtype=torch.int32, device="cuda")
     M.moe_route_histogram(ids, mask, E, ref, ws)
+    oracle_counts = mo.route_histogram(ids.cpu(), None if mask is None else mask.cpu(), E)
+    assert np.array_equal(ref.cpu().numpy(), oracle_counts)
     for _ in range(2):  # two calls in a row share the static scratch
         got = torch.full((E,), -1, dtype=torch.int32, device="cuda")
         M.moe_route_histogram_noalloc(ids, mask, E, got)
         M.moe_check_device_error()
         assert torch.equal(got, ref)
+        assert np.array_equal(got.cpu().numpy(), oracle_counts)
 
 
 def test_noalloc_histogram_rejects_chunks_beyond_its_scratch():
