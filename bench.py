@@ -136,7 +136,7 @@ def max_over_ranks(value: float, world: int, device) -> float:
 
 
 def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp8: bool = False,
-                     fused: bool = False, gather: bool = False) -> dict:
+                     fused: bool = False, gather: bool = False, w8a8: bool = False) -> dict:
     """Algorithmic bytes and FLOPs of one step, from the realised expert counts.
 
     Only touched experts' weights count; activations are counted once per
@@ -149,6 +149,18 @@ def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp
     counts = np.asarray(counts)
     R = int(counts.sum())
     touched = int(np.count_nonzero(counts))
+    if w8a8:
+        # E4M3 weights (codes + channel scales) and E4M3 activations (codes + row scales); h is written in
+        # bf16, read back by its quantizer, and read by the down kernel as codes
+        wgu, wdn = touched * 2 * f * (d + 4), touched * d * (f + 4)
+        gate_up = wgu + R * (d + 4) + R * f * 2
+        down = wdn + R * (f + 4) + R * d * 4
+        quant = T * d * 2 + T * (d + 4) + R * f * 2 + R * (f + 4)
+        scatter = T * d + R * (d + 4)
+        routing = T * E * 4 + T * k * 8
+        combine = R * d * 4 + T * d * 4
+        return {"R": R, "touched": touched, "gate_up_bytes": gate_up, "down_bytes": down,
+                "path_bytes": routing + quant + scatter + gate_up + down + combine, "flops": 6.0 * R * d * f}
     wgu = touched * 2 * f * (d + 4) if fp8 else touched * 2 * f * d * es
     wdn = touched * d * (f + 4) if fp8 else touched * d * f * es
     gate_up = wgu + R * d * es + R * f * es
@@ -203,8 +215,9 @@ def _time_oracle(inp, n_tokens: int):
         cache.clear()
         cache[n_tokens] = _oracle_inputs(inp, list(range(n_tokens)))
     logits, x, mask, bank = cache[n_tokens]
+    forward = mo.moe_forward_w8a8 if inp.get("w8a8") else mo.moe_forward
     t0 = time.perf_counter()
-    mo.moe_forward(logits, x, bank, cfg.k, mask)
+    forward(logits, x, bank, cfg.k, mask)
     return time.perf_counter() - t0
 
 
@@ -257,7 +270,8 @@ def run_reference(args, rank: int, world: int):
     cfg = _workload(args.workload, 0, args.tokens, args.experts)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(cfg, device="cpu", weights_device=dev)
-    inp["fp8"] = args.weights == "fp8"
+    inp["fp8"] = args.weights in ("fp8", "w8a8")
+    inp["w8a8"] = args.weights == "w8a8"
     per_step_budget = max(0.05, args.reference_budget_s / max(1, args.steps + args.warmup))
     n, _ = _size_oracle_sample(inp, per_step_budget)
     for _ in range(args.warmup):
@@ -390,13 +404,23 @@ def run_ours(args, rank: int, world: int):
     T, E, k, d, f = cfg.T, cfg.E, cfg.k, cfg.d, cfg.f
     dtype = inp["x"].dtype
     fp8 = args.weights == "fp8"
+    w8a8 = args.weights == "w8a8"
     fused = args.fused
-    if fused and (fp8 or args.router or dtype != torch.bfloat16):
+    if fused and (fp8 or w8a8 or args.router or dtype != torch.bfloat16):
         raise SystemExit("--fused runs the bf16 path with the workload's logits")
+    if w8a8 and (args.router or dtype != torch.bfloat16):
+        raise SystemExit("--weights w8a8 runs the bf16 workloads with their logits")
     # the FP8-weight path keeps its compact activations (xs, h) in fp16
-    bufs = M.MoEBuffers(T, E, k, d, f, torch.float16 if fp8 else dtype, device=dev)
+    bufs = (M.MoEBuffersW8A8(T, E, k, d, f, device=dev) if w8a8 else
+            M.MoEBuffers(T, E, k, d, f, torch.float16 if fp8 else dtype, device=dev))
     logits, x, mask = inp["logits"], inp["x"], inp["mask"]
-    if fp8:
+    if w8a8:
+        # load-time step, outside the timed region: E4M3 codes + per-channel scales
+        inp["fp8"] = inp["w8a8"] = True
+        wg, wu, wd = (M.moe_quantize_weights_fp8(inp[n]) for n in ("w_gate", "w_up", "w_down"))
+        torch.cuda.synchronize()
+        forward = M.moe_forward_w8a8
+    elif fp8:
         if dtype != torch.bfloat16:
             raise SystemExit("--weights fp8 needs a bf16 workload")
         # load-time step, outside the timed region: FP8 E4M3 codes + per-channel scales
@@ -413,28 +437,30 @@ def run_ours(args, rank: int, world: int):
     b = bufs
     # every call is marshalled once (M.bind); the timed loop replays the C calls.
     # Small chunks take A1-A4 in one launch, as moe_forward does.
-    small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES and not args.router
+    small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES and not args.router and not w8a8
     # fused: moe_forward_fused's automatic choice -- gather the token rows in
     # the gate/up kernel while experts get few rows, else the compact copy;
     # the combine in the down kernel while y fits in twice the L2, else the
     # unfused path
     if fused and args.fused_mode == "auto":
-        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        args.fused_mode = "gather" if T * k <= 16 * E else ("compact" if T * k * d * 4 <= 2 * l2 else "none")
+        args.fused_mode = {M.MOE_FUSED_GATHER: "gather", M.MOE_FUSED_COMPACT: "compact",
+                           M.MOE_FUSED_NONE: "none"}[M.moe_forward_fused_mode(T, E, k, d)]
     if args.fused_mode == "none":
         fused = False
     gather = fused and args.fused_mode == "gather"
     small = small and not fused
-    if fused and T <= SMALL_TOKENS and T * k <= SMALL_ROUTES:
+    if w8a8:
+        # E4M3 activations: the token rows and h quantized per row, E4M3 x E4M3 tensor-core MMAs
+        names = ("route", "quantize_x", "scatter", "gate_up", "quantize_h", "down", "combine")
+        routing = []
+    elif fused and T <= SMALL_TOKENS and T * k <= SMALL_ROUTES:
         names = ("route_scatter_small", "gate_up", "down_combine")
         routing = [M.bind(M.moe_route_scatter_small_fused, logits, x, mask, k, b, gather)]
     elif fused:
         # the combine runs inside the down kernel
-        names = ("topk", "histogram", "prefix", "scatter_index", "gate_up", "down_combine")
+        names = ("route", "scatter_index", "gate_up", "down_combine")
         routing = [
-            M.bind(M.moe_route_topk, logits, k, b.ids, b.w),
-            M.bind(M.moe_route_histogram, b.ids, mask, E, b.counts, b.ws),
-            M.bind(M.moe_prefix_offsets, b.counts, T, k, b.offsets, b.ws),
+            M.bind(M.moe_route_topk_offsets, logits, mask, k, b.ids, b.w, b.counts, b.offsets, b.ws),
             M.bind(M.moe_scatter_index, b.ids, mask, b.offsets, d, b.row_of_route, b.route_of_row, b.tile_counts,
                    b.out, b.ws, None if gather else x, None if gather else b.xs),
         ]
@@ -455,11 +481,10 @@ def run_ours(args, rank: int, world: int):
         names = ("route_scatter_small", "gate_up", "down", "combine")
         routing = [M.bind(M.moe_route_scatter_small, logits, x, mask, k, b)]
     else:
-        names = ("topk", "histogram", "prefix", "scatter", "gate_up", "down", "combine")
+        # A1-A3 in one launch (moe_route_topk_offsets), then the scatter
+        names = ("route", "scatter", "gate_up", "down", "combine")
         routing = [
-            M.bind(M.moe_route_topk, logits, k, b.ids, b.w),
-            M.bind(M.moe_route_histogram, b.ids, mask, E, b.counts, b.ws),
-            M.bind(M.moe_prefix_offsets, b.counts, T, k, b.offsets, b.ws),
+            M.bind(M.moe_route_topk_offsets, logits, mask, k, b.ids, b.w, b.counts, b.offsets, b.ws),
             M.bind(scatter_call, x, b.ids, mask, b.offsets, b.xs, b.row_of_route, b.route_of_row, b.ws),
         ]
     GU = names.index("gate_up")
@@ -475,12 +500,34 @@ def run_ours(args, rank: int, world: int):
             M.bind(M.moe_grouped_down_combine, b.h, b.offsets, wd, b.route_of_row, b.row_of_route, b.w, b.y,
                    b.tile_counts, b.out),
         ]
-    else:
+    elif w8a8:
+        calls = [
+            M.bind(M.moe_route_topk_offsets, logits, mask, k, b.ids, b.w, b.counts, b.offsets, b.ws),
+            M.bind(M.moe_quantize_weights_fp8, x, b.x_q, b.x_scales),
+            M.bind(M.moe_scatter_rows_e4m3, b.x_q, b.x_scales, b.ids, mask, b.offsets, b.xs, b.xs_scales,
+                   b.row_of_route, b.route_of_row, b.ws),
+            M.bind(M.moe_grouped_gate_up_w8a8, b.xs, b.xs_scales, b.offsets, wg, wu, b.h),
+            M.bind(M.moe_quantize_weights_fp8, b.h, b.h_q, b.h_scales),
+            M.bind(M.moe_grouped_down_w8a8, b.h_q, b.h_scales, b.offsets, wd, b.y),
+            M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
+        ]
+    elif fp8:
         calls = routing + [
             M.bind(gate_up_call, b.xs, b.offsets, wg, wu, b.h),
             M.bind(down_call, b.h, b.offsets, wd, b.y),
             M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
         ]
+    else:
+        # a plan holds the FFN launches' tensor maps, encoded once
+        plan = M.moe_plan_create(wg, wu, wd, b)
+        calls = routing + [
+            M.bind(M.moe_plan_grouped_gate_up, plan),
+            M.bind(M.moe_plan_grouped_down, plan),
+            M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
+        ]
+        if not args.router:
+            def forward(lg, xx, mm, _wg, _wu, _wd, _k, bb):
+                return M.moe_plan_forward(plan, lg, xx, mm, out=bb.out)
 
     def step(gu_events=None):
         for i, c in enumerate(calls):
@@ -535,6 +582,24 @@ def run_ours(args, rank: int, world: int):
     per_kernel = {n: statistics.mean(evk[s][i][0].elapsed_time(evk[s][i][1]) for s in range(n_bd))
                   for i, n in enumerate(names)}
 
+    # host cost of one whole-path call, with the argument checks and tensor-map encoding
+    # of moe_forward against a prepared plan (calls marshalled once; the GPU queue
+    # absorbs the launches, so the host time per call is what is measured)
+    host_us = None
+    if not (fused or fp8 or w8a8 or args.router):
+        host_us = {}
+        for label, call in (("moe_forward", M.bind(M.moe_forward, logits, x, mask, wg, wu, wd, k, b)),
+                            ("moe_plan_forward", M.bind(M.moe_plan_forward, plan, logits, x, mask))):
+            call()
+            torch.cuda.synchronize()
+            n_calls = 50
+            t0 = time.perf_counter()
+            for _ in range(n_calls):
+                call()
+            host_us[label] = 1e6 * (time.perf_counter() - t0) / n_calls
+            torch.cuda.synchronize()
+        M.moe_check_device_error()
+
     # the end-to-end leg runs moe_forward, which takes the logits as input: not with --router
     e2e = None if (args.no_e2e or args.router) else _run_e2e(args, M, world, dev, logits, x, mask, wg, wu, wd, k,
                                                              bufs, T, d, forward)
@@ -547,15 +612,17 @@ def run_ours(args, rank: int, world: int):
 
     # ---- roofline of the dominant kernel (grouped gate/up + SwiGLU)
     es = 2 if dtype == torch.bfloat16 else 4
-    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8, fused, gather)
+    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8, fused, gather, w8a8)
     R, touched = work["R"], work["touched"]
     gate_up_bytes = work["gate_up_bytes"]
     peaks = _peaks()
     achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic("gate_up_fp8" if fp8 else ("gate_up_gather" if gather else "gate_up"), cfg.name)
-    kname = "moe_grouped_gate_up_fp8 (ffn_fp8_kernel<gated>)" if fp8 else \
-        ("moe_grouped_gate_up_gather (ffn_tc_kernel<gated, fused>)" if gather else
-         "moe_grouped_gate_up (ffn_tc_kernel<gated>)")
+    traffic = _profiled_traffic("gate_up_w8a8" if w8a8 else "gate_up_fp8" if fp8 else
+                                ("gate_up_gather" if gather else "gate_up"), cfg.name)
+    kname = ("moe_grouped_gate_up_w8a8 (ffn_tc_kernel<gated, E4M3>)" if w8a8 else
+             "moe_grouped_gate_up_fp8 (ffn_fp8_kernel<gated>)" if fp8 else
+             "moe_grouped_gate_up_gather (ffn_tc_kernel<gated, fused>)" if gather else
+             "moe_grouped_gate_up (ffn_tc_kernel<gated>)")
     roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic, "peak_source": peaks["source"],
@@ -566,7 +633,9 @@ def run_ours(args, rank: int, world: int):
     if args.router:
         flops += 2.0 * T * E * d
         path_bytes += T * d * 2 + E * d * 2 - T * E * 4   # x and wr read instead of the logits
-    t_roof = max(flops / (peaks["bf16_tflops_sustained"] * 1e12), path_bytes / (peaks["hbm_gbs"] * 1e9))
+    # E4M3 x E4M3 MMAs run at twice the bf16 rate (the nominal dense fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s)
+    tensor_peak = peaks["bf16_tflops_sustained"] * (2.0 if w8a8 else 1.0)
+    t_roof = max(flops / (tensor_peak * 1e12), path_bytes / (peaks["hbm_gbs"] * 1e9))
     ms_per_step = elapsed_ms / args.steps
     value = world * T * args.steps / (elapsed_ms * 1e-3)
 
@@ -585,11 +654,14 @@ def run_ours(args, rank: int, world: int):
         "warmup": args.warmup, "ms_per_step": ms_per_step,
         "ms_per_step_median": step_median, "ms_per_step_mad": step_mad,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3" if w8a8 else ("bf16" if dtype == torch.bfloat16 else "f32"),
+        "data": "synthetic",
         "config": {"workload": cfg.name, "T": T, "d": d, "f": f, "E": E, "k": k, "mask_p": cfg.mask_p,
                    "routes_unmasked": R, "experts_touched": touched,
-                   "weights": "fp8_e4m3 codes + fp32 per-channel scales" if fp8 else
+                   "weights": "fp8_e4m3 codes + fp32 per-channel scales" if (fp8 or w8a8) else
                               ("bf16" if dtype == torch.bfloat16 else "f32"),
+                   "activations": "fp8_e4m3 codes + fp32 per-row scales (x and h)" if w8a8 else
+                                  ("fp16 (exact widening of bf16 x)" if fp8 else None),
                    "permutation": ("fused: token rows gathered by the gate/up kernel, weighted combine in the "
                                    "down kernel" if gather else "compact copy xs, weighted combine in the down "
                                    "kernel") if fused else "compact copy xs + separate combine",
@@ -605,6 +677,7 @@ def run_ours(args, rank: int, world: int):
                           "frac": t_roof * 1e3 / ms_per_step,
                           "tflops": flops / (ms_per_step * 1e-3) / 1e12},
         "kernels_ms": per_kernel,
+        "host_us_per_call": host_us,
         "kernels_ms_note": "separate loop after the timed region, CUDA events around every call; the timed "
                            "region records events around gate/up only (roofline.avg_launch_ms)",
         "cpu_baseline": cpu,
@@ -659,6 +732,8 @@ def run_routing_sweep(args):
         M.moe_check_device_error()
         R = int(counts.sum())
         times = {
+            "route_topk_offsets": timeit(lambda: M.moe_route_topk_offsets(logits, mask, k, ids, w, counts, offsets,
+                                                                          ws)),
             "topk": timeit(lambda: M.moe_route_topk(logits, k, ids, w)),
             "histogram": timeit(lambda: M.moe_route_histogram(ids, mask, E, counts, ws)),
             "prefix": timeit(lambda: M.moe_prefix_offsets(counts, T, k, offsets, ws)),
@@ -667,6 +742,7 @@ def run_routing_sweep(args):
         }
         M.moe_check_device_error()
         nbytes = {
+            "route_topk_offsets": T * E * 4 + T * k * 8 + T * k * 5,
             "topk": T * E * 4 + T * k * 8,
             "histogram": T * k * 9,
             "scatter": T * d * 2 + cap * d * 2 + T * k * 12,
@@ -697,9 +773,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
-    ap.add_argument("--weights", choices=("bf16", "fp8"), default="bf16",
-                    help="expert weight format: the workload's own (bf16), or FP8 E4M3 codes with per-channel "
-                         "scales quantized at load time")
+    ap.add_argument("--weights", choices=("bf16", "fp8", "w8a8"), default="bf16",
+                    help="expert weight format: the workload's own (bf16); FP8 E4M3 codes with per-channel "
+                         "scales quantized at load time, with fp16 activations (fp8) or with E4M3 activations "
+                         "quantized per row on the FP8 tensor cores (w8a8)")
     ap.add_argument("--fused", action="store_true",
                     help="the fused permutation (bf16): rows gathered in the gate/up kernel, combine in the down "
                          "kernel (moe_forward_fused)")

@@ -91,6 +91,12 @@ int moe_last_cuda_error(void);
  * fp16 range; the affected outputs hold infinities). */
 moe_status moe_check_device_error(void* stream);
 
+/* Enqueues on `stream` the clearing of the current device's sticky error
+ * word, without synchronising (moe_check_device_error reads and clears it
+ * after a synchronisation).  For a caller that has handled a reported error
+ * and wants the word clear before its next calls on `stream`. */
+moe_status moe_clear_device_error(void* stream);
+
 /* Diagnostic of the failure detection.  Every wait of the tensor-core
  * kernels on a copy or an MMA is bounded (2 s); when one runs out the kernel
  * abandons its work, drains what it has in flight, frees its tensor memory
@@ -145,6 +151,19 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k,
 moe_status moe_route_histogram(const int32_t* ids, const uint8_t* mask, int T, int k, int E,
                                int32_t* counts, void* ws, void* stream);
 
+/* A1 + A2 + A3 in one launch: the outputs of moe_route_topk,
+ * moe_route_histogram and moe_prefix_offsets (ids, w, counts, offsets, and
+ * the workspace the scatter reads), bit for bit.  One CTA per workspace
+ * chunk of tokens routes its tokens, ranks their routes and counts them;
+ * the last CTA to finish sums the counts and writes the prefix and the
+ * chunk bases.  Shapes other than E a multiple of 4 with 16-byte aligned
+ * logits run the three step kernels instead (same results).
+ *   logits [T][E], mask [T][k] or NULL, ids, w [T][k], counts [E],
+ *   offsets [E+1], ws: as for the three calls. */
+moe_status moe_route_topk_offsets(const float* logits, const uint8_t* mask, int T, int E, int k,
+                                  int32_t* ids, float* w, int32_t* counts, int32_t* offsets, void* ws,
+                                  void* stream);
+
 /* Allocation-free variant of moe_route_histogram.  The pages have no
  * counterpart of this entry point: it serves callers that cannot allocate
  * device memory, such as code plugged into a host framework that owns every
@@ -153,7 +172,7 @@ moe_status moe_route_histogram(const int32_t* ids, const uint8_t* mask, int T, i
  * inputs and outputs:
  *   ids, mask, T, k, E, counts  as for moe_route_histogram (same counts).
  * The scratch (per-chunk counts, in-chunk ranks and a completion counter,
- * 295 KB) is a static device array inside the library; every GPU that loads
+ * 384 KB) is a static device array inside the library; every GPU that loads
  * the library keeps it until the process exits.
  *   Limit: T*k <= 65536 routes; a larger chunk returns MOE_ERR_INVALID_ARG
  *   without enqueuing anything.
@@ -349,6 +368,61 @@ moe_status moe_forward_fp8(const float* logits, const void* x, const uint8_t* ma
                            void* h, float* y, float* out, void* ws, void* stream);
 
 /* ------------------------------------------------------------------------
+ * FP8 E4M3 weights AND activations on the FP8 tensor cores.  The pages'
+ * quantized expert matmuls take quantized activations too (the MMQ path of
+ * the page "perf(ggml): reuse ROCmFP4 weights across q=4 columns", whose
+ * weights come in ROCmFP4/FPX formats; page "perf(ds4): batch heterogeneous
+ * MoE prefill by expert", "Fresh main-snapshot requalification": a ROCmFP2
+ * model).  Here both operands of every expert GEMM are OCP E4M3 codes with
+ * one fp32 scale per row -- per output channel for the weights (the codes of
+ * moe_quantize_weights_fp8), per token row for x and per compact row for h
+ * (the same quantizer applied to the activation rows) -- and the tensor
+ * cores multiply the codes directly (tcgen05.mma kind::f8f6f4, K = 32 per
+ * instruction), the epilogue applying the two scales.  The method computed
+ * is the FFN on the values the codes stand for: x' = s_x * value(code_x),
+ * h = silu(x'.Wg') * (x'.Wu') rounded to bf16, h' = s_h * value(code_h) of
+ * that bf16 h, y = h'.Wd'; products accumulate in fp32.
+ * ------------------------------------------------------------------------ */
+
+/* A4 with E4M3 rows: the codes x_q [T][d] and row scales x_scales [T] of the
+ * token rows (moe_quantize_weights_fp8 applied to x, rows = T, K = d) are
+ * scattered like moe_scatter_rows scatters x: xs [T*k][d] uint8 (rows R ..
+ * T*k-1 zero codes) and xs_scales [T*k] (the token row's scale; 0 for rows
+ * R .. T*k-1).  ids, mask, offsets, row_of_route, route_of_row, ws: as for
+ * moe_scatter_rows.  d a multiple of 16. */
+moe_status moe_scatter_rows_e4m3(const uint8_t* x_q, const float* x_scales, const int32_t* ids, const uint8_t* mask,
+                                 const int32_t* offsets, int T, int k, int d, int E, uint8_t* xs, float* xs_scales,
+                                 int32_t* row_of_route, int32_t* route_of_row, void* ws, void* stream);
+
+/* A5 on E4M3 operands: h[i][j] = silu(g) * u, g = s_gate[e][j] *
+ * xs_scales[i] * (codes of xs[i] . codes of w_gate_q[e][j]) and u likewise;
+ * h [cap][f] bf16 out (rows R .. cap-1 zero-filled).  d and f multiples of
+ * 128; offsets checked on the device as for moe_grouped_gate_up. */
+moe_status moe_grouped_gate_up_w8a8(const uint8_t* xs, const float* xs_scales, const int32_t* offsets, int cap,
+                                    int E, int d, int f, const uint8_t* w_gate_q, const float* s_gate,
+                                    const uint8_t* w_up_q, const float* s_up, void* h, void* stream);
+
+/* A6 on E4M3 operands: y[i][j] = s_down[e][j] * h_scales[i] * (codes of
+ * h_q[i] . codes of w_down_q[e][j]); y [cap][d] fp32 out, rows R .. cap-1
+ * zero-filled.  h_q, h_scales: moe_quantize_weights_fp8 applied to the bf16
+ * h (rows = cap, K = f). */
+moe_status moe_grouped_down_w8a8(const uint8_t* h_q, const float* h_scales, const int32_t* offsets, int cap, int E,
+                                 int d, int f, const uint8_t* w_down_q, const float* s_down, float* y, void* stream);
+
+/* The whole path on E4M3 weights and activations: routing in one launch
+ * (moe_route_topk_offsets), the token rows quantized (x_q [T][d], x_scales
+ * [T]) and scattered (xs, xs_scales), moe_grouped_gate_up_w8a8 into h
+ * [T*k][f] bf16, h quantized (h_q [T*k][f], h_scales [T*k]),
+ * moe_grouped_down_w8a8 into y, moe_combine into out.  x is bf16; every
+ * other argument as for moe_forward. */
+moe_status moe_forward_w8a8(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k, int d,
+                            int f, const uint8_t* w_gate_q, const float* s_gate, const uint8_t* w_up_q,
+                            const float* s_up, const uint8_t* w_down_q, const float* s_down, int32_t* ids, float* w,
+                            int32_t* counts, int32_t* offsets, uint8_t* x_q, float* x_scales, uint8_t* xs,
+                            float* xs_scales, int32_t* row_of_route, int32_t* route_of_row, void* h, uint8_t* h_q,
+                            float* h_scales, float* y, float* out, void* ws, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused permutation (bf16 operands only).  The pages fuse the combine into
  * one expert-major kernel (page "perf(ds4): accelerate ROCm decode and
  * long-context selection", lucebox8 gfx1151 A/B; page "perf(ds4): extend
@@ -434,6 +508,12 @@ enum {
     MOE_FUSED_NONE = 3      /* the unfused path (moe_forward): y is written as moe_grouped_down writes it */
 };
 
+/* The mode moe_forward_fused chooses for MOE_FUSED_AUTO on the current
+ * device for a chunk of T tokens of width d (have_xs: a compact buffer xs
+ * is passed; without one the gather mode is the only choice).  *mode gets
+ * MOE_FUSED_GATHER, MOE_FUSED_COMPACT or MOE_FUSED_NONE. */
+moe_status moe_forward_fused_mode(int T, int E, int k, int d, int have_xs, int* mode);
+
 /* The whole path with the fused combine (bf16): the routing (one launch for
  * chunks with T <= 128 and T*k <= 512, else moe_route_topk,
  * moe_route_histogram, moe_prefix_offsets and moe_scatter_index), the gate/up
@@ -448,6 +528,47 @@ moe_status moe_forward_fused(const float* logits, const void* x, const uint8_t* 
                              int32_t* ids, float* w, int32_t* counts, int32_t* offsets, void* xs,
                              int32_t* row_of_route, int32_t* route_of_row,
                              void* h, float* y, int32_t* tile_counts, float* out, void* ws, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Plans: the path for fixed shapes, weights and buffers, prepared once.
+ * The verification batches of the page "perf(ggml): reuse ROCmFP4 weights
+ * across q=4 columns" (q=4 columns) and the decode-like chunks of the page
+ * "perf(ds4): accelerate ROCm decode and long-context selection" run the
+ * same small path over and over on the same buffers; a plan does the host
+ * work that depends only on shapes and pointers once -- the argument
+ * checks, the device lookup and the TMA tensor maps of the expert weights
+ * and of the compact buffers xs and h -- so that each call only launches.
+ * ------------------------------------------------------------------------ */
+typedef struct moe_plan moe_plan;
+
+/* Creates a plan for chunks of exactly T tokens (T >= 1) with the given
+ * weights and buffers, on the current device and CUDA context.  Arguments as
+ * for moe_forward (dtype MOE_BF16 or MOE_F32; the same shapes, alignment
+ * and workspace rules).  The plan records the pointers; it owns none of the
+ * memory, which must stay allocated while the plan is used.  The plan itself
+ * is host memory, released by moe_plan_destroy; nothing is allocated on the
+ * device.  *plan is set to NULL when creation fails. */
+moe_status moe_plan_create(int T, int E, int k, int d, int f, int dtype,
+                           const void* w_gate, const void* w_up, const void* w_down,
+                           int32_t* ids, float* w, int32_t* counts, int32_t* offsets, void* xs,
+                           int32_t* row_of_route, int32_t* route_of_row, void* h, float* y, void* ws,
+                           moe_plan** plan);
+
+/* Releases a plan (NULL is accepted). */
+moe_status moe_plan_destroy(moe_plan* plan);
+
+/* A5 and A6 on the plan's buffers (moe_grouped_gate_up / moe_grouped_down
+ * with the plan's xs, offsets, weights, h and y), launched from the
+ * prepared tensor maps.  MOE_ERR_INVALID_ARG when the current device or
+ * context is not the plan's. */
+moe_status moe_plan_grouped_gate_up(const moe_plan* plan, void* stream);
+moe_status moe_plan_grouped_down(const moe_plan* plan, void* stream);
+
+/* moe_forward on the plan's weights and buffers for one chunk: logits
+ * [T][E], x [T][d] (the plan's operand type), mask [T][k] or NULL, out
+ * [T][d] fp32.  Same kernels, same results bit for bit, as moe_forward. */
+moe_status moe_plan_forward(const moe_plan* plan, const float* logits, const void* x, const uint8_t* mask,
+                            float* out, void* stream);
 
 #ifdef __cplusplus
 }

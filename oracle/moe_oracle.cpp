@@ -189,6 +189,21 @@ double e4m3_round_one(double x) {
     return std::copysign(r, x);
 }
 
+// bf16 nearest value (ties to even): 8 significant bits with fp32's
+// exponent range; subnormals keep the 2^-133 spacing, magnitudes that round
+// beyond the largest finite bf16 become infinities.
+double bf16_round_one(double x) {
+    const double a = std::fabs(x);
+    if (!(a > 0.0) || std::isinf(a)) return x;
+    int ex = 0;
+    std::frexp(a, &ex);                             // a in [2^(ex-1), 2^ex)
+    const int binade = std::max(ex - 1, -126);
+    const double quantum = std::ldexp(1.0, binade - 7);
+    double r = std::nearbyint(a / quantum) * quantum;
+    if (r > std::ldexp(255.0 / 128.0, 127)) r = INFINITY;
+    return std::copysign(r, x);
+}
+
 uint8_t e4m3_encode_one(double v) {
     const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
     const double a = std::fabs(v);
@@ -431,11 +446,21 @@ int oracle_silu(const double* a, long long n, double* out) {
 //   scale = max|w| / 448 in fp32 (1 for an all-zero row),
 //   code  = E4M3 code of the nearest E4M3 value (ties to even, saturating)
 //           to the fp32 quotient w / scale.
-// The weight the FFN uses is scale * value(code).
+// The weight the FFN uses is scale * value(code).  (A float64 row is read
+// as its nearest fp32 values.)  The same quantizer, applied to the rows of x
+// and of h, gives the activations of the FP8-activation path.
 // ---------------------------------------------------------------------------
 int oracle_e4m3_round(const double* x, long long n, double* out) {
     if (n < 0 || (n > 0 && (!x || !out))) return 1;
     for (long long i = 0; i < n; ++i) out[i] = e4m3_round_one(x[i]);
+    return 0;
+}
+
+// An intermediate stored in bf16 (the h of the bf16 and FP8-activation
+// paths): the nearest bf16 value of each element, ties to even.
+int oracle_round_bf16(const double* x, long long n, double* out) {
+    if (n < 0 || (n > 0 && (!x || !out))) return 1;
+    for (long long i = 0; i < n; ++i) out[i] = bf16_round_one(x[i]);
     return 0;
 }
 
@@ -452,7 +477,7 @@ int oracle_e4m3_decode(const uint8_t* codes, long long n, double* v) {
 }
 
 int oracle_quantize_fp8(const void* w, int dtype, long long rows, int K, uint8_t* codes, float* scales) {
-    if ((dtype != ORC_F32 && dtype != ORC_BF16) || rows < 0 || K < 1) return 1;
+    if (!plain_dtype(dtype) || rows < 0 || K < 1) return 1;
     if (rows > 0 && (!w || !codes || !scales)) return 1;
 #pragma omp parallel for schedule(static)
     for (long long r = 0; r < rows; ++r) {

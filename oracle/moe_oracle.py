@@ -51,6 +51,7 @@ _SIGNATURES = {
     "oracle_silu": (_P, _L, _P),
     "oracle_e4m3_round": (_P, _L, _P),
     "oracle_e4m3_encode": (_P, _L, _P),
+    "oracle_round_bf16": (_P, _L, _P),
     "oracle_e4m3_decode": (_P, _L, _P),
     "oracle_quantize_fp8": (_P, _I, _L, _I, _P, _P),
     "oracle_dequantize_fp8": (_P, _P, _L, _I, _P),
@@ -381,6 +382,14 @@ def e4m3_round(x):
     return out
 
 
+def round_bf16(x):
+    """Nearest bf16 value of each element (ties to even), as float64."""
+    a = _np(x, np.float64)
+    out = np.empty_like(a)
+    _call("oracle_round_bf16", _ptr(a), a.size, _ptr(out))
+    return out
+
+
 def e4m3_encode(v):
     """Byte codes of E4M3 values."""
     a = _np(v, np.float64)
@@ -403,8 +412,6 @@ def quantize_weights_fp8(w):
     Returns (codes uint8 [..., M, K], scales float32 [..., M]).
     """
     data, code = _operand(w)
-    if code == ORC_F64:
-        data, code = np.ascontiguousarray(data, dtype=np.float32), ORC_F32
     K = data.shape[-1]
     rows = data.size // K if K else 0
     codes = np.empty(data.shape, dtype=np.uint8)
@@ -425,6 +432,43 @@ def dequantize_weights_fp8(codes, scales):
     out = np.empty(c.shape, dtype=np.float64)
     _call("oracle_dequantize_fp8", _ptr(c), _ptr(s), c.size // K if K else 0, K, _ptr(out))
     return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 weights and activations
+# ---------------------------------------------------------------------------
+#
+# Both operands of every expert GEMM are E4M3 codes with one fp32 scale per
+# row, made by the quantizer above: the weights per output channel, the
+# token rows x per token, the rows of h per compact row.  h is rounded to
+# bf16 (the intermediate the GPU stores) before its rows are quantized.  The
+# FFN then runs on the values the codes stand for, in float64.
+
+def moe_forward_w8a8(logits, x, weights_q, k: int, mask=None, h_decided=None):
+    """Every intermediate of the FP8-activation path for one chunk (A1 .. A7 in order), as a dict.
+
+    weights_q: (gate, up, down) QuantizedBanks, or fetch(e0, e1) returning them.
+    h_decided: the bf16 h [R][f] of the implementation under test, or None.  The E4M3 codes of h are an
+    integer decision taken from a floating-point h; where an implementation's h is given, the codes are
+    decided from it (in that implementation's precision), so that a one-ulp difference of h at an E4M3
+    rounding midpoint is not mistaken for an error of what follows.  Its agreement with this oracle's own
+    h is for the caller to check (res["h"]).
+    """
+    lg = _np(logits, np.float32)
+    T, E = lg.shape
+    ids, w = route_topk(lg, k)
+    counts = route_histogram(ids, mask, E)
+    offsets = prefix_offsets(counts)
+    row_of_route, route_of_row = scatter_permutation(ids, mask)
+    x_q = quantize_bank_fp8(x)
+    xs = scatter_rows(dequantize_weights_fp8(x_q.codes, x_q.scales), route_of_row, k)
+    h = grouped_swiglu(xs, offsets, weights_q)
+    h_bf16 = round_bf16(h) if h_decided is None else h_decided
+    h_q = quantize_bank_fp8(h_bf16)
+    y = grouped_down(dequantize_weights_fp8(h_q.codes, h_q.scales), offsets, weights_q)
+    out = combine(y, row_of_route, w, T, k)
+    return {"ids": ids, "w": w, "counts": counts, "offsets": offsets, "row_of_route": row_of_route,
+            "route_of_row": route_of_row, "x_q": x_q, "h": h, "h_bf16": h_bf16, "h_q": h_q, "y": y, "out": out}
 
 
 # ---------------------------------------------------------------------------

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <new>
 
 #include "moe_internal.cuh"
 
@@ -123,6 +124,13 @@ extern "C" moe_status moe_check_device_error(void* stream) {
     return MOE_ERR_RANGE;
 }
 
+extern "C" moe_status moe_clear_device_error(void* stream) {
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return cuda_status(cudaMemsetAsync(di.error_word, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream)));
+}
+
 namespace {
 
 moe_status check_ffn_args(const int32_t* offsets, int cap, int E, int d, int f, int dtype) {
@@ -199,9 +207,8 @@ extern "C" moe_status moe_forward(const float* logits, const void* x, const uint
                                           row_of_route, route_of_row, stream)) != MOE_OK)
             return st;
     } else {
-        if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
-        if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
-        if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK)
+            return st;
         if ((st = moe_scatter_rows(x, dtype, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
                                    stream)) != MOE_OK)
             return st;
@@ -284,15 +291,90 @@ extern "C" moe_status moe_forward_fp8(const float* logits, const void* x, const 
                                           row_of_route, route_of_row, stream)) != MOE_OK)
             return st;
     } else {
-        if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
-        if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
-        if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK)
+            return st;
         if ((st = moe_scatter_rows_f16(x, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
                                        stream)) != MOE_OK)
             return st;
     }
     if ((st = moe_grouped_ffn_fp8(xs, offsets, cap, E, d, f, w_gate_q, s_gate, w_up_q, s_up, w_down_q, s_down, h, y,
                                   stream)) != MOE_OK)
+        return st;
+    return moe_combine(y, row_of_route, w, T, k, d, out, stream);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 weights and activations (kind::f8f6f4 tensor-core MMAs)
+// ---------------------------------------------------------------------------
+
+namespace {
+
+moe_status check_w8a8_args(const int32_t* offsets, int cap, int E, int d, int f) {
+    MOE_REQUIRE(offsets && cap >= 0 && E >= 1 && E <= kMaxExperts && d >= 128 && f >= 128);
+    MOE_REQUIRE(d % 128 == 0 && f % 128 == 0);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_grouped_gate_up_w8a8(const uint8_t* xs, const float* xs_scales, const int32_t* offsets,
+                                               int cap, int E, int d, int f, const uint8_t* w_gate_q,
+                                               const float* s_gate, const uint8_t* w_up_q, const float* s_up,
+                                               void* h, void* stream) {
+    moe_status st = check_w8a8_args(offsets, cap, E, d, f);
+    if (st != MOE_OK) return st;
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(xs && xs_scales && w_gate_q && s_gate && w_up_q && s_up && h);
+    MOE_REQUIRE(aligned16(xs) && aligned16(w_gate_q) && aligned16(w_up_q) && aligned16(h));
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MOE_OK) return st;
+    return launch_ffn_w8a8_gate_up(xs, xs_scales, offsets, cap, E, d, f, w_gate_q, s_gate, w_up_q, s_up, h,
+                                   static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_grouped_down_w8a8(const uint8_t* h_q, const float* h_scales, const int32_t* offsets,
+                                            int cap, int E, int d, int f, const uint8_t* w_down_q,
+                                            const float* s_down, float* y, void* stream) {
+    moe_status st = check_w8a8_args(offsets, cap, E, d, f);
+    if (st != MOE_OK) return st;
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(h_q && h_scales && w_down_q && s_down && y);
+    MOE_REQUIRE(aligned16(h_q) && aligned16(w_down_q) && aligned16(y));
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MOE_OK) return st;
+    return launch_ffn_w8a8_down(h_q, h_scales, offsets, cap, E, d, f, w_down_q, s_down, y,
+                                static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_forward_w8a8(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k,
+                                       int d, int f, const uint8_t* w_gate_q, const float* s_gate,
+                                       const uint8_t* w_up_q, const float* s_up, const uint8_t* w_down_q,
+                                       const float* s_down, int32_t* ids, float* w, int32_t* counts,
+                                       int32_t* offsets, uint8_t* x_q, float* x_scales, uint8_t* xs,
+                                       float* xs_scales, int32_t* row_of_route, int32_t* route_of_row, void* h,
+                                       uint8_t* h_q, float* h_scales, float* y, float* out, void* ws,
+                                       void* stream) {
+    moe_status st = check_w8a8_args(offsets, T * k, E, d, f);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && k <= E);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && ids && w && counts && x_q && x_scales && xs && xs_scales && row_of_route &&
+                route_of_row && h && h_q && h_scales && y && out && ws);
+    MOE_REQUIRE(aligned16(x) && aligned16(x_q) && aligned16(xs) && aligned16(h) && aligned16(h_q) &&
+                aligned16(y) && aligned16(out) && aligned16(ws));
+    const int cap = T * k;
+    if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK) return st;
+    // E4M3 codes of the token rows, one scale per row (the weights' quantizer)
+    if ((st = moe_quantize_weights_fp8(x, MOE_BF16, T, d, x_q, x_scales, stream)) != MOE_OK) return st;
+    if ((st = moe_scatter_rows_e4m3(x_q, x_scales, ids, mask, offsets, T, k, d, E, xs, xs_scales, row_of_route,
+                                    route_of_row, ws, stream)) != MOE_OK)
+        return st;
+    if ((st = moe_grouped_gate_up_w8a8(xs, xs_scales, offsets, cap, E, d, f, w_gate_q, s_gate, w_up_q, s_up, h,
+                                       stream)) != MOE_OK)
+        return st;
+    // E4M3 codes of the rows of h (bf16), one scale per row
+    if ((st = moe_quantize_weights_fp8(h, MOE_BF16, cap, f, h_q, h_scales, stream)) != MOE_OK) return st;
+    if ((st = moe_grouped_down_w8a8(h_q, h_scales, offsets, cap, E, d, f, w_down_q, s_down, y, stream)) != MOE_OK)
         return st;
     return moe_combine(y, row_of_route, w, T, k, d, out, stream);
 }
@@ -344,6 +426,26 @@ extern "C" moe_status moe_grouped_down_combine(const void* h, const int32_t* off
 #define MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT 16
 #endif
 
+namespace {
+
+int fused_auto_mode(long long cap, int E, int d, bool have_xs, const DeviceInfo& di) {
+    if (!have_xs || cap <= static_cast<long long>(E) * MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT)
+        return MOE_FUSED_GATHER;
+    if (cap * d * 4 <= 2LL * di.l2_bytes) return MOE_FUSED_COMPACT;
+    return MOE_FUSED_NONE;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_forward_fused_mode(int T, int E, int k, int d, int have_xs, int* mode) {
+    MOE_REQUIRE(mode && T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 1);
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    *mode = fused_auto_mode(static_cast<long long>(T) * k, E, d, have_xs != 0, di);
+    return MOE_OK;
+}
+
 extern "C" moe_status moe_forward_fused(const float* logits, const void* x, const uint8_t* mask, int T, int E,
                                         int k, int d, int f, const void* w_gate, const void* w_up,
                                         const void* w_down, int mode, int32_t* ids, float* w, int32_t* counts,
@@ -365,14 +467,7 @@ extern "C" moe_status moe_forward_fused(const float* logits, const void* x, cons
     st = device_info(&di);
     if (st != MOE_OK) return st;
     const long long cap = static_cast<long long>(T) * k;
-    if (mode == MOE_FUSED_AUTO) {
-        if (xs == nullptr || cap <= static_cast<long long>(E) * MOE_FUSED_GATHER_MAX_ROUTES_PER_EXPERT)
-            mode = MOE_FUSED_GATHER;
-        else if (cap * d * 4 <= 2LL * di.l2_bytes)
-            mode = MOE_FUSED_COMPACT;
-        else
-            mode = MOE_FUSED_NONE;
-    }
+    if (mode == MOE_FUSED_AUTO) mode = fused_auto_mode(cap, E, d, xs != nullptr, di);
     if (mode == MOE_FUSED_NONE)
         return moe_forward(logits, x, mask, T, E, k, d, f, w_gate, w_up, w_down, MOE_BF16, ids, w, counts, offsets, xs,
                            row_of_route, route_of_row, h, y, out, ws, stream);
@@ -385,9 +480,8 @@ extern "C" moe_status moe_forward_fused(const float* logits, const void* x, cons
                                                    out, s, di)) != MOE_OK)
             return st;
     } else {
-        if ((st = moe_route_topk(logits, T, E, k, ids, w, stream)) != MOE_OK) return st;
-        if ((st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream)) != MOE_OK) return st;
-        if ((st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream)) != MOE_OK) return st;
+        if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK)
+            return st;
         if ((st = moe_scatter_index(ids, mask, offsets, T, k, d, E, gather ? nullptr : x, gather ? nullptr : xs,
                                     row_of_route, route_of_row, tile_counts, out, ws, stream)) != MOE_OK)
             return st;
@@ -414,4 +508,140 @@ extern "C" moe_status moe_router_topk(const void* x, const void* wr, int T, int 
     moe_status st = device_info(&di);
     if (st != MOE_OK) return st;
     return launch_router_topk(x, wr, T, E, d, k, logits, ids, w, static_cast<cudaStream_t>(stream), di);
+}
+
+// ---------------------------------------------------------------------------
+// Plans: the path for fixed shapes, weights and buffers, prepared once
+// ---------------------------------------------------------------------------
+
+struct moe_plan {
+    int device;
+    unsigned long long context;
+    int T, E, k, d, f, dtype;
+    const void *w_gate, *w_up, *w_down;
+    int32_t* ids;
+    float* w;
+    int32_t *counts, *offsets;
+    void* xs;
+    int32_t *row_of_route, *route_of_row;
+    void* h;
+    float* y;
+    void* ws;
+    moe::DeviceInfo di;
+    moe::FfnTcLaunch gate_up, down;   // bf16: the tensor maps, encoded once
+};
+
+extern "C" moe_status moe_plan_create(int T, int E, int k, int d, int f, int dtype, const void* w_gate,
+                                      const void* w_up, const void* w_down, int32_t* ids, float* w,
+                                      int32_t* counts, int32_t* offsets, void* xs, int32_t* row_of_route,
+                                      int32_t* route_of_row, void* h, float* y, void* ws, moe_plan** plan) {
+    MOE_REQUIRE(plan != nullptr);
+    *plan = nullptr;
+    moe_status st = check_ffn_args(offsets, T * k, E, d, f, dtype);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(T >= 1 && k >= 1 && k <= kMaxK && k <= E && d % 4 == 0);
+    MOE_REQUIRE(static_cast<long long>(T) * k < (1ll << 30));
+    MOE_REQUIRE(w_gate && w_up && w_down && ids && w && counts && xs && row_of_route && route_of_row && h && y &&
+                ws);
+    MOE_REQUIRE(aligned16(xs) && aligned16(h) && aligned16(y) && aligned16(ws) && aligned16(w_gate) &&
+                aligned16(w_up) && aligned16(w_down));
+    moe_plan p{};
+    MOE_CUDA_TRY(cudaGetDevice(&p.device));
+    if ((st = device_info(&p.di)) != MOE_OK) return st;
+    if ((st = current_context_id(&p.context)) != MOE_OK) return st;
+    p.T = T;
+    p.E = E;
+    p.k = k;
+    p.d = d;
+    p.f = f;
+    p.dtype = dtype;
+    p.w_gate = w_gate;
+    p.w_up = w_up;
+    p.w_down = w_down;
+    p.ids = ids;
+    p.w = w;
+    p.counts = counts;
+    p.offsets = offsets;
+    p.xs = xs;
+    p.row_of_route = row_of_route;
+    p.route_of_row = route_of_row;
+    p.h = h;
+    p.y = y;
+    p.ws = ws;
+    if (dtype == MOE_BF16) {
+        const int cap = T * k;
+        if ((st = prepare_ffn_tc_gate_up(xs, offsets, cap, E, d, f, w_gate, w_up, h, p.di, &p.gate_up)) != MOE_OK)
+            return st;
+        if ((st = prepare_ffn_tc_down(h, offsets, cap, E, d, f, w_down, y, p.di, &p.down)) != MOE_OK) return st;
+    }
+    moe_plan* heap = new (std::nothrow) moe_plan(p);
+    if (heap == nullptr) return MOE_ERR_CUDA;
+    *plan = heap;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_plan_destroy(moe_plan* plan) {
+    delete plan;
+    return MOE_OK;
+}
+
+namespace {
+
+// The plan belongs to the device and context it was made in.
+moe_status check_plan(const moe_plan* plan) {
+    MOE_REQUIRE(plan != nullptr);
+    int dev = -1;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    unsigned long long ctx = 0;
+    moe_status st = current_context_id(&ctx);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(dev == plan->device && ctx == plan->context);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_plan_grouped_gate_up(const moe_plan* plan, void* stream) {
+    moe_status st = check_plan(plan);
+    if (st != MOE_OK) return st;
+    const moe_plan& p = *plan;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.dtype == MOE_BF16) return launch_ffn_tc_prepared(p.gate_up, s, p.di);
+    return launch_ffn_simt_gate_up(static_cast<const float*>(p.xs), p.offsets, p.T * p.k, p.E, p.d, p.f,
+                                   static_cast<const float*>(p.w_gate), static_cast<const float*>(p.w_up),
+                                   static_cast<float*>(p.h), s, p.di);
+}
+
+extern "C" moe_status moe_plan_grouped_down(const moe_plan* plan, void* stream) {
+    moe_status st = check_plan(plan);
+    if (st != MOE_OK) return st;
+    const moe_plan& p = *plan;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.dtype == MOE_BF16) return launch_ffn_tc_prepared(p.down, s, p.di);
+    return launch_ffn_simt_down(static_cast<const float*>(p.h), p.offsets, p.T * p.k, p.E, p.d, p.f,
+                                static_cast<const float*>(p.w_down), p.y, s, p.di);
+}
+
+extern "C" moe_status moe_plan_forward(const moe_plan* plan, const float* logits, const void* x,
+                                       const uint8_t* mask, float* out, void* stream) {
+    moe_status st = check_plan(plan);
+    if (st != MOE_OK) return st;
+    const moe_plan& p = *plan;
+    MOE_REQUIRE(logits && x && out && aligned16(x) && aligned16(out));
+    const int T = p.T, E = p.E, k = p.k, d = p.d, cap = T * k;
+    if (T <= kSmallTokens && cap <= kSmallRoutes) {
+        if ((st = moe_route_scatter_small(logits, x, p.dtype, 0, mask, T, E, k, d, p.ids, p.w, p.counts, p.offsets,
+                                          p.xs, p.row_of_route, p.route_of_row, stream)) != MOE_OK)
+            return st;
+    } else {
+        if ((st = moe_route_topk_offsets(logits, mask, T, E, k, p.ids, p.w, p.counts, p.offsets, p.ws, stream)) !=
+            MOE_OK)
+            return st;
+        if ((st = moe_scatter_rows(x, p.dtype, p.ids, mask, p.offsets, T, k, d, E, p.xs, p.row_of_route,
+                                   p.route_of_row, p.ws, stream)) != MOE_OK)
+            return st;
+    }
+    if ((st = moe_plan_grouped_gate_up(plan, stream)) != MOE_OK) return st;
+    if ((st = moe_plan_grouped_down(plan, stream)) != MOE_OK) return st;
+    return moe_combine(p.y, p.row_of_route, p.w, T, k, d, out, stream);
 }

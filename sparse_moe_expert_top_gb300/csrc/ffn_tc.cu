@@ -163,6 +163,16 @@ struct FusedArgs {
     int T, k, cstride;
 };
 
+// Scales of the E4M3 instantiations (unused by the bf16 ones): the
+// accumulator of weight row m and compact row n is multiplied by a0[e*M + m]
+// (gate/up: the gate rows; down: the w_down rows) or a1[e*M + m] (the up
+// rows) and by b[n] (the compact row's own scale).
+struct OpScales {
+    const float* a0;
+    const float* a1;
+    const float* b;
+};
+
 // Shared memory: a 192 KB ring, carved per launch into 4 stages of 48 KB
 // (two 16 KB weight tiles + up to 128 rows; narrow items: two k-blocks of one
 // weight tile + up to 64 rows each) or, in big-item mode, 3 stages of 64 KB
@@ -200,12 +210,13 @@ struct Cfg {
 // A0 . h with A0 = w_down, M = d, K = f.
 // ---------------------------------------------------------------------------
 
-template <bool GATED, bool FUSED>
+template <bool GATED, bool FUSED, bool F8 = false>
 __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                   const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
                   const int32_t* __restrict__ offsets, int cap, int E,
-                  int K, int M, int narrow, void* __restrict__ out, unsigned* err, const FusedArgs fa) {
+                  int K, int M, int narrow, void* __restrict__ out, unsigned* err, const FusedArgs fa,
+                  const OpScales sc) {
     using C = Cfg<GATED>;
     using Ro = Roles<GATED, FUSED>;
     extern __shared__ uint8_t smem_raw[];
@@ -239,7 +250,9 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
     int* list_rows = list + 2 * BN;                                    // their compact rows, kMaxK per token
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_kb = K / BK;
+    // K elements per k-block: one 128-byte swizzle row of the operand type
+    constexpr int KBE = F8 ? 128 : BK;
+    const int n_kb = K / KBE;
     // Output features per work item.  Normal items: 128 (gate/up: a gate tile
     // and an up tile, two MMAs) or 256 (down: two tiles).  Narrow items (small
     // chunks, chosen on the host so that there are more items than waves of
@@ -420,20 +433,20 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
                         if (narrow) {
                             // k-block hk: A tile at hk * 16 KB (gate/up: 64 gate rows, then 64 up rows)
                             uint8_t* at = st + hk * C::kATileBytes;
-                            tma_load_2d(at, &map_a0, &full[s], kb * BK, wy, pol_w);
-                            if (GATED) tma_load_2d(at + C::kATileBytes / 2, &map_a1, &full[s], kb * BK, wy, pol_w);
+                            tma_load_2d(at, &map_a0, &full[s], kb * KBE, wy, pol_w);
+                            if (GATED) tma_load_2d(at + C::kATileBytes / 2, &map_a1, &full[s], kb * KBE, wy, pol_w);
                         } else {
-                            tma_load_2d(st, &map_a0, &full[s], kb * BK, wy, pol_w);
-                            tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * BK, wy1, pol_w);
+                            tma_load_2d(st, &map_a0, &full[s], kb * KBE, wy, pol_w);
+                            tma_load_2d(st + C::kATileBytes, &map_a1, &full[s], kb * KBE, wy1, pol_w);
                         }
                         if (GATED && FUSED) continue;
                         uint8_t* bdst = st + C::kA * C::kATileBytes + hk * row_bytes;
                         // the rows in as few boxes as possible: 64-row boxes, then 16-row ones
                         int r = 0;
                         for (; r + kBigBoxRows <= n16 * kBoxRows; r += kBigBoxRows)
-                            tma_load_2d(bdst + r * 128, &map_b_big, &full[s], kb * BK, item.row0 + r, pol_x);
+                            tma_load_2d(bdst + r * 128, &map_b_big, &full[s], kb * KBE, item.row0 + r, pol_x);
                         for (; r < n16 * kBoxRows; r += kBoxRows)
-                            tma_load_2d(bdst + r * 128, &map_b, &full[s], kb * BK, item.row0 + r, pol_x);
+                            tma_load_2d(bdst + r * 128, &map_b, &full[s], kb * KBE, item.row0 + r, pol_x);
                     }
                     if (++s == S) {
                         s = 0;
@@ -453,7 +466,7 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const Item item = item_at(it);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
-                const uint32_t idesc = idesc_bf16(BM, n16 * kBoxRows);
+                const uint32_t idesc = F8 ? idesc_e4m3(BM, n16 * kBoxRows) : idesc_bf16(BM, n16 * kBoxRows);
                 const bool both = item.rows > BN;
                 const int slot = both ? 0 : toggle;
                 const uint32_t use_s = slot ? use1 : use0;
@@ -483,7 +496,10 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
 #pragma unroll
                             for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                                 const uint32_t acc = (js | hk | kk) != 0 ? 1u : 0u;
-                                umma_bf16(d0, sdesc_from_lo(ah + 2 * kk), sdesc_from_lo(bh + 2 * kk), idesc, acc);
+                                if (F8)
+                                    umma_e4m3(d0, sdesc_from_lo(ah + 2 * kk), sdesc_from_lo(bh + 2 * kk), idesc, acc);
+                                else
+                                    umma_bf16(d0, sdesc_from_lo(ah + 2 * kk), sdesc_from_lo(bh + 2 * kk), idesc, acc);
                             }
                         }
                     } else {
@@ -491,8 +507,13 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
                         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                             const uint32_t acc = (js | kk) != 0 ? 1u : 0u;
                             const uint64_t bd = sdesc_from_lo(b + 2 * kk);
-                            umma_bf16(d0, sdesc_from_lo(a0 + 2 * kk), bd, idesc, acc);
-                            umma_bf16(d0 + 2 * BN, sdesc_from_lo(a1 + 2 * kk), bd, idesc, acc);
+                            if (F8) {
+                                umma_e4m3(d0, sdesc_from_lo(a0 + 2 * kk), bd, idesc, acc);
+                                umma_e4m3(d0 + 2 * BN, sdesc_from_lo(a1 + 2 * kk), bd, idesc, acc);
+                            } else {
+                                umma_bf16(d0, sdesc_from_lo(a0 + 2 * kk), bd, idesc, acc);
+                                umma_bf16(d0 + 2 * BN, sdesc_from_lo(a1 + 2 * kk), bd, idesc, acc);
+                            }
                         }
                     }
                     umma_commit(&empty[s]);
@@ -559,17 +580,29 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
                 tmem_ld32(taddr + c0, g);
                 if (!narrow) tmem_ld32(taddr + 2 * BN + c0, g1);
                 tmem_ld_wait();
+                // E4M3 operands: the weight row's scale times the compact row's scale
+                float rs[32];
+                if (F8) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) rs[j] = c0 + j < item.rows ? __ldg(sc.b + item.row0 + c0 + j) : 0.f;
+                }
                 if (GATED && narrow) {
                     // the up half (warps of lane quarters 2, 3) goes through shared memory
+                    float ws = 1.f;
+                    if (F8)
+                        ws = __ldg((q < 2 ? sc.a0 : sc.a1) + static_cast<size_t>(item.e) * M + item.mt * fw +
+                                   (q & 1) * 32 + lane);
                     if (q >= 2) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) up_stage[((q - 2) * 32 + lane) * 33 + j] = __uint_as_float(g[j]);
+                        for (int j = 0; j < 32; ++j)
+                            up_stage[((q - 2) * 32 + lane) * 33 + j] =
+                                F8 ? __uint_as_float(g[j]) * ws * rs[j] : __uint_as_float(g[j]);
                     }
                     epilogue_sync_n(kEpiThreads);
                     if (q < 2) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const float gv = __uint_as_float(g[j]);
+                            const float gv = F8 ? __uint_as_float(g[j]) * ws * rs[j] : __uint_as_float(g[j]);
                             const float hv = silu_fast(gv) * up_stage[(q * 32 + lane) * 33 + j];
                             out_stage[j * (BM / 2) + q * 32 + lane] = __float2bfloat16_rn(hv);
                         }
@@ -591,10 +624,16 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
                     epilogue_sync_n(kEpiThreads);
                 } else if (GATED) {
                     // SwiGLU into the staged tile: row j, feature q*32 + lane
+                    float wsg = 1.f, wsu = 1.f;
+                    if (F8) {
+                        wsg = __ldg(sc.a0 + static_cast<size_t>(item.e) * M + m);
+                        wsu = __ldg(sc.a1 + static_cast<size_t>(item.e) * M + m);
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float gv = __uint_as_float(g[j]);
-                        const float hv = silu_fast(gv) * __uint_as_float(g1[j]);
+                        const float gv = F8 ? __uint_as_float(g[j]) * wsg * rs[j] : __uint_as_float(g[j]);
+                        const float uv = F8 ? __uint_as_float(g1[j]) * wsu * rs[j] : __uint_as_float(g1[j]);
+                        const float hv = silu_fast(gv) * uv;
                         out_stage[j * BM + q * 32 + lane] = __float2bfloat16_rn(hv);
                     }
                     epilogue_sync_n(kEpiThreads);
@@ -621,13 +660,18 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
                     const int ystride = FUSED ? min(fw, M - item.mt * fw) : M;
                     float* y = static_cast<float*>(out) + (FUSED ? static_cast<size_t>(item.mt) * fw * cap : 0);
                     const int mo = FUSED ? m - item.mt * fw : m;
+                    float ws0 = 1.f, ws1 = 1.f;
+                    if (F8) {
+                        ws0 = __ldg(sc.a0 + static_cast<size_t>(item.e) * M + m);
+                        if (has1) ws1 = __ldg(sc.a0 + static_cast<size_t>(item.e) * M + m + BM);
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int n = c0 + j;
                         if (n < item.rows) {
                             float* yr = y + static_cast<size_t>(item.row0 + n) * ystride;
-                            yr[mo] = __uint_as_float(g[j]);
-                            if (has1) yr[mo + BM] = __uint_as_float(g1[j]);
+                            yr[mo] = F8 ? __uint_as_float(g[j]) * ws0 * rs[j] : __uint_as_float(g[j]);
+                            if (has1) yr[mo + BM] = F8 ? __uint_as_float(g1[j]) * ws1 * rs[j] : __uint_as_float(g1[j]);
                         }
                     }
                 }
@@ -863,7 +907,7 @@ __global__ void bounded_wait_probe_kernel(unsigned long long limit_ns, unsigned*
 // ---------------------------------------------------------------------------
 
 std::mutex g_mutex;
-bool g_attr_set[64][4];
+bool g_attr_set[64][8];
 
 // 2-D bf16 tensor map over a row-major [rows][K] matrix with a box of
 // 64 K-elements x box_rows rows and 128-byte swizzle.
@@ -872,29 +916,37 @@ moe_status encode_2d(CUtensorMap* map, const void* base, int K, long long rows, 
                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool GATED, bool FUSED>
+// 2-D E4M3 (one byte per element) tensor map with a box of 128 K-elements
+// (one 128-byte swizzle row, like 64 bf16 elements) x box_rows rows.
+moe_status encode_2d_u8(CUtensorMap* map, const void* base, int K, long long rows, int box_rows) {
+    return encode_2d_map(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, rows, 128, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <bool GATED, bool FUSED, bool F8>
 moe_status set_smem_attr() {
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
-    constexpr int v = (GATED ? 1 : 0) + (FUSED ? 2 : 0);
+    constexpr int v = (GATED ? 1 : 0) + (FUSED ? 2 : 0) + (F8 ? 4 : 0);
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_attr_set[dev][v]) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(ffn_tc_kernel<GATED, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          Cfg<GATED>::smem_bytes(FUSED)));
+        MOE_CUDA_TRY(cudaFuncSetAttribute(ffn_tc_kernel<GATED, FUSED, F8>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<GATED>::smem_bytes(FUSED)));
         g_attr_set[dev][v] = true;
     }
     return MOE_OK;
 }
 
-template <bool GATED, bool FUSED>
+template <bool GATED, bool FUSED, bool F8 = false>
 moe_status launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& bb,
                   const int32_t* offsets, int cap, int E, int K, int M, bool narrow, void* out, const FusedArgs& fa,
-                  cudaStream_t st, const DeviceInfo& di) {
+                  cudaStream_t st, const DeviceInfo& di, const OpScales& sc = OpScales{}) {
     moe_status s;
-    if ((s = set_smem_attr<GATED, FUSED>()) != MOE_OK) return s;
-    ffn_tc_kernel<GATED, FUSED><<<di.sm_count, Roles<GATED, FUSED>::kThreads, Cfg<GATED>::smem_bytes(FUSED), st>>>(
-        a0, a1, b, bb, offsets, cap, E, K, M, narrow ? 1 : 0, out, di.error_word, fa);
+    if ((s = set_smem_attr<GATED, FUSED, F8>()) != MOE_OK) return s;
+    ffn_tc_kernel<GATED, FUSED, F8>
+        <<<di.sm_count, Roles<GATED, FUSED>::kThreads, Cfg<GATED>::smem_bytes(FUSED), st>>>(
+            a0, a1, b, bb, offsets, cap, E, K, M, narrow ? 1 : 0, out, di.error_word, fa, sc);
     return cuda_status(cudaGetLastError());
 }
 
@@ -910,29 +962,99 @@ bool use_narrow(int cap, int E, int tiles_per_expert, const DeviceInfo& di) {
     return cap <= BN / 2 && experts * tiles_per_expert < 4LL * di.sm_count;
 }
 
+moe_status prepare_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                  const void* w_gate, const void* w_up, void* h, const DeviceInfo& di,
+                                  FfnTcLaunch* p) {
+    moe_status s;
+    p->narrow = use_narrow(cap, E, f / BM, di);
+    const int wbox = p->narrow ? BM / 2 : BM;
+    if ((s = encode_2d(&p->a0, w_gate, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
+    if ((s = encode_2d(&p->a1, w_up, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
+    if ((s = encode_2d(&p->b, xs, d, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_2d(&p->bb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
+    p->gated = true;
+    p->offsets = offsets;
+    p->cap = cap;
+    p->E = E;
+    p->K = d;
+    p->M = f;
+    p->out = h;
+    return MOE_OK;
+}
+
+moe_status prepare_ffn_tc_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                               const void* w_down, float* y, const DeviceInfo& di, FfnTcLaunch* p) {
+    moe_status s;
+    if ((s = encode_2d(&p->a0, w_down, f, static_cast<long long>(E) * d, BM)) != MOE_OK) return s;
+    p->a1 = p->a0;
+    if ((s = encode_2d(&p->b, h, f, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_2d(&p->bb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
+    p->narrow = use_narrow(cap, E, (d + 2 * BM - 1) / (2 * BM), di);
+    p->gated = false;
+    p->offsets = offsets;
+    p->cap = cap;
+    p->E = E;
+    p->K = f;
+    p->M = d;
+    p->out = y;
+    return MOE_OK;
+}
+
+moe_status launch_ffn_tc_prepared(const FfnTcLaunch& p, cudaStream_t st, const DeviceInfo& di) {
+    if (p.gated)
+        return launch<true, false>(p.a0, p.a1, p.b, p.bb, p.offsets, p.cap, p.E, p.K, p.M, p.narrow, p.out,
+                                   FusedArgs{}, st, di);
+    return launch<false, false>(p.a0, p.a1, p.b, p.bb, p.offsets, p.cap, p.E, p.K, p.M, p.narrow, p.out,
+                                FusedArgs{}, st, di);
+}
+
 moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
                                  const void* w_gate, const void* w_up, void* h, cudaStream_t st,
                                  const DeviceInfo& di) {
-    CUtensorMap ma0, ma1, mb, mbb;
-    moe_status s;
-    const bool narrow = use_narrow(cap, E, f / BM, di);
-    const int wbox = narrow ? BM / 2 : BM;
-    if ((s = encode_2d(&ma0, w_gate, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
-    if ((s = encode_2d(&ma1, w_up, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
-    if ((s = encode_2d(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
-    if ((s = encode_2d(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
-    return launch<true, false>(ma0, ma1, mb, mbb, offsets, cap, E, d, f, narrow, h, FusedArgs{}, st, di);
+    FfnTcLaunch p;
+    moe_status s = prepare_ffn_tc_gate_up(xs, offsets, cap, E, d, f, w_gate, w_up, h, di, &p);
+    if (s != MOE_OK) return s;
+    return launch_ffn_tc_prepared(p, st, di);
 }
 
 moe_status launch_ffn_tc_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
                               const void* w_down, float* y, cudaStream_t st, const DeviceInfo& di) {
+    FfnTcLaunch p;
+    moe_status s = prepare_ffn_tc_down(h, offsets, cap, E, d, f, w_down, y, di, &p);
+    if (s != MOE_OK) return s;
+    return launch_ffn_tc_prepared(p, st, di);
+}
+
+// A5 with E4M3 weights and E4M3 compact rows (kind::f8f6f4 MMAs).  Narrow
+// items hold two 128-element k-blocks per stage, so they need K to be a
+// multiple of 256.
+moe_status launch_ffn_w8a8_gate_up(const uint8_t* xs, const float* xs_scale, const int32_t* offsets, int cap, int E,
+                                   int d, int f, const uint8_t* q_gate, const float* s_gate, const uint8_t* q_up,
+                                   const float* s_up, void* h, cudaStream_t st, const DeviceInfo& di) {
+    CUtensorMap ma0, ma1, mb, mbb;
+    moe_status s;
+    const bool narrow = use_narrow(cap, E, f / BM, di) && d % 256 == 0;
+    const int wbox = narrow ? BM / 2 : BM;
+    if ((s = encode_2d_u8(&ma0, q_gate, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
+    if ((s = encode_2d_u8(&ma1, q_up, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
+    if ((s = encode_2d_u8(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_2d_u8(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
+    return launch<true, false, true>(ma0, ma1, mb, mbb, offsets, cap, E, d, f, narrow, h, FusedArgs{}, st, di,
+                                     OpScales{s_gate, s_up, xs_scale});
+}
+
+// A6 with E4M3 weights and E4M3 rows of h.
+moe_status launch_ffn_w8a8_down(const uint8_t* hq, const float* h_scale, const int32_t* offsets, int cap, int E,
+                                int d, int f, const uint8_t* q_down, const float* s_down, float* y, cudaStream_t st,
+                                const DeviceInfo& di) {
     CUtensorMap ma0, mb, mbb;
     moe_status s;
-    if ((s = encode_2d(&ma0, w_down, f, static_cast<long long>(E) * d, BM)) != MOE_OK) return s;
-    if ((s = encode_2d(&mb, h, f, cap, kBoxRows)) != MOE_OK) return s;
-    if ((s = encode_2d(&mbb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
-    const bool narrow = use_narrow(cap, E, (d + 2 * BM - 1) / (2 * BM), di);
-    return launch<false, false>(ma0, ma0, mb, mbb, offsets, cap, E, f, d, narrow, y, FusedArgs{}, st, di);
+    if ((s = encode_2d_u8(&ma0, q_down, f, static_cast<long long>(E) * d, BM)) != MOE_OK) return s;
+    if ((s = encode_2d_u8(&mb, hq, f, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_2d_u8(&mbb, hq, f, cap, kBigBoxRows)) != MOE_OK) return s;
+    const bool narrow = use_narrow(cap, E, (d + 2 * BM - 1) / (2 * BM), di) && f % 256 == 0;
+    return launch<false, false, true>(ma0, ma0, mb, mbb, offsets, cap, E, f, d, narrow, y, FusedArgs{}, st, di,
+                                      OpScales{s_down, nullptr, h_scale});
 }
 
 moe_status launch_ffn_tc_gate_up_gather(const void* x, int T, int k, const int32_t* route_of_row,

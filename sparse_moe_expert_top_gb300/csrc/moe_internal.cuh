@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,8 +16,6 @@ enum : unsigned {
     DEVERR_RANGE = 4u,     // a value did not fit the fp16 operands of the FP8-weight path
 };
 
-// Routes handled by one CTA of the histogram kernel (8 warps x 8 steps x 32 lanes).
-constexpr int kHistChunk = 2048;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxK = 16;
 // Chunks with T*k <= kSmallRoutes and T <= kSmallTokens can take A1-A4 in one
@@ -28,8 +27,17 @@ constexpr int kSmallTokens = 128;
 // then chunk_counts[n_chunks][256] (written by the histogram), local_rank[T*k]
 // (histogram), chunk_bases[n_chunks][256] (prefix).  The prefix reads the
 // counts and writes the bases elsewhere, so it can be repeated.
+// Chunks are token-aligned: chunk c holds the routes of tokens
+// [c*ct, (c+1)*ct), ct = ws_chunk_tokens(T), a multiple of 64 chosen so that
+// there are at most kMaxChunks chunks (one CTA of the histogram each).
 constexpr int kWsHeaderWords = 32;
-inline int ws_chunks(int T, int k) { return (T * k + kHistChunk - 1) / kHistChunk; }
+constexpr int kChunkTokenQuantum = 64;
+constexpr int kMaxChunks = 128;
+inline int ws_chunk_tokens(int T) {
+    const int m = (T + kChunkTokenQuantum * kMaxChunks - 1) / (kChunkTokenQuantum * kMaxChunks);
+    return kChunkTokenQuantum * (m > 1 ? m : 1);
+}
+inline int ws_chunks(int T, int /*k*/) { return (T + ws_chunk_tokens(T) - 1) / ws_chunk_tokens(T); }
 inline size_t ws_rank_offset(int T, int k) {
     return kWsHeaderWords + static_cast<size_t>(ws_chunks(T, k)) * kMaxExperts;
 }
@@ -84,6 +92,24 @@ inline int tile_counts_per_token(int d) { return (d + 127) / 128; }
 
 inline int dtype_size(int dtype) { return dtype == MOE_BF16 ? 2 : (dtype == MOE_F32 ? 4 : 0); }
 
+// A launch of the bf16 tensor-core grouped FFN kernel (gate/up + SwiGLU, or
+// down) prepared on the host: its TMA tensor maps encoded once, with the
+// launch arguments.  Replaying it needs no host work beyond the launch.
+struct FfnTcLaunch {
+    CUtensorMap a0, a1, b, bb;   // weight tiles (gate, up / down twice), rows (64-row and big-item boxes)
+    const int32_t* offsets;
+    int cap, E, K, M;
+    bool narrow, gated;
+    void* out;                   // h (bf16) or y (fp32)
+};
+
+moe_status prepare_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                  const void* w_gate, const void* w_up, void* h, const DeviceInfo& di,
+                                  FfnTcLaunch* p);
+moe_status prepare_ffn_tc_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                               const void* w_down, float* y, const DeviceInfo& di, FfnTcLaunch* p);
+moe_status launch_ffn_tc_prepared(const FfnTcLaunch& p, cudaStream_t st, const DeviceInfo& di);
+
 // Kernel launchers implemented in the other translation units.
 moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
                                  const void* w_gate, const void* w_up, void* h, cudaStream_t st,
@@ -110,6 +136,12 @@ moe_status launch_ffn_fp8_gate_up(const void* xs, const int32_t* offsets, int ca
 moe_status launch_ffn_fp8_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
                                const uint8_t* q_down, const float* s_down, float* y, cudaStream_t st,
                                const DeviceInfo& di);
+moe_status launch_ffn_w8a8_gate_up(const uint8_t* xs, const float* xs_scale, const int32_t* offsets, int cap, int E,
+                                   int d, int f, const uint8_t* q_gate, const float* s_gate, const uint8_t* q_up,
+                                   const float* s_up, void* h, cudaStream_t st, const DeviceInfo& di);
+moe_status launch_ffn_w8a8_down(const uint8_t* hq, const float* h_scale, const int32_t* offsets, int cap, int E,
+                                int d, int f, const uint8_t* q_down, const float* s_down, float* y, cudaStream_t st,
+                                const DeviceInfo& di);
 moe_status launch_router_topk(const void* x, const void* wr, int T, int E, int d, int k, float* logits,
                               int32_t* ids, float* w, cudaStream_t st, const DeviceInfo& di);
 // moe_route_scatter_small for the fused path: xs may be NULL (no row copy);

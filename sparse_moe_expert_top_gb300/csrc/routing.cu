@@ -163,20 +163,14 @@ __device__ __forceinline__ void bitonic_merge_desc(float (&g)[N]) {
 
 constexpr int kTopkCand = 32;  // candidate slots per token
 
+// Top-k of token t by the four lanes q = 0..3 of one quad (mask `quad`);
+// cv/ce/sv: the token's candidate list and selected values in shared memory.
+// Every synchronisation is among the quad's lanes.
 template <int KMAX>
-__global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                              int32_t* __restrict__ ids, float* __restrict__ w) {
+__device__ __forceinline__ void topk_quad_token(const float* __restrict__ logits, int t, int E, int k,
+                                                int32_t* __restrict__ ids, float* __restrict__ w, float* cv,
+                                                int* ce, float* sv, int q, unsigned quad) {
     constexpr int kNone = 0x7fffffff;
-    __shared__ float cand_v[4][8][kTopkCand];
-    __shared__ int cand_e[4][8][kTopkCand];
-    __shared__ float sel_v[4][8][KMAX];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3, tw = lane >> 2;
-    const unsigned quad = 0xfu << (lane & ~3);
-    const int t = blockIdx.x * 32 + warp * 8 + tw;
-    // every synchronisation below is among the four lanes of one token, so
-    // the quads of padding tokens past T leave at once (their -inf logits
-    // would all tie at tau and take the slow exact path)
-    if (t >= T) return;
     const int nvec = E >> 2;
 
     // this lane's 16 float4 groups (experts 4c .. 4c+3 for c = q + 4i)
@@ -222,9 +216,6 @@ __global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __
         if (q >= off) incl += o;
     }
     const int n_cand = __shfl_sync(quad, incl, 3, 4);
-    float* cv = cand_v[warp][tw];
-    int* ce = cand_e[warp][tw];
-    float* sv = sel_v[warp][tw];
     if (n_cand <= kTopkCand) {
         int pos = incl - mine;
         auto append = [&](float x, int e) {
@@ -333,97 +324,166 @@ __global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __
     }
 }
 
+template <int KMAX>
+__global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                              int32_t* __restrict__ ids, float* __restrict__ w) {
+    __shared__ float cand_v[4][8][kTopkCand];
+    __shared__ int cand_e[4][8][kTopkCand];
+    __shared__ float sel_v[4][8][KMAX];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane & 3, tw = lane >> 2;
+    const unsigned quad = 0xfu << (lane & ~3);
+    const int t = blockIdx.x * 32 + warp * 8 + tw;
+    // every synchronisation is among the four lanes of one token, so the
+    // quads of padding tokens past T leave at once (their -inf logits would
+    // all tie at tau and take the slow exact path)
+    if (t >= T) return;
+    topk_quad_token<KMAX>(logits, t, E, k, ids, w, cand_v[warp][tw], cand_e[warp][tw], sel_v[warp][tw], q, quad);
+}
+
 // ---------------------------------------------------------------------------
-// A2: route histogram with stable in-chunk ranks.
+// A2 (with TOPK and PREFIX: A1-A3 in one launch): route histogram with
+// stable ranks inside token-aligned chunks.
 //
-// CTA c owns routes [c*2048, (c+1)*2048); warp w of the CTA owns 256 of them
-// and walks them 32 at a time in route order.  __match_any_sync groups the
-// lanes that hit the same expert; a lane's rank is the warp's running count
-// for that expert plus the number of lower lanes in its group, so ranks
-// follow route order.  The per-warp counts are then scanned across warps in
-// warp order, giving every route its stable rank inside the chunk and the
-// chunk's per-expert count.  The last CTA to finish (completion counter in
-// the workspace) sums the chunk counts into counts[] and resets the counter.
+// Chunk c holds the routes of tokens [c*ct, (c+1)*ct), ct = ws_chunk_tokens(T),
+// and CTA c owns it.  The CTA walks its tokens 64 at a time; with TOPK it
+// first routes them (a quad of lanes per token, as route_topk_quad_kernel).
+// Warp w then takes the routes of tokens 8w .. 8w+7 of the pass, 32 at a
+// time in route order: __match_any_sync groups the lanes that hit one
+// expert, and a route's rank is the warp's running count for that expert
+// plus the number of lower lanes of its group.  A scan over the warps, in
+// warp order and on top of the earlier passes' counts, turns these into
+// ranks inside the chunk (route order) and finally the chunk's per-expert
+// counts.  The last CTA to finish (completion counter in the workspace header)
+// sums the chunk counts into counts[]; with PREFIX it also writes the
+// exclusive prefix offsets[] and every chunk's row bases (base[c][e] =
+// offsets[e] + the counts of expert e in the chunks before c), as
+// prefix_offsets_kernel does.  The counter is left at zero for the next call.
 // ---------------------------------------------------------------------------
 
-constexpr int kHistWarps = 8;
-constexpr int kHistSteps = kHistChunk / (kHistWarps * 32);
+constexpr int kChunkWarps = 8;
+constexpr int kPassTokens = kChunkWarps * 8;
 
-__global__ void __launch_bounds__(256) route_histogram_kernel(const int32_t* __restrict__ ids,
-                                                              const uint8_t* __restrict__ mask, int n_routes,
-                                                              int E, int32_t* __restrict__ ws,
-                                                              int32_t* __restrict__ counts, unsigned* err) {
-    __shared__ int cnt[kHistWarps][kMaxExperts];
+template <int KMAX, bool TOPK, bool PREFIX>
+__global__ void __launch_bounds__(256) route_chunks_kernel(const float* __restrict__ logits,
+                                                           const uint8_t* __restrict__ mask, int T, int E, int k,
+                                                           int chunk_tokens, int32_t* ids, float* __restrict__ w,
+                                                           int32_t* __restrict__ ws, int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets, unsigned* err) {
+    __shared__ float cand_v[TOPK ? kChunkWarps : 1][8][kTopkCand];
+    __shared__ int cand_e[TOPK ? kChunkWarps : 1][8][kTopkCand];
+    __shared__ float sel_v[TOPK ? kChunkWarps : 1][8][KMAX];
+    __shared__ int cnt[kChunkWarps][kMaxExperts];
+    __shared__ int running[kMaxExperts];
+    __shared__ int e_w[kChunkWarps][8 * kMaxK];      // expert of each route of the warp's tokens (-1: masked)
+    __shared__ int rank_w[kChunkWarps][8 * kMaxK];   // its rank among the warp's routes to that expert
+    __shared__ int warp_sum[kChunkWarps];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x, n_chunks = gridDim.x;
     int32_t* chunk_counts = ws + kWsHeaderWords;
-    int32_t* lrank = chunk_counts + static_cast<size_t>(gridDim.x) * kMaxExperts;
+    int32_t* lrank = chunk_counts + static_cast<size_t>(n_chunks) * kMaxExperts;
+    const int t_begin = c * chunk_tokens, t_end = min(T, t_begin + chunk_tokens);
 
-    for (int i = tid; i < kHistWarps * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    for (int i = tid; i < kChunkWarps * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    running[tid] = 0;   // blockDim.x == kMaxExperts
     __syncthreads();
 
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int base = blockIdx.x * kHistChunk + warp * (kHistSteps * 32);
-    int my_e[kHistSteps], my_rank[kHistSteps];
     bool bad = false;
-#pragma unroll
-    for (int step = 0; step < kHistSteps; ++step) {
-        const int r = base + step * 32 + lane;
-        int e = -1;
-        if (r < n_routes) {
-            e = __ldg(ids + r);
-            if (e < 0 || e >= E) {
-                bad = true;
-                e = -1;
-            } else if (mask != nullptr && __ldg(mask + r) != 0) {
-                e = -1;
+    for (int p0 = t_begin; p0 < t_end; p0 += kPassTokens) {
+        const int w0 = p0 + warp * 8;                           // the warp's first token
+        const int nt = max(0, min(8, t_end - w0));
+        if (TOPK) {
+            const int q = lane & 3, tw = lane >> 2;
+            // quads past the chunk's end skip the routing (their syncs are quad-local)
+            if (tw < nt)
+                topk_quad_token<KMAX>(logits, w0 + tw, E, k, ids, w, cand_v[warp][tw], cand_e[warp][tw],
+                                      sel_v[warp][tw], q, 0xfu << (lane & ~3));
+            __syncwarp();   // the warp's ids, written above, are read below by other lanes of the warp
+        }
+        const int n_r = nt * k, r0 = w0 * k;
+        for (int j0 = 0; j0 < n_r; j0 += 32) {
+            const int j = j0 + lane;
+            int e = -1;
+            if (j < n_r) {
+                e = ids[r0 + j];
+                if (e < 0 || e >= E) {
+                    bad = true;
+                    e = -1;
+                } else if (mask != nullptr && mask[r0 + j] != 0) {
+                    e = -1;
+                }
+            }
+            const unsigned peers = __match_any_sync(kFull, e);
+            const int rank = e >= 0 ? cnt[warp][e] + __popc(peers & lt_mask) : -1;
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp][e] += __popc(peers);
+            __syncwarp();
+            if (j < n_r) {
+                e_w[warp][j] = e;
+                rank_w[warp][j] = rank;
             }
         }
-        const unsigned peers = __match_any_sync(kFull, e);
-        int rank = -1;
-        if (e >= 0) rank = cnt[warp][e] + __popc(peers & lt_mask);
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp][e] += __popc(peers);
-        __syncwarp();
-        my_e[step] = e;
-        my_rank[step] = rank;
+        __syncthreads();
+        // per expert: the warps' counts in warp order, on top of the earlier passes
+        {
+            int run = running[tid];
+#pragma unroll
+            for (int ww = 0; ww < kChunkWarps; ++ww) {
+                const int cc = cnt[ww][tid];
+                cnt[ww][tid] = run;
+                run += cc;
+            }
+            running[tid] = run;
+        }
+        __syncthreads();
+        for (int j = lane; j < n_r; j += 32) {
+            const int e = e_w[warp][j];
+            lrank[r0 + j] = e >= 0 ? rank_w[warp][j] + cnt[warp][e] : -1;
+        }
+        __syncthreads();
+        for (int i = tid; i < kChunkWarps * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
+        __syncthreads();
     }
     if (bad) atomicOr(err, DEVERR_OFFSETS);
-    __syncthreads();
+    chunk_counts[static_cast<size_t>(c) * kMaxExperts + tid] = running[tid];
 
-    // exclusive scan over warps, per expert
-    for (int e = tid; e < kMaxExperts; e += blockDim.x) {
-        int run = 0;
-#pragma unroll
-        for (int w = 0; w < kHistWarps; ++w) {
-            const int c = cnt[w][e];
-            cnt[w][e] = run;
-            run += c;
-        }
-        chunk_counts[static_cast<size_t>(blockIdx.x) * kMaxExperts + e] = run;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int step = 0; step < kHistSteps; ++step) {
-        const int r = base + step * 32 + lane;
-        if (r < n_routes) lrank[r] = my_e[step] >= 0 ? my_rank[step] + cnt[warp][my_e[step]] : -1;
-    }
-
-    // last CTA reduces the chunk counts
+    // the last CTA reduces the chunk counts (and, with PREFIX, scans them)
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_last = (atomicAdd(reinterpret_cast<unsigned*>(ws), 1u) == gridDim.x - 1);
+    if (tid == 0) s_last = (atomicAdd(reinterpret_cast<unsigned*>(ws), 1u) == static_cast<unsigned>(n_chunks - 1));
     __syncthreads();
-    if (s_last) {
-        __threadfence();
-        for (int e = tid; e < E; e += blockDim.x) {
-            int sum = 0;
-            for (int c = 0; c < static_cast<int>(gridDim.x); ++c)
-                sum += __ldcg(chunk_counts + static_cast<size_t>(c) * kMaxExperts + e);
-            counts[e] = sum;
+    if (!s_last) return;
+    __threadfence();
+    const int e = tid;
+    int total = 0;
+    if (e < E)
+        for (int cc = 0; cc < n_chunks; ++cc) total += __ldcg(chunk_counts + static_cast<size_t>(cc) * kMaxExperts + e);
+    if (e < E) counts[e] = total;
+    if (PREFIX) {
+        int incl = total;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += o;
         }
-        if (tid == 0) atomicExch(reinterpret_cast<unsigned*>(ws), 0u);
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        int before = 0;
+        for (int ww = 0; ww < warp; ++ww) before += warp_sum[ww];
+        const int excl = before + incl - total;
+        if (e < E) offsets[e] = excl;
+        if (e == E - 1) offsets[E] = excl + total;
+        int32_t* bases = lrank + static_cast<size_t>(T) * k;
+        if (e < E) {
+            int run = excl;
+            for (int cc = 0; cc < n_chunks; ++cc) {
+                bases[static_cast<size_t>(cc) * kMaxExperts + e] = run;
+                run += __ldcg(chunk_counts + static_cast<size_t>(cc) * kMaxExperts + e);
+            }
+        }
     }
+    if (tid == 0) atomicExch(reinterpret_cast<unsigned*>(ws), 0u);
 }
 
 // ---------------------------------------------------------------------------
@@ -491,7 +551,9 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
                                                            int32_t* __restrict__ row_of_route,
                                                            int32_t* __restrict__ route_of_row, unsigned* err,
                                                            int32_t* __restrict__ tile_counts, int n_counts,
-                                                           float4* __restrict__ out, int d4) {
+                                                           float4* __restrict__ out, int d4, int chunk_tokens,
+                                                           const float* __restrict__ scale_in = nullptr,
+                                                           float* __restrict__ scale_out = nullptr) {
     __shared__ int rows[kMaxK];
     __shared__ int tails[kMaxK];
     const int t = blockIdx.x, tid = threadIdx.x;
@@ -503,7 +565,7 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
         bool bad = false;
         if (lr >= 0) {
             const int e = ids[r];
-            if (e >= 0 && e < E) row = bases[static_cast<size_t>(r / kHistChunk) * kMaxExperts + e] + lr;
+            if (e >= 0 && e < E) row = bases[static_cast<size_t>(t / chunk_tokens) * kMaxExperts + e] + lr;
             if (row < 0 || row >= n_routes) {
                 bad = true;
                 row = -1;
@@ -519,6 +581,11 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
         tails[tid] = tail;
         if (tail >= 0) route_of_row[tail] = -1;
         if (bad) atomicOr(err, DEVERR_OFFSETS);
+        if (scale_out != nullptr) {
+            // rows carrying E4M3 codes: each compact row gets its token row's scale
+            if (row >= 0) scale_out[row] = __ldg(scale_in + t);
+            if (tail >= 0) scale_out[tail] = 0.f;
+        }
     }
     __syncthreads();
     if (tile_counts != nullptr) {
@@ -561,7 +628,8 @@ __global__ void __launch_bounds__(256) scatter_index_kernel(const int32_t* __res
                                                             int32_t* __restrict__ row_of_route,
                                                             int32_t* __restrict__ route_of_row,
                                                             int32_t* __restrict__ tile_counts, int n_counts,
-                                                            float4* __restrict__ out, int d4, unsigned* err) {
+                                                            float4* __restrict__ out, int d4, unsigned* err,
+                                                            int chunk_tokens) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -573,7 +641,7 @@ __global__ void __launch_bounds__(256) scatter_index_kernel(const int32_t* __res
         bool bad = false;
         if (lr >= 0) {
             const int e = ids[r];
-            if (e >= 0 && e < E) row = bases[static_cast<size_t>(r / kHistChunk) * kMaxExperts + e] + lr;
+            if (e >= 0 && e < E) row = bases[static_cast<size_t>(t / chunk_tokens) * kMaxExperts + e] + lr;
             if (row < 0 || row >= n_routes) {
                 bad = true;
                 row = -1;
@@ -840,10 +908,19 @@ __global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
 moe_status launch_status() { return cuda_status(cudaGetLastError()); }
 
 // Largest chunk the allocation-free histogram accepts, and its scratch size:
-// header + per-chunk counts + one in-chunk rank per route (295 KB).
+// header + per-chunk counts (at most kMaxChunks chunks) + one in-chunk rank
+// per route (384 KB).
 constexpr int kNoAllocMaxRoutes = 65536;
-constexpr int kNoAllocWords =
-    kWsHeaderWords + ((kNoAllocMaxRoutes + kHistChunk - 1) / kHistChunk) * kMaxExperts + kNoAllocMaxRoutes;
+constexpr int kNoAllocWords = kWsHeaderWords + kMaxChunks * kMaxExperts + kNoAllocMaxRoutes;
+
+// A2 (histogram only) over the token-aligned chunks of `ws`.
+moe_status launch_histogram(const int32_t* ids, const uint8_t* mask, int T, int k, int E, int32_t* counts,
+                            int32_t* ws, cudaStream_t s, const DeviceInfo& di) {
+    route_chunks_kernel<8, false, false><<<ws_chunks(T, k), kMaxExperts, 0, s>>>(
+        nullptr, mask, T, E, k, ws_chunk_tokens(T), const_cast<int32_t*>(ids), nullptr, ws, counts, nullptr,
+        di.error_word);
+    return launch_status();
+}
 
 }  // namespace
 }  // namespace moe
@@ -936,9 +1013,38 @@ extern "C" moe_status moe_route_histogram(const int32_t* ids, const uint8_t* mas
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T == 0) return cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s));
     MOE_REQUIRE(ids);
-    const int n_routes = T * k;
-    route_histogram_kernel<<<ws_chunks(T, k), 256, 0, s>>>(ids, mask, n_routes, E, static_cast<int32_t*>(ws),
-                                                          counts, di.error_word);
+    return launch_histogram(ids, mask, T, k, E, counts, static_cast<int32_t*>(ws), s, di);
+}
+
+extern "C" moe_status moe_route_topk_offsets(const float* logits, const uint8_t* mask, int T, int E, int k,
+                                             int32_t* ids, float* w, int32_t* counts, int32_t* offsets, void* ws,
+                                             void* stream) {
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E);
+    MOE_REQUIRE(counts && offsets && ws && aligned16(ws));
+    if (T == 0) {
+        moe_status st = moe_route_histogram(nullptr, nullptr, 0, k, E, counts, ws, stream);
+        return st != MOE_OK ? st : moe_prefix_offsets(counts, 0, k, E, offsets, ws, stream);
+    }
+    MOE_REQUIRE(logits && ids && w);
+    if (E % 4 != 0 || !aligned16(logits)) {
+        // the quad top-k reads float4 groups: other shapes take the three step kernels
+        moe_status st = moe_route_topk(logits, T, E, k, ids, w, stream);
+        if (st == MOE_OK) st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream);
+        if (st == MOE_OK) st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream);
+        return st;
+    }
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int chunks = ws_chunks(T, k), ct = ws_chunk_tokens(T);
+    int32_t* w32 = static_cast<int32_t*>(ws);
+    if (k <= 8)
+        route_chunks_kernel<8, true, true><<<chunks, kMaxExperts, 0, s>>>(logits, mask, T, E, k, ct, ids, w, w32,
+                                                                        counts, offsets, di.error_word);
+    else
+        route_chunks_kernel<16, true, true><<<chunks, kMaxExperts, 0, s>>>(logits, mask, T, E, k, ct, ids, w, w32,
+                                                                         counts, offsets, di.error_word);
     return launch_status();
 }
 
@@ -975,7 +1081,7 @@ moe_status scatter_rows(const void* x, int es, bool to_f16, const int32_t* ids, 
     kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(x), ids, offsets, T, k, E, row_vecs, w32 + ws_rank_offset(T, k),
         w32 + ws_bases_offset(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word, nullptr, 0,
-        nullptr, 0);
+        nullptr, 0, ws_chunk_tokens(T), nullptr, nullptr);
     return launch_status();
 }
 
@@ -1016,12 +1122,33 @@ extern "C" moe_status moe_scatter_index(const int32_t* ids, const uint8_t* mask,
         scatter_rows_kernel<false><<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
             static_cast<const uint4*>(x), ids, offsets, T, k, E, d / 8, w32 + ws_rank_offset(T, k),
             w32 + ws_bases_offset(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word,
-            tile_counts, tile_counts_per_token(d), reinterpret_cast<float4*>(out), d / 4);
+            tile_counts, tile_counts_per_token(d), reinterpret_cast<float4*>(out), d / 4, ws_chunk_tokens(T));
         return launch_status();
     }
     scatter_index_kernel<<<(T + 7) / 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         ids, offsets, T, k, E, w32 + ws_rank_offset(T, k), w32 + ws_bases_offset(T, k), row_of_route, route_of_row,
-        tile_counts, tile_counts_per_token(d), reinterpret_cast<float4*>(out), d / 4, di.error_word);
+        tile_counts, tile_counts_per_token(d), reinterpret_cast<float4*>(out), d / 4, di.error_word,
+        ws_chunk_tokens(T));
+    return launch_status();
+}
+
+extern "C" moe_status moe_scatter_rows_e4m3(const uint8_t* x_codes, const float* x_scales, const int32_t* ids,
+                                            const uint8_t* mask, const int32_t* offsets, int T, int k, int d, int E,
+                                            uint8_t* xs, float* xs_scales, int32_t* row_of_route,
+                                            int32_t* route_of_row, void* ws, void* stream) {
+    (void)mask;  // folded into the workspace ranks by the histogram
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 16 && d % 16 == 0);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(x_codes && x_scales && ids && offsets && xs && xs_scales && row_of_route && route_of_row && ws);
+    MOE_REQUIRE(aligned16(x_codes) && aligned16(xs) && aligned16(ws));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    const int32_t* w32 = static_cast<const int32_t*>(ws);
+    scatter_rows_kernel<false><<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const uint4*>(x_codes), ids, offsets, T, k, E, d / 16, w32 + ws_rank_offset(T, k),
+        w32 + ws_bases_offset(T, k), reinterpret_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word,
+        nullptr, 0, nullptr, 0, ws_chunk_tokens(T), x_scales, xs_scales);
     return launch_status();
 }
 
@@ -1130,6 +1257,5 @@ extern "C" moe_status moe_route_histogram_noalloc(const int32_t* ids, const uint
     if (T == 0) return cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s));
     MOE_REQUIRE(ids != nullptr);
     MOE_CUDA_TRY(cudaMemsetAsync(scratch, 0, sizeof(int32_t), s));
-    route_histogram_kernel<<<ws_chunks(T, k), 256, 0, s>>>(ids, mask, T * k, E, scratch, counts, di.error_word);
-    return launch_status();
+    return launch_histogram(ids, mask, T, k, E, counts, scratch, s, di);
 }

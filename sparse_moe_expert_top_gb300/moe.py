@@ -60,6 +60,19 @@ SIGNATURES = {
     "moe_grouped_down_combine": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_forward_fused": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I,
                            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_clear_device_error": ([_P], _I),
+    "moe_scatter_rows_e4m3": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_gate_up_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_down_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_forward_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 6 + [_P] * 17, _I),
+    "moe_route_topk_offsets": ([_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_forward_fused_mode": ([_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)], _I),
+    "moe_plan_create": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                         ctypes.POINTER(ctypes.c_void_p)], _I),
+    "moe_plan_destroy": ([_P], _I),
+    "moe_plan_grouped_gate_up": ([_P, _P], _I),
+    "moe_plan_grouped_down": ([_P, _P], _I),
+    "moe_plan_forward": ([_P, _P, _P, _P, _P, _P], _I),
 }
 
 
@@ -181,6 +194,11 @@ def moe_check_device_error(stream=None) -> None:
     _check("moe_check_device_error", load().moe_check_device_error(_stream(stream)))
 
 
+def moe_clear_device_error(stream=None) -> None:
+    """Enqueue the clearing of the device error word on the stream (no synchronisation)."""
+    _check("moe_clear_device_error", load().moe_clear_device_error(_stream(stream)))
+
+
 def moe_selftest_bounded_wait(limit_ms: int, stream=None) -> None:
     """Run one bounded wait that is bound to run out (see include/moe.h)."""
     _check("moe_selftest_bounded_wait", load().moe_selftest_bounded_wait(limit_ms, _stream(stream)))
@@ -222,6 +240,21 @@ def moe_route_histogram(ids, mask, E, counts, ws, stream=None):
     _expect(counts, torch.int32, (E,), "counts")
     _check("moe_route_histogram", load().moe_route_histogram(_ptr(ids), _ptr(mask), T, k, E, _ptr(counts), _ptr(ws),
                                                              _stream(stream)))
+
+
+def moe_route_topk_offsets(logits, mask, k, ids, w, counts, offsets, ws, stream=None):
+    """A1-A3 in one launch (moe_route_topk + moe_route_histogram + moe_prefix_offsets)."""
+    T, E = logits.shape
+    _expect(logits, torch.float32, (T, E), "logits")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect(ids, torch.int32, (T, k), "ids")
+    _expect(w, torch.float32, (T, k), "w")
+    _expect(counts, torch.int32, (E,), "counts")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _check("moe_route_topk_offsets", load().moe_route_topk_offsets(
+        _ptr(logits), _ptr(mask), T, E, k, _ptr(ids), _ptr(w), _ptr(counts), _ptr(offsets), _ptr(ws),
+        _stream(stream)))
 
 
 def moe_route_histogram_noalloc(ids, mask, E, counts, stream=None):
@@ -499,12 +532,13 @@ def moe_forward_fused(logits, x, mask, w_gate, w_up, w_down, k: int, bufs: MoEBu
 # ---------------------------------------------------------------------------
 
 class FP8Weights:
-    """One expert bank in FP8 E4M3: ``codes`` uint8 [E][rows][K], ``scales`` fp32 [E][rows]."""
+    """Rows in FP8 E4M3: ``codes`` uint8 [..., rows, K] and one fp32 scale per row, ``scales`` [..., rows]
+    (an expert bank [E][rows][K], or activation rows [rows][K])."""
 
     def __init__(self, codes: torch.Tensor, scales: torch.Tensor):
-        if codes.dtype != torch.uint8 or scales.dtype != torch.float32 or codes.dim() != 3:
-            raise ValueError("expected uint8 codes [E][rows][K] and fp32 scales [E][rows]")
-        if tuple(scales.shape) != tuple(codes.shape[:2]):
+        if codes.dtype != torch.uint8 or scales.dtype != torch.float32 or codes.dim() < 2:
+            raise ValueError("expected uint8 codes [..., rows, K] and fp32 scales [..., rows]")
+        if tuple(scales.shape) != tuple(codes.shape[:-1]):
             raise ValueError(f"scales {tuple(scales.shape)} do not match codes {tuple(codes.shape)}")
         self.codes, self.scales = codes, scales
 
@@ -514,18 +548,20 @@ class FP8Weights:
 
 
 def moe_quantize_weights_fp8(w, codes=None, scales=None, stream=None) -> FP8Weights:
-    """Quantize a bank [E][rows][K] (bf16 or fp32) to FP8 E4M3 codes and per-row scales."""
-    if w.dim() != 3:
-        raise ValueError("expected a weight bank [E][rows][K]")
-    E, rows, K = w.shape
+    """Quantize rows (a bank [E][rows][K], or activation rows [rows][K]; bf16 or fp32) to FP8 E4M3 codes and
+    one scale per row."""
+    if w.dim() < 2:
+        raise ValueError("expected rows [..., rows, K]")
+    K = w.shape[-1]
+    n_rows = w.numel() // K if K else 0
     if codes is None:
-        codes = torch.empty(E, rows, K, dtype=torch.uint8, device=w.device)
+        codes = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
     if scales is None:
-        scales = torch.empty(E, rows, dtype=torch.float32, device=w.device)
-    _expect(codes, torch.uint8, (E, rows, K), "codes")
-    _expect(scales, torch.float32, (E, rows), "scales")
+        scales = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _expect(codes, torch.uint8, tuple(w.shape), "codes")
+    _expect(scales, torch.float32, tuple(w.shape[:-1]), "scales")
     _check("moe_quantize_weights_fp8", load().moe_quantize_weights_fp8(
-        _ptr(w), _dtype_code(w), E * rows, K, _ptr(codes), _ptr(scales), _stream(stream)))
+        _ptr(w), _dtype_code(w), n_rows, K, _ptr(codes), _ptr(scales), _stream(stream)))
     return FP8Weights(codes, scales)
 
 
@@ -598,4 +634,169 @@ def moe_forward_fp8(logits, x, mask, q_gate: FP8Weights, q_up: FP8Weights, q_dow
         _ptr(q_up.codes), _ptr(q_up.scales), _ptr(q_down.codes), _ptr(q_down.scales),
         _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
         _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
+    return b.out
+
+
+def moe_forward_fused_mode(T: int, E: int, k: int, d: int, have_xs: bool = True) -> int:
+    """The mode moe_forward_fused picks for MOE_FUSED_AUTO on the current device."""
+    mode = ctypes.c_int(-1)
+    _check("moe_forward_fused_mode", load().moe_forward_fused_mode(T, E, k, d, 1 if have_xs else 0,
+                                                                   ctypes.byref(mode)))
+    return mode.value
+
+
+# ---------------------------------------------------------------------------
+# Plans: shapes, weights and buffers fixed, host work done once
+# ---------------------------------------------------------------------------
+
+class MoEPlan:
+    """A moe_plan handle with the tensors behind its pointers (kept alive while the plan lives)."""
+
+    def __init__(self, handle, keep):
+        self._handle = handle
+        self._keep = keep
+
+    @property
+    def handle(self):
+        return self._handle
+
+    def close(self):
+        if self._handle is not None and _lib is not None:
+            load().moe_plan_destroy(self._handle)
+        self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # pragma: no cover - interpreter shutdown
+            pass
+
+
+def moe_plan_create(w_gate, w_up, w_down, bufs: MoEBuffers) -> MoEPlan:
+    """A plan for chunks of bufs.T tokens with these weights and buffers (see include/moe.h)."""
+    b = bufs
+    T, E, k, d, f = b.T, b.E, b.k, b.d, b.f
+    _expect(w_gate, b.dtype, (E, f, d), "w_gate")
+    _expect(w_up, b.dtype, (E, f, d), "w_up")
+    _expect(w_down, b.dtype, (E, d, f), "w_down")
+    handle = ctypes.c_void_p()
+    _check("moe_plan_create", load().moe_plan_create(
+        T, E, k, d, f, _dtype_code(w_gate), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(b.ids), _ptr(b.w),
+        _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route), _ptr(b.route_of_row), _ptr(b.h),
+        _ptr(b.y), _ptr(b.ws), ctypes.byref(handle)))
+    return MoEPlan(handle, (w_gate, w_up, w_down, b))
+
+
+def moe_plan_grouped_gate_up(plan: MoEPlan, stream=None):
+    _check("moe_plan_grouped_gate_up", load().moe_plan_grouped_gate_up(plan.handle, _stream(stream)))
+
+
+def moe_plan_grouped_down(plan: MoEPlan, stream=None):
+    _check("moe_plan_grouped_down", load().moe_plan_grouped_down(plan.handle, _stream(stream)))
+
+
+def moe_plan_forward(plan: MoEPlan, logits, x, mask, out=None, stream=None) -> torch.Tensor:
+    """moe_forward through the plan; returns out (default: the plan's bufs.out)."""
+    b = plan._keep[3]
+    out = b.out if out is None else out
+    _expect(logits, torch.float32, (b.T, b.E), "logits")
+    _expect(x, b.dtype, (b.T, b.d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (b.T, b.k), "mask")
+    _expect(out, torch.float32, (b.T, b.d), "out")
+    _check("moe_plan_forward", load().moe_plan_forward(plan.handle, _ptr(logits), _ptr(x), _ptr(mask), _ptr(out),
+                                                       _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 weights and activations (kind::f8f6f4 tensor-core MMAs)
+# ---------------------------------------------------------------------------
+
+class MoEBuffersW8A8:
+    """Caller-owned device buffers of the FP8-activation path for one chunk shape (bf16 x)."""
+
+    def __init__(self, T: int, E: int, k: int, d: int, f: int, device="cuda"):
+        self.T, self.E, self.k, self.d, self.f = T, E, k, d, f
+        cap = T * k
+        i32 = dict(dtype=torch.int32, device=device)
+        self.ids = torch.empty(T, k, **i32)
+        self.w = torch.empty(T, k, dtype=torch.float32, device=device)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.x_q = torch.empty(T, d, dtype=torch.uint8, device=device)
+        self.x_scales = torch.empty(T, dtype=torch.float32, device=device)
+        self.xs = torch.empty(cap, d, dtype=torch.uint8, device=device)
+        self.xs_scales = torch.empty(cap, dtype=torch.float32, device=device)
+        self.row_of_route = torch.empty(cap, **i32)
+        self.route_of_row = torch.empty(cap, **i32)
+        self.h = torch.empty(cap, f, dtype=torch.bfloat16, device=device)
+        self.h_q = torch.empty(cap, f, dtype=torch.uint8, device=device)
+        self.h_scales = torch.empty(cap, dtype=torch.float32, device=device)
+        self.y = torch.empty(cap, d, dtype=torch.float32, device=device)
+        self.out = torch.empty(T, d, dtype=torch.float32, device=device)
+        self.ws = torch.zeros(max(moe_workspace_size(T, k), 16) // 4 + 4, dtype=torch.int32, device=device)
+
+
+def moe_scatter_rows_e4m3(x_q, x_scales, ids, mask, offsets, xs, xs_scales, row_of_route, route_of_row, ws,
+                          stream=None):
+    T, d = x_q.shape
+    k = ids.shape[1]
+    E = offsets.shape[0] - 1
+    _expect(x_q, torch.uint8, (T, d), "x_q")
+    _expect(x_scales, torch.float32, (T,), "x_scales")
+    _expect(xs, torch.uint8, (T * k, d), "xs")
+    _expect(xs_scales, torch.float32, (T * k,), "xs_scales")
+    _check("moe_scatter_rows_e4m3", load().moe_scatter_rows_e4m3(
+        _ptr(x_q), _ptr(x_scales), _ptr(ids), _ptr(mask), _ptr(offsets), T, k, d, E, _ptr(xs), _ptr(xs_scales),
+        _ptr(row_of_route), _ptr(route_of_row), _ptr(ws), _stream(stream)))
+
+
+def moe_grouped_gate_up_w8a8(xs, xs_scales, offsets, q_gate: FP8Weights, q_up: FP8Weights, h, stream=None):
+    cap, d = xs.shape
+    E, f, _ = q_gate.shape
+    _expect(xs, torch.uint8, (cap, d), "xs")
+    _expect(xs_scales, torch.float32, (cap,), "xs_scales")
+    _expect_fp8(q_gate, (E, f, d), "q_gate")
+    _expect_fp8(q_up, (E, f, d), "q_up")
+    _expect(h, torch.bfloat16, (cap, f), "h")
+    _check("moe_grouped_gate_up_w8a8", load().moe_grouped_gate_up_w8a8(
+        _ptr(xs), _ptr(xs_scales), _ptr(offsets), cap, E, d, f, _ptr(q_gate.codes), _ptr(q_gate.scales),
+        _ptr(q_up.codes), _ptr(q_up.scales), _ptr(h), _stream(stream)))
+
+
+def moe_grouped_down_w8a8(h_q, h_scales, offsets, q_down: FP8Weights, y, stream=None):
+    cap, f = h_q.shape
+    E, d, _ = q_down.shape
+    _expect(h_q, torch.uint8, (cap, f), "h_q")
+    _expect(h_scales, torch.float32, (cap,), "h_scales")
+    _expect_fp8(q_down, (E, d, f), "q_down")
+    _expect(y, torch.float32, (cap, d), "y")
+    _check("moe_grouped_down_w8a8", load().moe_grouped_down_w8a8(
+        _ptr(h_q), _ptr(h_scales), _ptr(offsets), cap, E, d, f, _ptr(q_down.codes), _ptr(q_down.scales), _ptr(y),
+        _stream(stream)))
+
+
+def moe_forward_w8a8(logits, x, mask, q_gate: FP8Weights, q_up: FP8Weights, q_down: FP8Weights, k: int,
+                     bufs: MoEBuffersW8A8, stream=None) -> torch.Tensor:
+    """The whole path on E4M3 weights and activations; returns ``bufs.out`` ([T][d] fp32)."""
+    T, E = logits.shape
+    d = x.shape[1]
+    f = q_gate.shape[1]
+    if (bufs.T, bufs.E, bufs.k, bufs.d, bufs.f) != (T, E, k, d, f):
+        raise ValueError("buffers were allocated for another shape")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect_fp8(q_gate, (E, f, d), "q_gate")
+    _expect_fp8(q_up, (E, f, d), "q_up")
+    _expect_fp8(q_down, (E, d, f), "q_down")
+    b = bufs
+    _check("moe_forward_w8a8", load().moe_forward_w8a8(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, f, _ptr(q_gate.codes), _ptr(q_gate.scales),
+        _ptr(q_up.codes), _ptr(q_up.scales), _ptr(q_down.codes), _ptr(q_down.scales),
+        _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.x_q), _ptr(b.x_scales), _ptr(b.xs),
+        _ptr(b.xs_scales), _ptr(b.row_of_route), _ptr(b.route_of_row), _ptr(b.h), _ptr(b.h_q), _ptr(b.h_scales),
+        _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
     return b.out

@@ -94,13 +94,17 @@ def oracle_weights(w_gate, w_up, w_down, fp8=False, check_codes=None):
     (FP8 E4M3 codes + per-channel scales) and works on the values the codes stand for; check_codes, if
     given, is called as check_codes(e0, e1, banks) with the oracle's quantized banks of the block."""
     from oracle import moe_oracle as mo
+    quantized = {}
 
     def fetch(e0, e1):
         banks = tuple(None if w is None else w[e0:e1].detach().cpu() for w in (w_gate, w_up, w_down))
         if fp8:
-            banks = tuple(None if b is None else mo.quantize_bank_fp8(b) for b in banks)
-            if check_codes is not None:
-                check_codes(e0, e1, banks)
+            # each block is quantized once (the gate/up and the down step both visit it)
+            if (e0, e1) not in quantized:
+                quantized[(e0, e1)] = tuple(None if b is None else mo.quantize_bank_fp8(b) for b in banks)
+                if check_codes is not None:
+                    check_codes(e0, e1, quantized[(e0, e1)])
+            banks = quantized[(e0, e1)]
         return banks
 
     return fetch

@@ -39,7 +39,9 @@ def test_header_declares_the_path_entry_points():
                      "moe_route_scatter_small", "moe_router_topk", "moe_scatter_index",
                      "moe_grouped_gate_up_gather", "moe_grouped_down_combine", "moe_forward_fused",
                      "moe_tile_counts_size", "moe_route_scatter_small_fused",
-                     "moe_workspace_size", "moe_check_device_error"):
+                     "moe_workspace_size", "moe_check_device_error", "moe_clear_device_error",
+                     "moe_forward_fused_mode", "moe_plan_create", "moe_plan_destroy", "moe_plan_grouped_gate_up",
+                     "moe_plan_grouped_down", "moe_plan_forward"):
         assert required in names
 
 
@@ -62,8 +64,11 @@ def test_host_only_calls(lib):
     assert lib.moe_status_string(5) == b"a value out of the fp16 operand range"
     n = ctypes.c_size_t(0)
     assert lib.moe_workspace_size(2048, 6, ctypes.byref(n)) == 0
-    # header (32 words) + 6 chunks of 256 counts + 12288 ranks + 6 chunks of 256 bases, int32
-    assert n.value == 4 * (32 + 6 * 256 + 2048 * 6 + 6 * 256)
+    # header (32 words) + 32 chunks of 64 tokens x 256 counts + 12288 ranks + 32 chunks of 256 bases, int32
+    assert n.value == 4 * (32 + 32 * 256 + 2048 * 6 + 32 * 256)
+    # beyond 128 chunks of 64 tokens the chunks grow: 8193 tokens -> 65 chunks of 128 tokens
+    assert lib.moe_workspace_size(8193, 6, ctypes.byref(n)) == 0
+    assert n.value == 4 * (32 + 65 * 256 + 8193 * 6 + 65 * 256)
     assert lib.moe_workspace_size(10, 17, ctypes.byref(n)) == 1      # k > 16
     assert lib.moe_workspace_size(-1, 2, ctypes.byref(n)) == 1       # T < 0
     # argument checks reject before touching the device
@@ -101,6 +106,30 @@ def test_host_only_calls(lib):
                                  fake, None, None, None, None, None, None, None, None, None) == 1  # compact, no xs
     assert lib.moe_forward_fused(None, None, None, 4, 8, 2, 128, 128, None, None, None, 7, None, None, None,
                                  fake, fake, None, None, None, None, None, None, None, None) == 1  # mode
+
+
+def test_plan_entry_points_reject_bad_arguments(lib):
+    """Plan creation checks its arguments before touching a device and leaves *plan NULL on failure."""
+    fake = ctypes.c_void_p(4096)
+    plan = ctypes.c_void_p(1234)
+    args = [fake] * 13
+    assert lib.moe_plan_create(0, 8, 2, 128, 128, 1, *args, ctypes.byref(plan)) == 1      # T = 0
+    assert plan.value is None
+    plan = ctypes.c_void_p(1234)
+    assert lib.moe_plan_create(4, 8, 2, 100, 128, 1, *args, ctypes.byref(plan)) == 1      # bf16 d % 128
+    assert plan.value is None
+    assert lib.moe_plan_create(4, 8, 2, 128, 128, 7, *args, ctypes.byref(plan)) == 2      # dtype
+    bad = list(args)
+    bad[7] = None                                                                           # xs missing
+    assert lib.moe_plan_create(4, 8, 2, 128, 128, 1, *bad, ctypes.byref(plan)) == 1
+    assert lib.moe_plan_create(4, 8, 2, 128, 128, 1, *args, None) == 1                   # no handle
+    assert lib.moe_plan_destroy(None) == 0
+    assert lib.moe_plan_forward(None, fake, fake, None, fake, None) == 1
+    assert lib.moe_plan_grouped_gate_up(None, None) == 1
+    assert lib.moe_plan_grouped_down(None, None) == 1
+    mode = ctypes.c_int(-1)
+    assert lib.moe_forward_fused_mode(4, 300, 2, 128, 1, ctypes.byref(mode)) == 1          # E > 256
+    assert lib.moe_forward_fused_mode(4, 8, 2, 128, 1, None) == 1
 
 
 def test_product_path_does_not_import_the_oracle():

@@ -125,6 +125,56 @@ def test_histogram_prefix_scatter(T, E, k, p, d, dtype):
     assert torch.equal(res2["counts"], res["counts"])
 
 
+@pytest.mark.parametrize("T,E,k,p,d", [
+    (1, 8, 2, 0.0, 64),
+    (63, 16, 4, 0.2, 64),
+    (64, 256, 6, 0.1, 64),       # exactly one chunk
+    (65, 256, 6, 0.1, 64),       # a one-token second chunk
+    (401, 256, 6, 0.0, 256),
+    (2048, 256, 6, 0.1, 128),    # 32 chunks of 64 tokens
+    (3000, 256, 16, 0.3, 64),    # k = 16: 128 routes per warp and pass
+    (8192, 256, 6, 0.0, 64),     # 128 chunks, the most there are
+    (8193, 256, 6, 0.1, 64),     # 128-token chunks: two passes per chunk
+    (20000, 64, 8, 0.05, 64),    # 192-token chunks, ragged last chunk
+    (300, 10, 3, 0.0, 64),       # E not a multiple of 4: the three step kernels
+])
+def test_one_launch_routing_equals_the_step_kernels(T, E, k, p, d):
+    """moe_route_topk_offsets gives the step kernels' ids, weights, counts, offsets and workspace (the scatter
+    after it writes the same permutation), and the oracle's integer outputs."""
+    logits, mask = _routing_case(T, E, k, p, seed=T * 7 + E, skew=1.0)
+    x = torch.randn(T, d).to(torch.bfloat16)
+    steps = _run_index_path(logits, mask, k, x)
+    dev = "cuda"
+    ids = torch.full((T, k), -7, dtype=torch.int32, device=dev)
+    w = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev)
+    counts = torch.full((E,), -5, dtype=torch.int32, device=dev)
+    offsets = torch.full((E + 1,), -5, dtype=torch.int32, device=dev)
+    ws = torch.zeros(M.moe_workspace_size(T, k) // 4 + 4, dtype=torch.int32, device=dev)
+    md = None if mask is None else mask.cuda()
+    for _ in range(2):   # the workspace is left ready for the next call
+        M.moe_route_topk_offsets(logits.cuda(), md, k, ids, w, counts, offsets, ws)
+        M.moe_check_device_error()
+        assert torch.equal(ids, steps["ids"])
+        assert torch.equal(w.view(torch.int32), steps["w"].view(torch.int32))
+        assert torch.equal(counts, steps["counts"])
+        assert torch.equal(offsets, steps["offsets"])
+        assert torch.equal(ws, steps["ws"])
+    cap = T * k
+    xs = torch.empty(cap, d, dtype=torch.bfloat16, device=dev)
+    ror = torch.full((cap,), -9, dtype=torch.int32, device=dev)
+    rro = torch.full((cap,), -9, dtype=torch.int32, device=dev)
+    M.moe_scatter_rows(x.cuda(), ids, md, offsets, xs, ror, rro, ws)
+    M.moe_check_device_error()
+    ref_ids, _ = mo.route_topk(logits, k)
+    assert np.array_equal(to_np(ids), ref_ids)
+    ref_counts = mo.route_histogram(ref_ids, mask, E)
+    assert np.array_equal(to_np(counts), ref_counts)
+    assert np.array_equal(to_np(offsets), mo.prefix_offsets(ref_counts))
+    ref_ror, ref_rro = mo.scatter_permutation(ref_ids, mask)
+    assert np.array_equal(to_np(ror), ref_ror)
+    assert np.array_equal(to_np(rro), ref_rro)
+
+
 def test_all_masked_routes():
     T, E, k = 40, 8, 2
     logits, _ = _routing_case(T, E, k, 0.0, seed=1)

@@ -98,3 +98,48 @@ def test_quantized_bank_ffn_is_the_dequantized_ffn():
     ref = torch.nn.functional.linear(torch.nn.functional.silu(xt @ wg.T) * (xt @ wu.T), wd).numpy()
     got = mo.grouped_ffn(x, np.array([0, n], dtype=np.int32), tuple(q))
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_bf16_rounding_matches_torch_cast():
+    """bf16 rounding of float32 values (exact in float64) against PyTorch's float32 -> bfloat16 cast."""
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * 3,
+        (rng.standard_normal(2000) * 1e-38).astype(np.float32),          # fp32 subnormals
+        np.array([0.0, -0.0, 3.3895e38, -3.3895e38, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8], dtype=np.float32),
+    ])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = mo.round_bf16(x)
+    np.testing.assert_array_equal(got, ref)
+    assert np.array_equal(np.signbit(got), np.signbit(ref))
+    # hand-worked ties: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 (even: 1); 1 + 3*2^-8 -> 1 + 2^-6
+    assert mo.round_bf16(1.0 + 2.0 ** -8) == 1.0
+    assert mo.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+    assert np.isinf(mo.round_bf16(3.4e38))
+
+
+def test_w8a8_path_is_the_dense_ffn_on_quantized_operands():
+    """E=1, k=1: the FP8-activation path is a dense SwiGLU FFN on E4M3-quantized x, weights and h.  Here every
+    quantization and the bf16 rounding of h run through PyTorch's own casts (float8_e4m3fn, bfloat16)."""
+    g = torch.Generator().manual_seed(3)
+    T, d, f = 13, 32, 48
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(1, f, d, generator=g) / d ** 0.5).float()
+    wu = (torch.randn(1, f, d, generator=g) / d ** 0.5).float()
+    wd = (torch.randn(1, d, f, generator=g) / f ** 0.5).float()
+    logits = torch.randn(T, 1, generator=g)
+
+    def torch_quant(rows32):
+        # per-row scale amax / 448 in fp32, codes = E4M3 of the fp32 quotient; returns the values in float64
+        amax = rows32.abs().amax(dim=-1)
+        scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        q = (rows32 / scale[..., None]).to(torch.float8_e4m3fn)
+        return q.to(torch.float64) * scale.to(torch.float64)[..., None]
+
+    xq = torch_quant(x.float())
+    gq, uq, dq = (torch_quant(w[0]) for w in (wg, wu, wd))
+    h = torch.nn.functional.silu(xq @ gq.T) * (xq @ uq.T)
+    h_b = h.to(torch.float32).to(torch.bfloat16).float()
+    ref = (torch_quant(h_b) @ dq.T).numpy()
+    res = mo.moe_forward_w8a8(logits, x, tuple(mo.quantize_bank_fp8(w) for w in (wg, wu, wd)), 1)
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-12, atol=1e-14)

@@ -57,6 +57,8 @@ def _all_pins():
         fp8_pins.test_code_layout_and_round_trip,
         fp8_pins.test_per_channel_scaling_properties,
         fp8_pins.test_quantized_bank_ffn_is_the_dequantized_ffn,
+        fp8_pins.test_bf16_rounding_matches_torch_cast,
+        fp8_pins.test_w8a8_path_is_the_dense_ffn_on_quantized_operands,
         router_pins.test_hand_worked_router_case,
         router_pins.test_one_hot_router_rows_select_input_columns,
         router_pins.test_router_is_linear_and_permutation_equivariant,
@@ -99,9 +101,11 @@ MUTANTS = [
     ("histogram_counts_masked_routes",
      [("        if (mask && mask[r]) continue;\n        if (ids[r] < 0", "        if (ids[r] < 0")]),
     ("gather_uses_slot_not_token", [("route_of_row[i] / k);", "route_of_row[i] % k);")]),
-    ("e4m3_ties_away_from_zero", [("std::nearbyint(a / quantum)", "std::round(a / quantum)")]),
+    ("e4m3_ties_away_from_zero", [("std::nearbyint(a / quantum) * quantum;\n    r = std::min(r, 448.0);",
+                                   "std::round(a / quantum) * quantum;\n    r = std::min(r, 448.0);")]),
     ("e4m3_subnormal_binade_off_by_one", [("std::max(ex - 1, -6);", "std::max(ex - 1, -7);")]),
     ("fp8_scale_of_the_fnuz_variant", [("amax / 448.0f", "amax / 240.0f")]),
+    ("bf16_with_seven_significant_bits", [("std::ldexp(1.0, binade - 7);", "std::ldexp(1.0, binade - 6);")]),
     ("router_reads_wr_transposed",
      [("element(wr, wdtype, static_cast<size_t>(e) * d + c)", "element(wr, wdtype, static_cast<size_t>(c) * E + e)")]),
 ]
