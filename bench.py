@@ -136,7 +136,7 @@ def max_over_ranks(value: float, world: int, device) -> float:
 
 
 def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp8: bool = False,
-                     fused: bool = False, gather: bool = False, w8a8: bool = False) -> dict:
+                     fused: bool = False, gather: bool = False, w8a8: bool = False, fp4: bool = False) -> dict:
     """Algorithmic bytes and FLOPs of one step, from the realised expert counts.
 
     Only touched experts' weights count; activations are counted once per
@@ -155,14 +155,17 @@ def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp
         wgu, wdn = touched * 2 * f * (d + 4), touched * d * (f + 4)
         gate_up = wgu + R * (d + 4) + R * f * 2
         down = wdn + R * (f + 4) + R * d * 4
-        quant = T * d * 2 + T * (d + 4) + R * f * 2 + R * (f + 4)
-        scatter = T * d + R * (d + 4)
+        quant = R * f * 2 + R * (f + 4)                     # the rows of h
+        scatter = T * d * 2 + T * (d + 4) + R * (d + 4)      # token rows read, quantized, scattered
         routing = T * E * 4 + T * k * 8
         combine = R * d * 4 + T * d * 4
         return {"R": R, "touched": touched, "gate_up_bytes": gate_up, "down_bytes": down,
                 "path_bytes": routing + quant + scatter + gate_up + down + combine, "flops": 6.0 * R * d * f}
     wgu = touched * 2 * f * (d + 4) if fp8 else touched * 2 * f * d * es
     wdn = touched * d * (f + 4) if fp8 else touched * d * f * es
+    if fp4:   # two codes per byte, an E4M3 scale per 16 values, an fp32 scale per row
+        wgu = touched * 2 * f * (d // 2 + d // 16 + 4)
+        wdn = touched * d * (f // 2 + f // 16 + 4)
     gate_up = wgu + R * d * es + R * f * es
     down = wdn + R * f * es + R * d * 4
     routing = T * E * 4 + T * k * 8
@@ -200,7 +203,9 @@ def _oracle_inputs(inp, tokens):
     mask = None if inp["mask"] is None else inp["mask"].cpu()[tokens]
     if "_oracle_bank" not in inp:
         bank = tuple(inp[n].cpu() for n in ("w_gate", "w_up", "w_down"))
-        if inp.get("fp8"):
+        if inp.get("fp4"):
+            bank = tuple(mo.quantize_bank_fp4(b) for b in bank)
+        elif inp.get("fp8"):
             bank = tuple(mo.quantize_bank_fp8(b) for b in bank)
         inp["_oracle_bank"] = bank
     return logits, x, mask, inp["_oracle_bank"]
@@ -271,6 +276,7 @@ def run_reference(args, rank: int, world: int):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(cfg, device="cpu", weights_device=dev)
     inp["fp8"] = args.weights in ("fp8", "w8a8")
+    inp["fp4"] = args.weights == "fp4"
     inp["w8a8"] = args.weights == "w8a8"
     per_step_budget = max(0.05, args.reference_budget_s / max(1, args.steps + args.warmup))
     n, _ = _size_oracle_sample(inp, per_step_budget)
@@ -403,7 +409,8 @@ def run_ours(args, rank: int, world: int):
     inp = make_inputs(cfg, device=dev)
     T, E, k, d, f = cfg.T, cfg.E, cfg.k, cfg.d, cfg.f
     dtype = inp["x"].dtype
-    fp8 = args.weights == "fp8"
+    fp4 = args.weights == "fp4"
+    fp8 = args.weights == "fp8" or fp4      # the 4-bit path shares the FP8 path's fp16 activations and kernel
     w8a8 = args.weights == "w8a8"
     fused = args.fused
     if fused and (fp8 or w8a8 or args.router or dtype != torch.bfloat16):
@@ -425,9 +432,14 @@ def run_ours(args, rank: int, world: int):
             raise SystemExit("--weights fp8 needs a bf16 workload")
         # load-time step, outside the timed region: FP8 E4M3 codes + per-channel scales
         inp["fp8"] = True
-        wg, wu, wd = (M.moe_quantize_weights_fp8(inp[n]) for n in ("w_gate", "w_up", "w_down"))
+        inp["fp4"] = fp4
+        if fp4:
+            wg, wu, wd = (M.moe_quantize_weights_fp4(inp[n]) for n in ("w_gate", "w_up", "w_down"))
+            gate_up_call, down_call, forward = M.moe_grouped_gate_up_fp4, M.moe_grouped_down_fp4, M.moe_forward_fp4
+        else:
+            wg, wu, wd = (M.moe_quantize_weights_fp8(inp[n]) for n in ("w_gate", "w_up", "w_down"))
+            gate_up_call, down_call, forward = M.moe_grouped_gate_up_fp8, M.moe_grouped_down_fp8, M.moe_forward_fp8
         torch.cuda.synchronize()
-        gate_up_call, down_call, forward = M.moe_grouped_gate_up_fp8, M.moe_grouped_down_fp8, M.moe_forward_fp8
         scatter_call = M.moe_scatter_rows_f16
     else:
         wg, wu, wd = inp["w_gate"], inp["w_up"], inp["w_down"]
@@ -451,7 +463,7 @@ def run_ours(args, rank: int, world: int):
     small = small and not fused
     if w8a8:
         # E4M3 activations: the token rows and h quantized per row, E4M3 x E4M3 tensor-core MMAs
-        names = ("route", "quantize_x", "scatter", "gate_up", "quantize_h", "down", "combine")
+        names = ("route", "scatter_quant", "gate_up", "quantize_h", "down", "combine")
         routing = []
     elif fused and T <= SMALL_TOKENS and T * k <= SMALL_ROUTES:
         names = ("route_scatter_small", "gate_up", "down_combine")
@@ -503,11 +515,10 @@ def run_ours(args, rank: int, world: int):
     elif w8a8:
         calls = [
             M.bind(M.moe_route_topk_offsets, logits, mask, k, b.ids, b.w, b.counts, b.offsets, b.ws),
-            M.bind(M.moe_quantize_weights_fp8, x, b.x_q, b.x_scales),
-            M.bind(M.moe_scatter_rows_e4m3, b.x_q, b.x_scales, b.ids, mask, b.offsets, b.xs, b.xs_scales,
+            M.bind(M.moe_scatter_rows_quant_e4m3, x, b.ids, mask, b.offsets, b.x_q, b.x_scales, b.xs, b.xs_scales,
                    b.row_of_route, b.route_of_row, b.ws),
             M.bind(M.moe_grouped_gate_up_w8a8, b.xs, b.xs_scales, b.offsets, wg, wu, b.h),
-            M.bind(M.moe_quantize_weights_fp8, b.h, b.h_q, b.h_scales),
+            M.bind(M.moe_quantize_rows_e4m3, b.h, b.offsets, b.h_q, b.h_scales),
             M.bind(M.moe_grouped_down_w8a8, b.h_q, b.h_scales, b.offsets, wd, b.y),
             M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
         ]
@@ -612,14 +623,15 @@ def run_ours(args, rank: int, world: int):
 
     # ---- roofline of the dominant kernel (grouped gate/up + SwiGLU)
     es = 2 if dtype == torch.bfloat16 else 4
-    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8, fused, gather, w8a8)
+    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8, fused, gather, w8a8, fp4)
     R, touched = work["R"], work["touched"]
     gate_up_bytes = work["gate_up_bytes"]
     peaks = _peaks()
     achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic("gate_up_w8a8" if w8a8 else "gate_up_fp8" if fp8 else
+    traffic = _profiled_traffic("gate_up_w8a8" if w8a8 else "gate_up_fp4" if fp4 else "gate_up_fp8" if fp8 else
                                 ("gate_up_gather" if gather else "gate_up"), cfg.name)
     kname = ("moe_grouped_gate_up_w8a8 (ffn_tc_kernel<gated, E4M3>)" if w8a8 else
+             "moe_grouped_gate_up_fp4 (ffn_fp8_kernel<gated, FP4>)" if fp4 else
              "moe_grouped_gate_up_fp8 (ffn_fp8_kernel<gated>)" if fp8 else
              "moe_grouped_gate_up_gather (ffn_tc_kernel<gated, fused>)" if gather else
              "moe_grouped_gate_up (ffn_tc_kernel<gated>)")
@@ -658,7 +670,8 @@ def run_ours(args, rank: int, world: int):
         "data": "synthetic",
         "config": {"workload": cfg.name, "T": T, "d": d, "f": f, "E": E, "k": k, "mask_p": cfg.mask_p,
                    "routes_unmasked": R, "experts_touched": touched,
-                   "weights": "fp8_e4m3 codes + fp32 per-channel scales" if (fp8 or w8a8) else
+                   "weights": "e2m1 codes + e4m3 scale per 16 + fp32 per-channel scales" if fp4 else
+                              "fp8_e4m3 codes + fp32 per-channel scales" if (fp8 or w8a8) else
                               ("bf16" if dtype == torch.bfloat16 else "f32"),
                    "activations": "fp8_e4m3 codes + fp32 per-row scales (x and h)" if w8a8 else
                                   ("fp16 (exact widening of bf16 x)" if fp8 else None),
@@ -697,7 +710,7 @@ def run_routing_sweep(args):
     _build.build()
     from sparse_moe_expert_top_gb300 import moe as M
 
-    def timeit(fn, n=20):
+    def timeit(fn, n=args.sweep_reps):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -711,7 +724,11 @@ def run_routing_sweep(args):
 
     E, k, dev = 256, 6, "cuda"
     peak = _peaks()["hbm_gbs"]
-    for T, d in [(2048, 4096), (8192, 4096), (32768, 2048), (131072, 512), (262144, 256)]:
+    sizes = [(2048, 4096), (8192, 4096), (32768, 2048), (131072, 512), (262144, 256)]
+    if args.sweep_tokens:
+        keep = {int(t) for t in args.sweep_tokens.split(",")}
+        sizes = [(T, d) for T, d in sizes if T in keep]
+    for T, d in sizes:
         g = torch.Generator(device=dev).manual_seed(T)
         logits = torch.randn(T, E, device=dev, generator=g)
         x = torch.randn(T, d, device=dev, generator=g).to(torch.bfloat16)
@@ -773,10 +790,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
-    ap.add_argument("--weights", choices=("bf16", "fp8", "w8a8"), default="bf16",
+    ap.add_argument("--weights", choices=("bf16", "fp8", "w8a8", "fp4"), default="bf16",
                     help="expert weight format: the workload's own (bf16); FP8 E4M3 codes with per-channel "
                          "scales quantized at load time, with fp16 activations (fp8) or with E4M3 activations "
-                         "quantized per row on the FP8 tensor cores (w8a8)")
+                         "quantized per row on the FP8 tensor cores (w8a8); or 4-bit E2M1 codes with an E4M3 "
+                         "scale per 16 values and per-channel scales, with fp16 activations (fp4)")
     ap.add_argument("--fused", action="store_true",
                     help="the fused permutation (bf16): rows gathered in the gate/up kernel, combine in the down "
                          "kernel (moe_forward_fused)")
@@ -787,6 +805,8 @@ def main():
                     help="compute the router projection x . Wr^T on the GPU in front of the path (moe_router_topk)")
     ap.add_argument("--routing-sweep", action="store_true",
                     help="time the routing-side kernels over a T-sweep instead (JSON line per T)")
+    ap.add_argument("--sweep-tokens", default="", help="with --routing-sweep: the chunk sizes to run (comma list)")
+    ap.add_argument("--sweep-reps", type=int, default=20, help="with --routing-sweep: timed launches per kernel")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -154,10 +154,13 @@ moe_status moe_route_histogram(const int32_t* ids, const uint8_t* mask, int T, i
 /* A1 + A2 + A3 in one launch: the outputs of moe_route_topk,
  * moe_route_histogram and moe_prefix_offsets (ids, w, counts, offsets, and
  * the workspace the scatter reads), bit for bit.  One CTA per workspace
- * chunk of tokens routes its tokens, ranks their routes and counts them;
- * the last CTA to finish sums the counts and writes the prefix and the
- * chunk bases.  Shapes other than E a multiple of 4 with 16-byte aligned
- * logits run the three step kernels instead (same results).
+ * chunk of tokens routes its tokens (a warp per token), ranks their routes
+ * and counts them; the last CTA to finish sums the counts and writes the
+ * prefix and the chunk bases.  The gate weights equal moe_route_topk's bit
+ * for bit when E is a multiple of 4 (its streaming kernel sums the softmax
+ * in slot order, as this one does); for other E they may differ from it in
+ * the last bit.  Chunks of more than 8,192 tokens run the three step kernels
+ * (the streaming top-k scales better there).
  *   logits [T][E], mask [T][k] or NULL, ids, w [T][k], counts [E],
  *   offsets [E+1], ws: as for the three calls. */
 moe_status moe_route_topk_offsets(const float* logits, const uint8_t* mask, int T, int E, int k,
@@ -172,7 +175,7 @@ moe_status moe_route_topk_offsets(const float* logits, const uint8_t* mask, int 
  * inputs and outputs:
  *   ids, mask, T, k, E, counts  as for moe_route_histogram (same counts).
  * The scratch (per-chunk counts, in-chunk ranks and a completion counter,
- * 384 KB) is a static device array inside the library; every GPU that loads
+ * 512 KB) is a static device array inside the library; every GPU that loads
  * the library keeps it until the process exits.
  *   Limit: T*k <= 65536 routes; a larger chunk returns MOE_ERR_INVALID_ARG
  *   without enqueuing anything.
@@ -368,6 +371,60 @@ moe_status moe_forward_fp8(const float* logits, const void* x, const uint8_t* ma
                            void* h, float* y, float* out, void* ws, void* stream);
 
 /* ------------------------------------------------------------------------
+ * 4-bit block-scaled expert weights.  The pages stream ROCmFP4 (and FP2/3)
+ * expert weights (page "perf(ggml): reuse ROCmFP4 weights across q=4
+ * columns"; page "perf(ds4): batch heterogeneous MoE prefill by expert",
+ * "Fresh main-snapshot requalification").  Here a weight row of K values is
+ * stored as K E2M1 codes (the 4-bit OCP MX element type: values 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6 and their negatives), one E4M3 scale per block of 16
+ * consecutive values and one fp32 scale per row -- the block-scaled layout
+ * of NVFP4 with its per-tensor scale taken per channel.  The weight the FFN
+ * uses is row scale * block scale * E2M1 value, exactly.  The codes are
+ * widened inside the SM to fp16 (exact: code value times block scale has at
+ * most 6 significant bits), as on the FP8-weight path, so xs and h are fp16
+ * and the MMAs are kind::f16 with A in tensor memory.
+ * ------------------------------------------------------------------------ */
+
+/* Quantizes E banks of M rows of K values (load-time step), in fp32:
+ *   scale  = max|row| / 2688 (2688 = 6 * 448; 1 for an all-zero row);
+ *   block  = E4M3 code (nearest even, saturating) of (block max / 6) / scale;
+ *   code   = E2M1 code (nearest even, saturating at 6) of w / (value(block) *
+ *            scale), 0 when value(block) is 0.
+ *   w             [E][M][K] operand type `dtype` (MOE_BF16 or MOE_F32).
+ *   codes         [E][M][K/2] uint8 out: two codes per byte, the lower K
+ *                 index in the low nibble.
+ *   block_scales  [E][K/64][M][4] uint8 out: the four block scales of row m
+ *                 in 64-value tile t of expert e at [e][t][m][0..3] (one
+ *                 32-bit word per row and tile, the layout the FFN loads).
+ *   scales        [E][M] fp32 out.
+ * K a multiple of 64; w, codes and block_scales 16-byte aligned. */
+moe_status moe_quantize_weights_fp4(const void* w, int dtype, int E, int M, int K, uint8_t* codes,
+                                    uint8_t* block_scales, float* scales, void* stream);
+
+/* A5 with 4-bit weights: as moe_grouped_gate_up_fp8 with (codes, block
+ * scales, row scales) of moe_quantize_weights_fp4 for each bank: xs [cap][d]
+ * fp16, h [cap][f] fp16 out (|h| > 65504 reported as MOE_ERR_RANGE).  d and
+ * f multiples of 128. */
+moe_status moe_grouped_gate_up_fp4(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                   const uint8_t* w_gate_q, const uint8_t* b_gate, const float* s_gate,
+                                   const uint8_t* w_up_q, const uint8_t* b_up, const float* s_up, void* h,
+                                   void* stream);
+
+/* A6 with 4-bit weights: y [cap][d] fp32 out from h [cap][f] fp16. */
+moe_status moe_grouped_down_fp4(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                                const uint8_t* w_down_q, const uint8_t* b_down, const float* s_down, float* y,
+                                void* stream);
+
+/* The whole path with 4-bit weights (x bf16; xs and h fp16; every other
+ * argument as for moe_forward_fp8). */
+moe_status moe_forward_fp4(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k, int d,
+                           int f, const uint8_t* w_gate_q, const uint8_t* b_gate, const float* s_gate,
+                           const uint8_t* w_up_q, const uint8_t* b_up, const float* s_up, const uint8_t* w_down_q,
+                           const uint8_t* b_down, const float* s_down, int32_t* ids, float* w, int32_t* counts,
+                           int32_t* offsets, void* xs, int32_t* row_of_route, int32_t* route_of_row, void* h,
+                           float* y, float* out, void* ws, void* stream);
+
+/* ------------------------------------------------------------------------
  * FP8 E4M3 weights AND activations on the FP8 tensor cores.  The pages'
  * quantized expert matmuls take quantized activations too (the MMQ path of
  * the page "perf(ggml): reuse ROCmFP4 weights across q=4 columns", whose
@@ -394,6 +451,23 @@ moe_status moe_scatter_rows_e4m3(const uint8_t* x_q, const float* x_scales, cons
                                  const int32_t* offsets, int T, int k, int d, int E, uint8_t* xs, float* xs_scales,
                                  int32_t* row_of_route, int32_t* route_of_row, void* ws, void* stream);
 
+/* A4 with E4M3 rows straight from the bf16 token rows x [T][d]: every token
+ * row is read once and quantized -- x_q [T][d] codes and x_scales [T], the
+ * codes and scales moe_quantize_weights_fp8 would give -- and its codes and
+ * scale written to its compact rows as moe_scatter_rows_e4m3 writes them.
+ * d a multiple of 16 and at most 8192. */
+moe_status moe_scatter_rows_quant_e4m3(const void* x, const int32_t* ids, const uint8_t* mask,
+                                       const int32_t* offsets, int T, int k, int d, int E, uint8_t* x_q,
+                                       float* x_scales, uint8_t* xs, float* xs_scales, int32_t* row_of_route,
+                                       int32_t* route_of_row, void* ws, void* stream);
+
+/* E4M3 codes and one scale per row of the compact bf16 rows a [cap][K] (h
+ * of the FP8-activation path), the arithmetic of moe_quantize_weights_fp8;
+ * rows at or beyond R = offsets[E] (zero rows) get zero codes and scale 1
+ * without being read.  K a multiple of 16 and at most 2048. */
+moe_status moe_quantize_rows_e4m3(const void* a, const int32_t* offsets, int E, int cap, int K, uint8_t* codes,
+                                  float* scales, void* stream);
+
 /* A5 on E4M3 operands: h[i][j] = silu(g) * u, g = s_gate[e][j] *
  * xs_scales[i] * (codes of xs[i] . codes of w_gate_q[e][j]) and u likewise;
  * h [cap][f] bf16 out (rows R .. cap-1 zero-filled).  d and f multiples of
@@ -411,8 +485,9 @@ moe_status moe_grouped_down_w8a8(const uint8_t* h_q, const float* h_scales, cons
 
 /* The whole path on E4M3 weights and activations: routing in one launch
  * (moe_route_topk_offsets), the token rows quantized (x_q [T][d], x_scales
- * [T]) and scattered (xs, xs_scales), moe_grouped_gate_up_w8a8 into h
- * [T*k][f] bf16, h quantized (h_q [T*k][f], h_scales [T*k]),
+ * [T]) and scattered (xs, xs_scales) by moe_scatter_rows_quant_e4m3,
+ * moe_grouped_gate_up_w8a8 into h [T*k][f] bf16, h quantized by
+ * moe_quantize_rows_e4m3 (h_q [T*k][f], h_scales [T*k]),
  * moe_grouped_down_w8a8 into y, moe_combine into out.  x is bf16; every
  * other argument as for moe_forward. */
 moe_status moe_forward_w8a8(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k, int d,

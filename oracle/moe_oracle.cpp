@@ -79,6 +79,7 @@ enum : int {
     ORC_F32 = 1,
     ORC_BF16 = 2,   // raw bfloat16 bits (the high half of an fp32)
     ORC_E4M3 = 3,   // OCP FP8 E4M3 codes, with one fp32 scale per row
+    ORC_FP4 = 4,    // E2M1 codes, two per byte, an E4M3 scale per 16 values and an fp32 scale per row
 };
 
 // ---------------------------------------------------------------------------
@@ -103,6 +104,17 @@ double e4m3_value(uint8_t code) {
     return sign * mag;
 }
 
+// E2M1 (the 4-bit OCP MX element type): sign bit 3, exponent bits 2-1 with
+// bias 1, mantissa bit 0; exponent field 0 holds the subnormal 0.5 * m.
+// Values 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+double e2m1_value(uint8_t code) {
+    const double sign = (code & 0x8) ? -1.0 : 1.0;
+    const int e = (code >> 1) & 0x3;
+    const int m = code & 0x1;
+    const double mag = e > 0 ? std::ldexp(1.0 + m / 2.0, e - 1) : 0.5 * m;
+    return sign * mag;
+}
+
 double element(const void* p, int dtype, size_t i) {
     switch (dtype) {
         case ORC_F64: return static_cast<const double*>(p)[i];
@@ -113,7 +125,14 @@ double element(const void* p, int dtype, size_t i) {
 }
 
 bool plain_dtype(int dtype) { return dtype == ORC_F64 || dtype == ORC_F32 || dtype == ORC_BF16; }
-bool weight_dtype(int dtype) { return plain_dtype(dtype) || dtype == ORC_E4M3; }
+bool weight_dtype(int dtype) { return plain_dtype(dtype) || dtype == ORC_E4M3 || dtype == ORC_FP4; }
+
+// The 4-bit bank: codes [rows][K/2] (element 2i in the low nibble of byte
+// i), block scales [rows][K/16] (E4M3 codes), row scales [rows] (fp32).
+struct Fp4Bank {
+    const uint8_t* codes;
+    const uint8_t* block_scales;
+};
 
 // Rows row0 .. row0+n_rows-1 of a [rows][K] weight matrix as doubles.
 void decode_rows(const void* base, int dtype, const float* row_scale, size_t row0, size_t n_rows, size_t K,
@@ -126,6 +145,16 @@ void decode_rows(const void* base, int dtype, const float* row_scale, size_t row
             const uint8_t* codes = static_cast<const uint8_t*>(base) + row * K;
             const double s = row_scale[row];
             for (size_t c = 0; c < K; ++c) dst[c] = s * e4m3_value(codes[c]);
+        } else if (dtype == ORC_FP4) {
+            // w = row scale * block scale * E2M1 value, an exact product in double
+            const Fp4Bank* bank = static_cast<const Fp4Bank*>(base);
+            const uint8_t* codes = bank->codes + row * (K / 2);
+            const uint8_t* bs = bank->block_scales + row * (K / 16);
+            const double s = row_scale[row];
+            for (size_t c = 0; c < K; ++c) {
+                const uint8_t code = (c & 1) ? (codes[c / 2] >> 4) : (codes[c / 2] & 0xF);
+                dst[c] = s * e4m3_value(bs[c / 16]) * e2m1_value(code);
+            }
         } else {
             for (size_t c = 0; c < K; ++c) dst[c] = element(base, dtype, row * K + c);
         }
@@ -187,6 +216,31 @@ double e4m3_round_one(double x) {
     double r = std::nearbyint(a / quantum) * quantum;
     r = std::min(r, 448.0);
     return std::copysign(r, x);
+}
+
+// E2M1 nearest value (ties to even), saturating at +-6; the sign of x is
+// kept, also when the result is zero.
+double e2m1_round_one(double x) {
+    const double a = std::fabs(x);
+    int ex = 0;
+    std::frexp(a > 0.0 ? a : 1.0, &ex);             // a in [2^(ex-1), 2^ex)
+    const int binade = std::max(ex - 1, 0);          // the subnormal 0.5 shares the 2^0 binade's spacing
+    const double quantum = std::ldexp(1.0, binade - 1);
+    double r = std::nearbyint(a / quantum) * quantum;
+    r = std::min(r, 6.0);
+    return std::copysign(r, x);
+}
+
+uint8_t e2m1_encode_one(double v) {
+    const uint8_t sign = std::signbit(v) ? 0x8 : 0x0;
+    const double a = std::fabs(v);
+    if (a == 0.0) return sign;
+    if (a < 1.0) return sign | 0x1;                  // 0.5
+    int ex = 0;
+    std::frexp(a, &ex);
+    const int e_field = ex;                          // a in [2^(ex-1), 2^ex): biased exponent (ex - 1) + 1
+    const int mant = static_cast<int>(std::nearbyint(a / std::ldexp(1.0, ex - 1) * 2.0 - 2.0));
+    return static_cast<uint8_t>(sign | (e_field << 1) | mant);
 }
 
 // bf16 nearest value (ties to even): 8 significant bits with fp32's
@@ -343,7 +397,7 @@ int oracle_grouped_swiglu(const double* xs, const int32_t* offsets, int e0, int 
                           const void* w_gate, const void* w_up, int wdtype, const float* s_gate, const float* s_up,
                           double* h) {
     if (!weight_dtype(wdtype) || d < 1 || f < 1 || !check_offsets(offsets, e0, e1)) return 1;
-    if (wdtype == ORC_E4M3 && (!s_gate || !s_up)) return 1;
+    if ((wdtype == ORC_E4M3 || wdtype == ORC_FP4) && (!s_gate || !s_up)) return 1;
     std::vector<double> wg, wu;
     for (int e = e0; e < e1; ++e) {
         const long long lo = offsets[e], n = static_cast<long long>(offsets[e + 1]) - offsets[e];
@@ -375,7 +429,7 @@ int oracle_grouped_swiglu(const double* xs, const int32_t* offsets, int e0, int 
 int oracle_grouped_down(const double* h, const int32_t* offsets, int e0, int e1, int d, int f, const void* w_down,
                         int wdtype, const float* s_down, double* y) {
     if (!weight_dtype(wdtype) || d < 1 || f < 1 || !check_offsets(offsets, e0, e1)) return 1;
-    if (wdtype == ORC_E4M3 && !s_down) return 1;
+    if ((wdtype == ORC_E4M3 || wdtype == ORC_FP4) && !s_down) return 1;
     std::vector<double> wd;
     for (int e = e0; e < e1; ++e) {
         const long long lo = offsets[e], n = static_cast<long long>(offsets[e + 1]) - offsets[e];
@@ -497,6 +551,75 @@ int oracle_quantize_fp8(const void* w, int dtype, long long rows, int K, uint8_t
 int oracle_dequantize_fp8(const uint8_t* codes, const float* scales, long long rows, int K, double* w) {
     if (rows < 0 || K < 1 || (rows > 0 && (!codes || !scales || !w))) return 1;
     decode_rows(codes, ORC_E4M3, scales, 0, static_cast<size_t>(rows), static_cast<size_t>(K), w);
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// 4-bit expert weights: E2M1 codes with an E4M3 scale per block of 16
+// consecutive K-values and an fp32 scale per row (output channel) -- the
+// block-scaled 4-bit format of NVIDIA's NVFP4, its per-tensor scale taken
+// per channel.  For a row w of K values (fp32, or bf16 read exactly), in
+// fp32 arithmetic:
+//   s   = max|w| / 2688 (2688 = 6 * 448; 1 for an all-zero row),
+//   b_j = E4M3 code (nearest, ties to even, saturating) of
+//         (max over block j of |w|) / 6 / s (two divisions, in this order),
+//   q_i = E2M1 code (nearest, ties to even, saturating at 6) of
+//         w_i / (value(b_j) * s) for i in block j; 0 when value(b_j) is 0.
+// The weight the FFN uses is s * value(b_j) * value(q_i), exactly.
+// ---------------------------------------------------------------------------
+int oracle_e2m1_round(const double* x, long long n, double* out) {
+    if (n < 0 || (n > 0 && (!x || !out))) return 1;
+    for (long long i = 0; i < n; ++i) out[i] = e2m1_round_one(x[i]);
+    return 0;
+}
+
+int oracle_e2m1_encode(const double* v, long long n, uint8_t* codes) {
+    if (n < 0 || (n > 0 && (!v || !codes))) return 1;
+    for (long long i = 0; i < n; ++i) codes[i] = e2m1_encode_one(v[i]);
+    return 0;
+}
+
+int oracle_e2m1_decode(const uint8_t* codes, long long n, double* v) {
+    if (n < 0 || (n > 0 && (!v || !codes))) return 1;
+    for (long long i = 0; i < n; ++i) v[i] = e2m1_value(codes[i] & 0xF);
+    return 0;
+}
+
+int oracle_quantize_fp4(const void* w, int dtype, long long rows, int K, uint8_t* codes, uint8_t* block_scales,
+                        float* scales) {
+    if (!plain_dtype(dtype) || rows < 0 || K < 16 || K % 16 != 0) return 1;
+    if (rows > 0 && (!w || !codes || !block_scales || !scales)) return 1;
+#pragma omp parallel for schedule(static)
+    for (long long r = 0; r < rows; ++r) {
+        auto wv = [&](int c) { return static_cast<float>(element(w, dtype, static_cast<size_t>(r) * K + c)); };
+        float amax = 0.0f;
+        for (int c = 0; c < K; ++c) amax = std::max(amax, std::fabs(wv(c)));
+        const float s = amax > 0.0f ? amax / 2688.0f : 1.0f;
+        scales[r] = s;
+        uint8_t* cr = codes + static_cast<size_t>(r) * (K / 2);
+        for (int c = 0; c < K / 2; ++c) cr[c] = 0;
+        for (int j = 0; j < K / 16; ++j) {
+            float bmax = 0.0f;
+            for (int i = 16 * j; i < 16 * j + 16; ++i) bmax = std::max(bmax, std::fabs(wv(i)));
+            const float t = bmax / 6.0f / s;
+            const uint8_t b = e4m3_encode_one(e4m3_round_one(t));
+            block_scales[static_cast<size_t>(r) * (K / 16) + j] = b;
+            const float vb = static_cast<float>(e4m3_value(b));
+            const float denom = vb * s;
+            for (int i = 16 * j; i < 16 * j + 16; ++i) {
+                const uint8_t q = vb > 0.0f ? e2m1_encode_one(e2m1_round_one(wv(i) / denom)) : 0;
+                cr[i / 2] |= static_cast<uint8_t>(q << (4 * (i & 1)));
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_dequantize_fp4(const uint8_t* codes, const uint8_t* block_scales, const float* scales, long long rows,
+                          int K, double* w) {
+    if (rows < 0 || K < 16 || K % 16 != 0 || (rows > 0 && (!codes || !block_scales || !scales || !w))) return 1;
+    const Fp4Bank bank{codes, block_scales};
+    decode_rows(&bank, ORC_FP4, scales, 0, static_cast<size_t>(rows), static_cast<size_t>(K), w);
     return 0;
 }
 

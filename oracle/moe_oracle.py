@@ -32,7 +32,7 @@ import numpy as np
 
 from . import build as _build
 
-ORC_F64, ORC_F32, ORC_BF16, ORC_E4M3 = 0, 1, 2, 3
+ORC_F64, ORC_F32, ORC_BF16, ORC_E4M3, ORC_FP4 = 0, 1, 2, 3, 4
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -56,6 +56,11 @@ _SIGNATURES = {
     "oracle_quantize_fp8": (_P, _I, _L, _I, _P, _P),
     "oracle_dequantize_fp8": (_P, _P, _L, _I, _P),
     "oracle_router_logits": (_P, _I, _P, _I, _L, _I, _I, _P),
+    "oracle_e2m1_round": (_P, _L, _P),
+    "oracle_e2m1_encode": (_P, _L, _P),
+    "oracle_e2m1_decode": (_P, _L, _P),
+    "oracle_quantize_fp4": (_P, _I, _L, _I, _P, _P, _P),
+    "oracle_dequantize_fp4": (_P, _P, _P, _L, _I, _P),
 }
 
 _state = threading.local()
@@ -166,13 +171,50 @@ class QuantizedBank:
         return QuantizedBank(self.codes[sl], self.scales[sl])
 
 
-def _bank(w):
-    """(data array, storage code, row scales or None) of a weight bank."""
-    if isinstance(w, QuantizedBank):
-        return (np.ascontiguousarray(w.codes, dtype=np.uint8), ORC_E4M3,
-                np.ascontiguousarray(w.scales, dtype=np.float32))
-    data, code = _operand(w)
-    return data, code, None
+@dataclasses.dataclass
+class Fp4Bank:
+    """4-bit weights: E2M1 codes uint8 [..., M, K/2] (element 2i in the low nibble of byte i), E4M3 block
+    scales uint8 [..., M, K/16] (one per 16 consecutive values) and one fp32 scale per row, [..., M]."""
+
+    codes: np.ndarray
+    block_scales: np.ndarray
+    scales: np.ndarray
+
+    @property
+    def shape(self):
+        return self.codes.shape[:-1] + (2 * self.codes.shape[-1],)
+
+    def __getitem__(self, sl):
+        return Fp4Bank(self.codes[sl], self.block_scales[sl], self.scales[sl])
+
+
+class _Fp4BankC(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("block_scales", ctypes.c_void_p)]
+
+
+class _BankArg:
+    """A weight bank marshalled for the oracle: .ptr, .shape (logical [..., M, K]), .code, .scales."""
+
+    def __init__(self, w):
+        self.scales = None
+        if isinstance(w, Fp4Bank):
+            self._codes = np.ascontiguousarray(w.codes, dtype=np.uint8)
+            self._bs = np.ascontiguousarray(w.block_scales, dtype=np.uint8)
+            self.scales = np.ascontiguousarray(w.scales, dtype=np.float32)
+            self._struct = _Fp4BankC(self._codes.ctypes.data, self._bs.ctypes.data)
+            self.ptr = ctypes.cast(ctypes.pointer(self._struct), ctypes.c_void_p)
+            self.shape, self.code = w.shape, ORC_FP4
+        elif isinstance(w, QuantizedBank):
+            self._data = np.ascontiguousarray(w.codes, dtype=np.uint8)
+            self.scales = np.ascontiguousarray(w.scales, dtype=np.float32)
+            self.ptr, self.shape, self.code = _ptr(self._data), self._data.shape, ORC_E4M3
+        else:
+            self._data, self.code = _operand(w)
+            self.ptr, self.shape = _ptr(self._data), self._data.shape
+
+    @property
+    def scales_ptr(self):
+        return _opt_ptr(self.scales)
 
 
 def _fetcher(weights):
@@ -270,17 +312,16 @@ def grouped_swiglu(xs, offsets, weights):
     h = None
     for e0, e1 in _blocks(off, E):
         wg, wu, _ = fetch(e0, e1)
-        g, code, sg = _bank(wg)
-        u, code_u, su = _bank(wu)
-        assert code == code_u
+        g, u = _BankArg(wg), _BankArg(wu)
+        assert g.code == u.code
         f, d = g.shape[-2], g.shape[-1]
         if h is None:
             h = np.zeros((R, f), dtype=np.float64)
-        _call("oracle_grouped_swiglu", _ptr(xs), _ptr(off), e0, e1, d, f, _ptr(g), _ptr(u), code, _opt_ptr(sg),
-              _opt_ptr(su), _ptr(h))
+        _call("oracle_grouped_swiglu", _ptr(xs), _ptr(off), e0, e1, d, f, g.ptr, u.ptr, g.code, g.scales_ptr,
+              u.scales_ptr, _ptr(h))
     if h is None:
         _, wu, _ = fetch(0, 1)
-        h = np.zeros((R, _bank(wu)[0].shape[-2]), dtype=np.float64)
+        h = np.zeros((R, _BankArg(wu).shape[-2]), dtype=np.float64)
     return h
 
 
@@ -294,14 +335,14 @@ def grouped_down(h, offsets, weights):
     y = None
     for e0, e1 in _blocks(off, E):
         _, _, wd = fetch(e0, e1)
-        dn, code, sd = _bank(wd)
+        dn = _BankArg(wd)
         d, f = dn.shape[-2], dn.shape[-1]
         if y is None:
             y = np.zeros((R, d), dtype=np.float64)
-        _call("oracle_grouped_down", _ptr(h), _ptr(off), e0, e1, d, f, _ptr(dn), code, _opt_ptr(sd), _ptr(y))
+        _call("oracle_grouped_down", _ptr(h), _ptr(off), e0, e1, d, f, dn.ptr, dn.code, dn.scales_ptr, _ptr(y))
     if y is None:
         _, _, wd = fetch(0, 1)
-        y = np.zeros((R, _bank(wd)[0].shape[-2]), dtype=np.float64)
+        y = np.zeros((R, _BankArg(wd).shape[-2]), dtype=np.float64)
     return y
 
 
@@ -313,8 +354,8 @@ def grouped_ffn(xs, offsets, weights):
 def _one_expert(rows, *mats):
     rows = _np(rows, np.float64)
     off = np.array([0, rows.shape[0]], dtype=np.int32)
-    return rows, off, tuple(m[None] if not isinstance(m, QuantizedBank) else
-                            QuantizedBank(m.codes[None], m.scales[None]) for m in mats)
+    return rows, off, tuple(m[None] if not isinstance(m, (QuantizedBank, Fp4Bank)) else
+                            type(m)(*(getattr(m, f.name)[None] for f in dataclasses.fields(m))) for m in mats)
 
 
 def expert_swiglu(rows, w_gate_e, w_up_e):
@@ -431,6 +472,64 @@ def dequantize_weights_fp8(codes, scales):
     K = c.shape[-1]
     out = np.empty(c.shape, dtype=np.float64)
     _call("oracle_dequantize_fp8", _ptr(c), _ptr(s), c.size // K if K else 0, K, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# 4-bit weights: E2M1 codes, an E4M3 scale per 16 values, an fp32 scale per row
+# ---------------------------------------------------------------------------
+
+def e2m1_round(x):
+    """Nearest E2M1 value (ties to even), saturating at +-6, as float64."""
+    a = _np(x, np.float64)
+    out = np.empty_like(a)
+    _call("oracle_e2m1_round", _ptr(a), a.size, _ptr(out))
+    return out
+
+
+def e2m1_encode(v):
+    """4-bit codes (in uint8) of E2M1 values."""
+    a = _np(v, np.float64)
+    out = np.empty(a.shape, dtype=np.uint8)
+    _call("oracle_e2m1_encode", _ptr(a), a.size, _ptr(out))
+    return out
+
+
+def e2m1_decode(code):
+    """Values of 4-bit E2M1 codes (the low nibble of each uint8)."""
+    c = _np(code, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _call("oracle_e2m1_decode", _ptr(c), c.size, _ptr(out))
+    return out
+
+
+def quantize_weights_fp4(w):
+    """4-bit block-scaled quantization of rows [..., M, K] (K a multiple of 16).
+
+    Returns (codes uint8 [..., M, K/2], block scales uint8 [..., M, K/16], scales float32 [..., M]).
+    """
+    data, code = _operand(w)
+    K = data.shape[-1]
+    rows = data.size // K if K else 0
+    codes = np.empty(data.shape[:-1] + (K // 2,), dtype=np.uint8)
+    bs = np.empty(data.shape[:-1] + (K // 16,), dtype=np.uint8)
+    scales = np.empty(data.shape[:-1], dtype=np.float32)
+    _call("oracle_quantize_fp4", _ptr(data), code, rows, K, _ptr(codes), _ptr(bs), _ptr(scales))
+    return codes, bs, scales
+
+
+def quantize_bank_fp4(w) -> Fp4Bank:
+    return Fp4Bank(*quantize_weights_fp4(w))
+
+
+def dequantize_weights_fp4(codes, block_scales, scales):
+    """scale * block scale * value(code), float64 [..., M, K]."""
+    c = _np(codes, np.uint8)
+    b = _np(block_scales, np.uint8)
+    sc = _np(scales, np.float32)
+    K = 2 * c.shape[-1]
+    out = np.empty(c.shape[:-1] + (K,), dtype=np.float64)
+    _call("oracle_dequantize_fp4", _ptr(c), _ptr(b), _ptr(sc), sc.size, K, _ptr(out))
     return out
 
 

@@ -304,6 +304,84 @@ extern "C" moe_status moe_forward_fp8(const float* logits, const void* x, const 
 }
 
 // ---------------------------------------------------------------------------
+// 4-bit block-scaled expert weights
+// ---------------------------------------------------------------------------
+
+extern "C" moe_status moe_quantize_weights_fp4(const void* w, int dtype, int E, int M, int K, uint8_t* codes,
+                                               uint8_t* block_scales, float* scales, void* stream) {
+    if (dtype_size(dtype) == 0) return MOE_ERR_UNSUPPORTED;
+    MOE_REQUIRE(E >= 0 && M >= 0 && K >= 64 && K % 64 == 0);
+    if (static_cast<long long>(E) * M == 0) return MOE_OK;
+    MOE_REQUIRE(w && codes && block_scales && scales && aligned16(w) && aligned16(codes) && aligned16(block_scales));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_quantize_fp4(w, dtype, E, M, K, codes, block_scales, scales, static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_grouped_gate_up_fp4(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                              const uint8_t* w_gate_q, const uint8_t* b_gate, const float* s_gate,
+                                              const uint8_t* w_up_q, const uint8_t* b_up, const float* s_up, void* h,
+                                              void* stream) {
+    moe_status st = check_ffn_args(offsets, cap, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(xs && w_gate_q && b_gate && s_gate && w_up_q && b_up && s_up && h);
+    MOE_REQUIRE(aligned16(xs) && aligned16(w_gate_q) && aligned16(w_up_q) && aligned16(b_gate) && aligned16(b_up) &&
+                aligned16(h));
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MOE_OK) return st;
+    return launch_ffn_fp4_gate_up(xs, offsets, cap, E, d, f, w_gate_q, b_gate, s_gate, w_up_q, b_up, s_up, h,
+                                  static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_grouped_down_fp4(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                                           const uint8_t* w_down_q, const uint8_t* b_down, const float* s_down,
+                                           float* y, void* stream) {
+    moe_status st = check_ffn_args(offsets, cap, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(h && w_down_q && b_down && s_down && y);
+    MOE_REQUIRE(aligned16(h) && aligned16(w_down_q) && aligned16(b_down) && aligned16(y));
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MOE_OK) return st;
+    return launch_ffn_fp4_down(h, offsets, cap, E, d, f, w_down_q, b_down, s_down, y,
+                               static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_forward_fp4(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k,
+                                      int d, int f, const uint8_t* w_gate_q, const uint8_t* b_gate,
+                                      const float* s_gate, const uint8_t* w_up_q, const uint8_t* b_up,
+                                      const float* s_up, const uint8_t* w_down_q, const uint8_t* b_down,
+                                      const float* s_down, int32_t* ids, float* w, int32_t* counts,
+                                      int32_t* offsets, void* xs, int32_t* row_of_route, int32_t* route_of_row,
+                                      void* h, float* y, float* out, void* ws, void* stream) {
+    moe_status st = check_ffn_args(offsets, T * k, E, d, f, MOE_BF16);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && k <= E);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && ids && w && counts && xs && row_of_route && route_of_row && h && y && out && ws);
+    const int cap = T * k;
+    if (T <= kSmallTokens && cap <= kSmallRoutes) {
+        if ((st = moe_route_scatter_small(logits, x, MOE_BF16, 1, mask, T, E, k, d, ids, w, counts, offsets, xs,
+                                          row_of_route, route_of_row, stream)) != MOE_OK)
+            return st;
+    } else {
+        if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK)
+            return st;
+        if ((st = moe_scatter_rows_f16(x, ids, mask, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws,
+                                       stream)) != MOE_OK)
+            return st;
+    }
+    if ((st = moe_grouped_gate_up_fp4(xs, offsets, cap, E, d, f, w_gate_q, b_gate, s_gate, w_up_q, b_up, s_up, h,
+                                      stream)) != MOE_OK)
+        return st;
+    if ((st = moe_grouped_down_fp4(h, offsets, cap, E, d, f, w_down_q, b_down, s_down, y, stream)) != MOE_OK)
+        return st;
+    return moe_combine(y, row_of_route, w, T, k, d, out, stream);
+}
+
+// ---------------------------------------------------------------------------
 // FP8 E4M3 weights and activations (kind::f8f6f4 tensor-core MMAs)
 // ---------------------------------------------------------------------------
 
@@ -364,16 +442,26 @@ extern "C" moe_status moe_forward_w8a8(const float* logits, const void* x, const
                 aligned16(y) && aligned16(out) && aligned16(ws));
     const int cap = T * k;
     if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK) return st;
-    // E4M3 codes of the token rows, one scale per row (the weights' quantizer)
-    if ((st = moe_quantize_weights_fp8(x, MOE_BF16, T, d, x_q, x_scales, stream)) != MOE_OK) return st;
-    if ((st = moe_scatter_rows_e4m3(x_q, x_scales, ids, mask, offsets, T, k, d, E, xs, xs_scales, row_of_route,
-                                    route_of_row, ws, stream)) != MOE_OK)
-        return st;
+    // E4M3 codes of the token rows, one scale per row (the weights' quantizer's arithmetic), scattered
+    if (d <= 8 * 128 * 8) {
+        if ((st = moe_scatter_rows_quant_e4m3(x, ids, mask, offsets, T, k, d, E, x_q, x_scales, xs, xs_scales,
+                                              row_of_route, route_of_row, ws, stream)) != MOE_OK)
+            return st;
+    } else {
+        if ((st = moe_quantize_weights_fp8(x, MOE_BF16, T, d, x_q, x_scales, stream)) != MOE_OK) return st;
+        if ((st = moe_scatter_rows_e4m3(x_q, x_scales, ids, mask, offsets, T, k, d, E, xs, xs_scales, row_of_route,
+                                        route_of_row, ws, stream)) != MOE_OK)
+            return st;
+    }
     if ((st = moe_grouped_gate_up_w8a8(xs, xs_scales, offsets, cap, E, d, f, w_gate_q, s_gate, w_up_q, s_up, h,
                                        stream)) != MOE_OK)
         return st;
     // E4M3 codes of the rows of h (bf16), one scale per row
-    if ((st = moe_quantize_weights_fp8(h, MOE_BF16, cap, f, h_q, h_scales, stream)) != MOE_OK) return st;
+    if (f <= 8 * 32 * 8)
+        st = moe_quantize_rows_e4m3(h, offsets, E, cap, f, h_q, h_scales, stream);
+    else
+        st = moe_quantize_weights_fp8(h, MOE_BF16, cap, f, h_q, h_scales, stream);
+    if (st != MOE_OK) return st;
     if ((st = moe_grouped_down_w8a8(h_q, h_scales, offsets, cap, E, d, f, w_down_q, s_down, y, stream)) != MOE_OK)
         return st;
     return moe_combine(y, row_of_route, w, T, k, d, out, stream);

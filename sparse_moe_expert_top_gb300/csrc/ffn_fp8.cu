@@ -118,6 +118,58 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// 4-bit weights (E2M1 codes, two per byte with the lower K index in the low
+// nibble, and an E4M3 scale per 16 codes): one code pair -> one f16x2 word
+// (cvt.rn.f16x2.e2m1x2), exact -- every E2M1 value times every E4M3 value
+// is an fp16 value (at most 6 significant bits, magnitudes from 2^-10 to
+// 2688).
+
+// {value(b), value(b)} as f16x2 for the E4M3 code b.
+__device__ __forceinline__ uint32_t f16x2_splat_e4m3(uint32_t b) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(b | (b << 8))));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// The eight codes of a 32-bit word (four code pairs, the lowest byte first)
+// -> four f16x2 words: the word is split into its bytes by one mov.
+__device__ __forceinline__ void f16x2_from_e2m1x8(uint32_t word, uint32_t (&d)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(word));
+}
+
+// Row r of a 4-bit weight tile: 32 bytes of codes (64 K-values) at r * 32,
+// then, past the tile's CODE_BYTES, its four block scales as one word at
+// r * 4 (block j in byte j).  -> 32 f16x2 words of code value * block scale.
+template <int CODE_BYTES>
+__device__ __forceinline__ void convert_row_fp4(const uint8_t* tile, int r, uint32_t (&w)[32]) {
+    const uint4 v0 = *reinterpret_cast<const uint4*>(tile + r * 32);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(tile + r * 32 + 16);
+    const uint32_t sw = *reinterpret_cast<const uint32_t*>(tile + CODE_BYTES + r * 4);
+    const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        const uint32_t sc = f16x2_splat_e4m3((sw >> (8 * blk)) & 0xFFu);   // 16 codes = 2 words per block
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int q = 2 * blk + h;
+            uint32_t d[4];
+            f16x2_from_e2m1x8(words[q], d);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) w[4 * q + b] = hmul2_rn(d[b], sc);
+        }
+    }
+}
+
 __device__ __forceinline__ void convert16(const uint4 v, uint32_t* w) {
     convert4(v.x, w[0], w[1]);
     convert4(v.y, w[2], w[3]);
@@ -150,13 +202,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // M = f, K = d.  Otherwise y (fp32 [cap][M]) = s_d * (Q_d . h), M = d, K = f,
 // two 128-feature tiles per item.
 // ---------------------------------------------------------------------------
-template <bool GATED>
+template <bool GATED, bool FP4 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_fp8_kernel(const __grid_constant__ CUtensorMap map_q0, const __grid_constant__ CUtensorMap map_q1,
                    const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
                    const float* __restrict__ scale0, const float* __restrict__ scale1,
                    const int32_t* __restrict__ offsets, int cap, int E, int K, int M, void* __restrict__ out,
-                   unsigned* err) {
+                   unsigned* err, const __grid_constant__ CUtensorMap map_s0,
+                   const __grid_constant__ CUtensorMap map_s1) {
+    // Bytes of one weight tile (128 rows x 64 K) in the code ring: FP8 codes,
+    // or 4-bit codes followed by the tile's block scales (one word per row).
+    constexpr int kQCode = FP4 ? BM * BK / 2 : kQTileBytes;
+    constexpr int kQTile = FP4 ? kQCode + BM * 4 : kQTileBytes;
+    constexpr int kQStage = 2 * kQTile;
+    static_assert(kQStage <= kQStageBytes, "the code ring's stages hold either format");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -203,6 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&map_q0);
         if (GATED) prefetch_tmap(&map_q1);
+        if (FP4) {
+            prefetch_tmap(&map_s0);
+            if (GATED) prefetch_tmap(&map_s1);
+        }
         prefetch_tmap(&map_b);
         prefetch_tmap(&map_b_big);
     }
@@ -271,11 +334,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* st = qring + s * kQStageBytes;
-                    mbar_arrive_expect_tx(&q_full[s], kQStageBytes);
+                    uint8_t* st = qring + s * kQStage;
+                    mbar_arrive_expect_tx(&q_full[s], kQStage);
                     issued[s] = static_cast<int>(ph);
-                    tma_load_2d(st, &map_q0, &q_full[s], kb * BK, wy, pol_w);
-                    tma_load_2d(st + kQTileBytes, &map_q1, &q_full[s], kb * BK, wy1, pol_w);
+                    if (FP4) {
+                        // codes: 32 bytes of each of the 128 rows; block scales [E][K/64][M] words:
+                        // the words of rows m .. m+127 of k-tile kb
+                        const int m0 = item.mt * (GATED ? BM : 2 * BM), m1 = GATED ? m0 : m0 + BM;
+                        const int sy = item.e * n_kb + kb;
+                        tma_load_2d(st, &map_q0, &q_full[s], kb * (BK / 2), wy, pol_w);
+                        tma_load_2d(st + kQCode, &map_s0, &q_full[s], m0, sy, pol_w);
+                        tma_load_2d(st + kQTile, &map_q1, &q_full[s], kb * (BK / 2), wy1, pol_w);
+                        tma_load_2d(st + kQTile + kQCode, &map_s1, &q_full[s], m1, sy, pol_w);
+                    } else {
+                        tma_load_2d(st, &map_q0, &q_full[s], kb * BK, wy, pol_w);
+                        tma_load_2d(st + kQTileBytes, &map_q1, &q_full[s], kb * BK, wy1, pol_w);
+                    }
                     if (++s == kQStages) {
                         s = 0;
                         ph ^= 1u;
@@ -380,10 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint8_t* st = qring + s * kQStageBytes;
+            const uint8_t* st = qring + s * kQStage;
             uint32_t w0[32], w1[32];
-            convert_row(st, r, w0);
-            convert_row(st + kQTileBytes, r, w1);
+            if (FP4) {
+                convert_row_fp4<kQCode>(st, r, w0);
+                convert_row_fp4<kQCode>(st + kQTile, r, w1);
+            } else {
+                convert_row(st, r, w0);
+                convert_row(st + kQTileBytes, r, w1);
+            }
             // the codes are in registers: the ring slot may be refilled
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_empty[s]);
@@ -559,23 +638,88 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const T* __restrict__
     }
 }
 
+// The 4-bit quantizer, a warp per row (lane j takes the 16-value blocks j,
+// j + 32, ...), in the fp32 arithmetic of its definition:
+//   s = max|w| / 2688 (1 for an all-zero row);
+//   b = E4M3 code (nearest even, saturating) of (block max / 6) / s;
+//   q = E2M1 code (nearest even, saturating at 6) of w / (value(b) * s),
+//       0 when value(b) is 0.
+// Codes: two per byte, the lower K index in the low nibble.  Block scales:
+// [E][K/64][M] words, block j of row m in byte j % 4 of word (e, j / 4, m).
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+    unsigned short v;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(v)
+        : "f"(hi), "f"(lo));
+    return v & 0xFFu;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_fp4_kernel(const T* __restrict__ w, long long rows, int M, int K,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ bscales,
+                                                           float* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const int n_blk = K / 16;
+    for (long long row = gw; row < rows; row += nw) {
+        const T* wr = w + row * K;
+        float amax = 0.f;
+        for (int j = lane; j < n_blk; j += 32) {
+            float v[8];
+            load8(wr + 16 * j, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            load8(wr + 16 * j + 8, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float s = amax > 0.f ? __fdiv_rn(amax, 2688.f) : 1.f;
+        const long long e = row / M, m = row - e * M;
+        for (int j = lane; j < n_blk; j += 32) {
+            float v[16];
+            load8(wr + 16 * j, *reinterpret_cast<float(*)[8]>(v));
+            load8(wr + 16 * j + 8, *reinterpret_cast<float(*)[8]>(v + 8));
+            float bmax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+            const uint32_t b = e4m3x2_from_f32(__fdiv_rn(__fdiv_rn(bmax, 6.f), s), 0.f) & 0xFFu;
+            uint32_t half2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(half2) : "h"(static_cast<unsigned short>(b)));
+            const float vb = __half2float(__ushort_as_half(static_cast<unsigned short>(half2 & 0xFFFFu)));
+            const float denom = __fmul_rn(vb, s);
+            uint32_t p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                p[i] = vb > 0.f ? e2m1x2_from_f32(__fdiv_rn(v[2 * i], denom), __fdiv_rn(v[2 * i + 1], denom)) : 0u;
+            *reinterpret_cast<uint2*>(codes + row * (K / 2) + 8 * j) =
+                make_uint2(p[0] | (p[1] << 8) | (p[2] << 16) | (p[3] << 24), p[4] | (p[5] << 8) | (p[6] << 16) |
+                                                                                  (p[7] << 24));
+            bscales[((e * (K / 64) + j / 4) * M + m) * 4 + (j & 3)] = static_cast<uint8_t>(b);
+        }
+        if (lane == 0) scales[row] = s;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
 std::mutex g_attr_mutex;
-bool g_attr_set[64][2];
+bool g_attr_set[64][4];
 
-template <bool GATED>
+template <bool GATED, bool FP4 = false>
 moe_status set_smem_attr() {
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    if (!g_attr_set[dev][GATED ? 1 : 0]) {
-        MOE_CUDA_TRY(
-            cudaFuncSetAttribute(ffn_fp8_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-        g_attr_set[dev][GATED ? 1 : 0] = true;
+    constexpr int v = (GATED ? 1 : 0) + (FP4 ? 2 : 0);
+    if (!g_attr_set[dev][v]) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(ffn_fp8_kernel<GATED, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          kSmemBytes));
+        g_attr_set[dev][v] = true;
     }
     return MOE_OK;
 }
@@ -604,7 +748,7 @@ moe_status launch_ffn_fp8_gate_up(const void* xs, const int32_t* offsets, int ca
     if ((s = encode_rows(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
     if ((s = set_smem_attr<true>()) != MOE_OK) return s;
     ffn_fp8_kernel<true><<<di.sm_count, kThreads, kSmemBytes, st>>>(m0, m1, mb, mbb, s_gate, s_up, offsets, cap, E,
-                                                                    d, f, h, di.error_word);
+                                                                    d, f, h, di.error_word, m0, m1);
     return cuda_status(cudaGetLastError());
 }
 
@@ -618,7 +762,67 @@ moe_status launch_ffn_fp8_down(const void* h, const int32_t* offsets, int cap, i
     if ((s = encode_rows(&mbb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
     if ((s = set_smem_attr<false>()) != MOE_OK) return s;
     ffn_fp8_kernel<false><<<di.sm_count, kThreads, kSmemBytes, st>>>(m0, m0, mb, mbb, s_down, s_down, offsets, cap,
-                                                                     E, f, d, y, di.error_word);
+                                                                     E, f, d, y, di.error_word, m0, m0);
+    return cuda_status(cudaGetLastError());
+}
+
+// 4-bit code tiles: 32 bytes (64 K-values) x 128 rows, no swizzle
+moe_status encode_codes_fp4(CUtensorMap* map, const void* base, int K, long long rows) {
+    return encode_2d_map(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows, BK / 2, BM,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// 4-bit block scales [E][K/64][M] 32-bit words (a row's four block scales of
+// one 64-K tile in one word): 128 rows x one k-tile per box
+moe_status encode_scales_fp4(CUtensorMap* map, const void* base, int M, int E, int K) {
+    return encode_2d_map(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, M, static_cast<long long>(E) * (K / BK), BM, 1,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+moe_status launch_ffn_fp4_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                  const uint8_t* q_gate, const uint8_t* b_gate, const float* s_gate,
+                                  const uint8_t* q_up, const uint8_t* b_up, const float* s_up, void* h,
+                                  cudaStream_t st, const DeviceInfo& di) {
+    CUtensorMap m0, m1, mb, mbb, ms0, ms1;
+    moe_status s;
+    if ((s = encode_codes_fp4(&m0, q_gate, d, static_cast<long long>(E) * f)) != MOE_OK) return s;
+    if ((s = encode_codes_fp4(&m1, q_up, d, static_cast<long long>(E) * f)) != MOE_OK) return s;
+    if ((s = encode_scales_fp4(&ms0, b_gate, f, E, d)) != MOE_OK) return s;
+    if ((s = encode_scales_fp4(&ms1, b_up, f, E, d)) != MOE_OK) return s;
+    if ((s = encode_rows(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_rows(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
+    if ((s = set_smem_attr<true, true>()) != MOE_OK) return s;
+    ffn_fp8_kernel<true, true><<<di.sm_count, kThreads, kSmemBytes, st>>>(m0, m1, mb, mbb, s_gate, s_up, offsets, cap,
+                                                                          E, d, f, h, di.error_word, ms0, ms1);
+    return cuda_status(cudaGetLastError());
+}
+
+moe_status launch_ffn_fp4_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                               const uint8_t* q_down, const uint8_t* b_down, const float* s_down, float* y,
+                               cudaStream_t st, const DeviceInfo& di) {
+    CUtensorMap m0, mb, mbb, ms0;
+    moe_status s;
+    if ((s = encode_codes_fp4(&m0, q_down, f, static_cast<long long>(E) * d)) != MOE_OK) return s;
+    if ((s = encode_scales_fp4(&ms0, b_down, d, E, f)) != MOE_OK) return s;
+    if ((s = encode_rows(&mb, h, f, cap, kBoxRows)) != MOE_OK) return s;
+    if ((s = encode_rows(&mbb, h, f, cap, kBigBoxRows)) != MOE_OK) return s;
+    if ((s = set_smem_attr<false, true>()) != MOE_OK) return s;
+    ffn_fp8_kernel<false, true><<<di.sm_count, kThreads, kSmemBytes, st>>>(m0, m0, mb, mbb, s_down, s_down, offsets,
+                                                                           cap, E, f, d, y, di.error_word, ms0, ms0);
+    return cuda_status(cudaGetLastError());
+}
+
+moe_status launch_quantize_fp4(const void* w, int dtype, int E, int M, int K, uint8_t* codes, uint8_t* block_scales,
+                               float* scales, cudaStream_t st, const DeviceInfo& di) {
+    const long long rows = static_cast<long long>(E) * M;
+    const long long blocks_needed = (rows + 7) / 8;
+    const int blocks = static_cast<int>(blocks_needed < di.sm_count * 16LL ? blocks_needed : di.sm_count * 16LL);
+    if (dtype == MOE_BF16)
+        quantize_fp4_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w), rows, M, K,
+                                                                    codes, block_scales, scales);
+    else
+        quantize_fp4_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(w), rows, M, K, codes,
+                                                            block_scales, scales);
     return cuda_status(cudaGetLastError());
 }
 

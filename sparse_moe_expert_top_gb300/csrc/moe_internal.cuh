@@ -28,11 +28,11 @@ constexpr int kSmallTokens = 128;
 // (histogram), chunk_bases[n_chunks][256] (prefix).  The prefix reads the
 // counts and writes the bases elsewhere, so it can be repeated.
 // Chunks are token-aligned: chunk c holds the routes of tokens
-// [c*ct, (c+1)*ct), ct = ws_chunk_tokens(T), a multiple of 64 chosen so that
+// [c*ct, (c+1)*ct), ct = ws_chunk_tokens(T), a multiple of 32 chosen so that
 // there are at most kMaxChunks chunks (one CTA of the histogram each).
 constexpr int kWsHeaderWords = 32;
-constexpr int kChunkTokenQuantum = 64;
-constexpr int kMaxChunks = 128;
+constexpr int kChunkTokenQuantum = 32;
+constexpr int kMaxChunks = 256;
 inline int ws_chunk_tokens(int T) {
     const int m = (T + kChunkTokenQuantum * kMaxChunks - 1) / (kChunkTokenQuantum * kMaxChunks);
     return kChunkTokenQuantum * (m > 1 ? m : 1);
@@ -142,6 +142,15 @@ moe_status launch_ffn_w8a8_gate_up(const uint8_t* xs, const float* xs_scale, con
 moe_status launch_ffn_w8a8_down(const uint8_t* hq, const float* h_scale, const int32_t* offsets, int cap, int E,
                                 int d, int f, const uint8_t* q_down, const float* s_down, float* y, cudaStream_t st,
                                 const DeviceInfo& di);
+moe_status launch_ffn_fp4_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
+                                  const uint8_t* q_gate, const uint8_t* b_gate, const float* s_gate,
+                                  const uint8_t* q_up, const uint8_t* b_up, const float* s_up, void* h,
+                                  cudaStream_t st, const DeviceInfo& di);
+moe_status launch_ffn_fp4_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
+                               const uint8_t* q_down, const uint8_t* b_down, const float* s_down, float* y,
+                               cudaStream_t st, const DeviceInfo& di);
+moe_status launch_quantize_fp4(const void* w, int dtype, int E, int M, int K, uint8_t* codes, uint8_t* block_scales,
+                               float* scales, cudaStream_t st, const DeviceInfo& di);
 moe_status launch_router_topk(const void* x, const void* wr, int T, int E, int d, int k, float* logits,
                               int32_t* ids, float* w, cudaStream_t st, const DeviceInfo& di);
 // moe_route_scatter_small for the fused path: xs may be NULL (no row copy);

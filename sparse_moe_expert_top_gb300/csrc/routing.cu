@@ -344,39 +344,41 @@ __global__ void __launch_bounds__(128, 1) route_topk_quad_kernel(const float* __
 // A2 (with TOPK and PREFIX: A1-A3 in one launch): route histogram with
 // stable ranks inside token-aligned chunks.
 //
-// Chunk c holds the routes of tokens [c*ct, (c+1)*ct), ct = ws_chunk_tokens(T),
-// and CTA c owns it.  The CTA walks its tokens 64 at a time; with TOPK it
-// first routes them (a quad of lanes per token, as route_topk_quad_kernel).
-// Warp w then takes the routes of tokens 8w .. 8w+7 of the pass, 32 at a
-// time in route order: __match_any_sync groups the lanes that hit one
-// expert, and a route's rank is the warp's running count for that expert
-// plus the number of lower lanes of its group.  A scan over the warps, in
-// warp order and on top of the earlier passes' counts, turns these into
-// ranks inside the chunk (route order) and finally the chunk's per-expert
-// counts.  The last CTA to finish (completion counter in the workspace header)
-// sums the chunk counts into counts[]; with PREFIX it also writes the
-// exclusive prefix offsets[] and every chunk's row bases (base[c][e] =
+// Chunk c holds the routes of tokens [c*ct, (c+1)*ct), ct = ws_chunk_tokens(T)
+// (a multiple of 32), and CTA c (32 warps) owns it.  The CTA walks its tokens
+// 32 at a time: warp w takes token w of the pass -- with TOPK it routes it
+// first (k rounds of a warp arg-max over order keys, the softmax summed in
+// slot order, as the small-chunk kernel does), else it reads the token's ids --
+// and leaves the experts of its unmasked routes in shared memory.  Warp 0
+// then ranks the pass's routes in route order, 32 at a time:
+// __match_any_sync groups the lanes that hit one expert, and a route's rank
+// inside the chunk is its expert's running count plus the number of lower
+// lanes of its group.  After the last pass the running counts are the
+// chunk's per-expert counts.  The last CTA to finish (completion counter in
+// the workspace header) sums the chunk counts into counts[], four threads
+// per expert each over a quarter of the chunks; with PREFIX it also writes
+// the exclusive prefix offsets[] and every chunk's row bases (base[c][e] =
 // offsets[e] + the counts of expert e in the chunks before c), as
 // prefix_offsets_kernel does.  The counter is left at zero for the next call.
+// A warp per token keeps the latency of a pass short: at prefill chunk
+// sizes every token of the chunk is in flight at once.
 // ---------------------------------------------------------------------------
 
-constexpr int kChunkWarps = 8;
-constexpr int kPassTokens = kChunkWarps * 8;
+constexpr int kChunkThreads = 1024;
+constexpr int kChunkWarps = kChunkThreads / 32;   // tokens per pass
+static_assert(kChunkThreads == 4 * kMaxExperts, "the tail takes four threads per expert");
 
-template <int KMAX, bool TOPK, bool PREFIX>
-__global__ void __launch_bounds__(256) route_chunks_kernel(const float* __restrict__ logits,
-                                                           const uint8_t* __restrict__ mask, int T, int E, int k,
-                                                           int chunk_tokens, int32_t* ids, float* __restrict__ w,
-                                                           int32_t* __restrict__ ws, int32_t* __restrict__ counts,
-                                                           int32_t* __restrict__ offsets, unsigned* err) {
-    __shared__ float cand_v[TOPK ? kChunkWarps : 1][8][kTopkCand];
-    __shared__ int cand_e[TOPK ? kChunkWarps : 1][8][kTopkCand];
-    __shared__ float sel_v[TOPK ? kChunkWarps : 1][8][KMAX];
-    __shared__ int cnt[kChunkWarps][kMaxExperts];
-    __shared__ int running[kMaxExperts];
-    __shared__ int e_w[kChunkWarps][8 * kMaxK];      // expert of each route of the warp's tokens (-1: masked)
-    __shared__ int rank_w[kChunkWarps][8 * kMaxK];   // its rank among the warp's routes to that expert
-    __shared__ int warp_sum[kChunkWarps];
+template <bool TOPK, bool PREFIX>
+__global__ void __launch_bounds__(kChunkThreads) route_chunks_kernel(const float* __restrict__ logits,
+                                                                     const uint8_t* __restrict__ mask, int T, int E,
+                                                                     int k, int chunk_tokens, int32_t* ids,
+                                                                     float* __restrict__ w, int32_t* __restrict__ ws,
+                                                                     int32_t* __restrict__ counts,
+                                                                     int32_t* __restrict__ offsets, unsigned* err) {
+    __shared__ int s_e[kChunkWarps * kMaxK];   // expert of each route of the pass (-1: masked)
+    __shared__ int s_cnt[kMaxExperts];         // running per-expert counts of the chunk; later the offsets
+    __shared__ int psum[4][kMaxExperts];       // the tail's partial sums over quarters of the chunks
+    __shared__ int warp_sum[8];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x, n_chunks = gridDim.x;
@@ -384,69 +386,84 @@ __global__ void __launch_bounds__(256) route_chunks_kernel(const float* __restri
     int32_t* lrank = chunk_counts + static_cast<size_t>(n_chunks) * kMaxExperts;
     const int t_begin = c * chunk_tokens, t_end = min(T, t_begin + chunk_tokens);
 
-    for (int i = tid; i < kChunkWarps * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
-    running[tid] = 0;   // blockDim.x == kMaxExperts
-    __syncthreads();
-
-    const unsigned lt_mask = (1u << lane) - 1u;
+    if (tid < kMaxExperts) s_cnt[tid] = 0;
     bool bad = false;
-    for (int p0 = t_begin; p0 < t_end; p0 += kPassTokens) {
-        const int w0 = p0 + warp * 8;                           // the warp's first token
-        const int nt = max(0, min(8, t_end - w0));
-        if (TOPK) {
-            const int q = lane & 3, tw = lane >> 2;
-            // quads past the chunk's end skip the routing (their syncs are quad-local)
-            if (tw < nt)
-                topk_quad_token<KMAX>(logits, w0 + tw, E, k, ids, w, cand_v[warp][tw], cand_e[warp][tw],
-                                      sel_v[warp][tw], q, 0xfu << (lane & ~3));
-            __syncwarp();   // the warp's ids, written above, are read below by other lanes of the warp
-        }
-        const int n_r = nt * k, r0 = w0 * k;
-        for (int j0 = 0; j0 < n_r; j0 += 32) {
-            const int j = j0 + lane;
-            int e = -1;
-            if (j < n_r) {
-                e = ids[r0 + j];
+    for (int p0 = t_begin; p0 < t_end; p0 += kChunkWarps) {
+        const int t = p0 + warp;
+        const int nt = min(kChunkWarps, t_end - p0);
+        if (t < t_end) {
+            int e = -1;   // lane s < k: the expert of slot s
+            if (TOPK) {
+                const float* row = logits + static_cast<size_t>(t) * E;
+                unsigned long long key[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int ee = lane + 32 * jj;
+                    key[jj] = (ee < E) ? topk_order_key(__ldg(row + ee), ee) : 0ull;
+                }
+                float sel_val = 0.f;
+                int sel_id = 0;
+                for (int sl = 0; sl < k; ++sl) {
+                    unsigned long long best = key[0];
+#pragma unroll
+                    for (int jj = 1; jj < 8; ++jj) best = key[jj] > best ? key[jj] : best;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const unsigned long long o = __shfl_xor_sync(kFull, best, off);
+                        best = o > best ? o : best;
+                    }
+                    const int eb = 0xFFFF - static_cast<int>(best & 0xFFFFu);
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        if (lane + 32 * jj == eb) key[jj] = 0ull;
+                    if (lane == sl) {
+                        sel_val = topk_key_value(best);
+                        sel_id = eb;
+                    }
+                }
+                // softmax over the k selected logits, summed in slot order
+                const float top = __shfl_sync(kFull, sel_val, 0);
+                float sum = 0.f;
+                for (int r = 0; r < k; ++r) sum += expf(__shfl_sync(kFull, sel_val, r) - top);
+                const float inv = 1.f / sum;
+                if (lane < k) {
+                    ids[static_cast<size_t>(t) * k + lane] = sel_id;
+                    w[static_cast<size_t>(t) * k + lane] = expf(sel_val - top) * inv;
+                    e = sel_id;
+                }
+            } else if (lane < k) {
+                e = ids[static_cast<size_t>(t) * k + lane];
                 if (e < 0 || e >= E) {
                     bad = true;
                     e = -1;
-                } else if (mask != nullptr && mask[r0 + j] != 0) {
-                    e = -1;
                 }
             }
-            const unsigned peers = __match_any_sync(kFull, e);
-            const int rank = e >= 0 ? cnt[warp][e] + __popc(peers & lt_mask) : -1;
-            __syncwarp();
-            if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp][e] += __popc(peers);
-            __syncwarp();
-            if (j < n_r) {
-                e_w[warp][j] = e;
-                rank_w[warp][j] = rank;
+            if (lane < k) {
+                if (e >= 0 && mask != nullptr && mask[static_cast<size_t>(t) * k + lane] != 0) e = -1;
+                s_e[warp * k + lane] = e;
             }
         }
         __syncthreads();
-        // per expert: the warps' counts in warp order, on top of the earlier passes
-        {
-            int run = running[tid];
-#pragma unroll
-            for (int ww = 0; ww < kChunkWarps; ++ww) {
-                const int cc = cnt[ww][tid];
-                cnt[ww][tid] = run;
-                run += cc;
+        if (warp == 0) {
+            // the pass's routes in route order: local route j is slot j % k of token p0 + j / k
+            const unsigned lt_mask = (1u << lane) - 1u;
+            const int n_r = nt * k;
+            const size_t r0 = static_cast<size_t>(p0) * k;
+            for (int j0 = 0; j0 < n_r; j0 += 32) {
+                const int j = j0 + lane;
+                const int e = j < n_r ? s_e[j] : -1;
+                const unsigned peers = __match_any_sync(kFull, e);
+                const int rank = e >= 0 ? s_cnt[e] + __popc(peers & lt_mask) : -1;
+                __syncwarp();
+                if (e >= 0 && lane == __ffs(peers) - 1) s_cnt[e] += __popc(peers);
+                __syncwarp();
+                if (j < n_r) lrank[r0 + j] = rank;
             }
-            running[tid] = run;
         }
-        __syncthreads();
-        for (int j = lane; j < n_r; j += 32) {
-            const int e = e_w[warp][j];
-            lrank[r0 + j] = e >= 0 ? rank_w[warp][j] + cnt[warp][e] : -1;
-        }
-        __syncthreads();
-        for (int i = tid; i < kChunkWarps * kMaxExperts; i += blockDim.x) (&cnt[0][0])[i] = 0;
         __syncthreads();
     }
     if (bad) atomicOr(err, DEVERR_OFFSETS);
-    chunk_counts[static_cast<size_t>(c) * kMaxExperts + tid] = running[tid];
+    if (tid < kMaxExperts) chunk_counts[static_cast<size_t>(c) * kMaxExperts + tid] = s_cnt[tid];
 
     // the last CTA reduces the chunk counts (and, with PREFIX, scans them)
     __threadfence();
@@ -455,29 +472,42 @@ __global__ void __launch_bounds__(256) route_chunks_kernel(const float* __restri
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    const int e = tid;
-    int total = 0;
+    const int e = tid & (kMaxExperts - 1), part = tid / kMaxExperts;
+    const int per = (n_chunks + 3) / 4;
+    const int c_lo = min(n_chunks, part * per), c_hi = min(n_chunks, c_lo + per);
+    int part_sum = 0;
     if (e < E)
-        for (int cc = 0; cc < n_chunks; ++cc) total += __ldcg(chunk_counts + static_cast<size_t>(cc) * kMaxExperts + e);
-    if (e < E) counts[e] = total;
+        for (int cc = c_lo; cc < c_hi; ++cc) part_sum += __ldcg(chunk_counts + static_cast<size_t>(cc) * kMaxExperts + e);
+    psum[part][e] = part_sum;
+    __syncthreads();
+    const int total = psum[0][e] + psum[1][e] + psum[2][e] + psum[3][e];
+    if (part == 0 && e < E) counts[e] = total;
     if (PREFIX) {
+        // exclusive scan of the totals over the experts, by the 256 threads of part 0
         int incl = total;
+        if (part == 0) {
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(kFull, incl, off);
-            if (lane >= off) incl += o;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(kFull, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (lane == 31) warp_sum[warp] = incl;
         }
-        if (lane == 31) warp_sum[warp] = incl;
         __syncthreads();
-        int before = 0;
-        for (int ww = 0; ww < warp; ++ww) before += warp_sum[ww];
-        const int excl = before + incl - total;
-        if (e < E) offsets[e] = excl;
-        if (e == E - 1) offsets[E] = excl + total;
+        if (part == 0) {
+            int before = 0;
+            for (int ww = 0; ww < warp; ++ww) before += warp_sum[ww];
+            const int excl = before + incl - total;
+            s_cnt[e] = excl;
+            if (e < E) offsets[e] = excl;
+            if (e == E - 1) offsets[E] = excl + total;
+        }
+        __syncthreads();
         int32_t* bases = lrank + static_cast<size_t>(T) * k;
         if (e < E) {
-            int run = excl;
-            for (int cc = 0; cc < n_chunks; ++cc) {
+            int run = s_cnt[e];
+            for (int pp = 0; pp < part; ++pp) run += psum[pp][e];
+            for (int cc = c_lo; cc < c_hi; ++cc) {
                 bases[static_cast<size_t>(cc) * kMaxExperts + e] = run;
                 run += __ldcg(chunk_counts + static_cast<size_t>(cc) * kMaxExperts + e);
             }
@@ -614,6 +644,165 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
         }
     }
     if (TO_F16 && __syncthreads_or(range) && tid == 0) atomicOr(err, DEVERR_RANGE);
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 activation rows (the FP8-activation path).  The arithmetic is the
+// weights' quantizer's: scale = max|row| / 448 (IEEE fp32 division; 1 for an
+// all-zero row), code = E4M3 of the IEEE fp32 quotient v / scale, rounded to
+// nearest even and saturating -- so that the codes are the weight
+// quantizer's bit for bit.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t e4m3x2_rn(float lo, float hi) {
+    unsigned short v;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(hi), "f"(lo));
+    return v;
+}
+
+// The 8 bf16 values of `u` as 8 E4M3 codes of v / s.
+__device__ __forceinline__ uint2 e4m3x8_of_bf16x8(uint4 u, float s) {
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        p[i] = e4m3x2_rn(__fdiv_rn(__uint_as_float(wv[i] << 16), s), __fdiv_rn(__uint_as_float(wv[i] & 0xFFFF0000u), s));
+    return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+__device__ __forceinline__ float amax_bf16x8(uint4 u) {
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[i] << 16)), fabsf(__uint_as_float(wv[i] & 0xFFFF0000u))));
+    return m;
+}
+
+// Largest `v` of the CTA, returned to every thread (red: one float per warp).
+__device__ __forceinline__ float block_max(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, off));
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float m = 0.f;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+    return m;
+}
+
+constexpr int kQuantWarps = 8;   // rows per CTA of the row quantizer
+constexpr int kQuantVec = 8;     // uint4 (8 bf16) per lane: rows of up to 2048 values in registers
+
+// Rows of a bf16 matrix [cap][K] to E4M3 codes and one scale per row, a warp
+// per row holding its row in registers (read once, reduced with shuffles).
+// Rows at or beyond R = offsets[E] are the zero-filled unused compact rows:
+// their codes are 0 and their scale 1 (an all-zero row), without reading them.
+__global__ void __launch_bounds__(32 * kQuantWarps) quantize_rows_e4m3_kernel(const uint4* __restrict__ a, int K8,
+                                                                            int cap, const int32_t* __restrict__ offsets,
+                                                                            int E, uint2* __restrict__ codes,
+                                                                            float* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+    if (row >= cap) return;
+    uint2* crow = codes + static_cast<size_t>(row) * K8;
+    if (row >= __ldg(offsets + E)) {
+        for (int v = lane; v < K8; v += 32) crow[v] = make_uint2(0u, 0u);
+        if (lane == 0) scales[row] = 1.f;
+        return;
+    }
+    uint4 u[kQuantVec];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < kQuantVec; ++j) {
+        const int v = lane + 32 * j;
+        if (v < K8) {
+            u[j] = __ldg(a + static_cast<size_t>(row) * K8 + v);
+            amax = fmaxf(amax, amax_bf16x8(u[j]));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+#pragma unroll
+    for (int j = 0; j < kQuantVec; ++j) {
+        const int v = lane + 32 * j;
+        if (v < K8) crow[v] = e4m3x8_of_bf16x8(u[j], s);
+    }
+    if (lane == 0) scales[row] = s;
+}
+
+// A4 of the FP8-activation path straight from the bf16 token rows, a CTA per
+// token: the row is read once, quantized (codes x_q and scale x_scales of the
+// token) and its codes written to the token's compact rows with their scale;
+// k of the unused tail rows R .. T*k-1 get zero codes and scale 0.  The
+// compact rows come from the workspace exactly as in scatter_rows_kernel.
+template <int VPT>
+__global__ void __launch_bounds__(128) scatter_quant_e4m3_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets, int T, int k,
+    int E, int d8, const int32_t* __restrict__ lrank, const int32_t* __restrict__ bases, int chunk_tokens,
+    uint2* __restrict__ x_q, float* __restrict__ x_scales, uint2* __restrict__ xs, float* __restrict__ xs_scales,
+    int32_t* __restrict__ row_of_route, int32_t* __restrict__ route_of_row, unsigned* err) {
+    __shared__ int rows[kMaxK];
+    __shared__ int tails[kMaxK];
+    __shared__ float red[4];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const int n_routes = T * k;
+    if (tid < k) {
+        const int r = t * k + tid;
+        const int lr = lrank[r];
+        int row = -1;
+        bool bad = false;
+        if (lr >= 0) {
+            const int e = ids[r];
+            if (e >= 0 && e < E) row = bases[static_cast<size_t>(t / chunk_tokens) * kMaxExperts + e] + lr;
+            if (row < 0 || row >= n_routes) {
+                bad = true;
+                row = -1;
+            }
+        }
+        rows[tid] = row;
+        row_of_route[r] = row;
+        if (row >= 0) route_of_row[row] = r;
+        const int R = __ldg(offsets + E);
+        int tail = -1;
+        if (R < 0 || R > n_routes) bad = true;
+        else if (R + r < n_routes) tail = R + r;
+        tails[tid] = tail;
+        if (tail >= 0) route_of_row[tail] = -1;
+        if (bad) atomicOr(err, DEVERR_OFFSETS);
+    }
+    uint4 u[VPT];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = tid + j * 128;
+        if (v < d8) {
+            u[j] = __ldg(x + static_cast<size_t>(t) * d8 + v);
+            amax = fmaxf(amax, amax_bf16x8(u[j]));
+        }
+    }
+    amax = block_max(amax, red);   // its barrier also publishes rows[] and tails[]
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = tid + j * 128;
+        if (v < d8) {
+            const uint2 q = e4m3x8_of_bf16x8(u[j], s);
+            x_q[static_cast<size_t>(t) * d8 + v] = q;
+            for (int sl = 0; sl < k; ++sl) {
+                const int row = rows[sl];
+                if (row >= 0) xs[static_cast<size_t>(row) * d8 + v] = q;
+                const int tail = tails[sl];
+                if (tail >= 0) xs[static_cast<size_t>(tail) * d8 + v] = make_uint2(0u, 0u);
+            }
+        }
+    }
+    if (tid < k) {
+        if (rows[tid] >= 0) xs_scales[rows[tid]] = s;
+        if (tails[tid] >= 0) xs_scales[tails[tid]] = 0.f;
+    }
+    if (tid == 0) x_scales[t] = s;
 }
 
 // A4 without the row copy, for the fused path (the gate/up kernel gathers
@@ -909,14 +1098,14 @@ moe_status launch_status() { return cuda_status(cudaGetLastError()); }
 
 // Largest chunk the allocation-free histogram accepts, and its scratch size:
 // header + per-chunk counts (at most kMaxChunks chunks) + one in-chunk rank
-// per route (384 KB).
+// per route (512 KB).
 constexpr int kNoAllocMaxRoutes = 65536;
 constexpr int kNoAllocWords = kWsHeaderWords + kMaxChunks * kMaxExperts + kNoAllocMaxRoutes;
 
 // A2 (histogram only) over the token-aligned chunks of `ws`.
 moe_status launch_histogram(const int32_t* ids, const uint8_t* mask, int T, int k, int E, int32_t* counts,
                             int32_t* ws, cudaStream_t s, const DeviceInfo& di) {
-    route_chunks_kernel<8, false, false><<<ws_chunks(T, k), kMaxExperts, 0, s>>>(
+    route_chunks_kernel<false, false><<<ws_chunks(T, k), kChunkThreads, 0, s>>>(
         nullptr, mask, T, E, k, ws_chunk_tokens(T), const_cast<int32_t*>(ids), nullptr, ws, counts, nullptr,
         di.error_word);
     return launch_status();
@@ -1026,8 +1215,9 @@ extern "C" moe_status moe_route_topk_offsets(const float* logits, const uint8_t*
         return st != MOE_OK ? st : moe_prefix_offsets(counts, 0, k, E, offsets, ws, stream);
     }
     MOE_REQUIRE(logits && ids && w);
-    if (E % 4 != 0 || !aligned16(logits)) {
-        // the quad top-k reads float4 groups: other shapes take the three step kernels
+    if (ws_chunk_tokens(T) > kChunkWarps) {
+        // beyond kMaxChunks chunks of one pass the CTAs would walk their tokens
+        // serially: the streaming top-k kernel and the histogram scale better
         moe_status st = moe_route_topk(logits, T, E, k, ids, w, stream);
         if (st == MOE_OK) st = moe_route_histogram(ids, mask, T, k, E, counts, ws, stream);
         if (st == MOE_OK) st = moe_prefix_offsets(counts, T, k, E, offsets, ws, stream);
@@ -1039,12 +1229,8 @@ extern "C" moe_status moe_route_topk_offsets(const float* logits, const uint8_t*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int chunks = ws_chunks(T, k), ct = ws_chunk_tokens(T);
     int32_t* w32 = static_cast<int32_t*>(ws);
-    if (k <= 8)
-        route_chunks_kernel<8, true, true><<<chunks, kMaxExperts, 0, s>>>(logits, mask, T, E, k, ct, ids, w, w32,
-                                                                        counts, offsets, di.error_word);
-    else
-        route_chunks_kernel<16, true, true><<<chunks, kMaxExperts, 0, s>>>(logits, mask, T, E, k, ct, ids, w, w32,
-                                                                         counts, offsets, di.error_word);
+    route_chunks_kernel<true, true><<<chunks, kChunkThreads, 0, s>>>(logits, mask, T, E, k, ct, ids, w, w32, counts,
+                                                                    offsets, di.error_word);
     return launch_status();
 }
 
@@ -1149,6 +1335,45 @@ extern "C" moe_status moe_scatter_rows_e4m3(const uint8_t* x_codes, const float*
         reinterpret_cast<const uint4*>(x_codes), ids, offsets, T, k, E, d / 16, w32 + ws_rank_offset(T, k),
         w32 + ws_bases_offset(T, k), reinterpret_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word,
         nullptr, 0, nullptr, 0, ws_chunk_tokens(T), x_scales, xs_scales);
+    return launch_status();
+}
+
+extern "C" moe_status moe_scatter_rows_quant_e4m3(const void* x, const int32_t* ids, const uint8_t* mask,
+                                                   const int32_t* offsets, int T, int k, int d, int E, uint8_t* x_q,
+                                                   float* x_scales, uint8_t* xs, float* xs_scales,
+                                                   int32_t* row_of_route, int32_t* route_of_row, void* ws,
+                                                   void* stream) {
+    (void)mask;  // folded into the workspace ranks by the histogram
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 16 && d % 16 == 0);
+    MOE_REQUIRE(d <= 8 * 128 * 8);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(x && ids && offsets && x_q && x_scales && xs && xs_scales && row_of_route && route_of_row && ws);
+    MOE_REQUIRE(aligned16(x) && aligned16(x_q) && aligned16(xs) && aligned16(ws));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    const int32_t* w32 = static_cast<const int32_t*>(ws);
+    const int d8 = d / 8;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto kernel = d8 <= 4 * 128 ? scatter_quant_e4m3_kernel<4> : scatter_quant_e4m3_kernel<8>;
+    kernel<<<T, 128, 0, s>>>(static_cast<const uint4*>(x), ids, offsets, T, k, E, d8, w32 + ws_rank_offset(T, k),
+                             w32 + ws_bases_offset(T, k), ws_chunk_tokens(T), reinterpret_cast<uint2*>(x_q),
+                             x_scales, reinterpret_cast<uint2*>(xs), xs_scales, row_of_route, route_of_row,
+                             di.error_word);
+    return launch_status();
+}
+
+extern "C" moe_status moe_quantize_rows_e4m3(const void* a, const int32_t* offsets, int E, int cap, int K,
+                                             uint8_t* codes, float* scales, void* stream) {
+    MOE_REQUIRE(E >= 1 && E <= kMaxExperts && cap >= 0 && K >= 16 && K % 16 == 0 && K <= 8 * 32 * kQuantVec);
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(a && offsets && codes && scales && aligned16(a) && aligned16(codes));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    quantize_rows_e4m3_kernel<<<(cap + kQuantWarps - 1) / kQuantWarps, 32 * kQuantWarps, 0,
+                                static_cast<cudaStream_t>(stream)>>>(static_cast<const uint4*>(a), K / 8, cap, offsets,
+                                                                     E, reinterpret_cast<uint2*>(codes), scales);
     return launch_status();
 }
 

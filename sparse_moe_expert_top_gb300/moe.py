@@ -61,7 +61,13 @@ SIGNATURES = {
     "moe_forward_fused": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I,
                            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_clear_device_error": ([_P], _I),
+    "moe_quantize_weights_fp4": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_grouped_gate_up_fp4": ([_P, _P, _I, _I, _I, _I] + [_P] * 8, _I),
+    "moe_grouped_down_fp4": ([_P, _P, _I, _I, _I, _I] + [_P] * 5, _I),
+    "moe_forward_fp4": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 9 + [_P] * 12, _I),
     "moe_scatter_rows_e4m3": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_scatter_rows_quant_e4m3": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_quantize_rows_e4m3": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
     "moe_grouped_gate_up_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_down_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_forward_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 6 + [_P] * 17, _I),
@@ -752,6 +758,31 @@ def moe_scatter_rows_e4m3(x_q, x_scales, ids, mask, offsets, xs, xs_scales, row_
         _ptr(row_of_route), _ptr(route_of_row), _ptr(ws), _stream(stream)))
 
 
+def moe_scatter_rows_quant_e4m3(x, ids, mask, offsets, x_q, x_scales, xs, xs_scales, row_of_route, route_of_row,
+                                ws, stream=None):
+    T, d = x.shape
+    k = ids.shape[1]
+    E = offsets.shape[0] - 1
+    _expect(x, torch.bfloat16, (T, d), "x")
+    _expect(x_q, torch.uint8, (T, d), "x_q")
+    _expect(x_scales, torch.float32, (T,), "x_scales")
+    _expect(xs, torch.uint8, (T * k, d), "xs")
+    _expect(xs_scales, torch.float32, (T * k,), "xs_scales")
+    _check("moe_scatter_rows_quant_e4m3", load().moe_scatter_rows_quant_e4m3(
+        _ptr(x), _ptr(ids), _ptr(mask), _ptr(offsets), T, k, d, E, _ptr(x_q), _ptr(x_scales), _ptr(xs),
+        _ptr(xs_scales), _ptr(row_of_route), _ptr(route_of_row), _ptr(ws), _stream(stream)))
+
+
+def moe_quantize_rows_e4m3(a, offsets, codes, scales, stream=None):
+    cap, K = a.shape
+    E = offsets.shape[0] - 1
+    _expect(a, torch.bfloat16, (cap, K), "a")
+    _expect(codes, torch.uint8, (cap, K), "codes")
+    _expect(scales, torch.float32, (cap,), "scales")
+    _check("moe_quantize_rows_e4m3", load().moe_quantize_rows_e4m3(
+        _ptr(a), _ptr(offsets), E, cap, K, _ptr(codes), _ptr(scales), _stream(stream)))
+
+
 def moe_grouped_gate_up_w8a8(xs, xs_scales, offsets, q_gate: FP8Weights, q_up: FP8Weights, h, stream=None):
     cap, d = xs.shape
     E, f, _ = q_gate.shape
@@ -799,4 +830,91 @@ def moe_forward_w8a8(logits, x, mask, q_gate: FP8Weights, q_up: FP8Weights, q_do
         _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.x_q), _ptr(b.x_scales), _ptr(b.xs),
         _ptr(b.xs_scales), _ptr(b.row_of_route), _ptr(b.route_of_row), _ptr(b.h), _ptr(b.h_q), _ptr(b.h_scales),
         _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
+    return b.out
+
+
+# ---------------------------------------------------------------------------
+# 4-bit block-scaled expert weights
+# ---------------------------------------------------------------------------
+
+class FP4Weights:
+    """One expert bank in the 4-bit format: ``codes`` uint8 [E][M][K/2], ``block_scales`` uint8 [E][K/64][M][4]
+    (E4M3), ``scales`` fp32 [E][M]."""
+
+    def __init__(self, codes, block_scales, scales):
+        E, M, K2 = codes.shape
+        if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or scales.dtype != torch.float32:
+            raise ValueError("expected uint8 codes and block scales, fp32 scales")
+        if tuple(block_scales.shape) != (E, 2 * K2 // 64, M, 4) or tuple(scales.shape) != (E, M):
+            raise ValueError("block scales [E][K/64][M][4] and scales [E][M] do not match the codes")
+        self.codes, self.block_scales, self.scales = codes, block_scales, scales
+
+    @property
+    def shape(self):
+        E, M, K2 = self.codes.shape
+        return (E, M, 2 * K2)
+
+
+def moe_quantize_weights_fp4(w, stream=None) -> FP4Weights:
+    """Quantize a bank [E][M][K] (bf16 or fp32, K a multiple of 64) to the 4-bit block-scaled format."""
+    E, M, K = w.shape
+    codes = torch.empty(E, M, K // 2, dtype=torch.uint8, device=w.device)
+    bs = torch.empty(E, K // 64, M, 4, dtype=torch.uint8, device=w.device)
+    scales = torch.empty(E, M, dtype=torch.float32, device=w.device)
+    _check("moe_quantize_weights_fp4", load().moe_quantize_weights_fp4(
+        _ptr(w), _dtype_code(w), E, M, K, _ptr(codes), _ptr(bs), _ptr(scales), _stream(stream)))
+    return FP4Weights(codes, bs, scales)
+
+
+def _expect_fp4(q, shape, name):
+    if not isinstance(q, FP4Weights) or tuple(q.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected FP4Weights of shape {tuple(shape)}")
+
+
+def moe_grouped_gate_up_fp4(xs, offsets, q_gate: FP4Weights, q_up: FP4Weights, h, stream=None):
+    cap, d = xs.shape
+    E, f, _ = q_gate.shape
+    _expect(xs, torch.float16, (cap, d), "xs")
+    _expect_fp4(q_gate, (E, f, d), "q_gate")
+    _expect_fp4(q_up, (E, f, d), "q_up")
+    _expect(h, torch.float16, (cap, f), "h")
+    _check("moe_grouped_gate_up_fp4", load().moe_grouped_gate_up_fp4(
+        _ptr(xs), _ptr(offsets), cap, E, d, f, _ptr(q_gate.codes), _ptr(q_gate.block_scales), _ptr(q_gate.scales),
+        _ptr(q_up.codes), _ptr(q_up.block_scales), _ptr(q_up.scales), _ptr(h), _stream(stream)))
+
+
+def moe_grouped_down_fp4(h, offsets, q_down: FP4Weights, y, stream=None):
+    cap, f = h.shape
+    E, d, _ = q_down.shape
+    _expect(h, torch.float16, (cap, f), "h")
+    _expect_fp4(q_down, (E, d, f), "q_down")
+    _expect(y, torch.float32, (cap, d), "y")
+    _check("moe_grouped_down_fp4", load().moe_grouped_down_fp4(
+        _ptr(h), _ptr(offsets), cap, E, d, f, _ptr(q_down.codes), _ptr(q_down.block_scales), _ptr(q_down.scales),
+        _ptr(y), _stream(stream)))
+
+
+def moe_forward_fp4(logits, x, mask, q_gate: FP4Weights, q_up: FP4Weights, q_down: FP4Weights, k: int,
+                    bufs: MoEBuffers, stream=None) -> torch.Tensor:
+    """The whole path with 4-bit weights; ``bufs`` holds fp16 compact activations; returns ``bufs.out``."""
+    T, E = logits.shape
+    d = x.shape[1]
+    f = q_gate.shape[1]
+    if (bufs.T, bufs.E, bufs.k, bufs.d, bufs.f, bufs.dtype) != (T, E, k, d, f, torch.float16):
+        raise ValueError("buffers were allocated for another shape (the 4-bit path keeps xs and h in fp16)")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect_fp4(q_gate, (E, f, d), "q_gate")
+    _expect_fp4(q_up, (E, f, d), "q_up")
+    _expect_fp4(q_down, (E, d, f), "q_down")
+    b = bufs
+    _check("moe_forward_fp4", load().moe_forward_fp4(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, f,
+        _ptr(q_gate.codes), _ptr(q_gate.block_scales), _ptr(q_gate.scales),
+        _ptr(q_up.codes), _ptr(q_up.block_scales), _ptr(q_up.scales),
+        _ptr(q_down.codes), _ptr(q_down.block_scales), _ptr(q_down.scales),
+        _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
+        _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
     return b.out

@@ -64,11 +64,11 @@ def test_host_only_calls(lib):
     assert lib.moe_status_string(5) == b"a value out of the fp16 operand range"
     n = ctypes.c_size_t(0)
     assert lib.moe_workspace_size(2048, 6, ctypes.byref(n)) == 0
-    # header (32 words) + 32 chunks of 64 tokens x 256 counts + 12288 ranks + 32 chunks of 256 bases, int32
-    assert n.value == 4 * (32 + 32 * 256 + 2048 * 6 + 32 * 256)
-    # beyond 128 chunks of 64 tokens the chunks grow: 8193 tokens -> 65 chunks of 128 tokens
+    # header (32 words) + 64 chunks of 32 tokens x 256 counts + 12288 ranks + 64 chunks of 256 bases, int32
+    assert n.value == 4 * (32 + 64 * 256 + 2048 * 6 + 64 * 256)
+    # beyond 256 chunks of 32 tokens the chunks grow: 8193 tokens -> 129 chunks of 64 tokens
     assert lib.moe_workspace_size(8193, 6, ctypes.byref(n)) == 0
-    assert n.value == 4 * (32 + 65 * 256 + 8193 * 6 + 65 * 256)
+    assert n.value == 4 * (32 + 129 * 256 + 8193 * 6 + 129 * 256)
     assert lib.moe_workspace_size(10, 17, ctypes.byref(n)) == 1      # k > 16
     assert lib.moe_workspace_size(-1, 2, ctypes.byref(n)) == 1       # T < 0
     # argument checks reject before touching the device

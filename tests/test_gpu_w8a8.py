@@ -153,3 +153,39 @@ def test_w8a8_full_size_workload(name):
     _check_against_oracle(b, ref, q, cfg.k, cfg.d)
     st = assert_close(out, ref["out"], "bf16")
     print(f"{name} W8A8: rel_fro={st['rel_fro']:.2e} max/rms={st['max_abs'] / st['rms_ref']:.2e}")
+
+
+@pytest.mark.parametrize("T,E,k,d,f,p", [(300, 16, 4, 512, 384, 0.1), (40, 8, 6, 4096, 2048, 0.0),
+                                         (33, 4, 2, 8192, 128, 0.2), (20, 4, 2, 256, 1920, 0.0)])
+def test_fused_quantizers_equal_the_weight_quantizer(T, E, k, d, f, p):
+    """The scatter that quantizes the token rows, and the row quantizer of h, give the codes and scales of
+    moe_quantize_weights_fp8 (and of moe_scatter_rows_e4m3 on them) bit for bit."""
+    logits, mask, x, *_ = _case(T, E, k, 128, 128, p, seed=d + T)
+    x = torch.randn(T, d).to(torch.bfloat16).cuda()
+    md = None if mask is None else mask.cuda()
+    a = M.MoEBuffersW8A8(T, E, k, d, f)
+    M.moe_route_topk_offsets(logits.cuda(), md, k, a.ids, a.w, a.counts, a.offsets, a.ws)
+    ref_q = M.moe_quantize_weights_fp8(x)
+    ref_xs = torch.empty_like(a.xs)
+    ref_sc = torch.empty_like(a.xs_scales)
+    ref_ror, ref_rro = torch.empty_like(a.row_of_route), torch.empty_like(a.route_of_row)
+    M.moe_scatter_rows_e4m3(ref_q.codes, ref_q.scales, a.ids, md, a.offsets, ref_xs, ref_sc, ref_ror, ref_rro, a.ws)
+    a.xs.fill_(7)
+    a.xs_scales.fill_(float("nan"))
+    M.moe_scatter_rows_quant_e4m3(x, a.ids, md, a.offsets, a.x_q, a.x_scales, a.xs, a.xs_scales, a.row_of_route,
+                                  a.route_of_row, a.ws)
+    M.moe_check_device_error()
+    assert torch.equal(a.x_q, ref_q.codes) and torch.equal(a.x_scales, ref_q.scales)
+    assert torch.equal(a.xs, ref_xs) and torch.equal(a.xs_scales.view(torch.int32), ref_sc.view(torch.int32))
+    assert torch.equal(a.row_of_route, ref_ror) and torch.equal(a.route_of_row, ref_rro)
+    # rows of h: the rows below R as the weight quantizer gives them, the rows beyond it zero codes, scale 1
+    R = int(a.offsets[-1])
+    h = torch.randn(T * k, f, device="cuda").to(torch.bfloat16)
+    h[R:] = 0
+    h[0, :5] = -0.0
+    codes = torch.full((T * k, f), 9, dtype=torch.uint8, device="cuda")
+    scales = torch.full((T * k,), float("nan"), device="cuda")
+    M.moe_quantize_rows_e4m3(h, a.offsets, codes, scales)
+    M.moe_check_device_error()
+    ref_h = M.moe_quantize_weights_fp8(h)
+    assert torch.equal(codes, ref_h.codes) and torch.equal(scales, ref_h.scales)

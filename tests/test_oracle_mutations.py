@@ -17,6 +17,7 @@ import pytest
 
 from oracle import build as obuild
 from oracle import moe_oracle as mo
+import tests.test_oracle_fp4 as fp4_pins
 import tests.test_oracle_fp8 as fp8_pins
 import tests.test_oracle_pins as pins
 import tests.test_oracle_router as router_pins
@@ -59,6 +60,11 @@ def _all_pins():
         fp8_pins.test_quantized_bank_ffn_is_the_dequantized_ffn,
         fp8_pins.test_bf16_rounding_matches_torch_cast,
         fp8_pins.test_w8a8_path_is_the_dense_ffn_on_quantized_operands,
+        fp4_pins.test_e2m1_code_table,
+        fp4_pins.test_e2m1_rounding_against_brute_force,
+        fp4_pins.test_fp4_quantizer_hand_worked_row,
+        fp4_pins.test_fp4_quantizer_picks_the_nearest_value_of_each_block,
+        fp4_pins.test_fp4_bank_ffn_is_the_dequantized_ffn,
         router_pins.test_hand_worked_router_case,
         router_pins.test_one_hot_router_rows_select_input_columns,
         router_pins.test_router_is_linear_and_permutation_equivariant,
@@ -106,6 +112,12 @@ MUTANTS = [
     ("e4m3_subnormal_binade_off_by_one", [("std::max(ex - 1, -6);", "std::max(ex - 1, -7);")]),
     ("fp8_scale_of_the_fnuz_variant", [("amax / 448.0f", "amax / 240.0f")]),
     ("bf16_with_seven_significant_bits", [("std::ldexp(1.0, binade - 7);", "std::ldexp(1.0, binade - 6);")]),
+    ("e2m1_ties_away_from_zero", [("std::nearbyint(a / quantum) * quantum;\n    r = std::min(r, 6.0);",
+                                   "std::round(a / quantum) * quantum;\n    r = std::min(r, 6.0);")]),
+    ("fp4_block_scale_from_max_over_4", [("bmax / 6.0f / s", "bmax / 4.0f / s")]),
+    ("fp4_row_scale_without_the_e2m1_max", [("amax / 2688.0f", "amax / 448.0f")]),
+    ("fp4_nibbles_swapped", [("q << (4 * (i & 1))", "q << (4 * (1 - (i & 1)))")]),
+    ("fp4_blocks_of_8_when_decoding", [("e4m3_value(bs[c / 16])", "e4m3_value(bs[c / 8])")]),
     ("router_reads_wr_transposed",
      [("element(wr, wdtype, static_cast<size_t>(e) * d + c)", "element(wr, wdtype, static_cast<size_t>(c) * E + e)")]),
 ]
