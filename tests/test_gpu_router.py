@@ -59,7 +59,13 @@ def test_router_matches_oracle(T, E, d, k):
     ids, w, logits = _run(x, wr, k)
     xf, wf = to_np(x).astype(np.float64), to_np(wr).astype(np.float64)
     ref_logits, ref_ids, ref_w = mo.route_from_router(xf, wf, k)
-    bound = d * 2.0 ** -24 * (np.abs(xf) @ np.abs(wf).T)
+    # Accumulation model: the products of bf16 operands are exact in fp32; the d products are then added in
+    # fp32 in some order (the K split over the cluster reorders them) by an adder that either rounds to
+    # nearest or truncates.  Any order of d - 1 such additions errs by at most
+    # (d - 1) u / (1 - (d - 1) u) * sum |x_j w_j| with u = 2^-23, the unit roundoff of truncation (twice
+    # that of rounding to nearest), so the bound holds whichever the tensor cores do.
+    u = 2.0 ** -23
+    bound = (d - 1) * u / (1 - (d - 1) * u) * (np.abs(xf) @ np.abs(wf).T)
     assert np.all(np.abs(logits - ref_logits) <= bound)
 
     n_sep = 0
