@@ -628,12 +628,16 @@ def run_ours(args, rank: int, world: int):
     gate_up_bytes = work["gate_up_bytes"]
     peaks = _peaks()
     achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic("gate_up_w8a8" if w8a8 else "gate_up_fp4" if fp4 else "gate_up_fp8" if fp8 else
-                                ("gate_up_gather" if gather else "gate_up"), cfg.name)
-    kname = ("moe_grouped_gate_up_w8a8 (ffn_tc_kernel<gated, E4M3>)" if w8a8 else
+    # chunks of many routes run the bf16 and E4M3 projections on pairs of SMs (the library's choice)
+    paired = dtype == torch.bfloat16 and not (fp8 or fp4 or gather) and M.moe_ffn_paired(T * k)
+    traffic = _profiled_traffic(("gate_up_w8a8" if w8a8 else "gate_up_fp4" if fp4 else "gate_up_fp8" if fp8 else
+                                 "gate_up_gather" if gather else "gate_up") + ("_pair" if paired else ""), cfg.name)
+    kname = ("moe_grouped_gate_up_w8a8 (ffn_pair_kernel<gated, E4M3>)" if w8a8 and paired else
+             "moe_grouped_gate_up_w8a8 (ffn_tc_kernel<gated, E4M3>)" if w8a8 else
              "moe_grouped_gate_up_fp4 (ffn_fp8_kernel<gated, FP4>)" if fp4 else
              "moe_grouped_gate_up_fp8 (ffn_fp8_kernel<gated>)" if fp8 else
              "moe_grouped_gate_up_gather (ffn_tc_kernel<gated, fused>)" if gather else
+             "moe_grouped_gate_up (ffn_pair_kernel<gated>)" if paired else
              "moe_grouped_gate_up (ffn_tc_kernel<gated>)")
     roofline = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],

@@ -266,6 +266,14 @@ moe_status moe_grouped_gate_up(const void* xs, const int32_t* offsets, int cap, 
 moe_status moe_grouped_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
                             const void* w_down, int dtype, float* y, void* stream);
 
+/* Which tensor-core kernels the bf16 and E4M3 (W8A8) grouped projections
+ * run for a capacity of `cap` compact rows: *paired = 1 when clusters of two
+ * CTAs issue M = 256 MMAs over two SMs (chunks of many routes), 0 when each
+ * CTA works alone.  The results agree within the fp32 accumulation's
+ * rounding either way.  Host only; MOE_ERR_INVALID_ARG if paired is NULL or
+ * cap < 0. */
+moe_status moe_ffn_paired(int cap, int* paired);
+
 /* A5 + A6 in one call (two kernels on `stream`). */
 moe_status moe_grouped_ffn(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,
                            const void* w_gate, const void* w_up, const void* w_down, int dtype,

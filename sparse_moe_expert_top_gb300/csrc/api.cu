@@ -525,6 +525,12 @@ int fused_auto_mode(long long cap, int E, int d, bool have_xs, const DeviceInfo&
 
 }  // namespace
 
+extern "C" moe_status moe_ffn_paired(int cap, int* paired) {
+    MOE_REQUIRE(paired && cap >= 0);
+    *paired = use_pair_ffn(cap) ? 1 : 0;
+    return MOE_OK;
+}
+
 extern "C" moe_status moe_forward_fused_mode(int T, int E, int k, int d, int have_xs, int* mode) {
     MOE_REQUIRE(mode && T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 1);
     DeviceInfo di;

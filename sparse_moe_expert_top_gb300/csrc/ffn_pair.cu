@@ -1,0 +1,597 @@
+// Grouped expert FFN (A5 gate/up + SwiGLU, A6 down) on pairs of SMs.
+//
+// The same work as the one-SM tensor-core kernel, for chunks with many rows
+// per expert: a cluster of two CTAs issues tcgen05.mma.cta_group::2 with
+// M = 256, so one MMA instruction covers 256 weight rows (128 in each CTA's
+// shared memory) against up to 256 compact rows (the CTA's own half of them
+// in its shared memory, exchanged between the two SMs by the tensor cores).
+// Per 64-K stage each SM then loads 32 KB of weights and at most 16 KB of
+// rows, where the one-SM kernel loads 32 KB and up to 32 KB for the same
+// MMA work, and each SM's shared memory serves half the operand reads.
+//
+// Roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (active in the even
+// CTA of the pair only), then the epilogue warps (4 for gate/up, 8 for down).
+// Both CTAs run the same item loop.  The odd CTA's TMA loads complete on the
+// even CTA's full barrier (the cta_group::2 form of the bulk tensor copy);
+// the MMA thread's commits arrive on the barriers of both CTAs (multicast);
+// the odd CTA's epilogue releases an accumulator on the even CTA's barrier.
+//
+// Work item: (expert e, a 256-feature tile of gate/up or a 512-feature tile
+// of down, a slice of at most 256 of the expert's compact rows).  The item's
+// rows are padded to N = 32 * ceil(rows / 32); the even CTA holds rows
+// [0, N/2) of the slice and the odd CTA rows [N/2, N), so accumulator column
+// c belongs to compact row row0 + c in both CTAs' tensor memory.
+#include <cuda_bf16.h>
+
+#include "tc_common.cuh"
+
+#ifndef MOE_PAIR_MIN_ROUTES
+#define MOE_PAIR_MIN_ROUTES 24576
+#endif
+
+namespace moe {
+namespace {
+
+constexpr int PBM = 128;                 // weight rows per CTA and tile
+constexpr int kRowBytes = 128;           // one 128-byte swizzle row of K per operand row and stage
+constexpr int kPairSlice = 256;          // compact rows per item at most (the MMA's N)
+constexpr int kPairStages = 4;
+constexpr int kATile = PBM * kRowBytes;  // 16 KB
+constexpr int kBTile = 128 * kRowBytes;  // 16 KB: the CTA's half of N rows
+constexpr int kStageBytes = 2 * kATile + kBTile;
+constexpr int kRingBytes = kPairStages * kStageBytes;  // 192 KB
+constexpr int kCtrlBytes = 4096;
+constexpr int kSmallBox = 16;            // rows per small TMA box
+constexpr int kLargeBox = 64;            // rows per large TMA box
+constexpr int kTmemCols = 512;           // gate (tile 0) at 0, up (tile 1) at 256; two 128-column slots each
+
+template <bool GATED>
+struct PairCfg {
+    static constexpr int kEpiWarps = GATED ? 4 : 8;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kFeat = GATED ? 2 * PBM : 4 * PBM;  // output features per item (the pair's)
+    static constexpr int kOutStage = GATED ? 32 * PBM * 2 : 0;
+    static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kOutStage + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+};
+
+__device__ __forceinline__ float silu_pair(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+
+// Named barrier 1 among the epilogue threads of this CTA.
+__device__ __forceinline__ void epilogue_sync_n_pair(int threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// All threads of both CTAs; returns once every thread of the pair has arrived.
+__device__ __forceinline__ void pair_sync() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 2-D tile load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+template <bool F8>
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    if (F8)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// Arrives on the barrier at this shared-memory offset in both CTAs once every
+// MMA issued so far has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+    const uint16_t both = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(both)
+        : "memory");
+}
+
+// Rows of the item held by each CTA (a multiple of 16).
+__device__ __forceinline__ int half_rows(int rows) { return 16 * ((rows + 31) / 32); }
+
+// ---------------------------------------------------------------------------
+// GATED: out = h (bf16 [cap][M]) = silu(A0 . xs) * (A1 . xs), A0 = w_gate,
+// A1 = w_up, M = f, K = d.  Otherwise out = y (fp32 [cap][M]) = A0 . h,
+// A0 = w_down, M = d, K = f.  F8: E4M3 operands (kind::f8f6f4), the
+// accumulators scaled in the epilogue by the weight row's and the compact
+// row's scales.
+// ---------------------------------------------------------------------------
+template <bool GATED, bool F8>
+__global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
+    ffn_pair_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
+                    const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
+                    const int32_t* __restrict__ offsets, int cap, int E, int K, int M, void* __restrict__ out,
+                    unsigned* err, const float* __restrict__ sa0, const float* __restrict__ sa1,
+                    const float* __restrict__ sb) {
+    using C = PairCfg<GATED>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* ctrl = smem + kRingBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+    uint64_t* empty = full + kPairStages;
+    uint64_t* acc_full = empty + kPairStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* issued = reinterpret_cast<int*>(tmem_slot + 2);
+    int* item_off = issued + kPairStages;           // E + 1 entries
+    int* ntiles = item_off + kMaxExperts + 1;        // E entries
+    volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
+    int* order = const_cast<int*>(epi_flag + 2);     // experts: the heavy ones, then the light ones (E entries)
+    int* heavy_items = order + kMaxExperts;          // items of the heavy experts
+    __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kCtrlBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    constexpr int KBE = F8 ? 128 : 64;   // K elements per stage
+    const int n_kb = K / KBE;
+    const int n_mt = (M + C::kFeat - 1) / C::kFeat;
+
+    // ---- prologue ------------------------------------------------------------
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            issued[s] = -1;
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 2 * C::kEpiWarps);   // the epilogue warps of both CTAs
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&map_a0);
+        if (GATED) prefetch_tmap(&map_a1);
+        prefetch_tmap(&map_b);
+        prefetch_tmap(&map_b_big);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    if (warp == 2) {
+        // Item table (identical in both CTAs).  Experts with more than one
+        // row slice ("heavy": their weight tiles serve several slices from L2,
+        // the MMAs set the pace) come first in `order`, the others ("light":
+        // each weight tile streamed from HBM for one slice) after them, each
+        // group in expert-id order; item_off is the exclusive scan of the item
+        // counts in that order.  The items are then handed out interleaved
+        // (item_at below), so that at any time some pairs run tensor-bound
+        // heavy items while others stream light ones.
+        bool bad = false;
+        for (int e = lane; e < E; e += 32) {
+            const int lo = offsets[e], hi = offsets[e + 1];
+            bad |= lo < 0 || hi < lo || hi > cap;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        const int per = (E + 31) / 32;                 // lane j owns experts / positions [j*per, (j+1)*per)
+        const int first = min(lane * per, E);
+        int nheavy = 0;
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e < E) {
+                const int n = bad ? 0 : offsets[e + 1] - offsets[e];
+                ntiles[e] = (n + kPairSlice - 1) / kPairSlice;
+                nheavy += ntiles[e] > 1 ? 1 : 0;
+            }
+        }
+        int hincl = nheavy;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, hincl, off);
+            if (lane >= off) hincl += o;
+        }
+        const int n_heavy = __shfl_sync(0xffffffffu, hincl, 31);
+        int hpos = hincl - nheavy;                      // heavy experts before this lane's
+        int lpos = n_heavy + (first - hpos);            // light experts go after all heavy ones
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e < E) order[ntiles[e] > 1 ? hpos++ : lpos++] = e;
+        }
+        __syncwarp();
+        int local = 0;
+        for (int i = 0; i < per; ++i) {
+            const int p = lane * per + i;
+            if (p < E) local += ntiles[order[p]] * n_mt;
+        }
+        int incl = local;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - local;
+        for (int i = 0; i < per; ++i) {
+            const int p = lane * per + i;
+            if (p < E) {
+                item_off[p] = run;
+                run += ntiles[order[p]] * n_mt;
+            }
+        }
+        if (lane == 31) item_off[E] = run;
+        __syncwarp();
+        if (lane == 0) *heavy_items = item_off[n_heavy];
+        if (bad && lane == 0 && rank == 0) atomicOr(err, DEVERR_OFFSETS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    pair_sync();   // both CTAs' barriers are initialised before either signals the other's
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_items = item_off[E];
+    const int n_heavy_items = *heavy_items;
+    // Position p of the hand-out order takes the next heavy item when
+    // floor((p + 1) * H / n) > floor(p * H / n) (H heavy items of n), else the
+    // next light item: every stretch of positions holds heavy and light items
+    // in proportion.
+    auto item_at = [&](int p) {
+        const long long hb = static_cast<long long>(p) * n_heavy_items / n_items;
+        const long long hb1 = static_cast<long long>(p + 1) * n_heavy_items / n_items;
+        const int u = hb1 > hb ? static_cast<int>(hb) : n_heavy_items + p - static_cast<int>(hb);
+        return decode_item_ordered(u, item_off, order, ntiles, offsets, E, kPairSlice);
+    };
+
+    if (warp == 0) {
+        // ---- TMA producer (both CTAs) ------------------------------------------
+        if (lane == 0) {
+            const uint64_t pol_once = l2_policy(1);
+            const uint64_t pol_shared = l2_policy(2);
+            const uint64_t pol_x = l2_policy(2);
+            const uint32_t full_lead = map_to_rank(smem_u32(full), 0);   // the even CTA's full[0]
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int it = pair; ok && it < n_items; it += n_pairs) {
+                const Item item = item_at(it);
+                const int nh = half_rows(item.rows);
+                const int my0 = item.row0 + static_cast<int>(rank) * nh;
+                const uint32_t bytes = 2 * kATile + nh * kRowBytes;   // this CTA's share of a stage
+                // weight tiles past the expert's last feature read the next
+                // expert's rows (or zero fill past the bank); none of their
+                // results is stored
+                const int wy0 = item.e * M + item.mt * C::kFeat + static_cast<int>(rank) * PBM;
+                const int wy1 = GATED ? wy0 : wy0 + 2 * PBM;
+                const uint64_t pol_w = ntiles[item.e] > 1 ? pol_shared : pol_once;
+                for (int kb = 0; kb < n_kb; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + s * kStageBytes;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * bytes);
+                    issued[s] = static_cast<int>(ph);
+                    const uint32_t bar = full_lead + 8u * static_cast<uint32_t>(s);
+                    tma_load_2d_pair(st, &map_a0, bar, kb * KBE, wy0, pol_w);
+                    tma_load_2d_pair(st + kATile, GATED ? &map_a1 : &map_a0, bar, kb * KBE, wy1, pol_w);
+                    uint8_t* bdst = st + 2 * kATile;
+                    int r = 0;
+                    for (; r + kLargeBox <= nh; r += kLargeBox)
+                        tma_load_2d_pair(bdst + r * kRowBytes, &map_b_big, bar, kb * KBE, my0 + r, pol_x);
+                    for (; r < nh; r += kSmallBox)
+                        tma_load_2d_pair(bdst + r * kRowBytes, &map_b, bar, kb * KBE, my0 + r, pol_x);
+                    if (++s == kPairStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer (even CTA) ---------------------------------------------
+        if (lane == 0 && rank == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int toggle = 0;
+            uint32_t use0 = 0, use1 = 0;
+            bool ok = true;
+            for (int it = pair; ok && it < n_items; it += n_pairs) {
+                const Item item = item_at(it);
+                const int N = 2 * half_rows(item.rows);
+                const uint32_t idesc = F8 ? idesc_e4m3(2 * PBM, N) : idesc_bf16(2 * PBM, N);
+                const bool both = item.rows > 128;
+                const int slot = both ? 0 : toggle;
+                const uint32_t use_s = slot ? use1 : use0;
+                if (!mbar_wait(&acc_empty[slot], (use_s & 1u) ^ 1u, abort_flag, err)) break;
+                if (both && !mbar_wait(&acc_empty[1], (use1 & 1u) ^ 1u, abort_flag, err)) break;
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + static_cast<uint32_t>(slot * 128);
+                for (int kb = 0; kb < n_kb; ++kb) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sdesc_lo(smem_u32(smem + s * kStageBytes));
+                    const uint32_t a1 = a0 + (kATile >> 4);
+                    const uint32_t b = a0 + ((2 * kATile) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        const uint64_t bd = sdesc_from_lo(b + 2 * kk);
+                        umma_pair<F8>(d0, sdesc_from_lo(a0 + 2 * kk), bd, idesc, acc);
+                        umma_pair<F8>(d0 + 256, sdesc_from_lo(a1 + 2 * kk), bd, idesc, acc);
+                    }
+                    umma_commit_pair(&empty[s]);
+                    if (++s == kPairStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(&acc_full[slot]);
+                if (slot) ++use1;
+                else ++use0;
+                if (both) {
+                    umma_commit_pair(&acc_full[1]);
+                    ++use1;
+                    toggle = 0;
+                } else {
+                    toggle ^= 1;
+                }
+            }
+            // every MMA issued above has completed once `drain` flips (in both CTAs)
+            umma_commit_pair(drain);
+            mbar_drain(drain, 0);
+        }
+    } else {
+        // ---- epilogue (both CTAs) ----------------------------------------------
+        const int q = warp & 3;
+        const int et = threadIdx.x - 64;
+        constexpr int kEpiThreads = 32 * C::kEpiWarps;
+        const int grp = (warp - 2) >> 2;
+        const uint32_t acc_empty_lead = map_to_rank(smem_u32(acc_empty), 0);
+        int local = 0;
+        int toggle = 0;
+        uint32_t use0 = 0, use1 = 0;
+        bool ok = true;
+        for (int it = pair; it < n_items; it += n_pairs, ++local) {
+            const Item item = item_at(it);
+            const bool both = item.rows > 128;
+            const int slot = both ? 0 : toggle;
+            const int buf = local & 1;
+            if (et == 0) {
+                bool got = mbar_wait(&acc_full[slot], (slot ? use1 : use0) & 1u, abort_flag, err);
+                if (got && both) got = mbar_wait(&acc_full[1], use1 & 1u, abort_flag, err);
+                epi_flag[buf] = got ? 1 : 0;
+            }
+            epilogue_sync_n_pair(kEpiThreads);
+            if (!epi_flag[buf]) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // this CTA's features: tile 0 at fb + [0, 128), tile 1 (down) at fb + 256 + [0, 128)
+            const int fb = item.mt * C::kFeat + static_cast<int>(rank) * PBM;
+            const int m = fb + q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(slot * 128);
+            const int n_groups = (!GATED && both) ? 2 : 1;
+            for (int c0 = 32 * grp; grp < n_groups && c0 < item.rows; c0 += 32 * n_groups) {
+                uint32_t g[32], g1[32];
+                tmem_ld32(taddr + c0, g);
+                tmem_ld32(taddr + 256 + c0, g1);
+                tmem_ld_wait();
+                float rs[32];
+                if (F8) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) rs[j] = c0 + j < item.rows ? __ldg(sb + item.row0 + c0 + j) : 0.f;
+                }
+                if (GATED) {
+                    const bool valid = fb < M;   // the whole 128-feature tile, f being a multiple of 128
+                    float wsg = 1.f, wsu = 1.f;
+                    if (F8 && valid) {
+                        wsg = __ldg(sa0 + static_cast<size_t>(item.e) * M + m);
+                        wsu = __ldg(sa1 + static_cast<size_t>(item.e) * M + m);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float gv = F8 ? __uint_as_float(g[j]) * wsg * rs[j] : __uint_as_float(g[j]);
+                        const float uv = F8 ? __uint_as_float(g1[j]) * wsu * rs[j] : __uint_as_float(g1[j]);
+                        out_stage[j * PBM + q * 32 + lane] = __float2bfloat16_rn(silu_pair(gv) * uv);
+                    }
+                    epilogue_sync_n_pair(kEpiThreads);
+                    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
+                    const int chunk = et & 15;
+#pragma unroll
+                    for (int pass = 0; pass < 4; ++pass) {
+                        const int j = pass * 8 + (et >> 4);
+                        const int n = c0 + j;
+                        if (valid && n < item.rows) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(out_stage + j * PBM + chunk * 8);
+                            *reinterpret_cast<uint4*>(h + static_cast<size_t>(item.row0 + n) * M + fb + chunk * 8) = v;
+                        }
+                    }
+                    epilogue_sync_n_pair(kEpiThreads);
+                } else {
+                    const bool has0 = m < M, has1 = m + 2 * PBM < M;
+                    float ws0 = 1.f, ws1 = 1.f;
+                    if (F8) {
+                        if (has0) ws0 = __ldg(sa0 + static_cast<size_t>(item.e) * M + m);
+                        if (has1) ws1 = __ldg(sa0 + static_cast<size_t>(item.e) * M + m + 2 * PBM);
+                    }
+                    float* y = static_cast<float*>(out);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int n = c0 + j;
+                        if (n < item.rows) {
+                            float* yr = y + static_cast<size_t>(item.row0 + n) * M;
+                            if (has0) yr[m] = F8 ? __uint_as_float(g[j]) * ws0 * rs[j] : __uint_as_float(g[j]);
+                            if (has1)
+                                yr[m + 2 * PBM] = F8 ? __uint_as_float(g1[j]) * ws1 * rs[j] : __uint_as_float(g1[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                // release the accumulator slots to the MMA thread of the even CTA
+                mbar_arrive_remote(acc_empty_lead + 8u * static_cast<uint32_t>(slot));
+                if (both) mbar_arrive_remote(acc_empty_lead + 8u);
+            }
+            if (slot) ++use1;
+            else ++use0;
+            if (both) {
+                ++use1;
+                toggle = 0;
+            } else {
+                toggle ^= 1;
+            }
+        }
+        // zero-fill the unused compact rows R .. cap-1
+        const int R = offsets[E];
+        if (ok && R >= 0 && R <= cap) {
+            const int vecs = M * (GATED ? 2 : 4) / 16;
+            const int gw = blockIdx.x * C::kEpiWarps + (warp - 2);
+            const int nw = gridDim.x * C::kEpiWarps;
+            uint4* o = static_cast<uint4*>(out);
+            for (int row = R + gw; row < cap; row += nw)
+                for (int v = lane; v < vecs; v += 32) o[static_cast<size_t>(row) * vecs + v] = make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // ---- teardown ----------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (rank == 0 && *abort_flag) {
+            // copies still in flight (both CTAs' shares count on these barriers)
+            for (int s = 0; s < kPairStages; ++s)
+                if (issued[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued[s]));
+        }
+        // the even CTA's final commit reaches this CTA's drain barrier too
+        if (rank == 1) mbar_drain(drain, 0);
+    }
+    __syncthreads();
+    // neither CTA leaves while the other may still signal its barriers or
+    // the tensor cores may still read its shared memory
+    pair_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+struct PairCache {
+    unsigned long long ctx;
+    int pairs;   // co-resident clusters of two
+};
+std::mutex g_pair_mutex;
+PairCache g_pair_cache[64][4];
+
+template <bool GATED, bool F8>
+moe_status launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& bb,
+                       const int32_t* offsets, int cap, int E, int K, int M, void* out, const float* sa0,
+                       const float* sa1, const float* sb, cudaStream_t st, const DeviceInfo& di) {
+    using C = PairCfg<GATED>;
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    unsigned long long ctx = 0;
+    moe_status s = current_context_id(&ctx);
+    if (s != MOE_OK) return s;
+    auto kern = ffn_pair_kernel<GATED, F8>;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int pairs = 0;
+    {
+        constexpr int v = (GATED ? 1 : 0) + (F8 ? 2 : 0);
+        std::lock_guard<std::mutex> lock(g_pair_mutex);
+        PairCache& pc = g_pair_cache[dev][v];
+        if (pc.ctx != ctx || pc.pairs <= 0) {
+            MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+            cfg.gridDim = dim3(di.sm_count / 2 * 2);
+            int n = 0;
+            MOE_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+            pc.ctx = ctx;
+            pc.pairs = n < di.sm_count / 2 ? n : di.sm_count / 2;
+        }
+        pairs = pc.pairs;
+    }
+    if (pairs < 1) return MOE_ERR_UNSUPPORTED;
+    cfg.gridDim = dim3(2 * pairs);
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a0, a1, b, bb, offsets, cap, E, K, M, out, di.error_word, sa0, sa1,
+                                    sb));
+    return MOE_OK;
+}
+
+}  // namespace
+
+// Chunks of at least this many routes (T * k) take the paired kernels.
+bool use_pair_ffn(int cap) { return cap >= MOE_PAIR_MIN_ROUTES; }
+
+moe_status launch_ffn_pair_prepared(const FfnTcLaunch& p, cudaStream_t st, const DeviceInfo& di) {
+    if (p.gated)
+        return launch_pair<true, false>(p.a0, p.a1, p.b, p.bb, p.offsets, p.cap, p.E, p.K, p.M, p.out, nullptr,
+                                        nullptr, nullptr, st, di);
+    return launch_pair<false, false>(p.a0, p.a1, p.b, p.bb, p.offsets, p.cap, p.E, p.K, p.M, p.out, nullptr, nullptr,
+                                     nullptr, st, di);
+}
+
+moe_status launch_ffn_pair_w8a8(bool gated, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                                const CUtensorMap& bb, const int32_t* offsets, int cap, int E, int K, int M, void* out,
+                                const float* sa0, const float* sa1, const float* sb, cudaStream_t st,
+                                const DeviceInfo& di) {
+    if (gated) return launch_pair<true, true>(a0, a1, b, bb, offsets, cap, E, K, M, out, sa0, sa1, sb, st, di);
+    return launch_pair<false, true>(a0, a1, b, bb, offsets, cap, E, K, M, out, sa0, sa1, sb, st, di);
+}
+
+}  // namespace moe

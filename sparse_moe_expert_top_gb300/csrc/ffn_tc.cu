@@ -129,29 +129,6 @@ __device__ __forceinline__ void combine_sync() { asm volatile("bar.sync 2, 128;"
 // takes one group).
 constexpr int kSlotGroup = 6;
 
-// Item `it` of the table built in expert order: item_off[p] = first item of
-// the p-th expert in that order, order[p] = that expert, ntiles[e] = its
-// compact row slices.  Items of one expert are ordered mt-major, nt-minor.
-__device__ __forceinline__ Item decode_item_ordered(int it, const int* item_off, const int* order, const int* ntiles,
-                                                    const int32_t* offsets, int E, int slice) {
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (item_off[mid] <= it) lo = mid;
-        else hi = mid - 1;
-    }
-    Item r;
-    r.e = order[lo];
-    const int local = it - item_off[lo];
-    const int n = ntiles[r.e];
-    r.mt = local / n;
-    const int nt = local - r.mt * n;
-    const int seg_lo = __ldg(offsets + r.e), seg_hi = __ldg(offsets + r.e + 1);
-    r.row0 = seg_lo + nt * slice;
-    r.rows = min(slice, seg_hi - r.row0);
-    return r;
-}
-
 // Arguments of the fused permutation (unused by the plain instantiations).
 struct FusedArgs {
     const uint8_t* x;             // gate/up: token rows, bf16 [T][d]
@@ -1001,6 +978,7 @@ moe_status prepare_ffn_tc_down(const void* h, const int32_t* offsets, int cap, i
 }
 
 moe_status launch_ffn_tc_prepared(const FfnTcLaunch& p, cudaStream_t st, const DeviceInfo& di) {
+    if (!p.narrow && use_pair_ffn(p.cap)) return launch_ffn_pair_prepared(p, st, di);
     if (p.gated)
         return launch<true, false>(p.a0, p.a1, p.b, p.bb, p.offsets, p.cap, p.E, p.K, p.M, p.narrow, p.out,
                                    FusedArgs{}, st, di);
@@ -1039,6 +1017,8 @@ moe_status launch_ffn_w8a8_gate_up(const uint8_t* xs, const float* xs_scale, con
     if ((s = encode_2d_u8(&ma1, q_up, d, static_cast<long long>(E) * f, wbox)) != MOE_OK) return s;
     if ((s = encode_2d_u8(&mb, xs, d, cap, kBoxRows)) != MOE_OK) return s;
     if ((s = encode_2d_u8(&mbb, xs, d, cap, kBigBoxRows)) != MOE_OK) return s;
+    if (!narrow && use_pair_ffn(cap))
+        return launch_ffn_pair_w8a8(true, ma0, ma1, mb, mbb, offsets, cap, E, d, f, h, s_gate, s_up, xs_scale, st, di);
     return launch<true, false, true>(ma0, ma1, mb, mbb, offsets, cap, E, d, f, narrow, h, FusedArgs{}, st, di,
                                      OpScales{s_gate, s_up, xs_scale});
 }
@@ -1053,6 +1033,9 @@ moe_status launch_ffn_w8a8_down(const uint8_t* hq, const float* h_scale, const i
     if ((s = encode_2d_u8(&mb, hq, f, cap, kBoxRows)) != MOE_OK) return s;
     if ((s = encode_2d_u8(&mbb, hq, f, cap, kBigBoxRows)) != MOE_OK) return s;
     const bool narrow = use_narrow(cap, E, (d + 2 * BM - 1) / (2 * BM), di) && f % 256 == 0;
+    if (!narrow && use_pair_ffn(cap))
+        return launch_ffn_pair_w8a8(false, ma0, ma0, mb, mbb, offsets, cap, E, f, d, y, s_down, nullptr, h_scale, st,
+                                    di);
     return launch<false, false, true>(ma0, ma0, mb, mbb, offsets, cap, E, f, d, narrow, y, FusedArgs{}, st, di,
                                       OpScales{s_down, nullptr, h_scale});
 }

@@ -109,6 +109,15 @@ moe_status prepare_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int ca
 moe_status prepare_ffn_tc_down(const void* h, const int32_t* offsets, int cap, int E, int d, int f,
                                const void* w_down, float* y, const DeviceInfo& di, FfnTcLaunch* p);
 moe_status launch_ffn_tc_prepared(const FfnTcLaunch& p, cudaStream_t st, const DeviceInfo& di);
+// The paired-SM kernels (clusters of two CTAs, M = 256 MMAs) for chunks of
+// many routes; the tensor maps are the one-SM kernels' (weights: 128-row
+// boxes; rows: 16- and 64-row boxes).
+bool use_pair_ffn(int cap);
+moe_status launch_ffn_pair_prepared(const FfnTcLaunch& p, cudaStream_t st, const DeviceInfo& di);
+moe_status launch_ffn_pair_w8a8(bool gated, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                                const CUtensorMap& bb, const int32_t* offsets, int cap, int E, int K, int M, void* out,
+                                const float* sa0, const float* sa1, const float* sb, cudaStream_t st,
+                                const DeviceInfo& di);
 
 // Kernel launchers implemented in the other translation units.
 moe_status launch_ffn_tc_gate_up(const void* xs, const int32_t* offsets, int cap, int E, int d, int f,

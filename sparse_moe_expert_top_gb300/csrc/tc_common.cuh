@@ -279,6 +279,29 @@ __device__ __forceinline__ Item decode_item(int it, const int* item_off, const i
     return r;
 }
 
+// Item `it` of the table built in expert order: item_off[p] = first item of
+// the p-th expert in that order, order[p] = that expert, ntiles[e] = its
+// compact row slices.  Items of one expert are ordered mt-major, nt-minor.
+__device__ __forceinline__ Item decode_item_ordered(int it, const int* item_off, const int* order, const int* ntiles,
+                                                    const int32_t* offsets, int E, int slice) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (item_off[mid] <= it) lo = mid;
+        else hi = mid - 1;
+    }
+    Item r;
+    r.e = order[lo];
+    const int local = it - item_off[lo];
+    const int n = ntiles[r.e];
+    r.mt = local / n;
+    const int nt = local - r.mt * n;
+    const int seg_lo = __ldg(offsets + r.e), seg_hi = __ldg(offsets + r.e + 1);
+    r.row0 = seg_lo + nt * slice;
+    r.rows = min(slice, seg_hi - r.row0);
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // Host side: tensor maps
 // ---------------------------------------------------------------------------

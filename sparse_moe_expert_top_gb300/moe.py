@@ -73,6 +73,7 @@ SIGNATURES = {
     "moe_forward_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 6 + [_P] * 17, _I),
     "moe_route_topk_offsets": ([_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_forward_fused_mode": ([_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)], _I),
+    "moe_ffn_paired": ([_I, ctypes.POINTER(ctypes.c_int)], _I),
     "moe_plan_create": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                          ctypes.POINTER(ctypes.c_void_p)], _I),
     "moe_plan_destroy": ([_P], _I),
@@ -641,6 +642,13 @@ def moe_forward_fp8(logits, x, mask, q_gate: FP8Weights, q_up: FP8Weights, q_dow
         _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
         _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
     return b.out
+
+
+def moe_ffn_paired(cap: int) -> bool:
+    """Whether the bf16 and E4M3 grouped projections run on pairs of SMs for `cap` compact rows."""
+    paired = ctypes.c_int(-1)
+    _check("moe_ffn_paired", load().moe_ffn_paired(cap, ctypes.byref(paired)))
+    return paired.value == 1
 
 
 def moe_forward_fused_mode(T: int, E: int, k: int, d: int, have_xs: bool = True) -> int:

@@ -41,7 +41,7 @@ def test_header_declares_the_path_entry_points():
                      "moe_tile_counts_size", "moe_route_scatter_small_fused",
                      "moe_workspace_size", "moe_check_device_error", "moe_clear_device_error",
                      "moe_forward_fused_mode", "moe_plan_create", "moe_plan_destroy", "moe_plan_grouped_gate_up",
-                     "moe_plan_grouped_down", "moe_plan_forward"):
+                     "moe_plan_grouped_down", "moe_plan_forward", "moe_ffn_paired"):
         assert required in names
 
 
@@ -130,6 +130,11 @@ def test_plan_entry_points_reject_bad_arguments(lib):
     mode = ctypes.c_int(-1)
     assert lib.moe_forward_fused_mode(4, 300, 2, 128, 1, ctypes.byref(mode)) == 1          # E > 256
     assert lib.moe_forward_fused_mode(4, 8, 2, 128, 1, None) == 1
+    paired = ctypes.c_int(-1)
+    assert lib.moe_ffn_paired(12288, ctypes.byref(paired)) == 0 and paired.value == 0      # 2,048 tokens, top-6
+    assert lib.moe_ffn_paired(49152, ctypes.byref(paired)) == 0 and paired.value == 1      # 8,192 tokens, top-6
+    assert lib.moe_ffn_paired(-1, ctypes.byref(paired)) == 1
+    assert lib.moe_ffn_paired(4, None) == 1
 
 
 def test_product_path_does_not_import_the_oracle():
