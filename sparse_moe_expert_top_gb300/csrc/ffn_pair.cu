@@ -47,10 +47,11 @@ constexpr int kTmemCols = 512;           // gate (tile 0) at 0, up (tile 1) at 2
 
 template <bool GATED>
 struct PairCfg {
-    static constexpr int kEpiWarps = GATED ? 4 : 8;
+    // two groups of 4 epilogue warps take alternate 32-row chunks of an item
+    static constexpr int kEpiWarps = 8;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kFeat = GATED ? 2 * PBM : 4 * PBM;  // output features per item (the pair's)
-    static constexpr int kOutStage = GATED ? 32 * PBM * 2 : 0;
+    static constexpr int kOutStage = GATED ? 2 * 32 * PBM * 2 : 0;   // a 32-row bf16 tile of h per group
     static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kOutStage + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
@@ -61,6 +62,9 @@ __device__ __forceinline__ float silu_pair(float g) { return __fdividef(g, 1.f +
 __device__ __forceinline__ void epilogue_sync_n_pair(int threads) {
     asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
+
+// Named barrier 2 + g among the 128 threads of epilogue group g.
+__device__ __forceinline__ void group_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -383,6 +387,7 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
         const int et = threadIdx.x - 64;
         constexpr int kEpiThreads = 32 * C::kEpiWarps;
         const int grp = (warp - 2) >> 2;
+        __nv_bfloat16* stage_g = out_stage + grp * 32 * PBM;   // gate/up: this group's staging tile
         const uint32_t acc_empty_lead = map_to_rank(smem_u32(acc_empty), 0);
         int local = 0;
         int toggle = 0;
@@ -408,7 +413,8 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
             const int fb = item.mt * C::kFeat + static_cast<int>(rank) * PBM;
             const int m = fb + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(slot * 128);
-            const int n_groups = (!GATED && both) ? 2 : 1;
+            // down: the second group only for 256-row items (light items' stores are few)
+            const int n_groups = (GATED || both) ? 2 : 1;
             for (int c0 = 32 * grp; grp < n_groups && c0 < item.rows; c0 += 32 * n_groups) {
                 uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
@@ -430,21 +436,22 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
                     for (int j = 0; j < 32; ++j) {
                         const float gv = F8 ? __uint_as_float(g[j]) * wsg * rs[j] : __uint_as_float(g[j]);
                         const float uv = F8 ? __uint_as_float(g1[j]) * wsu * rs[j] : __uint_as_float(g1[j]);
-                        out_stage[j * PBM + q * 32 + lane] = __float2bfloat16_rn(silu_pair(gv) * uv);
+                        stage_g[j * PBM + q * 32 + lane] = __float2bfloat16_rn(silu_pair(gv) * uv);
                     }
-                    epilogue_sync_n_pair(kEpiThreads);
+                    group_sync(grp);
                     __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
-                    const int chunk = et & 15;
+                    const int eg = et - 128 * grp;   // thread of the group
+                    const int chunk = eg & 15;
 #pragma unroll
                     for (int pass = 0; pass < 4; ++pass) {
-                        const int j = pass * 8 + (et >> 4);
+                        const int j = pass * 8 + (eg >> 4);
                         const int n = c0 + j;
                         if (valid && n < item.rows) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(out_stage + j * PBM + chunk * 8);
+                            const uint4 v = *reinterpret_cast<const uint4*>(stage_g + j * PBM + chunk * 8);
                             *reinterpret_cast<uint4*>(h + static_cast<size_t>(item.row0 + n) * M + fb + chunk * 8) = v;
                         }
                     }
-                    epilogue_sync_n_pair(kEpiThreads);
+                    group_sync(grp);   // (the groups run different numbers of chunks: no CTA-wide barrier here)
                 } else {
                     const bool has0 = m < M, has1 = m + 2 * PBM < M;
                     float ws0 = 1.f, ws1 = 1.f;
