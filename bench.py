@@ -136,7 +136,8 @@ def max_over_ranks(value: float, world: int, device) -> float:
 
 
 def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp8: bool = False,
-                     fused: bool = False, gather: bool = False, w8a8: bool = False, fp4: bool = False) -> dict:
+                     fused: bool = False, gather: bool = False, w8a8: bool = False, fp4: bool = False,
+                     w4a4: bool = False) -> dict:
     """Algorithmic bytes and FLOPs of one step, from the realised expert counts.
 
     Only touched experts' weights count; activations are counted once per
@@ -149,6 +150,19 @@ def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp
     counts = np.asarray(counts)
     R = int(counts.sum())
     touched = int(np.count_nonzero(counts))
+    if w4a4:
+        # 4-bit weights and activations: per row of K values, K/2 code bytes, K/16 block-scale bytes and an
+        # fp32 scale; h is written in bf16, read back by its quantizer, and read by the down kernel as codes
+        rd, rf = d // 2 + d // 16 + 4, f // 2 + f // 16 + 4
+        wgu, wdn = touched * 2 * f * rd, touched * d * rf
+        gate_up = wgu + R * rd + R * f * 2
+        down = wdn + R * rf + R * d * 4
+        quant = R * f * 2 + R * rf                           # the rows of h
+        scatter = T * d * 2 + T * rd + T * rd + R * rd       # token rows quantized, then scattered
+        routing = T * E * 4 + T * k * 8
+        combine = R * d * 4 + T * d * 4
+        return {"R": R, "touched": touched, "gate_up_bytes": gate_up, "down_bytes": down,
+                "path_bytes": routing + quant + scatter + gate_up + down + combine, "flops": 6.0 * R * d * f}
     if w8a8:
         # E4M3 weights (codes + channel scales) and E4M3 activations (codes + row scales); h is written in
         # bf16, read back by its quantizer, and read by the down kernel as codes
@@ -220,7 +234,8 @@ def _time_oracle(inp, n_tokens: int):
         cache.clear()
         cache[n_tokens] = _oracle_inputs(inp, list(range(n_tokens)))
     logits, x, mask, bank = cache[n_tokens]
-    forward = mo.moe_forward_w8a8 if inp.get("w8a8") else mo.moe_forward
+    forward = (mo.moe_forward_w8a8 if inp.get("w8a8") else mo.moe_forward_w4a4 if inp.get("w4a4") else
+               mo.moe_forward)
     t0 = time.perf_counter()
     forward(logits, x, bank, cfg.k, mask)
     return time.perf_counter() - t0
@@ -276,8 +291,9 @@ def run_reference(args, rank: int, world: int):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(cfg, device="cpu", weights_device=dev)
     inp["fp8"] = args.weights in ("fp8", "w8a8")
-    inp["fp4"] = args.weights == "fp4"
+    inp["fp4"] = args.weights in ("fp4", "w4a4")
     inp["w8a8"] = args.weights == "w8a8"
+    inp["w4a4"] = args.weights == "w4a4"
     per_step_budget = max(0.05, args.reference_budget_s / max(1, args.steps + args.warmup))
     n, _ = _size_oracle_sample(inp, per_step_budget)
     for _ in range(args.warmup):
@@ -412,16 +428,24 @@ def run_ours(args, rank: int, world: int):
     fp4 = args.weights == "fp4"
     fp8 = args.weights == "fp8" or fp4      # the 4-bit path shares the FP8 path's fp16 activations and kernel
     w8a8 = args.weights == "w8a8"
+    w4a4 = args.weights == "w4a4"
     fused = args.fused
-    if fused and (fp8 or w8a8 or args.router or dtype != torch.bfloat16):
+    if fused and (fp8 or w8a8 or w4a4 or args.router or dtype != torch.bfloat16):
         raise SystemExit("--fused runs the bf16 path with the workload's logits")
-    if w8a8 and (args.router or dtype != torch.bfloat16):
-        raise SystemExit("--weights w8a8 runs the bf16 workloads with their logits")
+    if (w8a8 or w4a4) and (args.router or dtype != torch.bfloat16):
+        raise SystemExit("--weights w8a8 / w4a4 run the bf16 workloads with their logits")
     # the FP8-weight path keeps its compact activations (xs, h) in fp16
     bufs = (M.MoEBuffersW8A8(T, E, k, d, f, device=dev) if w8a8 else
+            M.MoEBuffersW4A4(T, E, k, d, f, device=dev) if w4a4 else
             M.MoEBuffers(T, E, k, d, f, torch.float16 if fp8 else dtype, device=dev))
     logits, x, mask = inp["logits"], inp["x"], inp["mask"]
-    if w8a8:
+    if w4a4:
+        # load-time step, outside the timed region: the 4-bit banks
+        inp["fp4"] = inp["w4a4"] = True
+        wg, wu, wd = (M.moe_quantize_weights_fp4(inp[n]) for n in ("w_gate", "w_up", "w_down"))
+        torch.cuda.synchronize()
+        forward = M.moe_forward_w4a4
+    elif w8a8:
         # load-time step, outside the timed region: E4M3 codes + per-channel scales
         inp["fp8"] = inp["w8a8"] = True
         wg, wu, wd = (M.moe_quantize_weights_fp8(inp[n]) for n in ("w_gate", "w_up", "w_down"))
@@ -449,7 +473,7 @@ def run_ours(args, rank: int, world: int):
     b = bufs
     # every call is marshalled once (M.bind); the timed loop replays the C calls.
     # Small chunks take A1-A4 in one launch, as moe_forward does.
-    small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES and not args.router and not w8a8
+    small = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES and not args.router and not w8a8 and not w4a4
     # fused: moe_forward_fused's automatic choice -- gather the token rows in
     # the gate/up kernel while experts get few rows, else the compact copy;
     # the combine in the down kernel while y fits in twice the L2, else the
@@ -464,6 +488,10 @@ def run_ours(args, rank: int, world: int):
     if w8a8:
         # E4M3 activations: the token rows and h quantized per row, E4M3 x E4M3 tensor-core MMAs
         names = ("route", "scatter_quant", "gate_up", "quantize_h", "down", "combine")
+        routing = []
+    elif w4a4:
+        # 4-bit activations: the token rows and h quantized by the 4-bit quantizer, block-scaled MMAs
+        names = ("route", "quantize_x", "scatter", "gate_up", "quantize_h", "down", "combine")
         routing = []
     elif fused and T <= SMALL_TOKENS and T * k <= SMALL_ROUTES:
         names = ("route_scatter_small", "gate_up", "down_combine")
@@ -511,6 +539,17 @@ def run_ours(args, rank: int, world: int):
             M.bind(M.moe_grouped_gate_up, b.xs, b.offsets, wg, wu, b.h),
             M.bind(M.moe_grouped_down_combine, b.h, b.offsets, wd, b.route_of_row, b.row_of_route, b.w, b.y,
                    b.tile_counts, b.out),
+        ]
+    elif w4a4:
+        calls = [
+            M.bind(M.moe_route_topk_offsets, logits, mask, k, b.ids, b.w, b.counts, b.offsets, b.ws),
+            M.bind(M.moe_quantize_rows_fp4, x, b.x_q),
+            M.bind(M.moe_scatter_rows_fp4, b.x_q, b.ids, mask, b.offsets, b.xs_q, b.row_of_route, b.route_of_row,
+                   b.ws),
+            M.bind(M.moe_grouped_gate_up_w4a4, b.xs_q, b.offsets, wg, wu, b.h),
+            M.bind(M.moe_quantize_rows_fp4, b.h, b.h_q),
+            M.bind(M.moe_grouped_down_w4a4, b.h_q, b.offsets, wd, b.y),
+            M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
         ]
     elif w8a8:
         calls = [
@@ -597,7 +636,7 @@ def run_ours(args, rank: int, world: int):
     # of moe_forward against a prepared plan (calls marshalled once; the GPU queue
     # absorbs the launches, so the host time per call is what is measured)
     host_us = None
-    if not (fused or fp8 or w8a8 or args.router):
+    if not (fused or fp8 or w8a8 or w4a4 or args.router):
         host_us = {}
         for label, call in (("moe_forward", M.bind(M.moe_forward, logits, x, mask, wg, wu, wd, k, b)),
                             ("moe_plan_forward", M.bind(M.moe_plan_forward, plan, logits, x, mask))):
@@ -623,16 +662,18 @@ def run_ours(args, rank: int, world: int):
 
     # ---- roofline of the dominant kernel (grouped gate/up + SwiGLU)
     es = 2 if dtype == torch.bfloat16 else 4
-    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8, fused, gather, w8a8, fp4)
+    work = algorithmic_work(bufs.counts.cpu().numpy(), T, E, k, d, f, es, fp8, fused, gather, w8a8, fp4, w4a4)
     R, touched = work["R"], work["touched"]
     gate_up_bytes = work["gate_up_bytes"]
     peaks = _peaks()
     achieved = gate_up_bytes / (gu_ms * 1e-3) / 1e9
     # chunks of many routes run the bf16 and E4M3 projections on pairs of SMs (the library's choice)
-    paired = dtype == torch.bfloat16 and not (fp8 or fp4 or gather) and M.moe_ffn_paired(T * k)
-    traffic = _profiled_traffic(("gate_up_w8a8" if w8a8 else "gate_up_fp4" if fp4 else "gate_up_fp8" if fp8 else
-                                 "gate_up_gather" if gather else "gate_up") + ("_pair" if paired else ""), cfg.name)
-    kname = ("moe_grouped_gate_up_w8a8 (ffn_pair_kernel<gated, E4M3>)" if w8a8 and paired else
+    paired = dtype == torch.bfloat16 and not (fp8 or fp4 or gather or w4a4) and M.moe_ffn_paired(T * k)
+    traffic = _profiled_traffic(("gate_up_w4a4" if w4a4 else "gate_up_w8a8" if w8a8 else "gate_up_fp4" if fp4 else
+                                 "gate_up_fp8" if fp8 else "gate_up_gather" if gather else "gate_up") +
+                                ("_pair" if paired else ""), cfg.name)
+    kname = ("moe_grouped_gate_up_w4a4 (ffn_nvf4_kernel<gated>)" if w4a4 else
+             "moe_grouped_gate_up_w8a8 (ffn_pair_kernel<gated, E4M3>)" if w8a8 and paired else
              "moe_grouped_gate_up_w8a8 (ffn_tc_kernel<gated, E4M3>)" if w8a8 else
              "moe_grouped_gate_up_fp4 (ffn_fp8_kernel<gated, FP4>)" if fp4 else
              "moe_grouped_gate_up_fp8 (ffn_fp8_kernel<gated>)" if fp8 else
@@ -649,8 +690,9 @@ def run_ours(args, rank: int, world: int):
     if args.router:
         flops += 2.0 * T * E * d
         path_bytes += T * d * 2 + E * d * 2 - T * E * 4   # x and wr read instead of the logits
-    # E4M3 x E4M3 MMAs run at twice the bf16 rate (the nominal dense fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s)
-    tensor_peak = peaks["bf16_tflops_sustained"] * (2.0 if w8a8 else 1.0)
+    # E4M3 x E4M3 MMAs run at twice the bf16 rate (the nominal dense fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s),
+    # 4-bit block-scaled MMAs at six times (13.5 / 2.25)
+    tensor_peak = peaks["bf16_tflops_sustained"] * (2.0 if w8a8 else 6.0 if w4a4 else 1.0)
     t_roof = max(flops / (tensor_peak * 1e12), path_bytes / (peaks["hbm_gbs"] * 1e9))
     ms_per_step = elapsed_ms / args.steps
     value = world * T * args.steps / (elapsed_ms * 1e-3)
@@ -670,21 +712,24 @@ def run_ours(args, rank: int, world: int):
         "warmup": args.warmup, "ms_per_step": ms_per_step,
         "ms_per_step_median": step_median, "ms_per_step_mad": step_mad,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3" if w8a8 else ("bf16" if dtype == torch.bfloat16 else "f32"),
+        "vs_baseline": None,
+        "dtype": "e4m3" if w8a8 else "e2m1" if w4a4 else ("bf16" if dtype == torch.bfloat16 else "f32"),
         "data": "synthetic",
         "config": {"workload": cfg.name, "T": T, "d": d, "f": f, "E": E, "k": k, "mask_p": cfg.mask_p,
                    "routes_unmasked": R, "experts_touched": touched,
-                   "weights": "e2m1 codes + e4m3 scale per 16 + fp32 per-channel scales" if fp4 else
+                   "weights": "e2m1 codes + e4m3 scale per 16 + fp32 per-channel scales" if (fp4 or w4a4) else
                               "fp8_e4m3 codes + fp32 per-channel scales" if (fp8 or w8a8) else
                               ("bf16" if dtype == torch.bfloat16 else "f32"),
                    "activations": "fp8_e4m3 codes + fp32 per-row scales (x and h)" if w8a8 else
+                                  "e2m1 codes + e4m3 scale per 16 + fp32 per-row scales (x and h)" if w4a4 else
                                   ("fp16 (exact widening of bf16 x)" if fp8 else None),
                    "permutation": ("fused: token rows gathered by the gate/up kernel, weighted combine in the "
                                    "down kernel" if gather else "compact copy xs, weighted combine in the down "
                                    "kernel") if fused else "compact copy xs + separate combine",
                    "router": "x . Wr^T on the tensor cores (moe_router_topk, Wr ~ N(0, 1/d) bf16) in front of "
                              "the histogram; the workload's own logits unused" if args.router else None,
-                   "l2": f"inputs larger than L2: {touched * 3 * d * f * (1 if fp8 else es) / 1e9:.1f} GB of "
+                   "l2": f"inputs larger than L2: "
+                         f"{touched * 3 * d * f * (0.5625 if (fp4 or w4a4) else 1 if fp8 else es) / 1e9:.1f} GB of "
                          "touched expert weights streamed per step (L2 129 MB), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "e2e": e2e,
@@ -794,11 +839,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
-    ap.add_argument("--weights", choices=("bf16", "fp8", "w8a8", "fp4"), default="bf16",
+    ap.add_argument("--weights", choices=("bf16", "fp8", "w8a8", "fp4", "w4a4"), default="bf16",
                     help="expert weight format: the workload's own (bf16); FP8 E4M3 codes with per-channel "
                          "scales quantized at load time, with fp16 activations (fp8) or with E4M3 activations "
                          "quantized per row on the FP8 tensor cores (w8a8); or 4-bit E2M1 codes with an E4M3 "
-                         "scale per 16 values and per-channel scales, with fp16 activations (fp4)")
+                         "scale per 16 values and per-channel scales, with fp16 activations (fp4) or with "
+                         "activations in the same 4-bit format on the block-scaled tensor cores (w4a4)")
     ap.add_argument("--fused", action="store_true",
                     help="the fused permutation (bf16): rows gathered in the gate/up kernel, combine in the down "
                          "kernel (moe_forward_fused)")

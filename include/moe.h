@@ -506,6 +506,82 @@ moe_status moe_forward_w8a8(const float* logits, const void* x, const uint8_t* m
                             float* h_scales, float* y, float* out, void* ws, void* stream);
 
 /* ------------------------------------------------------------------------
+ * 4-bit operands on both sides (W4A4).  The weights are the 4-bit banks of
+ * moe_quantize_weights_fp4; the token rows and the rows of h are quantized
+ * into the same format (E2M1 codes, an E4M3 scale per 16 values, an fp32
+ * scale per row) -- the NVIDIA "NVFP4" layout, and the 4-bit counterpart of
+ * the FP8-activation path above (page "perf(ggml): reuse ROCmFP4 weights
+ * across q=4 columns": 4-bit weights on a quantized-activation matrix path).
+ * The tensor cores multiply the codes with their block scales directly
+ * (tcgen05.mma kind::mxf4nvf4 with block scaling, K = 64 per instruction);
+ * the epilogue applies the two row scales.  The method computed is the FFN
+ * on the values the codes stand for: x' = s_x * b_x * value(code_x), h =
+ * silu(x'.Wg') * (x'.Wu') rounded to bf16, h' the same quantizer applied to
+ * that bf16 h, y = h'.Wd'; products accumulate in fp32.
+ *
+ * Rows of activations keep their block scales tile-major like the weights:
+ * [K/64][ld][4] uint8, the four scales of row r in 64-value tile t at
+ * [t][r][0..3], ld >= rows a multiple of 4 (the path uses ld = 4*ceil(rows/4)).
+ * ------------------------------------------------------------------------ */
+
+/* The 4-bit quantizer of moe_quantize_weights_fp4 applied to `rows` rows of
+ * activations a [rows][K] (dtype MOE_BF16 or MOE_F32): codes [rows][K/2],
+ * block_scales [K/64][ld][4] (columns rows .. ld-1 untouched), scales
+ * [rows].  K a multiple of 64; a, codes, block_scales 16-byte aligned. */
+moe_status moe_quantize_rows_fp4(const void* a, int dtype, int rows, int ld, int K, uint8_t* codes,
+                                 uint8_t* block_scales, float* scales, void* stream);
+
+/* A4 with 4-bit rows: the token rows' codes x_codes [T][d/2], block scales
+ * x_block_scales [d/64][ld_x][4] and scales x_scales [T] (moe_quantize_rows_fp4
+ * of x) are scattered like moe_scatter_rows scatters x, into xs_codes
+ * [T*k][d/2], xs_block_scales [d/64][ld_xs][4] and xs_scales [T*k]; rows R ..
+ * T*k-1 get zero codes, zero block scales and scale 0.  ld_x >= T and ld_xs
+ * >= T*k multiples of 4; d a multiple of 64; other arguments as for
+ * moe_scatter_rows. */
+moe_status moe_scatter_rows_fp4(const uint8_t* x_codes, const uint8_t* x_block_scales, int ld_x,
+                                const float* x_scales, const int32_t* ids, const uint8_t* mask,
+                                const int32_t* offsets, int T, int k, int d, int E, uint8_t* xs_codes,
+                                uint8_t* xs_block_scales, int ld_xs, float* xs_scales, int32_t* row_of_route,
+                                int32_t* route_of_row, void* ws, void* stream);
+
+/* A5 on 4-bit operands: h[i][j] = silu(g) * u with g = s_gate[e][j] *
+ * xs_scales[i] * sum over K of (b_gate * value(code)) (xs block scale *
+ * value(code)) and u likewise; h [cap][f] bf16 out (rows R .. cap-1
+ * zero-filled).  xs_*: compact rows in the 4-bit row format (leading
+ * dimension ld of the block scales, ld >= cap a multiple of 4); weights as
+ * moe_quantize_weights_fp4 writes them.  d and f multiples of 128. */
+moe_status moe_grouped_gate_up_w4a4(const uint8_t* xs_codes, const uint8_t* xs_block_scales, int ld,
+                                    const float* xs_scales, const int32_t* offsets, int cap, int E, int d, int f,
+                                    const uint8_t* w_gate_q, const uint8_t* b_gate, const float* s_gate,
+                                    const uint8_t* w_up_q, const uint8_t* b_up, const float* s_up, void* h,
+                                    void* stream);
+
+/* A6 on 4-bit operands: y [cap][d] fp32 out (rows R .. cap-1 zero-filled)
+ * from the 4-bit rows of h (moe_quantize_rows_fp4 of the bf16 h, rows = cap,
+ * K = f, leading dimension ld). */
+moe_status moe_grouped_down_w4a4(const uint8_t* h_codes, const uint8_t* h_block_scales, int ld,
+                                 const float* h_scales, const int32_t* offsets, int cap, int E, int d, int f,
+                                 const uint8_t* w_down_q, const uint8_t* b_down, const float* s_down, float* y,
+                                 void* stream);
+
+/* The whole path on 4-bit weights and activations: moe_route_topk_offsets;
+ * x quantized by moe_quantize_rows_fp4 (x_codes [T][d/2], x_block_scales
+ * [d/64][4*ceil(T/4)][4], x_scales [T]) and scattered by
+ * moe_scatter_rows_fp4 (xs_codes [T*k][d/2], xs_block_scales
+ * [d/64][4*ceil(T*k/4)][4], xs_scales [T*k]); moe_grouped_gate_up_w4a4 into
+ * h [T*k][f] bf16; h quantized (h_codes [T*k][f/2], h_block_scales
+ * [f/64][4*ceil(T*k/4)][4], h_scales [T*k]); moe_grouped_down_w4a4 into y;
+ * moe_combine into out.  x is bf16; every other argument as for moe_forward. */
+moe_status moe_forward_w4a4(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k, int d,
+                            int f, const uint8_t* w_gate_q, const uint8_t* b_gate, const float* s_gate,
+                            const uint8_t* w_up_q, const uint8_t* b_up, const float* s_up, const uint8_t* w_down_q,
+                            const uint8_t* b_down, const float* s_down, int32_t* ids, float* w, int32_t* counts,
+                            int32_t* offsets, uint8_t* x_codes, uint8_t* x_block_scales, float* x_scales,
+                            uint8_t* xs_codes, uint8_t* xs_block_scales, float* xs_scales, int32_t* row_of_route,
+                            int32_t* route_of_row, void* h, uint8_t* h_codes, uint8_t* h_block_scales,
+                            float* h_scales, float* y, float* out, void* ws, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused permutation (bf16 operands only).  The pages fuse the combine into
  * one expert-major kernel (page "perf(ds4): accelerate ROCm decode and
  * long-context selection", lucebox8 gfx1151 A/B; page "perf(ds4): extend

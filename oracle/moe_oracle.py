@@ -570,6 +570,31 @@ def moe_forward_w8a8(logits, x, weights_q, k: int, mask=None, h_decided=None):
             "route_of_row": route_of_row, "x_q": x_q, "h": h, "h_bf16": h_bf16, "h_q": h_q, "y": y, "out": out}
 
 
+def moe_forward_w4a4(logits, x, weights_q, k: int, mask=None, h_decided=None):
+    """Every intermediate of the 4-bit-activation path for one chunk (A1 .. A7 in order), as a dict.
+
+    The FP8-activation path with the 4-bit block-scaled format in place of E4M3: the token rows and the
+    bf16 rows of h are quantized by the weights' 4-bit quantizer and the FFN runs on the values the codes
+    stand for.  weights_q: (gate, up, down) Fp4Banks, or fetch(e0, e1) returning them.  h_decided: as for
+    moe_forward_w8a8 (the codes of h decided from the implementation's own bf16 h).
+    """
+    lg = _np(logits, np.float32)
+    T, E = lg.shape
+    ids, w = route_topk(lg, k)
+    counts = route_histogram(ids, mask, E)
+    offsets = prefix_offsets(counts)
+    row_of_route, route_of_row = scatter_permutation(ids, mask)
+    x_q = quantize_bank_fp4(x)
+    xs = scatter_rows(dequantize_weights_fp4(x_q.codes, x_q.block_scales, x_q.scales), route_of_row, k)
+    h = grouped_swiglu(xs, offsets, weights_q)
+    h_bf16 = round_bf16(h) if h_decided is None else h_decided
+    h_q = quantize_bank_fp4(h_bf16)
+    y = grouped_down(dequantize_weights_fp4(h_q.codes, h_q.block_scales, h_q.scales), offsets, weights_q)
+    out = combine(y, row_of_route, w, T, k)
+    return {"ids": ids, "w": w, "counts": counts, "offsets": offsets, "row_of_route": row_of_route,
+            "route_of_row": route_of_row, "x_q": x_q, "h": h, "h_bf16": h_bf16, "h_q": h_q, "y": y, "out": out}
+
+
 # ---------------------------------------------------------------------------
 # The router projection in front of A1
 # ---------------------------------------------------------------------------

@@ -22,7 +22,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmoe_gb300.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "routing.cu", "ffn_simt.cu", "ffn_tc.cu", "ffn_pair.cu", "ffn_fp8.cu", "router.cu"]
+SOURCES = ["api.cu", "routing.cu", "ffn_simt.cu", "ffn_tc.cu", "ffn_pair.cu", "ffn_nvf4.cu", "ffn_fp8.cu", "router.cu"]
 
 
 def _nvcc() -> str:

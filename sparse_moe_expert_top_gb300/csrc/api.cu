@@ -468,6 +468,104 @@ extern "C" moe_status moe_forward_w8a8(const float* logits, const void* x, const
 }
 
 // ---------------------------------------------------------------------------
+// 4-bit operands on both sides (block-scaled tensor-core MMAs)
+// ---------------------------------------------------------------------------
+
+extern "C" moe_status moe_quantize_rows_fp4(const void* a, int dtype, int rows, int ld, int K, uint8_t* codes,
+                                            uint8_t* block_scales, float* scales, void* stream) {
+    if (dtype_size(dtype) == 0) return MOE_ERR_UNSUPPORTED;
+    MOE_REQUIRE(rows >= 0 && ld >= rows && ld % 4 == 0 && K >= 64 && K % 64 == 0);
+    if (rows == 0) return MOE_OK;
+    MOE_REQUIRE(a && codes && block_scales && scales && aligned16(a) && aligned16(codes) && aligned16(block_scales));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    return launch_quantize_rows_fp4(a, dtype, rows, ld, K, codes, block_scales, scales,
+                                    static_cast<cudaStream_t>(stream), di);
+}
+
+namespace {
+int rows_ld(int rows) { return (rows + 3) / 4 * 4; }
+}  // namespace
+
+extern "C" moe_status moe_grouped_gate_up_w4a4(const uint8_t* xs_codes, const uint8_t* xs_block_scales, int ld,
+                                               const float* xs_scales, const int32_t* offsets, int cap, int E, int d,
+                                               int f, const uint8_t* w_gate_q, const uint8_t* b_gate,
+                                               const float* s_gate, const uint8_t* w_up_q, const uint8_t* b_up,
+                                               const float* s_up, void* h, void* stream) {
+    moe_status st = check_w8a8_args(offsets, cap, E, d, f);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(ld >= cap && ld % 4 == 0);
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(xs_codes && xs_block_scales && xs_scales && w_gate_q && b_gate && s_gate && w_up_q && b_up && s_up &&
+                h);
+    MOE_REQUIRE(aligned16(xs_codes) && aligned16(xs_block_scales) && aligned16(w_gate_q) && aligned16(b_gate) &&
+                aligned16(w_up_q) && aligned16(b_up) && aligned16(h));
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MOE_OK) return st;
+    return launch_ffn_w4a4_gate_up(xs_codes, xs_block_scales, ld, xs_scales, offsets, cap, E, d, f, w_gate_q, b_gate,
+                                   s_gate, w_up_q, b_up, s_up, h, static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_grouped_down_w4a4(const uint8_t* h_codes, const uint8_t* h_block_scales, int ld,
+                                            const float* h_scales, const int32_t* offsets, int cap, int E, int d,
+                                            int f, const uint8_t* w_down_q, const uint8_t* b_down,
+                                            const float* s_down, float* y, void* stream) {
+    moe_status st = check_w8a8_args(offsets, cap, E, d, f);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(ld >= cap && ld % 4 == 0);
+    if (cap == 0) return MOE_OK;
+    MOE_REQUIRE(h_codes && h_block_scales && h_scales && w_down_q && b_down && s_down && y);
+    MOE_REQUIRE(aligned16(h_codes) && aligned16(h_block_scales) && aligned16(w_down_q) && aligned16(b_down) &&
+                aligned16(y));
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MOE_OK) return st;
+    return launch_ffn_w4a4_down(h_codes, h_block_scales, ld, h_scales, offsets, cap, E, d, f, w_down_q, b_down, s_down,
+                                y, static_cast<cudaStream_t>(stream), di);
+}
+
+extern "C" moe_status moe_forward_w4a4(const float* logits, const void* x, const uint8_t* mask, int T, int E, int k,
+                                       int d, int f, const uint8_t* w_gate_q, const uint8_t* b_gate,
+                                       const float* s_gate, const uint8_t* w_up_q, const uint8_t* b_up,
+                                       const float* s_up, const uint8_t* w_down_q, const uint8_t* b_down,
+                                       const float* s_down, int32_t* ids, float* w, int32_t* counts,
+                                       int32_t* offsets, uint8_t* x_codes, uint8_t* x_block_scales,
+                                       float* x_scales, uint8_t* xs_codes, uint8_t* xs_block_scales,
+                                       float* xs_scales, int32_t* row_of_route, int32_t* route_of_row, void* h,
+                                       uint8_t* h_codes, uint8_t* h_block_scales, float* h_scales, float* y,
+                                       float* out, void* ws, void* stream) {
+    moe_status st = check_w8a8_args(offsets, T * k, E, d, f);
+    if (st != MOE_OK) return st;
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && k <= E);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && ids && w && counts && x_codes && x_block_scales && x_scales && xs_codes &&
+                xs_block_scales && xs_scales && row_of_route && route_of_row && h && h_codes && h_block_scales &&
+                h_scales && y && out && ws);
+    MOE_REQUIRE(aligned16(x) && aligned16(h) && aligned16(y) && aligned16(out) && aligned16(ws));
+    const int cap = T * k;
+    if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK) return st;
+    // NVFP4 token rows, scattered to the compact rows
+    if ((st = moe_quantize_rows_fp4(x, MOE_BF16, T, rows_ld(T), d, x_codes, x_block_scales, x_scales, stream)) !=
+        MOE_OK)
+        return st;
+    if ((st = moe_scatter_rows_fp4(x_codes, x_block_scales, rows_ld(T), x_scales, ids, mask, offsets, T, k, d, E,
+                                   xs_codes, xs_block_scales, rows_ld(cap), xs_scales, row_of_route, route_of_row, ws,
+                                   stream)) != MOE_OK)
+        return st;
+    if ((st = moe_grouped_gate_up_w4a4(xs_codes, xs_block_scales, rows_ld(cap), xs_scales, offsets, cap, E, d, f,
+                                       w_gate_q, b_gate, s_gate, w_up_q, b_up, s_up, h, stream)) != MOE_OK)
+        return st;
+    // NVFP4 rows of h (bf16; the unused rows are zero and quantize to zero codes)
+    if ((st = moe_quantize_rows_fp4(h, MOE_BF16, cap, rows_ld(cap), f, h_codes, h_block_scales, h_scales, stream)) !=
+        MOE_OK)
+        return st;
+    if ((st = moe_grouped_down_w4a4(h_codes, h_block_scales, rows_ld(cap), h_scales, offsets, cap, E, d, f, w_down_q,
+                                    b_down, s_down, y, stream)) != MOE_OK)
+        return st;
+    return moe_combine(y, row_of_route, w, T, k, d, out, stream);
+}
+
+// ---------------------------------------------------------------------------
 // Fused permutation (bf16)
 // ---------------------------------------------------------------------------
 

@@ -826,6 +826,21 @@ moe_status launch_quantize_fp4(const void* w, int dtype, int E, int M, int K, ui
     return cuda_status(cudaGetLastError());
 }
 
+// Rows of activations: block scales [K/64][ld][4] (the weights' layout with
+// one expert of ld rows, of which the first `rows` are written).
+moe_status launch_quantize_rows_fp4(const void* a, int dtype, int rows, int ld, int K, uint8_t* codes,
+                                    uint8_t* block_scales, float* scales, cudaStream_t st, const DeviceInfo& di) {
+    const long long blocks_needed = (rows + 7) / 8;
+    const int blocks = static_cast<int>(blocks_needed < di.sm_count * 16LL ? blocks_needed : di.sm_count * 16LL);
+    if (dtype == MOE_BF16)
+        quantize_fp4_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a), rows, ld, K,
+                                                                    codes, block_scales, scales);
+    else
+        quantize_fp4_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(a), rows, ld, K, codes,
+                                                            block_scales, scales);
+    return cuda_status(cudaGetLastError());
+}
+
 moe_status launch_quantize_fp8(const void* w, int dtype, long long rows, int K, uint8_t* codes, float* scales,
                                cudaStream_t st, const DeviceInfo& di) {
     const long long warps = rows;

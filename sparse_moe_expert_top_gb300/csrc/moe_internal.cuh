@@ -160,6 +160,17 @@ moe_status launch_ffn_fp4_down(const void* h, const int32_t* offsets, int cap, i
                                cudaStream_t st, const DeviceInfo& di);
 moe_status launch_quantize_fp4(const void* w, int dtype, int E, int M, int K, uint8_t* codes, uint8_t* block_scales,
                                float* scales, cudaStream_t st, const DeviceInfo& di);
+moe_status launch_quantize_rows_fp4(const void* a, int dtype, int rows, int ld, int K, uint8_t* codes,
+                                    uint8_t* block_scales, float* scales, cudaStream_t st, const DeviceInfo& di);
+moe_status launch_ffn_w4a4_gate_up(const uint8_t* xs, const uint8_t* xs_bs, int ld, const float* xs_s,
+                                   const int32_t* offsets, int cap, int E, int d, int f, const uint8_t* q_gate,
+                                   const uint8_t* b_gate, const float* s_gate, const uint8_t* q_up,
+                                   const uint8_t* b_up, const float* s_up, void* h, cudaStream_t st,
+                                   const DeviceInfo& di);
+moe_status launch_ffn_w4a4_down(const uint8_t* hq, const uint8_t* h_bs, int ld, const float* h_s,
+                                const int32_t* offsets, int cap, int E, int d, int f, const uint8_t* q_down,
+                                const uint8_t* b_down, const float* s_down, float* y, cudaStream_t st,
+                                const DeviceInfo& di);
 moe_status launch_router_topk(const void* x, const void* wr, int T, int E, int d, int k, float* logits,
                               int32_t* ids, float* w, cudaStream_t st, const DeviceInfo& di);
 // moe_route_scatter_small for the fused path: xs may be NULL (no row copy);

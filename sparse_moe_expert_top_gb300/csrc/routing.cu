@@ -583,7 +583,10 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
                                                            int32_t* __restrict__ tile_counts, int n_counts,
                                                            float4* __restrict__ out, int d4, int chunk_tokens,
                                                            const float* __restrict__ scale_in = nullptr,
-                                                           float* __restrict__ scale_out = nullptr) {
+                                                           float* __restrict__ scale_out = nullptr,
+                                                           const uint32_t* __restrict__ sf_in = nullptr,
+                                                           int ld_in = 0, uint32_t* __restrict__ sf_out = nullptr,
+                                                           int ld_out = 0, int n_sf = 0) {
     __shared__ int rows[kMaxK];
     __shared__ int tails[kMaxK];
     const int t = blockIdx.x, tid = threadIdx.x;
@@ -641,6 +644,18 @@ __global__ void __launch_bounds__(128) scatter_rows_kernel(const uint4* __restri
             if (row >= 0) xs[static_cast<size_t>(row) * row_vecs + v] = val;
             const int tail = tails[s];
             if (tail >= 0) xs[static_cast<size_t>(tail) * row_vecs + v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    if (sf_out != nullptr) {
+        // 4-bit rows: the token's block-scale words [tile][ld] go to its compact rows' columns
+        for (int j = tid; j < n_sf; j += blockDim.x) {
+            const uint32_t v = __ldg(sf_in + static_cast<size_t>(j) * ld_in + t);
+            for (int s = 0; s < k; ++s) {
+                const int row = rows[s];
+                if (row >= 0) sf_out[static_cast<size_t>(j) * ld_out + row] = v;
+                const int tail = tails[s];
+                if (tail >= 0) sf_out[static_cast<size_t>(j) * ld_out + tail] = 0u;
+            }
         }
     }
     if (TO_F16 && __syncthreads_or(range) && tid == 0) atomicOr(err, DEVERR_RANGE);
@@ -1267,7 +1282,7 @@ moe_status scatter_rows(const void* x, int es, bool to_f16, const int32_t* ids, 
     kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(x), ids, offsets, T, k, E, row_vecs, w32 + ws_rank_offset(T, k),
         w32 + ws_bases_offset(T, k), static_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word, nullptr, 0,
-        nullptr, 0, ws_chunk_tokens(T), nullptr, nullptr);
+        nullptr, 0, ws_chunk_tokens(T), nullptr, nullptr, nullptr, 0, nullptr, 0, 0);
     return launch_status();
 }
 
@@ -1335,6 +1350,32 @@ extern "C" moe_status moe_scatter_rows_e4m3(const uint8_t* x_codes, const float*
         reinterpret_cast<const uint4*>(x_codes), ids, offsets, T, k, E, d / 16, w32 + ws_rank_offset(T, k),
         w32 + ws_bases_offset(T, k), reinterpret_cast<uint4*>(xs), row_of_route, route_of_row, di.error_word,
         nullptr, 0, nullptr, 0, ws_chunk_tokens(T), x_scales, xs_scales);
+    return launch_status();
+}
+
+extern "C" moe_status moe_scatter_rows_fp4(const uint8_t* x_codes, const uint8_t* x_block_scales, int ld_x,
+                                           const float* x_scales, const int32_t* ids, const uint8_t* mask,
+                                           const int32_t* offsets, int T, int k, int d, int E, uint8_t* xs_codes,
+                                           uint8_t* xs_block_scales, int ld_xs, float* xs_scales,
+                                           int32_t* row_of_route, int32_t* route_of_row, void* ws, void* stream) {
+    (void)mask;  // folded into the workspace ranks by the histogram
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 64 && d % 64 == 0);
+    MOE_REQUIRE(ld_x >= T && ld_x % 4 == 0 && ld_xs >= T * k && ld_xs % 4 == 0);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(x_codes && x_block_scales && x_scales && ids && offsets && xs_codes && xs_block_scales &&
+                xs_scales && row_of_route && route_of_row && ws);
+    MOE_REQUIRE(aligned16(x_codes) && aligned16(xs_codes) && aligned16(x_block_scales) &&
+                aligned16(xs_block_scales) && aligned16(ws));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    const int32_t* w32 = static_cast<const int32_t*>(ws);
+    scatter_rows_kernel<false><<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const uint4*>(x_codes), ids, offsets, T, k, E, d / 32, w32 + ws_rank_offset(T, k),
+        w32 + ws_bases_offset(T, k), reinterpret_cast<uint4*>(xs_codes), row_of_route, route_of_row, di.error_word,
+        nullptr, 0, nullptr, 0, ws_chunk_tokens(T), x_scales, xs_scales,
+        reinterpret_cast<const uint32_t*>(x_block_scales), ld_x, reinterpret_cast<uint32_t*>(xs_block_scales), ld_xs,
+        d / 64);
     return launch_status();
 }
 

@@ -71,6 +71,11 @@ SIGNATURES = {
     "moe_grouped_gate_up_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_down_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_forward_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 6 + [_P] * 17, _I),
+    "moe_quantize_rows_fp4": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_scatter_rows_fp4": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P], _I),
+    "moe_grouped_gate_up_w4a4": ([_P, _P, _I, _P, _P, _I, _I, _I, _I] + [_P] * 8, _I),
+    "moe_grouped_down_w4a4": ([_P, _P, _I, _P, _P, _I, _I, _I, _I] + [_P] * 5, _I),
+    "moe_forward_w4a4": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 9 + [_P] * 20, _I),
     "moe_route_topk_offsets": ([_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_forward_fused_mode": ([_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)], _I),
     "moe_ffn_paired": ([_I, ctypes.POINTER(ctypes.c_int)], _I),
@@ -925,4 +930,145 @@ def moe_forward_fp4(logits, x, mask, q_gate: FP4Weights, q_up: FP4Weights, q_dow
         _ptr(q_down.codes), _ptr(q_down.block_scales), _ptr(q_down.scales),
         _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets), _ptr(b.xs), _ptr(b.row_of_route),
         _ptr(b.route_of_row), _ptr(b.h), _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
+    return b.out
+
+
+# ---------------------------------------------------------------------------
+# 4-bit operands on both sides (block-scaled tensor-core MMAs)
+# ---------------------------------------------------------------------------
+
+def fp4_ld(rows: int) -> int:
+    """Leading dimension of the block scales of `rows` activation rows (a multiple of 4)."""
+    return (rows + 3) // 4 * 4
+
+
+class FP4Rows:
+    """Rows of activations in the 4-bit format: ``codes`` uint8 [rows][K/2], ``block_scales`` uint8
+    [K/64][ld][4] (E4M3, ld = fp4_ld(rows)), ``scales`` fp32 [rows]."""
+
+    def __init__(self, codes, block_scales, scales):
+        rows, K2 = codes.shape
+        if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or scales.dtype != torch.float32:
+            raise ValueError("expected uint8 codes and block scales, fp32 scales")
+        if tuple(block_scales.shape) != (2 * K2 // 64, fp4_ld(rows), 4) or tuple(scales.shape) != (rows,):
+            raise ValueError("block scales [K/64][ld][4] and scales [rows] do not match the codes")
+        self.codes, self.block_scales, self.scales = codes, block_scales, scales
+
+    @classmethod
+    def empty(cls, rows: int, K: int, device="cuda"):
+        return cls(torch.empty(rows, K // 2, dtype=torch.uint8, device=device),
+                   torch.zeros(K // 64, fp4_ld(rows), 4, dtype=torch.uint8, device=device),
+                   torch.empty(rows, dtype=torch.float32, device=device))
+
+    @property
+    def rows(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def K(self) -> int:
+        return 2 * self.codes.shape[1]
+
+    @property
+    def ld(self) -> int:
+        return self.block_scales.shape[1]
+
+
+def moe_quantize_rows_fp4(a, out: "FP4Rows | None" = None, stream=None) -> FP4Rows:
+    """The 4-bit quantizer applied to the rows of ``a`` [rows][K] (bf16 or fp32, K a multiple of 64)."""
+    rows, K = a.shape
+    out = FP4Rows.empty(rows, K, a.device) if out is None else out
+    if (out.rows, out.K) != (rows, K):
+        raise ValueError("output rows were allocated for another shape")
+    _check("moe_quantize_rows_fp4", load().moe_quantize_rows_fp4(
+        _ptr(a), _dtype_code(a), rows, out.ld, K, _ptr(out.codes), _ptr(out.block_scales), _ptr(out.scales),
+        _stream(stream)))
+    return out
+
+
+def moe_scatter_rows_fp4(x_q: FP4Rows, ids, mask, offsets, xs_q: FP4Rows, row_of_route, route_of_row, ws,
+                         stream=None):
+    T, k = ids.shape
+    E = offsets.shape[0] - 1
+    d = x_q.K
+    if x_q.rows != T or xs_q.rows != T * k or xs_q.K != d:
+        raise ValueError("4-bit rows do not match the routing")
+    _check("moe_scatter_rows_fp4", load().moe_scatter_rows_fp4(
+        _ptr(x_q.codes), _ptr(x_q.block_scales), x_q.ld, _ptr(x_q.scales), _ptr(ids), _ptr(mask), _ptr(offsets),
+        T, k, d, E, _ptr(xs_q.codes), _ptr(xs_q.block_scales), xs_q.ld, _ptr(xs_q.scales), _ptr(row_of_route),
+        _ptr(route_of_row), _ptr(ws), _stream(stream)))
+
+
+def moe_grouped_gate_up_w4a4(xs_q: FP4Rows, offsets, q_gate: FP4Weights, q_up: FP4Weights, h, stream=None):
+    E, f, d = q_gate.shape
+    cap = xs_q.rows
+    _expect_fp4(q_up, (E, f, d), "q_up")
+    _expect(h, torch.bfloat16, (cap, f), "h")
+    if xs_q.K != d:
+        raise ValueError("compact rows do not match the weights")
+    _check("moe_grouped_gate_up_w4a4", load().moe_grouped_gate_up_w4a4(
+        _ptr(xs_q.codes), _ptr(xs_q.block_scales), xs_q.ld, _ptr(xs_q.scales), _ptr(offsets), cap, E, d, f,
+        _ptr(q_gate.codes), _ptr(q_gate.block_scales), _ptr(q_gate.scales), _ptr(q_up.codes),
+        _ptr(q_up.block_scales), _ptr(q_up.scales), _ptr(h), _stream(stream)))
+
+
+def moe_grouped_down_w4a4(h_q: FP4Rows, offsets, q_down: FP4Weights, y, stream=None):
+    E, d, f = q_down.shape
+    cap = h_q.rows
+    _expect(y, torch.float32, (cap, d), "y")
+    if h_q.K != f:
+        raise ValueError("rows of h do not match the weights")
+    _check("moe_grouped_down_w4a4", load().moe_grouped_down_w4a4(
+        _ptr(h_q.codes), _ptr(h_q.block_scales), h_q.ld, _ptr(h_q.scales), _ptr(offsets), cap, E, d, f,
+        _ptr(q_down.codes), _ptr(q_down.block_scales), _ptr(q_down.scales), _ptr(y), _stream(stream)))
+
+
+class MoEBuffersW4A4:
+    """Caller-owned device buffers of the 4-bit-activation path for one chunk shape (bf16 x)."""
+
+    def __init__(self, T: int, E: int, k: int, d: int, f: int, device="cuda"):
+        self.T, self.E, self.k, self.d, self.f = T, E, k, d, f
+        cap = T * k
+        i32 = dict(dtype=torch.int32, device=device)
+        self.ids = torch.empty(T, k, **i32)
+        self.w = torch.empty(T, k, dtype=torch.float32, device=device)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.x_q = FP4Rows.empty(T, d, device)
+        self.xs_q = FP4Rows.empty(cap, d, device)
+        self.row_of_route = torch.empty(cap, **i32)
+        self.route_of_row = torch.empty(cap, **i32)
+        self.h = torch.empty(cap, f, dtype=torch.bfloat16, device=device)
+        self.h_q = FP4Rows.empty(cap, f, device)
+        self.y = torch.empty(cap, d, dtype=torch.float32, device=device)
+        self.out = torch.empty(T, d, dtype=torch.float32, device=device)
+        self.ws = torch.zeros(max(moe_workspace_size(T, k), 16) // 4 + 4, dtype=torch.int32, device=device)
+
+
+def moe_forward_w4a4(logits, x, mask, q_gate: FP4Weights, q_up: FP4Weights, q_down: FP4Weights, k: int,
+                     bufs: MoEBuffersW4A4, stream=None) -> torch.Tensor:
+    """The whole path on 4-bit weights and activations; returns ``bufs.out`` ([T][d] fp32)."""
+    T, E = logits.shape
+    d = x.shape[1]
+    f = q_gate.shape[1]
+    if (bufs.T, bufs.E, bufs.k, bufs.d, bufs.f) != (T, E, k, d, f):
+        raise ValueError("buffers were allocated for another shape")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _expect_fp4(q_gate, (E, f, d), "q_gate")
+    _expect_fp4(q_up, (E, f, d), "q_up")
+    _expect_fp4(q_down, (E, d, f), "q_down")
+    b = bufs
+    _check("moe_forward_w4a4", load().moe_forward_w4a4(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, f,
+        _ptr(q_gate.codes), _ptr(q_gate.block_scales), _ptr(q_gate.scales),
+        _ptr(q_up.codes), _ptr(q_up.block_scales), _ptr(q_up.scales),
+        _ptr(q_down.codes), _ptr(q_down.block_scales), _ptr(q_down.scales),
+        _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets),
+        _ptr(b.x_q.codes), _ptr(b.x_q.block_scales), _ptr(b.x_q.scales),
+        _ptr(b.xs_q.codes), _ptr(b.xs_q.block_scales), _ptr(b.xs_q.scales),
+        _ptr(b.row_of_route), _ptr(b.route_of_row), _ptr(b.h),
+        _ptr(b.h_q.codes), _ptr(b.h_q.block_scales), _ptr(b.h_q.scales),
+        _ptr(b.y), _ptr(b.out), _ptr(b.ws), _stream(stream)))
     return b.out

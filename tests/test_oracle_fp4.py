@@ -125,3 +125,42 @@ def test_fp4_bank_ffn_is_the_dequantized_ffn():
     ref = torch.nn.functional.linear(torch.nn.functional.silu(xt @ wg.T) * (xt @ wu.T), wd).numpy()
     got = mo.grouped_ffn(x, np.array([0, n], dtype=np.int32), tuple(q))
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def _restated_fp4_values(rows32):
+    """The 4-bit format restated here, in fp32 like the quantizer: s = amax / 2688, block scale = E4M3 (PyTorch's
+    float8_e4m3fn cast) of (block max / 6) / s, codes by brute force over the E2M1 table; returns the values
+    the codes stand for, float64."""
+    r = rows32.to(torch.float32)
+    amax = r.abs().amax(dim=-1)
+    s = torch.where(amax > 0, amax / 2688.0, torch.ones_like(amax))
+    blocks = r.reshape(*r.shape[:-1], -1, 16)
+    bmax = blocks.abs().amax(dim=-1)
+    bv = ((bmax / 6.0) / s[..., None]).to(torch.float8_e4m3fn).to(torch.float32)
+    denom = bv * s[..., None]
+    q = torch.where(denom[..., None] > 0, blocks / denom[..., None], torch.zeros_like(blocks))
+    vals = np.vectorize(_brute_round)(q.numpy().astype(np.float64))
+    # the value a code stands for: s * value(block scale) * value(code), exactly (float64)
+    unit = bv.numpy().astype(np.float64) * s.numpy().astype(np.float64)[..., None]
+    out = vals * unit[..., None]
+    return torch.from_numpy(out.reshape(r.shape))
+
+
+def test_w4a4_path_is_the_dense_ffn_on_quantized_operands():
+    """E=1, k=1: the 4-bit-activation path is a dense SwiGLU FFN on 4-bit-quantized x, weights and h, each
+    quantization restated here (PyTorch's E4M3 cast for the block scales, a brute-force E2M1 search), and
+    the bf16 rounding of h by PyTorch's cast."""
+    g = torch.Generator().manual_seed(4)
+    T, d, f = 9, 64, 48
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(1, f, d, generator=g) / d ** 0.5).float()
+    wu = (torch.randn(1, f, d, generator=g) / d ** 0.5).float()
+    wd = (torch.randn(1, d, f, generator=g) / f ** 0.5).float()
+    logits = torch.randn(T, 1, generator=g)
+    xq = _restated_fp4_values(x.float())
+    gq, uq, dq = (_restated_fp4_values(w[0]) for w in (wg, wu, wd))
+    h = torch.nn.functional.silu(xq @ gq.T) * (xq @ uq.T)
+    h_b = h.to(torch.float32).to(torch.bfloat16).float()
+    ref = (_restated_fp4_values(h_b) @ dq.T).numpy()
+    res = mo.moe_forward_w4a4(logits, x, tuple(mo.quantize_bank_fp4(w) for w in (wg, wu, wd)), 1)
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-12, atol=1e-14)

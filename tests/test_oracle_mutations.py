@@ -65,6 +65,7 @@ def _all_pins():
         fp4_pins.test_fp4_quantizer_hand_worked_row,
         fp4_pins.test_fp4_quantizer_picks_the_nearest_value_of_each_block,
         fp4_pins.test_fp4_bank_ffn_is_the_dequantized_ffn,
+        fp4_pins.test_w4a4_path_is_the_dense_ffn_on_quantized_operands,
         router_pins.test_hand_worked_router_case,
         router_pins.test_one_hot_router_rows_select_input_columns,
         router_pins.test_router_is_linear_and_permutation_equivariant,
