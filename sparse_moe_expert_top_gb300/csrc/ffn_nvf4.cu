@@ -19,10 +19,12 @@
 //
 // Per stage (256 K): two 16 KB code tiles of 128 weight rows, up to 64
 // compact rows (8 KB), the weight rows' block-scale words (2 x 2 KB) and the
-// compact rows' (1,088 bytes); four stages of 46 KB.  Work item: (expert, 128 output features
-// -- 256 for down, as two tiles -- and a slice of at most 64 of the expert's
-// compact rows).  Tensor memory: accumulators of two item slots of 64 columns
-// per weight tile (columns 0-255), block scales of the four stages after them.
+// compact rows' (1,088 bytes); four stages of 46 KB.  Work item: (expert, 128
+// output features -- 256 for down, as two tiles -- and a slice of at most 64
+// of the expert's compact rows; 128 in big-item mode, three stages of 55 KB).
+// Tensor memory: accumulators of two item slots of 64 columns per weight tile
+// (columns 0-255; an item of more than 64 rows takes both), block scales of
+// the stages after them.
 #include <cuda_bf16.h>
 
 #include "tc_common.cuh"
@@ -51,6 +53,18 @@ constexpr int kOffSb = kOffSa1 + kSfaTile;
 constexpr int kNStageBytes = (kOffSb + kSfbTile + 1023) / 1024 * 1024;   // 46 KB
 static_assert(kNStageBytes % 1024 == 0, "stages keep the code tiles 1024-byte aligned");
 constexpr int kNRingBytes = kNStages * kNStageBytes;
+// Big-item mode (chunks where most rows lie beyond the first 64 of their
+// expert): slices of up to 128 rows (N <= 128, both accumulator slots), three
+// stages of 55 KB (16 KB of rows, the row scales' box 132 rows).
+constexpr int kSliceBig = 128;
+constexpr int kNStagesBig = 3;
+constexpr int kSfbRowsBig = kSliceBig + 4;
+constexpr int kNStageBytesBig = (2 * kCodeTile + kSliceBig * 128 + 2 * kSfaTile + kMmasPerStage * kSfbRowsBig * 4 +
+                                 1023) / 1024 * 1024;
+static_assert(kNStagesBig * kNStageBytesBig <= kNRingBytes, "both carve-ups fit the ring");
+#ifndef MOE_NVF4_BIG_MODE_PCT
+#define MOE_NVF4_BIG_MODE_PCT 50
+#endif
 constexpr int kNCtrlBytes = 4096;
 constexpr int kNOutStage = 32 * NBM * 2;                  // gate/up: a 32-row x 128-feature bf16 tile of h
 constexpr int kNSmemBytes = kNRingBytes + kNCtrlBytes + kNOutStage + 1024;
@@ -123,7 +137,8 @@ template <bool GATED>
 __global__ void __launch_bounds__(kNThreads, 1)
     ffn_nvf4_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                     const __grid_constant__ CUtensorMap map_sa0, const __grid_constant__ CUtensorMap map_sa1,
-                    const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sb,
+                    const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
+                    const __grid_constant__ CUtensorMap map_sb, const __grid_constant__ CUtensorMap map_sb_big,
                     const int32_t* __restrict__ offsets, int cap, int E, int K, int M, void* __restrict__ out,
                     unsigned* err, const float* __restrict__ sa0, const float* __restrict__ sa1,
                     const float* __restrict__ sb) {
@@ -143,6 +158,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
     int* item_off = issued + kNStages;               // E + 1 entries
     int* ntiles = item_off + kMaxExperts + 1;        // E entries
     volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
+    int* mode_big = const_cast<int*>(epi_flag + 2);   // launch-wide carve-up
     __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kNCtrlBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -169,7 +185,9 @@ __global__ void __launch_bounds__(kNThreads, 1)
         prefetch_tmap(&map_sa0);
         prefetch_tmap(&map_sa1);
         prefetch_tmap(&map_b);
+        prefetch_tmap(&map_b_big);
         prefetch_tmap(&map_sb);
+        prefetch_tmap(&map_sb_big);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -178,20 +196,35 @@ __global__ void __launch_bounds__(kNThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (warp == 2) {
-        // item table in expert order: row slices of 64 per expert
+        // item table in expert order: row slices of 64 per expert, or of 128
+        // when more than half of the rows lie beyond the first 64 of their expert
         bool bad = false;
+        long long rows = 0, excess = 0;
         for (int e = lane; e < E; e += 32) {
             const int lo = offsets[e], hi = offsets[e + 1];
             bad |= lo < 0 || hi < lo || hi > cap;
+            const int n = hi - lo;
+            rows += n > 0 ? n : 0;
+            excess += n > kSliceN ? n - kSliceN : 0;
         }
         bad = __any_sync(0xffffffffu, bad);
+        for (int off = 16; off > 0; off >>= 1) {
+            rows += __shfl_xor_sync(0xffffffffu, rows, off);
+            excess += __shfl_xor_sync(0xffffffffu, excess, off);
+        }
+        // (the down projection keeps 64-row items: its fp32 stores of a 128-row item
+        // would hold the tensor cores longer than the halved weight re-reads save)
+        const bool big =
+            GATED && rows > 0 && excess * 100 >= static_cast<long long>(MOE_NVF4_BIG_MODE_PCT) * rows;
+        const int slice = big ? kSliceBig : kSliceN;
+        if (lane == 0) *mode_big = big ? 1 : 0;
         const int per = (E + 31) / 32;
         int local = 0;
         for (int i = 0; i < per; ++i) {
             const int e = lane * per + i;
             if (e < E) {
                 const int n = bad ? 0 : offsets[e + 1] - offsets[e];
-                ntiles[e] = (n + kSliceN - 1) / kSliceN;
+                ntiles[e] = (n + slice - 1) / slice;
                 local += ntiles[e] * n_mt;
             }
         }
@@ -216,7 +249,14 @@ __global__ void __launch_bounds__(kNThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int n_items = item_off[E];
-    auto item_at = [&](int it) { return decode_item(it, item_off, ntiles, offsets, E, kSliceN); };
+    const bool big = *mode_big != 0;
+    const int S = big ? kNStagesBig : kNStages;
+    const int stage_bytes = big ? kNStageBytesBig : kNStageBytes;
+    const int off_sa0 = kOffB + (big ? kSliceBig : kSliceN) * 128;   // after the rows
+    const int off_sa1 = off_sa0 + kSfaTile;
+    const int off_sb = off_sa1 + kSfaTile;
+    const int sfb_rows = big ? kSfbRowsBig : kSfbRows;
+    auto item_at = [&](int it) { return decode_item(it, item_off, ntiles, offsets, E, big ? kSliceBig : kSliceN); };
 
     if (warp == 0) {
         // ---- TMA producer --------------------------------------------------------
@@ -230,7 +270,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const Item item = item_at(it);
                 const int n16 = (item.rows + 15) / 16;
-                const uint32_t bytes = 2 * kCodeTile + n16 * 16 * 128 + 2 * kSfaTile + kSfbTile;
+                const uint32_t bytes = 2 * kCodeTile + n16 * 16 * 128 + 2 * kSfaTile + kMmasPerStage * sfb_rows * 4;
                 const int m0 = item.mt * fw;                  // first feature of tile 0
                 const int m1 = GATED ? m0 : m0 + NBM;         // tile 1: the up rows, or the next 128 features
                 const uint64_t pol_w = ntiles[item.e] > 1 ? pol_shared : pol_once;
@@ -239,18 +279,23 @@ __global__ void __launch_bounds__(kNThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* st = smem + s * kNStageBytes;
+                    uint8_t* st = smem + s * stage_bytes;
                     mbar_arrive_expect_tx(&full[s], bytes);
                     issued[s] = static_cast<int>(ph);
                     // codes: x = byte offset in the row (two values per byte); scales: 3-D (word, 64-K tile, expert)
                     tma_load_2d(st, &map_a0, &full[s], js * 128, item.e * M + m0, pol_w);
                     tma_load_2d(st + kOffA1, &map_a1, &full[s], js * 128, item.e * M + m1, pol_w);
-                    tma_load_3d(st + kOffSa0, &map_sa0, &full[s], m0, js * kMmasPerStage, item.e, pol_w);
-                    tma_load_3d(st + kOffSa1, &map_sa1, &full[s], m1, js * kMmasPerStage, item.e, pol_w);
-                    for (int r = 0; r < n16; ++r)
-                        tma_load_2d(st + kOffB + r * 16 * 128, &map_b, &full[s], js * 128, item.row0 + 16 * r, pol_x);
-                    tma_load_2d(st + kOffSb, &map_sb, &full[s], item.row0 & ~3, js * kMmasPerStage, pol_x);
-                    if (++s == kNStages) {
+                    tma_load_3d(st + off_sa0, &map_sa0, &full[s], m0, js * kMmasPerStage, item.e, pol_w);
+                    tma_load_3d(st + off_sa1, &map_sa1, &full[s], m1, js * kMmasPerStage, item.e, pol_w);
+                    // the rows in as few boxes as possible: 64-row boxes, then 16-row ones
+                    int r = 0;
+                    for (; r + 64 <= n16 * 16; r += 64)
+                        tma_load_2d(st + kOffB + r * 128, &map_b_big, &full[s], js * 128, item.row0 + r, pol_x);
+                    for (; r < n16 * 16; r += 16)
+                        tma_load_2d(st + kOffB + r * 128, &map_b, &full[s], js * 128, item.row0 + r, pol_x);
+                    tma_load_2d(st + off_sb, big ? &map_sb_big : &map_sb, &full[s], item.row0 & ~3,
+                                js * kMmasPerStage, pol_x);
+                    if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -269,7 +314,11 @@ __global__ void __launch_bounds__(kNThreads, 1)
                 const Item item = item_at(it);
                 const int N = (item.rows + 15) / 16 * 16;
                 const uint32_t idesc = idesc_nvf4(NBM, N);
+                // an item of more than 64 rows takes both slots (128 columns per weight tile)
+                const bool both = item.rows > kSliceN;
+                if (both) slot = 0;
                 if (!mbar_wait(&acc_empty[slot], ((slot ? use1 : use0) & 1u) ^ 1u, abort_flag, err)) break;
+                if (both && !mbar_wait(&acc_empty[1], (use1 & 1u) ^ 1u, abort_flag, err)) break;
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(slot * kAccCols);
                 const uint32_t d1 = d0 + 2 * kAccCols;
@@ -279,7 +328,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = sdesc_lo(smem_u32(smem + s * kNStageBytes));
+                    const uint32_t a0 = sdesc_lo(smem_u32(smem + s * stage_bytes));
                     const uint32_t a1 = a0 + (kOffA1 >> 4);
                     const uint32_t b = a0 + (kOffB >> 4);
                     const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + s * kSfStageCols);
@@ -292,7 +341,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
                         umma_nvf4(d1, sdesc_from_lo(a1 + 2 * c), bd, idesc, sf + 16 + 4 * c, sf + 32 + 4 * c, acc);
                     }
                     umma_commit(&empty[s]);
-                    if (++s == kNStages) {
+                    if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -301,7 +350,13 @@ __global__ void __launch_bounds__(kNThreads, 1)
                 umma_commit(&acc_full[slot]);
                 if (slot) ++use1;
                 else ++use0;
-                slot ^= 1;
+                if (both) {
+                    umma_commit(&acc_full[1]);
+                    ++use1;
+                    slot = 0;
+                } else {
+                    slot ^= 1;
+                }
             }
             umma_commit(drain);
             mbar_drain(drain, 0);
@@ -317,8 +372,13 @@ __global__ void __launch_bounds__(kNThreads, 1)
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
             const Item item = item_at(it);
             const int buf = local & 1;
-            if (et == 0)
-                epi_flag[buf] = mbar_wait(&acc_full[slot], (slot ? use1 : use0) & 1u, abort_flag, err) ? 1 : 0;
+            const bool both = item.rows > kSliceN;
+            if (both) slot = 0;
+            if (et == 0) {
+                bool got = mbar_wait(&acc_full[slot], (slot ? use1 : use0) & 1u, abort_flag, err);
+                if (got && both) got = mbar_wait(&acc_full[1], use1 & 1u, abort_flag, err);
+                epi_flag[buf] = got ? 1 : 0;
+            }
             epi_sync();
             if (!epi_flag[buf]) {
                 ok = false;
@@ -377,10 +437,18 @@ __global__ void __launch_bounds__(kNThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[slot]);
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[slot]);
+                if (both) mbar_arrive(&acc_empty[1]);
+            }
             if (slot) ++use1;
             else ++use0;
-            slot ^= 1;
+            if (both) {
+                ++use1;
+                slot = 0;
+            } else {
+                slot ^= 1;
+            }
         }
         const int R = offsets[E];
         if (ok && R >= 0 && R <= cap) {
@@ -408,10 +476,10 @@ __global__ void __launch_bounds__(kNThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + s * kNStageBytes);
-                const uint32_t* sa_0 = st + kOffSa0 / 4;   // [c][128] words
-                const uint32_t* sa_1 = st + kOffSa1 / 4;
-                const uint32_t* sbw = st + kOffSb / 4 + off;   // [c][68] words
+                const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + s * stage_bytes);
+                const uint32_t* sa_0 = st + off_sa0 / 4;   // [c][128] words
+                const uint32_t* sa_1 = st + off_sa1 / 4;
+                const uint32_t* sbw = st + off_sb / 4 + off;   // [c][sfb_rows] words
                 uint32_t v[16];
                 const uint32_t col = lane_base + static_cast<uint32_t>(kSfBase + s * kSfStageCols);
 #pragma unroll
@@ -427,13 +495,14 @@ __global__ void __launch_bounds__(kNThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[4 * c + j] = j < 2 ? sbw[c * kSfbRows + 32 * j + lane] : 0u;
+                    for (int j = 0; j < 4; ++j)
+                        v[4 * c + j] = (j < 2 || big) ? sbw[c * sfb_rows + 32 * j + lane] : 0u;
                 tmem_st16(col + 32, v);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sf_full[s]);
-                if (++s == kNStages) {
+                if (++s == S) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -445,7 +514,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
-        for (int s = 0; s < kNStages; ++s)
+        for (int s = 0; s < S; ++s)
             if (issued[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued[s]));
     }
     __syncthreads();
@@ -485,9 +554,9 @@ moe_status encode_wscales_nvf4(CUtensorMap* map, const uint8_t* base, int E, int
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
-// Row block scales [K/64][ld][4] as 32-bit words: dims (ld, K/64), box (68, 4).
-moe_status encode_rscales_nvf4(CUtensorMap* map, const uint8_t* base, int ld, int K) {
-    return encode_2d_map(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ld, K / 64, kSfbRows, kMmasPerStage,
+// Row block scales [K/64][ld][4] as 32-bit words: dims (ld, K/64), box (box_rows, 4).
+moe_status encode_rscales_nvf4(CUtensorMap* map, const uint8_t* base, int ld, int K, int box_rows) {
+    return encode_2d_map(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ld, K / 64, box_rows, kMmasPerStage,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -496,14 +565,16 @@ moe_status launch_nvf4(const uint8_t* a0, const uint8_t* sa0b, const float* sa0,
                        const uint8_t* sa1b, const float* sa1, const uint8_t* b, const uint8_t* sbb, int ld,
                        const float* sb, const int32_t* offsets, int cap, int E, int K, int M, void* out,
                        cudaStream_t st, const DeviceInfo& di) {
-    CUtensorMap ma0, ma1, msa0, msa1, mb, msb;
+    CUtensorMap ma0, ma1, msa0, msa1, mb, mbb, msb, msbb;
     moe_status s;
     if ((s = encode_codes_nvf4(&ma0, a0, K, static_cast<long long>(E) * M, NBM)) != MOE_OK) return s;
     if ((s = encode_codes_nvf4(&ma1, a1, K, static_cast<long long>(E) * M, NBM)) != MOE_OK) return s;
     if ((s = encode_wscales_nvf4(&msa0, sa0b, E, M, K)) != MOE_OK) return s;
     if ((s = encode_wscales_nvf4(&msa1, sa1b, E, M, K)) != MOE_OK) return s;
     if ((s = encode_codes_nvf4(&mb, b, K, cap, 16)) != MOE_OK) return s;
-    if ((s = encode_rscales_nvf4(&msb, sbb, ld, K)) != MOE_OK) return s;
+    if ((s = encode_codes_nvf4(&mbb, b, K, cap, 64)) != MOE_OK) return s;
+    if ((s = encode_rscales_nvf4(&msb, sbb, ld, K, kSfbRows)) != MOE_OK) return s;
+    if ((s = encode_rscales_nvf4(&msbb, sbb, ld, K, kSfbRowsBig)) != MOE_OK) return s;
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
@@ -515,8 +586,8 @@ moe_status launch_nvf4(const uint8_t* a0, const uint8_t* sa0b, const float* sa0,
             g_nvf4_attr[dev][GATED ? 1 : 0] = true;
         }
     }
-    ffn_nvf4_kernel<GATED><<<di.sm_count, kNThreads, kNSmemBytes, st>>>(ma0, ma1, msa0, msa1, mb, msb, offsets, cap,
-                                                                          E, K, M, out, di.error_word, sa0, sa1, sb);
+    ffn_nvf4_kernel<GATED><<<di.sm_count, kNThreads, kNSmemBytes, st>>>(
+        ma0, ma1, msa0, msa1, mb, mbb, msb, msbb, offsets, cap, E, K, M, out, di.error_word, sa0, sa1, sb);
     return cuda_status(cudaGetLastError());
 }
 
