@@ -158,7 +158,7 @@ def algorithmic_work(counts, T: int, E: int, k: int, d: int, f: int, es: int, fp
         gate_up = wgu + R * rd + R * f * 2
         down = wdn + R * rf + R * d * 4
         quant = R * f * 2 + R * rf                           # the rows of h
-        scatter = T * d * 2 + T * rd + T * rd + R * rd       # token rows quantized, then scattered
+        scatter = T * d * 2 + T * rd + R * rd                # token rows read, quantized, scattered
         routing = T * E * 4 + T * k * 8
         combine = R * d * 4 + T * d * 4
         return {"R": R, "touched": touched, "gate_up_bytes": gate_up, "down_bytes": down,
@@ -491,7 +491,7 @@ def run_ours(args, rank: int, world: int):
         routing = []
     elif w4a4:
         # 4-bit activations: the token rows and h quantized by the 4-bit quantizer, block-scaled MMAs
-        names = ("route", "quantize_x", "scatter", "gate_up", "quantize_h", "down", "combine")
+        names = ("route", "scatter_quant", "gate_up", "quantize_h", "down", "combine")
         routing = []
     elif fused and T <= SMALL_TOKENS and T * k <= SMALL_ROUTES:
         names = ("route_scatter_small", "gate_up", "down_combine")
@@ -543,9 +543,8 @@ def run_ours(args, rank: int, world: int):
     elif w4a4:
         calls = [
             M.bind(M.moe_route_topk_offsets, logits, mask, k, b.ids, b.w, b.counts, b.offsets, b.ws),
-            M.bind(M.moe_quantize_rows_fp4, x, b.x_q),
-            M.bind(M.moe_scatter_rows_fp4, b.x_q, b.ids, mask, b.offsets, b.xs_q, b.row_of_route, b.route_of_row,
-                   b.ws),
+            M.bind(M.moe_scatter_rows_quant_fp4, x, b.ids, mask, b.offsets, b.x_q, b.xs_q, b.row_of_route,
+                   b.route_of_row, b.ws),
             M.bind(M.moe_grouped_gate_up_w4a4, b.xs_q, b.offsets, wg, wu, b.h),
             M.bind(M.moe_quantize_rows_fp4, b.h, b.h_q),
             M.bind(M.moe_grouped_down_w4a4, b.h_q, b.offsets, wd, b.y),

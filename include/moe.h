@@ -544,6 +544,16 @@ moe_status moe_scatter_rows_fp4(const uint8_t* x_codes, const uint8_t* x_block_s
                                 uint8_t* xs_block_scales, int ld_xs, float* xs_scales, int32_t* row_of_route,
                                 int32_t* route_of_row, void* ws, void* stream);
 
+/* A4 with 4-bit rows straight from the bf16 token rows x [T][d]: every token
+ * row is read once and quantized -- x_codes, x_block_scales, x_scales, what
+ * moe_quantize_rows_fp4 would give -- and written to its compact rows as
+ * moe_scatter_rows_fp4 writes them.  d a multiple of 64 and at most 8192. */
+moe_status moe_scatter_rows_quant_fp4(const void* x, const int32_t* ids, const uint8_t* mask, const int32_t* offsets,
+                                      int T, int k, int d, int E, uint8_t* x_codes, uint8_t* x_block_scales,
+                                      int ld_x, float* x_scales, uint8_t* xs_codes, uint8_t* xs_block_scales,
+                                      int ld_xs, float* xs_scales, int32_t* row_of_route, int32_t* route_of_row,
+                                      void* ws, void* stream);
+
 /* A5 on 4-bit operands: h[i][j] = silu(g) * u with g = s_gate[e][j] *
  * xs_scales[i] * sum over K of (b_gate * value(code)) (xs block scale *
  * value(code)) and u likewise; h [cap][f] bf16 out (rows R .. cap-1
@@ -565,9 +575,9 @@ moe_status moe_grouped_down_w4a4(const uint8_t* h_codes, const uint8_t* h_block_
                                  void* stream);
 
 /* The whole path on 4-bit weights and activations: moe_route_topk_offsets;
- * x quantized by moe_quantize_rows_fp4 (x_codes [T][d/2], x_block_scales
- * [d/64][4*ceil(T/4)][4], x_scales [T]) and scattered by
- * moe_scatter_rows_fp4 (xs_codes [T*k][d/2], xs_block_scales
+ * x quantized and scattered by moe_scatter_rows_quant_fp4 (above d = 8192:
+ * moe_quantize_rows_fp4, then moe_scatter_rows_fp4): x_codes [T][d/2],
+ * x_block_scales [d/64][4*ceil(T/4)][4], x_scales [T]; xs_codes [T*k][d/2], xs_block_scales
  * [d/64][4*ceil(T*k/4)][4], xs_scales [T*k]); moe_grouped_gate_up_w4a4 into
  * h [T*k][f] bf16; h quantized (h_codes [T*k][f/2], h_block_scales
  * [f/64][4*ceil(T*k/4)][4], h_scales [T*k]); moe_grouped_down_w4a4 into y;

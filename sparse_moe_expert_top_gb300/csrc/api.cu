@@ -544,14 +544,21 @@ extern "C" moe_status moe_forward_w4a4(const float* logits, const void* x, const
     MOE_REQUIRE(aligned16(x) && aligned16(h) && aligned16(y) && aligned16(out) && aligned16(ws));
     const int cap = T * k;
     if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK) return st;
-    // NVFP4 token rows, scattered to the compact rows
-    if ((st = moe_quantize_rows_fp4(x, MOE_BF16, T, rows_ld(T), d, x_codes, x_block_scales, x_scales, stream)) !=
-        MOE_OK)
-        return st;
-    if ((st = moe_scatter_rows_fp4(x_codes, x_block_scales, rows_ld(T), x_scales, ids, mask, offsets, T, k, d, E,
-                                   xs_codes, xs_block_scales, rows_ld(cap), xs_scales, row_of_route, route_of_row, ws,
-                                   stream)) != MOE_OK)
-        return st;
+    // 4-bit token rows, scattered to the compact rows (one kernel up to d = 8192)
+    if (d <= 4 * 128 * 16) {
+        if ((st = moe_scatter_rows_quant_fp4(x, ids, mask, offsets, T, k, d, E, x_codes, x_block_scales, rows_ld(T),
+                                             x_scales, xs_codes, xs_block_scales, rows_ld(cap), xs_scales,
+                                             row_of_route, route_of_row, ws, stream)) != MOE_OK)
+            return st;
+    } else {
+        if ((st = moe_quantize_rows_fp4(x, MOE_BF16, T, rows_ld(T), d, x_codes, x_block_scales, x_scales, stream)) !=
+            MOE_OK)
+            return st;
+        if ((st = moe_scatter_rows_fp4(x_codes, x_block_scales, rows_ld(T), x_scales, ids, mask, offsets, T, k, d, E,
+                                       xs_codes, xs_block_scales, rows_ld(cap), xs_scales, row_of_route,
+                                       route_of_row, ws, stream)) != MOE_OK)
+            return st;
+    }
     if ((st = moe_grouped_gate_up_w4a4(xs_codes, xs_block_scales, rows_ld(cap), xs_scales, offsets, cap, E, d, f,
                                        w_gate_q, b_gate, s_gate, w_up_q, b_up, s_up, h, stream)) != MOE_OK)
         return st;

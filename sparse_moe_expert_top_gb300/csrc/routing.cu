@@ -820,6 +820,131 @@ __global__ void __launch_bounds__(128) scatter_quant_e4m3_kernel(
     if (tid == 0) x_scales[t] = s;
 }
 
+// ---------------------------------------------------------------------------
+// 4-bit activation rows (the 4-bit-activation path), quantized in the
+// scatter.  The arithmetic is the 4-bit weight quantizer's, bit for bit: row
+// scale s = max|row| / 2688 (1 for an all-zero row); per block of 16 values
+// the E4M3 block scale b of (block max / 6) / s (two IEEE fp32 divisions,
+// nearest even, saturating); codes = E2M1 of v / (value(b) * s), nearest
+// even, saturating at 6; 0 when value(b) is 0.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+    unsigned short v;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(v)
+        : "f"(hi), "f"(lo));
+    return v & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_code_value(uint32_t b) {
+    uint32_t half2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(half2) : "h"(static_cast<unsigned short>(b)));
+    float v;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(v) : "h"(static_cast<unsigned short>(half2 & 0xFFFFu)));
+    return v;
+}
+
+// One CTA of 128 threads per token; thread i takes blocks of 16 values i, i +
+// 128, ... (at most VPB of them: d <= VPB * 2048).  Writes the token's codes,
+// block scales and scale (x_codes [T][d/2], x_bs [d/64][ld_x][4], x_scales [T])
+// and the same to each of its compact rows (xs_*), zeros to rows R .. T*k-1.
+template <int VPB>
+__global__ void __launch_bounds__(128) scatter_quant_fp4_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets, int T, int k,
+    int E, int n_blk, const int32_t* __restrict__ lrank, const int32_t* __restrict__ bases, int chunk_tokens,
+    uint2* __restrict__ x_codes, uint8_t* __restrict__ x_bs, int ld_x, float* __restrict__ x_scales,
+    uint2* __restrict__ xs_codes, uint8_t* __restrict__ xs_bs, int ld_xs, float* __restrict__ xs_scales,
+    int32_t* __restrict__ row_of_route, int32_t* __restrict__ route_of_row, unsigned* err) {
+    __shared__ int rows[kMaxK];
+    __shared__ int tails[kMaxK];
+    __shared__ float red[4];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const int n_routes = T * k;
+    if (tid < k) {
+        const int r = t * k + tid;
+        const int lr = lrank[r];
+        int row = -1;
+        bool bad = false;
+        if (lr >= 0) {
+            const int e = ids[r];
+            if (e >= 0 && e < E) row = bases[static_cast<size_t>(t / chunk_tokens) * kMaxExperts + e] + lr;
+            if (row < 0 || row >= n_routes) {
+                bad = true;
+                row = -1;
+            }
+        }
+        rows[tid] = row;
+        row_of_route[r] = row;
+        if (row >= 0) route_of_row[row] = r;
+        const int R = __ldg(offsets + E);
+        int tail = -1;
+        if (R < 0 || R > n_routes) bad = true;
+        else if (R + r < n_routes) tail = R + r;
+        tails[tid] = tail;
+        if (tail >= 0) route_of_row[tail] = -1;
+        if (bad) atomicOr(err, DEVERR_OFFSETS);
+    }
+    uint4 u[VPB][2];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPB; ++j) {
+        const int v = tid + j * 128;
+        if (v < n_blk) {
+            u[j][0] = __ldg(x + (static_cast<size_t>(t) * n_blk + v) * 2);
+            u[j][1] = __ldg(x + (static_cast<size_t>(t) * n_blk + v) * 2 + 1);
+            amax = fmaxf(amax, fmaxf(amax_bf16x8(u[j][0]), amax_bf16x8(u[j][1])));
+        }
+    }
+    amax = block_max(amax, red);   // its barrier also publishes rows[] and tails[]
+    const float s = amax > 0.f ? __fdiv_rn(amax, 2688.f) : 1.f;
+#pragma unroll
+    for (int j = 0; j < VPB; ++j) {
+        const int v = tid + j * 128;
+        if (v < n_blk) {
+            float val[16];
+            const uint32_t wv[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w,
+                                    u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
+            float bmax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                val[2 * i] = __uint_as_float(wv[i] << 16);
+                val[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+                bmax = fmaxf(bmax, fmaxf(fabsf(val[2 * i]), fabsf(val[2 * i + 1])));
+            }
+            const uint32_t b = e4m3x2_rn(__fdiv_rn(__fdiv_rn(bmax, 6.f), s), 0.f) & 0xFFu;
+            const float vb = e4m3_code_value(b);
+            const float denom = __fmul_rn(vb, s);
+            uint32_t p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                p[i] = vb > 0.f ? e2m1x2_rn(__fdiv_rn(val[2 * i], denom), __fdiv_rn(val[2 * i + 1], denom)) : 0u;
+            const uint2 q = make_uint2(p[0] | (p[1] << 8) | (p[2] << 16) | (p[3] << 24),
+                                       p[4] | (p[5] << 8) | (p[6] << 16) | (p[7] << 24));
+            const size_t sf = static_cast<size_t>(v >> 2);   // 64-value tile of this block
+            x_codes[static_cast<size_t>(t) * n_blk + v] = q;
+            x_bs[(sf * ld_x + t) * 4 + (v & 3)] = static_cast<uint8_t>(b);
+            for (int sl = 0; sl < k; ++sl) {
+                const int row = rows[sl];
+                if (row >= 0) {
+                    xs_codes[static_cast<size_t>(row) * n_blk + v] = q;
+                    xs_bs[(sf * ld_xs + row) * 4 + (v & 3)] = static_cast<uint8_t>(b);
+                }
+                const int tail = tails[sl];
+                if (tail >= 0) {
+                    xs_codes[static_cast<size_t>(tail) * n_blk + v] = make_uint2(0u, 0u);
+                    xs_bs[(sf * ld_xs + tail) * 4 + (v & 3)] = 0;
+                }
+            }
+        }
+    }
+    if (tid < k) {
+        if (rows[tid] >= 0) xs_scales[rows[tid]] = s;
+        if (tails[tid] >= 0) xs_scales[tails[tid]] = 0.f;
+    }
+    if (tid == 0) x_scales[t] = s;
+}
+
 // A4 without the row copy, for the fused path (the gate/up kernel gathers
 // the token rows itself).  One warp per token: the compact row of each slot
 // exactly as scatter_rows_kernel computes it, both index maps, and the
@@ -1376,6 +1501,34 @@ extern "C" moe_status moe_scatter_rows_fp4(const uint8_t* x_codes, const uint8_t
         nullptr, 0, nullptr, 0, ws_chunk_tokens(T), x_scales, xs_scales,
         reinterpret_cast<const uint32_t*>(x_block_scales), ld_x, reinterpret_cast<uint32_t*>(xs_block_scales), ld_xs,
         d / 64);
+    return launch_status();
+}
+
+extern "C" moe_status moe_scatter_rows_quant_fp4(const void* x, const int32_t* ids, const uint8_t* mask,
+                                                  const int32_t* offsets, int T, int k, int d, int E,
+                                                  uint8_t* x_codes, uint8_t* x_block_scales, int ld_x,
+                                                  float* x_scales, uint8_t* xs_codes, uint8_t* xs_block_scales,
+                                                  int ld_xs, float* xs_scales, int32_t* row_of_route,
+                                                  int32_t* route_of_row, void* ws, void* stream) {
+    (void)mask;  // folded into the workspace ranks by the histogram
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 64 && d % 64 == 0);
+    MOE_REQUIRE(d <= 4 * 128 * 16);
+    MOE_REQUIRE(ld_x >= T && ld_x % 4 == 0 && ld_xs >= T * k && ld_xs % 4 == 0);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(x && ids && offsets && x_codes && x_block_scales && x_scales && xs_codes && xs_block_scales &&
+                xs_scales && row_of_route && route_of_row && ws);
+    MOE_REQUIRE(aligned16(x) && aligned16(x_codes) && aligned16(xs_codes) && aligned16(ws));
+    DeviceInfo di;
+    moe_status st = device_info(&di);
+    if (st != MOE_OK) return st;
+    const int32_t* w32 = static_cast<const int32_t*>(ws);
+    const int n_blk = d / 16;
+    auto kernel = n_blk <= 2 * 128 ? scatter_quant_fp4_kernel<2> : scatter_quant_fp4_kernel<4>;
+    kernel<<<T, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(x), ids, offsets, T, k, E, n_blk, w32 + ws_rank_offset(T, k),
+        w32 + ws_bases_offset(T, k), ws_chunk_tokens(T), reinterpret_cast<uint2*>(x_codes), x_block_scales, ld_x,
+        x_scales, reinterpret_cast<uint2*>(xs_codes), xs_block_scales, ld_xs, xs_scales, row_of_route, route_of_row,
+        di.error_word);
     return launch_status();
 }
 

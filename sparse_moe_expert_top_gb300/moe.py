@@ -73,6 +73,8 @@ SIGNATURES = {
     "moe_forward_w8a8": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 6 + [_P] * 17, _I),
     "moe_quantize_rows_fp4": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_scatter_rows_fp4": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P], _I),
+    "moe_scatter_rows_quant_fp4": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P],
+                                   _I),
     "moe_grouped_gate_up_w4a4": ([_P, _P, _I, _P, _P, _I, _I, _I, _I] + [_P] * 8, _I),
     "moe_grouped_down_w4a4": ([_P, _P, _I, _P, _P, _I, _I, _I, _I] + [_P] * 5, _I),
     "moe_forward_w4a4": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 9 + [_P] * 20, _I),
@@ -995,6 +997,21 @@ def moe_scatter_rows_fp4(x_q: FP4Rows, ids, mask, offsets, xs_q: FP4Rows, row_of
     _check("moe_scatter_rows_fp4", load().moe_scatter_rows_fp4(
         _ptr(x_q.codes), _ptr(x_q.block_scales), x_q.ld, _ptr(x_q.scales), _ptr(ids), _ptr(mask), _ptr(offsets),
         T, k, d, E, _ptr(xs_q.codes), _ptr(xs_q.block_scales), xs_q.ld, _ptr(xs_q.scales), _ptr(row_of_route),
+        _ptr(route_of_row), _ptr(ws), _stream(stream)))
+
+
+def moe_scatter_rows_quant_fp4(x, ids, mask, offsets, x_q: FP4Rows, xs_q: FP4Rows, row_of_route, route_of_row, ws,
+                               stream=None):
+    """Quantizes the bf16 token rows x [T][d] into x_q and scatters them into xs_q, in one kernel."""
+    T, d = x.shape
+    k = ids.shape[1]
+    E = offsets.shape[0] - 1
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if x_q.rows != T or x_q.K != d or xs_q.rows != T * k or xs_q.K != d:
+        raise ValueError("4-bit rows do not match the routing")
+    _check("moe_scatter_rows_quant_fp4", load().moe_scatter_rows_quant_fp4(
+        _ptr(x), _ptr(ids), _ptr(mask), _ptr(offsets), T, k, d, E, _ptr(x_q.codes), _ptr(x_q.block_scales), x_q.ld,
+        _ptr(x_q.scales), _ptr(xs_q.codes), _ptr(xs_q.block_scales), xs_q.ld, _ptr(xs_q.scales), _ptr(row_of_route),
         _ptr(route_of_row), _ptr(ws), _stream(stream)))
 
 

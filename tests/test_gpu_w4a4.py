@@ -163,3 +163,31 @@ def test_w4a4_full_size_workload(name):
     _check_against_oracle(b, ref, cfg.k)
     st = assert_close(out, ref["out"], "bf16")
     print(f"{name} W4A4: rel_fro={st['rel_fro']:.2e} max/rms={st['max_abs'] / st['rms_ref']:.2e}")
+
+
+@pytest.mark.parametrize("T,E,k,d,p", [(300, 16, 4, 512, 0.1), (40, 8, 6, 4096, 0.0), (33, 4, 2, 8192, 0.2),
+                                       (20, 4, 2, 128, 0.0)])
+def test_fused_quantize_scatter_equals_the_two_steps(T, E, k, d, p):
+    """The scatter that quantizes the token rows gives the codes, block scales and scales of
+    moe_quantize_rows_fp4 followed by moe_scatter_rows_fp4, bit for bit."""
+    logits, mask, *_ = _case(T, E, k, 128, 128, p, seed=d + T)
+    x = (torch.randn(T, d) * 2).to(torch.bfloat16).cuda()
+    x[0, :16] = 0.0
+    md = None if mask is None else mask.cuda()
+    a = M.MoEBuffersW4A4(T, E, k, d, 128)
+    M.moe_route_topk_offsets(logits.cuda(), md, k, a.ids, a.w, a.counts, a.offsets, a.ws)
+    ref_x = M.moe_quantize_rows_fp4(x)
+    ref_xs = M.FP4Rows.empty(T * k, d)
+    ref_ror, ref_rro = torch.empty_like(a.row_of_route), torch.empty_like(a.route_of_row)
+    M.moe_scatter_rows_fp4(ref_x, a.ids, md, a.offsets, ref_xs, ref_ror, ref_rro, a.ws)
+    a.xs_q.codes.fill_(7)
+    a.xs_q.scales.fill_(float("nan"))
+    M.moe_scatter_rows_quant_fp4(x, a.ids, md, a.offsets, a.x_q, a.xs_q, a.row_of_route, a.route_of_row, a.ws)
+    M.moe_check_device_error()
+    for got, ref in ((a.x_q, ref_x), (a.xs_q, ref_xs)):
+        n = got.rows
+        assert torch.equal(got.codes, ref.codes)
+        assert torch.equal(got.block_scales[:, :n], ref.block_scales[:, :n])
+        assert torch.equal(got.scales.view(torch.int32), ref.scales.view(torch.int32))
+    assert torch.equal(a.row_of_route, ref_ror) and torch.equal(a.route_of_row, ref_rro)
+    _check_rows(a.x_q, mo.quantize_bank_fp4(x.cpu()))
