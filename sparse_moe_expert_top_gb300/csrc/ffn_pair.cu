@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
     volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
     int* order = const_cast<int*>(epi_flag + 2);     // experts: the heavy ones, then the light ones (E entries)
     int* heavy_items = order + kMaxExperts;          // items of the heavy experts
+    int* heavy_experts = heavy_items + 1;            // how many experts are heavy
     __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kCtrlBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -258,7 +259,10 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
         }
         if (lane == 31) item_off[E] = run;
         __syncwarp();
-        if (lane == 0) *heavy_items = item_off[n_heavy];
+        if (lane == 0) {
+            *heavy_items = item_off[n_heavy];
+            *heavy_experts = n_heavy;
+        }
         if (bad && lane == 0 && rank == 0) atomicOr(err, DEVERR_OFFSETS);
     }
     tc_fence_before();
@@ -268,14 +272,35 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int n_items = item_off[E];
     const int n_heavy_items = *heavy_items;
-    // Position p of the hand-out order takes the next heavy item when
-    // floor((p + 1) * H / n) > floor(p * H / n) (H heavy items of n), else the
-    // next light item: every stretch of positions holds heavy and light items
-    // in proportion.
+    const int n_groups = *heavy_experts * n_mt;       // heavy (expert, feature tile) groups
+    const int n_light = n_items - n_heavy_items;
+    // The hand-out order is a sequence of blocks, one per heavy group b (in
+    // expert, feature-tile order): the group's row slices, consecutive so
+    // that pairs running them at the same time share its weight tiles in L2,
+    // then the next floor((b+1) L / G) - floor(b L / G) light items (L light
+    // items, G groups).  Block b starts at position
+    //   B(b) = item_off[b / n_mt] + (b % n_mt) * ntiles + floor(b L / G).
     auto item_at = [&](int p) {
-        const long long hb = static_cast<long long>(p) * n_heavy_items / n_items;
-        const long long hb1 = static_cast<long long>(p + 1) * n_heavy_items / n_items;
-        const int u = hb1 > hb ? static_cast<int>(hb) : n_heavy_items + p - static_cast<int>(hb);
+        int u = p;
+        if (n_groups > 0) {
+            auto block_start = [&](int b) {
+                const int ei = b / n_mt, mt = b - ei * n_mt;
+                return item_off[ei] + mt * ntiles[order[ei]] +
+                       static_cast<int>(static_cast<long long>(b) * n_light / n_groups);
+            };
+            int lo = 0, hi = n_groups - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (block_start(mid) <= p) lo = mid;
+                else hi = mid - 1;
+            }
+            const int ei = lo / n_mt, mt = lo - ei * n_mt;
+            const int size = ntiles[order[ei]];
+            const int o = p - block_start(lo);
+            u = o < size ? item_off[ei] + mt * size + o
+                         : n_heavy_items + static_cast<int>(static_cast<long long>(lo) * n_light / n_groups) +
+                               (o - size);
+        }
         return decode_item_ordered(u, item_off, order, ntiles, offsets, E, kPairSlice);
     };
 
