@@ -122,3 +122,19 @@ def test_pair_w8a8_matches_oracle(T, E, k, d, f, p, dead, heavy):
     assert_close(b.y[:R], y_ref, "bf16")
     assert torch.all(b.y[R:] == 0)
     assert_close(out, ref["out"], "bf16")
+
+
+def test_pair_kernels_reject_inconsistent_offsets():
+    """offsets[E] beyond the capacity: both paired kernels skip their work and flag it; nothing hangs."""
+    E, d, f, cap = 4, 128, 128, 24576
+    assert M.moe_ffn_paired(cap)
+    xs = torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda")
+    wg = torch.zeros(E, f, d, dtype=torch.bfloat16, device="cuda")
+    h = torch.zeros(cap, f, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(cap, d, dtype=torch.float32, device="cuda")
+    offsets = torch.tensor([0, 4000, 8000, 12000, cap + 100], dtype=torch.int32, device="cuda")
+    M.moe_grouped_ffn(xs, offsets, wg, wg, wg.transpose(1, 2).contiguous(), h, y)
+    with pytest.raises(M.MoEError) as exc:
+        M.moe_check_device_error()
+    assert exc.value.status == M.MOE_ERR_INVALID_ARG
+    M.moe_check_device_error()  # the error word was cleared

@@ -191,3 +191,54 @@ def test_fused_quantize_scatter_equals_the_two_steps(T, E, k, d, p):
         assert torch.equal(got.scales.view(torch.int32), ref.scales.view(torch.int32))
     assert torch.equal(a.row_of_route, ref_ror) and torch.equal(a.route_of_row, ref_rro)
     _check_rows(a.x_q, mo.quantize_bank_fp4(x.cpu()))
+
+
+def test_w4a4_kernels_reject_inconsistent_offsets():
+    """offsets[E] beyond the capacity: the 4-bit kernels skip their work and flag it; nothing hangs."""
+    E, d, f, cap = 4, 256, 256, 64
+    w = [M.moe_quantize_weights_fp4(torch.zeros(E, f, d, dtype=torch.bfloat16, device="cuda")) for _ in range(2)]
+    wd = M.moe_quantize_weights_fp4(torch.zeros(E, d, f, dtype=torch.bfloat16, device="cuda"))
+    xs = M.moe_quantize_rows_fp4(torch.zeros(cap, d, dtype=torch.bfloat16, device="cuda"))
+    h = torch.zeros(cap, f, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(cap, d, dtype=torch.float32, device="cuda")
+    offsets = torch.tensor([0, 16, 32, 48, cap + 9], dtype=torch.int32, device="cuda")
+    M.moe_grouped_gate_up_w4a4(xs, offsets, w[0], w[1], h)
+    with pytest.raises(M.MoEError) as exc:
+        M.moe_check_device_error()
+    assert exc.value.status == M.MOE_ERR_INVALID_ARG
+    hq = M.moe_quantize_rows_fp4(h)
+    M.moe_grouped_down_w4a4(hq, offsets, wd, y)
+    with pytest.raises(M.MoEError) as exc:
+        M.moe_check_device_error()
+    assert exc.value.status == M.MOE_ERR_INVALID_ARG
+    M.moe_check_device_error()
+
+
+@pytest.mark.parametrize("fmt", ["w4a4", "w8a8"])
+def test_low_bit_paths_are_capturable_in_a_cuda_graph(fmt):
+    """No allocation, synchronisation or host read inside the 4-bit and E4M3 paths: a CUDA graph of one
+    call replays it bit for bit."""
+    T, E, k, d, f = 300, 16, 4, 256, 256
+    logits, mask, x, wg, wu, wd = (t.cuda() if t is not None else None
+                                   for t in _case(T, E, k, d, f, 0.1, seed=43))
+    if fmt == "w4a4":
+        q = [M.moe_quantize_weights_fp4(w) for w in (wg, wu, wd)]
+        b, fwd = M.MoEBuffersW4A4(T, E, k, d, f), M.moe_forward_w4a4
+    else:
+        q = [M.moe_quantize_weights_fp8(w) for w in (wg, wu, wd)]
+        b, fwd = M.MoEBuffersW8A8(T, E, k, d, f), M.moe_forward_w8a8
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ref = fwd(logits, x, mask, *q, k, b).clone()      # warm-up call off the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fwd(logits, x, mask, *q, k, b)
+    b.out.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    M.moe_check_device_error()
+    assert torch.equal(b.out.view(torch.int32), ref.view(torch.int32))
