@@ -490,8 +490,11 @@ def run_ours(args, rank: int, world: int):
         names = ("route", "scatter_quant", "gate_up", "quantize_h", "down", "combine")
         routing = []
     elif w4a4:
-        # 4-bit activations: the token rows and h quantized by the 4-bit quantizer, block-scaled MMAs
-        names = ("route", "scatter_quant", "gate_up", "quantize_h", "down", "combine")
+        # 4-bit activations: the token rows and h quantized by the 4-bit quantizer, block-scaled MMAs; small
+        # chunks take the routing, quantization and scatter in one launch, as moe_forward_w4a4 does
+        small4 = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES
+        names = (("route_scatter_quant_small",) if small4 else ("route", "scatter_quant")) + (
+            "gate_up", "quantize_h", "down", "combine")
         routing = []
     elif fused and T <= SMALL_TOKENS and T * k <= SMALL_ROUTES:
         names = ("route_scatter_small", "gate_up", "down_combine")
@@ -541,10 +544,10 @@ def run_ours(args, rank: int, world: int):
                    b.tile_counts, b.out),
         ]
     elif w4a4:
-        calls = [
+        calls = ([M.bind(M.moe_route_scatter_quant_small_fp4, logits, x, mask, k, b)] if small4 else [
             M.bind(M.moe_route_topk_offsets, logits, mask, k, b.ids, b.w, b.counts, b.offsets, b.ws),
             M.bind(M.moe_scatter_rows_quant_fp4, x, b.ids, mask, b.offsets, b.x_q, b.xs_q, b.row_of_route,
-                   b.route_of_row, b.ws),
+                   b.route_of_row, b.ws)]) + [
             M.bind(M.moe_grouped_gate_up_w4a4, b.xs_q, b.offsets, wg, wu, b.h),
             M.bind(M.moe_quantize_rows_fp4, b.h, b.h_q),
             M.bind(M.moe_grouped_down_w4a4, b.h_q, b.offsets, wd, b.y),

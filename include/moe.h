@@ -554,6 +554,18 @@ moe_status moe_scatter_rows_quant_fp4(const void* x, const int32_t* ids, const u
                                       int ld_xs, float* xs_scales, int32_t* row_of_route, int32_t* route_of_row,
                                       void* ws, void* stream);
 
+/* A1-A4 with 4-bit rows in one launch for small chunks (T <= 128 and T*k
+ * <= 512, as moe_route_scatter_small): the routing outputs of
+ * moe_route_topk_offsets (ids, w, counts, offsets, row_of_route,
+ * route_of_row; no workspace) and the quantized, scattered rows of
+ * moe_scatter_rows_quant_fp4, bit for bit.  d a multiple of 64. */
+moe_status moe_route_scatter_quant_small_fp4(const float* logits, const void* x, const uint8_t* mask, int T, int E,
+                                             int k, int d, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                             uint8_t* x_codes, uint8_t* x_block_scales, int ld_x, float* x_scales,
+                                             uint8_t* xs_codes, uint8_t* xs_block_scales, int ld_xs,
+                                             float* xs_scales, int32_t* row_of_route, int32_t* route_of_row,
+                                             void* stream);
+
 /* A5 on 4-bit operands: h[i][j] = silu(g) * u with g = s_gate[e][j] *
  * xs_scales[i] * sum over K of (b_gate * value(code)) (xs block scale *
  * value(code)) and u likewise; h [cap][f] bf16 out (rows R .. cap-1
@@ -575,7 +587,9 @@ moe_status moe_grouped_down_w4a4(const uint8_t* h_codes, const uint8_t* h_block_
                                  void* stream);
 
 /* The whole path on 4-bit weights and activations: moe_route_topk_offsets;
- * x quantized and scattered by moe_scatter_rows_quant_fp4 (above d = 8192:
+ * x quantized and scattered by moe_scatter_rows_quant_fp4 (small chunks: the
+ * routing and this step in one launch, moe_route_scatter_quant_small_fp4;
+ * above d = 8192:
  * moe_quantize_rows_fp4, then moe_scatter_rows_fp4): x_codes [T][d/2],
  * x_block_scales [d/64][4*ceil(T/4)][4], x_scales [T]; xs_codes [T*k][d/2], xs_block_scales
  * [d/64][4*ceil(T*k/4)][4], xs_scales [T*k]); moe_grouped_gate_up_w4a4 into

@@ -543,9 +543,17 @@ extern "C" moe_status moe_forward_w4a4(const float* logits, const void* x, const
                 h_scales && y && out && ws);
     MOE_REQUIRE(aligned16(x) && aligned16(h) && aligned16(y) && aligned16(out) && aligned16(ws));
     const int cap = T * k;
-    if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK) return st;
-    // 4-bit token rows, scattered to the compact rows (one kernel up to d = 8192)
-    if (d <= 4 * 128 * 16) {
+    if (T <= kSmallTokens && cap <= kSmallRoutes) {
+        // small chunks: routing, quantization and scatter in one launch
+        if ((st = moe_route_scatter_quant_small_fp4(logits, x, mask, T, E, k, d, ids, w, counts, offsets, x_codes,
+                                                    x_block_scales, rows_ld(T), x_scales, xs_codes, xs_block_scales,
+                                                    rows_ld(cap), xs_scales, row_of_route, route_of_row, stream)) !=
+            MOE_OK)
+            return st;
+    } else if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK) {
+        return st;
+    } else if (d <= 4 * 128 * 16) {
+        // 4-bit token rows, scattered to the compact rows (one kernel up to d = 8192)
         if ((st = moe_scatter_rows_quant_fp4(x, ids, mask, offsets, T, k, d, E, x_codes, x_block_scales, rows_ld(T),
                                              x_scales, xs_codes, xs_block_scales, rows_ld(cap), xs_scales,
                                              row_of_route, route_of_row, ws, stream)) != MOE_OK)

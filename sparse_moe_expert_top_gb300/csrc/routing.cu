@@ -845,6 +845,30 @@ __device__ __forceinline__ float e4m3_code_value(uint32_t b) {
     return v;
 }
 
+// The 16 bf16 values of (a, b) as 8 bytes of E2M1 codes (the lower value of
+// each pair in the low nibble) under row scale s; *bscale gets the block's
+// E4M3 scale code.
+__device__ __forceinline__ uint2 quant_block_fp4(uint4 a, uint4 b, float s, uint32_t& bscale) {
+    float val[16];
+    const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float bmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        val[2 * i] = __uint_as_float(wv[i] << 16);
+        val[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+        bmax = fmaxf(bmax, fmaxf(fabsf(val[2 * i]), fabsf(val[2 * i + 1])));
+    }
+    const uint32_t bs = e4m3x2_rn(__fdiv_rn(__fdiv_rn(bmax, 6.f), s), 0.f) & 0xFFu;
+    const float vb = e4m3_code_value(bs);
+    const float denom = __fmul_rn(vb, s);
+    uint32_t p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        p[i] = vb > 0.f ? e2m1x2_rn(__fdiv_rn(val[2 * i], denom), __fdiv_rn(val[2 * i + 1], denom)) : 0u;
+    bscale = bs;
+    return make_uint2(p[0] | (p[1] << 8) | (p[2] << 16) | (p[3] << 24), p[4] | (p[5] << 8) | (p[6] << 16) | (p[7] << 24));
+}
+
 // One CTA of 128 threads per token; thread i takes blocks of 16 values i, i +
 // 128, ... (at most VPB of them: d <= VPB * 2048).  Writes the token's codes,
 // block scales and scale (x_codes [T][d/2], x_bs [d/64][ld_x][4], x_scales [T])
@@ -902,25 +926,8 @@ __global__ void __launch_bounds__(128) scatter_quant_fp4_kernel(
     for (int j = 0; j < VPB; ++j) {
         const int v = tid + j * 128;
         if (v < n_blk) {
-            float val[16];
-            const uint32_t wv[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w,
-                                    u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
-            float bmax = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                val[2 * i] = __uint_as_float(wv[i] << 16);
-                val[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
-                bmax = fmaxf(bmax, fmaxf(fabsf(val[2 * i]), fabsf(val[2 * i + 1])));
-            }
-            const uint32_t b = e4m3x2_rn(__fdiv_rn(__fdiv_rn(bmax, 6.f), s), 0.f) & 0xFFu;
-            const float vb = e4m3_code_value(b);
-            const float denom = __fmul_rn(vb, s);
-            uint32_t p[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                p[i] = vb > 0.f ? e2m1x2_rn(__fdiv_rn(val[2 * i], denom), __fdiv_rn(val[2 * i + 1], denom)) : 0u;
-            const uint2 q = make_uint2(p[0] | (p[1] << 8) | (p[2] << 16) | (p[3] << 24),
-                                       p[4] | (p[5] << 8) | (p[6] << 16) | (p[7] << 24));
+            uint32_t b;
+            const uint2 q = quant_block_fp4(u[j][0], u[j][1], s, b);
             const size_t sf = static_cast<size_t>(v >> 2);   // 64-value tile of this block
             x_codes[static_cast<size_t>(t) * n_blk + v] = q;
             x_bs[(sf * ld_x + t) * 4 + (v & 3)] = static_cast<uint8_t>(b);
@@ -1075,21 +1082,21 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
 
 constexpr int kSmallThreads = 512;
 
-template <bool TO_F16>
-__global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
-    const float* __restrict__ logits, const uint4* __restrict__ x, const uint8_t* __restrict__ mask, int T, int E,
-    int k, int row_vecs, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, uint4* __restrict__ xs, int32_t* __restrict__ row_of_route,
-    int32_t* __restrict__ route_of_row, unsigned* err, int32_t* __restrict__ tile_counts, int n_counts,
-    float4* __restrict__ out, int d4) {
-    __shared__ int s_e[kSmallRoutes];     // expert of route r, -1 when masked
-    __shared__ int s_row[kSmallRoutes];   // rank, then compact row (-1 masked)
-    __shared__ int s_cnt[kMaxExperts];
-    __shared__ int s_off[kMaxExperts + 1];
+// A1-A3 of a small chunk in shared memory, by every CTA of the launch: the
+// top-k (warp per token), stable ranks in route order, the prefix; s_row gets
+// each route's compact row (-1 masked).  The CTA with `writer` set also
+// writes ids, w, counts, offsets and both index maps.  Returns R.  Ends with a
+// barrier.
+__device__ __forceinline__ int small_chunk_routing(const float* __restrict__ logits,
+                                                   const uint8_t* __restrict__ mask, int T, int E, int k,
+                                                   bool writer, int32_t* __restrict__ ids, float* __restrict__ w,
+                                                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                   int32_t* __restrict__ row_of_route,
+                                                   int32_t* __restrict__ route_of_row, int* s_e, int* s_row,
+                                                   int* s_cnt, int* s_off) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kWarps = kSmallThreads / 32;
     const int n_routes = T * k;
-    const bool writer = blockIdx.x == 0;
     for (int e = tid; e < kMaxExperts; e += kSmallThreads) s_cnt[e] = 0;
 
     // A1: warp per token, k rounds of a warp arg-max over order keys
@@ -1193,6 +1200,26 @@ __global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
         if (tid == 0) offsets[E] = R;
         for (int j = R + tid; j < n_routes; j += kSmallThreads) route_of_row[j] = -1;
     }
+    __syncthreads();
+    return R;
+}
+
+template <bool TO_F16>
+__global__ void __launch_bounds__(kSmallThreads) route_scatter_small_kernel(
+    const float* __restrict__ logits, const uint4* __restrict__ x, const uint8_t* __restrict__ mask, int T, int E,
+    int k, int row_vecs, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, uint4* __restrict__ xs, int32_t* __restrict__ row_of_route,
+    int32_t* __restrict__ route_of_row, unsigned* err, int32_t* __restrict__ tile_counts, int n_counts,
+    float4* __restrict__ out, int d4) {
+    __shared__ int s_e[kSmallRoutes];     // expert of route r, -1 when masked
+    __shared__ int s_row[kSmallRoutes];   // compact row of route r (-1 masked)
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    const int tid = threadIdx.x;
+    const int n_routes = T * k;
+    const bool writer = blockIdx.x == 0;
+    const int R = small_chunk_routing(logits, mask, T, E, k, writer, ids, w, counts, offsets, row_of_route,
+                                      route_of_row, s_e, s_row, s_cnt, s_off);
     __syncthreads();
 
     // the fused combine's preparation (fused path): this CTA's share of the
@@ -1576,6 +1603,86 @@ extern "C" moe_status moe_scatter_rows_f16(const void* x, const int32_t* ids, co
                                            int32_t* row_of_route, int32_t* route_of_row, void* ws, void* stream) {
     (void)mask;
     return scatter_rows(x, 2, true, ids, offsets, T, k, d, E, xs, row_of_route, route_of_row, ws, stream);
+}
+
+namespace moe {
+namespace {
+
+// A1-A4 with 4-bit rows in one launch for small chunks (T <= kSmallTokens,
+// T*k <= kSmallRoutes): CTA t takes the chunk's routing in shared memory (CTA
+// 0 writes the index outputs), quantizes token row t with the 4-bit
+// quantizer's arithmetic and writes its codes, block scales and scale to x_*
+// and to the token's compact rows; the rows R .. T*k-1 get zeros, spread
+// over the CTAs.
+__global__ void __launch_bounds__(kSmallThreads) route_scatter_quant_small_fp4_kernel(
+    const float* __restrict__ logits, const uint4* __restrict__ x, const uint8_t* __restrict__ mask, int T, int E,
+    int k, int n_blk, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, uint2* __restrict__ x_codes, uint8_t* __restrict__ x_bs, int ld_x,
+    float* __restrict__ x_scales, uint2* __restrict__ xs_codes, uint8_t* __restrict__ xs_bs, int ld_xs,
+    float* __restrict__ xs_scales, int32_t* __restrict__ row_of_route, int32_t* __restrict__ route_of_row) {
+    __shared__ int s_e[kSmallRoutes];
+    __shared__ int s_row[kSmallRoutes];
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ float red[kSmallThreads / 32];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const int n_routes = T * k;
+    const int R = small_chunk_routing(logits, mask, T, E, k, t == 0, ids, w, counts, offsets, row_of_route,
+                                      route_of_row, s_e, s_row, s_cnt, s_off);
+    const uint4* xr = x + static_cast<size_t>(t) * n_blk * 2;
+    float amax = 0.f;
+    for (int v = tid; v < n_blk; v += kSmallThreads)
+        amax = fmaxf(amax, fmaxf(amax_bf16x8(__ldg(xr + 2 * v)), amax_bf16x8(__ldg(xr + 2 * v + 1))));
+    amax = block_max(amax, red);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 2688.f) : 1.f;
+    for (int v = tid; v < n_blk; v += kSmallThreads) {
+        uint32_t b;
+        const uint2 q = quant_block_fp4(__ldg(xr + 2 * v), __ldg(xr + 2 * v + 1), s, b);
+        const size_t sf = static_cast<size_t>(v >> 2);
+        x_codes[static_cast<size_t>(t) * n_blk + v] = q;
+        x_bs[(sf * ld_x + t) * 4 + (v & 3)] = static_cast<uint8_t>(b);
+        for (int sl = 0; sl < k; ++sl) {
+            const int row = s_row[t * k + sl];
+            if (row >= 0) {
+                xs_codes[static_cast<size_t>(row) * n_blk + v] = q;
+                xs_bs[(sf * ld_xs + row) * 4 + (v & 3)] = static_cast<uint8_t>(b);
+            }
+        }
+    }
+    if (tid < k && s_row[t * k + tid] >= 0) xs_scales[s_row[t * k + tid]] = s;
+    if (tid == 0) x_scales[t] = s;
+    for (int j = R + t; j < n_routes; j += gridDim.x) {
+        for (int v = tid; v < n_blk; v += kSmallThreads) {
+            xs_codes[static_cast<size_t>(j) * n_blk + v] = make_uint2(0u, 0u);
+            xs_bs[((static_cast<size_t>(v) >> 2) * ld_xs + j) * 4 + (v & 3)] = 0;
+        }
+        if (tid == 0) xs_scales[j] = 0.f;
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_route_scatter_quant_small_fp4(const float* logits, const void* x, const uint8_t* mask,
+                                                         int T, int E, int k, int d, int32_t* ids, float* w,
+                                                         int32_t* counts, int32_t* offsets, uint8_t* x_codes,
+                                                         uint8_t* x_block_scales, int ld_x, float* x_scales,
+                                                         uint8_t* xs_codes, uint8_t* xs_block_scales, int ld_xs,
+                                                         float* xs_scales, int32_t* row_of_route,
+                                                         int32_t* route_of_row, void* stream) {
+    using namespace moe;
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 64 && d % 64 == 0);
+    MOE_REQUIRE(T <= kSmallTokens && T * k <= kSmallRoutes);
+    MOE_REQUIRE(ld_x >= T && ld_x % 4 == 0 && ld_xs >= T * k && ld_xs % 4 == 0);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && ids && w && counts && offsets && x_codes && x_block_scales && x_scales && xs_codes &&
+                xs_block_scales && xs_scales && row_of_route && route_of_row);
+    MOE_REQUIRE(aligned16(x) && aligned16(x_codes) && aligned16(xs_codes));
+    route_scatter_quant_small_fp4_kernel<<<T, kSmallThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        logits, static_cast<const uint4*>(x), mask, T, E, k, d / 16, ids, w, counts, offsets,
+        reinterpret_cast<uint2*>(x_codes), x_block_scales, ld_x, x_scales, reinterpret_cast<uint2*>(xs_codes),
+        xs_block_scales, ld_xs, xs_scales, row_of_route, route_of_row);
+    return launch_status();
 }
 
 extern "C" moe_status moe_route_scatter_small(const float* logits, const void* x, int dtype, int xs_f16,

@@ -75,6 +75,8 @@ SIGNATURES = {
     "moe_scatter_rows_fp4": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P], _I),
     "moe_scatter_rows_quant_fp4": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P],
                                    _I),
+    "moe_route_scatter_quant_small_fp4": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P,
+                                           _P, _P, _P], _I),
     "moe_grouped_gate_up_w4a4": ([_P, _P, _I, _P, _P, _I, _I, _I, _I] + [_P] * 8, _I),
     "moe_grouped_down_w4a4": ([_P, _P, _I, _P, _P, _I, _I, _I, _I] + [_P] * 5, _I),
     "moe_forward_w4a4": ([_P, _P, _P, _I, _I, _I, _I, _I] + [_P] * 9 + [_P] * 20, _I),
@@ -1013,6 +1015,24 @@ def moe_scatter_rows_quant_fp4(x, ids, mask, offsets, x_q: FP4Rows, xs_q: FP4Row
         _ptr(x), _ptr(ids), _ptr(mask), _ptr(offsets), T, k, d, E, _ptr(x_q.codes), _ptr(x_q.block_scales), x_q.ld,
         _ptr(x_q.scales), _ptr(xs_q.codes), _ptr(xs_q.block_scales), xs_q.ld, _ptr(xs_q.scales), _ptr(row_of_route),
         _ptr(route_of_row), _ptr(ws), _stream(stream)))
+
+
+def moe_route_scatter_quant_small_fp4(logits, x, mask, k: int, bufs: "MoEBuffersW4A4", stream=None):
+    """A1-A4 with 4-bit rows in one launch for small chunks (T <= 128, T*k <= 512), into ``bufs``."""
+    T, E = logits.shape
+    d = x.shape[1]
+    b = bufs
+    if (b.T, b.E, b.k, b.d) != (T, E, k, d):
+        raise ValueError("buffers were allocated for another shape")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _check("moe_route_scatter_quant_small_fp4", load().moe_route_scatter_quant_small_fp4(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets),
+        _ptr(b.x_q.codes), _ptr(b.x_q.block_scales), b.x_q.ld, _ptr(b.x_q.scales), _ptr(b.xs_q.codes),
+        _ptr(b.xs_q.block_scales), b.xs_q.ld, _ptr(b.xs_q.scales), _ptr(b.row_of_route), _ptr(b.route_of_row),
+        _stream(stream)))
 
 
 def moe_grouped_gate_up_w4a4(xs_q: FP4Rows, offsets, q_gate: FP4Weights, q_up: FP4Weights, h, stream=None):

@@ -242,3 +242,30 @@ def test_low_bit_paths_are_capturable_in_a_cuda_graph(fmt):
     torch.cuda.synchronize()
     M.moe_check_device_error()
     assert torch.equal(b.out.view(torch.int32), ref.view(torch.int32))
+
+
+@pytest.mark.parametrize("T,E,k,d,p", [(4, 64, 6, 256, 0.0), (100, 8, 2, 256, 0.1), (64, 10, 8, 512, 0.3),
+                                       (128, 256, 4, 128, 0.0), (1, 4, 2, 4096, 0.0)])
+def test_small_chunk_routing_quantize_scatter_in_one_launch(T, E, k, d, p):
+    """moe_route_scatter_quant_small_fp4 gives the routing outputs of moe_route_topk_offsets and the rows of
+    moe_scatter_rows_quant_fp4, bit for bit."""
+    logits, mask, *_ = _case(T, E, k, 128, 128, p, seed=T + d)
+    x = (torch.randn(T, d) * 2).to(torch.bfloat16).cuda()
+    lg, md = logits.cuda(), None if mask is None else mask.cuda()
+    a = M.MoEBuffersW4A4(T, E, k, d, 128)
+    M.moe_route_topk_offsets(lg, md, k, a.ids, a.w, a.counts, a.offsets, a.ws)
+    M.moe_scatter_rows_quant_fp4(x, a.ids, md, a.offsets, a.x_q, a.xs_q, a.row_of_route, a.route_of_row, a.ws)
+    b = M.MoEBuffersW4A4(T, E, k, d, 128)
+    b.xs_q.codes.fill_(5)
+    b.xs_q.scales.fill_(float("nan"))
+    b.route_of_row.fill_(77)
+    M.moe_route_scatter_quant_small_fp4(lg, x, md, k, b)
+    M.moe_check_device_error()
+    for name in ("ids", "counts", "offsets", "row_of_route", "route_of_row"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert torch.equal(a.w.view(torch.int32), b.w.view(torch.int32))
+    for qa, qb in ((a.x_q, b.x_q), (a.xs_q, b.xs_q)):
+        n = qa.rows
+        assert torch.equal(qa.codes, qb.codes)
+        assert torch.equal(qa.block_scales[:, :n], qb.block_scales[:, :n])
+        assert torch.equal(qa.scales.view(torch.int32), qb.scales.view(torch.int32))
