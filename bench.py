@@ -486,8 +486,11 @@ def run_ours(args, rank: int, world: int):
     gather = fused and args.fused_mode == "gather"
     small = small and not fused
     if w8a8:
-        # E4M3 activations: the token rows and h quantized per row, E4M3 x E4M3 tensor-core MMAs
-        names = ("route", "scatter_quant", "gate_up", "quantize_h", "down", "combine")
+        # E4M3 activations: the token rows and h quantized per row, E4M3 x E4M3 tensor-core MMAs; small chunks
+        # take the routing, quantization and scatter in one launch, as moe_forward_w8a8 does
+        small8 = T <= SMALL_TOKENS and T * k <= SMALL_ROUTES
+        names = (("route_scatter_quant_small",) if small8 else ("route", "scatter_quant")) + (
+            "gate_up", "quantize_h", "down", "combine")
         routing = []
     elif w4a4:
         # 4-bit activations: the token rows and h quantized by the 4-bit quantizer, block-scaled MMAs; small
@@ -554,10 +557,10 @@ def run_ours(args, rank: int, world: int):
             M.bind(M.moe_combine, b.y, b.row_of_route, b.w, b.out),
         ]
     elif w8a8:
-        calls = [
+        calls = ([M.bind(M.moe_route_scatter_quant_small_e4m3, logits, x, mask, k, b)] if small8 else [
             M.bind(M.moe_route_topk_offsets, logits, mask, k, b.ids, b.w, b.counts, b.offsets, b.ws),
             M.bind(M.moe_scatter_rows_quant_e4m3, x, b.ids, mask, b.offsets, b.x_q, b.x_scales, b.xs, b.xs_scales,
-                   b.row_of_route, b.route_of_row, b.ws),
+                   b.row_of_route, b.route_of_row, b.ws)]) + [
             M.bind(M.moe_grouped_gate_up_w8a8, b.xs, b.xs_scales, b.offsets, wg, wu, b.h),
             M.bind(M.moe_quantize_rows_e4m3, b.h, b.offsets, b.h_q, b.h_scales),
             M.bind(M.moe_grouped_down_w8a8, b.h_q, b.h_scales, b.offsets, wd, b.y),

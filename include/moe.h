@@ -469,6 +469,15 @@ moe_status moe_scatter_rows_quant_e4m3(const void* x, const int32_t* ids, const 
                                        float* x_scales, uint8_t* xs, float* xs_scales, int32_t* row_of_route,
                                        int32_t* route_of_row, void* ws, void* stream);
 
+/* A1-A4 with E4M3 rows in one launch for small chunks (T <= 128 and T*k <=
+ * 512): the routing outputs of moe_route_topk_offsets (no workspace) and the
+ * rows of moe_scatter_rows_quant_e4m3, bit for bit.  d a multiple of 16. */
+moe_status moe_route_scatter_quant_small_e4m3(const float* logits, const void* x, const uint8_t* mask, int T, int E,
+                                              int k, int d, int32_t* ids, float* w, int32_t* counts,
+                                              int32_t* offsets, uint8_t* x_q, float* x_scales, uint8_t* xs,
+                                              float* xs_scales, int32_t* row_of_route, int32_t* route_of_row,
+                                              void* stream);
+
 /* E4M3 codes and one scale per row of the compact bf16 rows a [cap][K] (h
  * of the FP8-activation path), the arithmetic of moe_quantize_weights_fp8;
  * rows at or beyond R = offsets[E] (zero rows) get zero codes and scale 1
@@ -493,7 +502,8 @@ moe_status moe_grouped_down_w8a8(const uint8_t* h_q, const float* h_scales, cons
 
 /* The whole path on E4M3 weights and activations: routing in one launch
  * (moe_route_topk_offsets), the token rows quantized (x_q [T][d], x_scales
- * [T]) and scattered (xs, xs_scales) by moe_scatter_rows_quant_e4m3,
+ * [T]) and scattered (xs, xs_scales) by moe_scatter_rows_quant_e4m3 (small
+ * chunks: the three in one launch, moe_route_scatter_quant_small_e4m3),
  * moe_grouped_gate_up_w8a8 into h [T*k][f] bf16, h quantized by
  * moe_quantize_rows_e4m3 (h_q [T*k][f], h_scales [T*k]),
  * moe_grouped_down_w8a8 into y, moe_combine into out.  x is bf16; every

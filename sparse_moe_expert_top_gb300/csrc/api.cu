@@ -441,9 +441,16 @@ extern "C" moe_status moe_forward_w8a8(const float* logits, const void* x, const
     MOE_REQUIRE(aligned16(x) && aligned16(x_q) && aligned16(xs) && aligned16(h) && aligned16(h_q) &&
                 aligned16(y) && aligned16(out) && aligned16(ws));
     const int cap = T * k;
-    if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK) return st;
-    // E4M3 codes of the token rows, one scale per row (the weights' quantizer's arithmetic), scattered
-    if (d <= 8 * 128 * 8) {
+    if (T <= kSmallTokens && cap <= kSmallRoutes) {
+        // small chunks: routing, quantization and scatter in one launch
+        if ((st = moe_route_scatter_quant_small_e4m3(logits, x, mask, T, E, k, d, ids, w, counts, offsets, x_q,
+                                                     x_scales, xs, xs_scales, row_of_route, route_of_row, stream)) !=
+            MOE_OK)
+            return st;
+    } else if ((st = moe_route_topk_offsets(logits, mask, T, E, k, ids, w, counts, offsets, ws, stream)) != MOE_OK) {
+        return st;
+    } else if (d <= 8 * 128 * 8) {
+        // E4M3 codes of the token rows, one scale per row (the weights' quantizer's arithmetic), scattered
         if ((st = moe_scatter_rows_quant_e4m3(x, ids, mask, offsets, T, k, d, E, x_q, x_scales, xs, xs_scales,
                                               row_of_route, route_of_row, ws, stream)) != MOE_OK)
             return st;

@@ -1660,8 +1660,65 @@ __global__ void __launch_bounds__(kSmallThreads) route_scatter_quant_small_fp4_k
     }
 }
 
+// The same for E4M3 rows (the FP8-activation path): one scale per token row
+// (max|row| / 448), codes x_q [T][d] and, per compact row, xs [T*k][d].
+__global__ void __launch_bounds__(kSmallThreads) route_scatter_quant_small_e4m3_kernel(
+    const float* __restrict__ logits, const uint4* __restrict__ x, const uint8_t* __restrict__ mask, int T, int E,
+    int k, int d8, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, uint2* __restrict__ x_q, float* __restrict__ x_scales, uint2* __restrict__ xs,
+    float* __restrict__ xs_scales, int32_t* __restrict__ row_of_route, int32_t* __restrict__ route_of_row) {
+    __shared__ int s_e[kSmallRoutes];
+    __shared__ int s_row[kSmallRoutes];
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ float red[kSmallThreads / 32];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const int n_routes = T * k;
+    const int R = small_chunk_routing(logits, mask, T, E, k, t == 0, ids, w, counts, offsets, row_of_route,
+                                      route_of_row, s_e, s_row, s_cnt, s_off);
+    const uint4* xr = x + static_cast<size_t>(t) * d8;
+    float amax = 0.f;
+    for (int v = tid; v < d8; v += kSmallThreads) amax = fmaxf(amax, amax_bf16x8(__ldg(xr + v)));
+    amax = block_max(amax, red);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    for (int v = tid; v < d8; v += kSmallThreads) {
+        const uint2 q = e4m3x8_of_bf16x8(__ldg(xr + v), s);
+        x_q[static_cast<size_t>(t) * d8 + v] = q;
+        for (int sl = 0; sl < k; ++sl) {
+            const int row = s_row[t * k + sl];
+            if (row >= 0) xs[static_cast<size_t>(row) * d8 + v] = q;
+        }
+    }
+    if (tid < k && s_row[t * k + tid] >= 0) xs_scales[s_row[t * k + tid]] = s;
+    if (tid == 0) x_scales[t] = s;
+    for (int j = R + t; j < n_routes; j += gridDim.x) {
+        for (int v = tid; v < d8; v += kSmallThreads) xs[static_cast<size_t>(j) * d8 + v] = make_uint2(0u, 0u);
+        if (tid == 0) xs_scales[j] = 0.f;
+    }
+}
+
 }  // namespace
 }  // namespace moe
+
+extern "C" moe_status moe_route_scatter_quant_small_e4m3(const float* logits, const void* x, const uint8_t* mask,
+                                                          int T, int E, int k, int d, int32_t* ids, float* w,
+                                                          int32_t* counts, int32_t* offsets, uint8_t* x_q,
+                                                          float* x_scales, uint8_t* xs, float* xs_scales,
+                                                          int32_t* row_of_route, int32_t* route_of_row,
+                                                          void* stream) {
+    using namespace moe;
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && d >= 16 && d % 16 == 0);
+    MOE_REQUIRE(T <= kSmallTokens && T * k <= kSmallRoutes);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(logits && x && ids && w && counts && offsets && x_q && x_scales && xs && xs_scales && row_of_route &&
+                route_of_row);
+    MOE_REQUIRE(aligned16(x) && aligned16(x_q) && aligned16(xs));
+    route_scatter_quant_small_e4m3_kernel<<<T, kSmallThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        logits, static_cast<const uint4*>(x), mask, T, E, k, d / 8, ids, w, counts, offsets,
+        reinterpret_cast<uint2*>(x_q), x_scales, reinterpret_cast<uint2*>(xs), xs_scales, row_of_route,
+        route_of_row);
+    return launch_status();
+}
 
 extern "C" moe_status moe_route_scatter_quant_small_fp4(const float* logits, const void* x, const uint8_t* mask,
                                                          int T, int E, int k, int d, int32_t* ids, float* w,

@@ -75,6 +75,7 @@ SIGNATURES = {
     "moe_scatter_rows_fp4": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P], _I),
     "moe_scatter_rows_quant_fp4": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P],
                                    _I),
+    "moe_route_scatter_quant_small_e4m3": ([_P, _P, _P, _I, _I, _I, _I] + [_P] * 11, _I),
     "moe_route_scatter_quant_small_fp4": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P,
                                            _P, _P, _P], _I),
     "moe_grouped_gate_up_w4a4": ([_P, _P, _I, _P, _P, _I, _I, _I, _I] + [_P] * 8, _I),
@@ -773,6 +774,23 @@ def moe_scatter_rows_e4m3(x_q, x_scales, ids, mask, offsets, xs, xs_scales, row_
     _check("moe_scatter_rows_e4m3", load().moe_scatter_rows_e4m3(
         _ptr(x_q), _ptr(x_scales), _ptr(ids), _ptr(mask), _ptr(offsets), T, k, d, E, _ptr(xs), _ptr(xs_scales),
         _ptr(row_of_route), _ptr(route_of_row), _ptr(ws), _stream(stream)))
+
+
+def moe_route_scatter_quant_small_e4m3(logits, x, mask, k: int, bufs: "MoEBuffersW8A8", stream=None):
+    """A1-A4 with E4M3 rows in one launch for small chunks (T <= 128, T*k <= 512), into ``bufs``."""
+    T, E = logits.shape
+    d = x.shape[1]
+    b = bufs
+    if (b.T, b.E, b.k, b.d) != (T, E, k, d):
+        raise ValueError("buffers were allocated for another shape")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(x, torch.bfloat16, (T, d), "x")
+    if mask is not None:
+        _expect(mask, torch.uint8, (T, k), "mask")
+    _check("moe_route_scatter_quant_small_e4m3", load().moe_route_scatter_quant_small_e4m3(
+        _ptr(logits), _ptr(x), _ptr(mask), T, E, k, d, _ptr(b.ids), _ptr(b.w), _ptr(b.counts), _ptr(b.offsets),
+        _ptr(b.x_q), _ptr(b.x_scales), _ptr(b.xs), _ptr(b.xs_scales), _ptr(b.row_of_route), _ptr(b.route_of_row),
+        _stream(stream)))
 
 
 def moe_scatter_rows_quant_e4m3(x, ids, mask, offsets, x_q, x_scales, xs, xs_scales, row_of_route, route_of_row,

@@ -189,3 +189,27 @@ def test_fused_quantizers_equal_the_weight_quantizer(T, E, k, d, f, p):
     M.moe_check_device_error()
     ref_h = M.moe_quantize_weights_fp8(h)
     assert torch.equal(codes, ref_h.codes) and torch.equal(scales, ref_h.scales)
+
+
+@pytest.mark.parametrize("T,E,k,d,p", [(4, 64, 6, 256, 0.0), (100, 8, 2, 256, 0.1), (64, 10, 8, 512, 0.3),
+                                       (128, 256, 4, 128, 0.0), (1, 4, 2, 4096, 0.0)])
+def test_small_chunk_routing_quantize_scatter_in_one_launch(T, E, k, d, p):
+    """moe_route_scatter_quant_small_e4m3 gives the routing outputs of moe_route_topk_offsets and the rows of
+    moe_scatter_rows_quant_e4m3, bit for bit."""
+    logits, mask, *_ = _case(T, E, k, 128, 128, p, seed=T + d)
+    x = (torch.randn(T, d) * 2).to(torch.bfloat16).cuda()
+    lg, md = logits.cuda(), None if mask is None else mask.cuda()
+    a = M.MoEBuffersW8A8(T, E, k, d, 128)
+    M.moe_route_topk_offsets(lg, md, k, a.ids, a.w, a.counts, a.offsets, a.ws)
+    M.moe_scatter_rows_quant_e4m3(x, a.ids, md, a.offsets, a.x_q, a.x_scales, a.xs, a.xs_scales, a.row_of_route,
+                                  a.route_of_row, a.ws)
+    b = M.MoEBuffersW8A8(T, E, k, d, 128)
+    b.xs.fill_(5)
+    b.xs_scales.fill_(float("nan"))
+    b.route_of_row.fill_(77)
+    M.moe_route_scatter_quant_small_e4m3(lg, x, md, k, b)
+    M.moe_check_device_error()
+    for name in ("ids", "counts", "offsets", "row_of_route", "route_of_row", "x_q", "xs"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    for name in ("w", "x_scales", "xs_scales"):
+        assert torch.equal(getattr(a, name).view(torch.int32), getattr(b, name).view(torch.int32)), name
