@@ -88,6 +88,8 @@ W4A4_CASES = [
     (150, 3, 2, 384, 256, 0.0),     # d = 384: K = 128 mod 256 in the down projection's partner; half-empty stage
     (20, 16, 4, 512, 512, 0.1),
     (4, 64, 6, 256, 256, 0.0),      # a verification-width batch
+    (12, 16, 4, 384, 384, 0.1),     # d and f = 128 mod 256 in a small chunk
+    (30, 1, 1, 256, 512, 0.0),      # one expert
     (700, 8, 2, 256, 256, 0.0),     # heavy experts: many 64-row slices
 ]
 
