@@ -14,8 +14,9 @@
 // quarter q of the accumulator reads them from its own quarter: the layout
 // is 32 lanes wide and repeated in each of the four lane quarters.  Four
 // scale warps (one per lane quarter) write it per stage from the scale words
-// the TMA brought into shared memory, then signal the MMA thread; scale groups
-// start at multiples of four columns.
+// the TMA brought into shared memory (on a barrier of their own, loaded ahead
+// of the codes), then signal the MMA thread; scale groups start at multiples
+// of four columns.
 //
 // Per stage (256 K): two 16 KB code tiles of 128 weight rows, up to 64
 // compact rows (8 KB), the weight rows' block-scale words (2 x 2 KB) and the
@@ -152,7 +153,8 @@ __global__ void __launch_bounds__(kNThreads, 1)
     uint64_t* acc_full = empty + kNStages;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* drain = acc_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sf_in = drain + 1;                     // a stage's block-scale words have landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_in + kNStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* issued = reinterpret_cast<int*>(tmem_slot + 2);
     int* item_off = issued + kNStages;               // E + 1 entries
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNStages; ++s) {
             mbar_init(&full[s], 1);
+            mbar_init(&sf_in[s], 1);
             mbar_init(&sf_full[s], kSfWarps);
             mbar_init(&empty[s], 1);
             issued[s] = -1;
@@ -270,7 +273,8 @@ __global__ void __launch_bounds__(kNThreads, 1)
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const Item item = item_at(it);
                 const int n16 = (item.rows + 15) / 16;
-                const uint32_t bytes = 2 * kCodeTile + n16 * 16 * 128 + 2 * kSfaTile + kMmasPerStage * sfb_rows * 4;
+                const uint32_t bytes = 2 * kCodeTile + n16 * 16 * 128;              // codes and rows
+                const uint32_t sf_bytes = 2 * kSfaTile + kMmasPerStage * sfb_rows * 4;   // their block scales
                 const int m0 = item.mt * fw;                  // first feature of tile 0
                 const int m1 = GATED ? m0 : m0 + NBM;         // tile 1: the up rows, or the next 128 features
                 const uint64_t pol_w = ntiles[item.e] > 1 ? pol_shared : pol_once;
@@ -280,21 +284,24 @@ __global__ void __launch_bounds__(kNThreads, 1)
                         break;
                     }
                     uint8_t* st = smem + s * stage_bytes;
-                    mbar_arrive_expect_tx(&full[s], bytes);
                     issued[s] = static_cast<int>(ph);
+                    // the small block-scale loads first, on their own barrier, so that the scale
+                    // warps have them in tensor memory by the time the codes land
+                    mbar_arrive_expect_tx(&sf_in[s], sf_bytes);
+                    tma_load_3d(st + off_sa0, &map_sa0, &sf_in[s], m0, js * kMmasPerStage, item.e, pol_w);
+                    tma_load_3d(st + off_sa1, &map_sa1, &sf_in[s], m1, js * kMmasPerStage, item.e, pol_w);
+                    tma_load_2d(st + off_sb, big ? &map_sb_big : &map_sb, &sf_in[s], item.row0 & ~3,
+                                js * kMmasPerStage, pol_x);
                     // codes: x = byte offset in the row (two values per byte); scales: 3-D (word, 64-K tile, expert)
+                    mbar_arrive_expect_tx(&full[s], bytes);
                     tma_load_2d(st, &map_a0, &full[s], js * 128, item.e * M + m0, pol_w);
                     tma_load_2d(st + kOffA1, &map_a1, &full[s], js * 128, item.e * M + m1, pol_w);
-                    tma_load_3d(st + off_sa0, &map_sa0, &full[s], m0, js * kMmasPerStage, item.e, pol_w);
-                    tma_load_3d(st + off_sa1, &map_sa1, &full[s], m1, js * kMmasPerStage, item.e, pol_w);
                     // the rows in as few boxes as possible: 64-row boxes, then 16-row ones
                     int r = 0;
                     for (; r + 64 <= n16 * 16; r += 64)
                         tma_load_2d(st + kOffB + r * 128, &map_b_big, &full[s], js * 128, item.row0 + r, pol_x);
                     for (; r < n16 * 16; r += 16)
                         tma_load_2d(st + kOffB + r * 128, &map_b, &full[s], js * 128, item.row0 + r, pol_x);
-                    tma_load_2d(st + off_sb, big ? &map_sb_big : &map_sb, &full[s], item.row0 & ~3,
-                                js * kMmasPerStage, pol_x);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -472,7 +479,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
         for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
             const int off = item_at(it).row0 & 3;   // the item's first row within the scale box
             for (int js = 0; js < n_st; ++js) {
-                if (!warp_wait_nvf4(&full[s], ph, abort_flag, err)) {
+                if (!warp_wait_nvf4(&sf_in[s], ph, abort_flag, err)) {
                     ok = false;
                     break;
                 }
@@ -515,7 +522,10 @@ __global__ void __launch_bounds__(kNThreads, 1)
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
         for (int s = 0; s < S; ++s)
-            if (issued[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued[s]));
+            if (issued[s] >= 0) {
+                mbar_drain(&full[s], static_cast<uint32_t>(issued[s]));
+                mbar_drain(&sf_in[s], static_cast<uint32_t>(issued[s]));
+            }
     }
     __syncthreads();
     if (warp == 1) {
