@@ -41,6 +41,11 @@ constexpr int kBTile = 128 * kRowBytes;  // 16 KB: the CTA's half of N rows
 constexpr int kStageBytes = 2 * kATile + kBTile;
 constexpr int kRingBytes = kPairStages * kStageBytes;  // 192 KB
 constexpr int kCtrlBytes = 4096;
+// The first kPairList items of a pair's hand-out sequence, decoded once at
+// the start: decoding an item takes a few microseconds of dependent
+// arithmetic and loads, which every role would otherwise pay between items.
+constexpr int kPairList = 512;
+constexpr int kListBytes = kPairList * 16;
 constexpr int kSmallBox = 16;            // rows per small TMA box
 constexpr int kLargeBox = 64;            // rows per large TMA box
 constexpr int kTmemCols = 512;           // gate (tile 0) at 0, up (tile 1) at 256; two 128-column slots each
@@ -52,7 +57,7 @@ struct PairCfg {
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kFeat = GATED ? 2 * PBM : 4 * PBM;  // output features per item (the pair's)
     static constexpr int kOutStage = GATED ? 2 * 32 * PBM * 2 : 0;   // a 32-row bf16 tile of h per group
-    static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kOutStage + 1024;
+    static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kListBytes + kOutStage + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
@@ -172,7 +177,8 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
     int* order = const_cast<int*>(epi_flag + 2);     // experts: the heavy ones, then the light ones (E entries)
     int* heavy_items = order + kMaxExperts;          // items of the heavy experts
     int* heavy_experts = heavy_items + 1;            // how many experts are heavy
-    __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kCtrlBytes);
+    Item* plist = reinterpret_cast<Item*>(ctrl + kCtrlBytes);   // this pair's items, in hand-out order
+    __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kCtrlBytes + kListBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -309,6 +315,12 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
         }
         return decode_item_ordered(u, item_off, order, ntiles, offsets, E, kPairSlice);
     };
+    // item j of this pair is hand-out position pair + j * n_pairs
+    const int n_list = pair < n_items ? min((n_items - pair + n_pairs - 1) / n_pairs, kPairList) : 0;
+    if (warp >= 2)
+        for (int j = threadIdx.x - 64; j < n_list; j += 32 * C::kEpiWarps) plist[j] = item_at(pair + j * n_pairs);
+    __syncthreads();
+    auto my_item = [&](int j, int it) { return j < kPairList ? plist[j] : item_at(it); };
 
     if (warp == 0) {
         // ---- TMA producer (both CTAs) ------------------------------------------
@@ -320,8 +332,8 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int it = pair; ok && it < n_items; it += n_pairs) {
-                const Item item = item_at(it);
+            for (int it = pair, j = 0; ok && it < n_items; it += n_pairs, ++j) {
+                const Item item = my_item(j, it);
                 const int nh = half_rows(item.rows);
                 const int my0 = item.row0 + static_cast<int>(rank) * nh;
                 const uint32_t bytes = 2 * kATile + nh * kRowBytes;   // this CTA's share of a stage
@@ -363,8 +375,8 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
             int toggle = 0;
             uint32_t use0 = 0, use1 = 0;
             bool ok = true;
-            for (int it = pair; ok && it < n_items; it += n_pairs) {
-                const Item item = item_at(it);
+            for (int it = pair, j = 0; ok && it < n_items; it += n_pairs, ++j) {
+                const Item item = my_item(j, it);
                 const int N = 2 * half_rows(item.rows);
                 const uint32_t idesc = F8 ? idesc_e4m3(2 * PBM, N) : idesc_bf16(2 * PBM, N);
                 const bool both = item.rows > 128;
@@ -425,7 +437,7 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
         uint32_t use0 = 0, use1 = 0;
         bool ok = true;
         for (int it = pair; it < n_items; it += n_pairs, ++local) {
-            const Item item = item_at(it);
+            const Item item = my_item(local, it);
             const bool both = item.rows > 128;
             const int slot = both ? 0 : toggle;
             const int buf = local & 1;
