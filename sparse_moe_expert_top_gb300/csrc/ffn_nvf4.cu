@@ -67,8 +67,13 @@ static_assert(kNStagesBig * kNStageBytesBig <= kNRingBytes, "both carve-ups fit 
 #define MOE_NVF4_BIG_MODE_PCT 50
 #endif
 constexpr int kNCtrlBytes = 4096;
+// The first kNList items of a CTA's hand-out sequence, decoded once at the
+// start (an item's decode -- a search over the experts and two loads of the
+// offsets -- takes microseconds under load, on every role's path between items).
+constexpr int kNList = 512;
+constexpr int kNListBytes = kNList * 16;
 constexpr int kNOutStage = 32 * NBM * 2;                  // gate/up: a 32-row x 128-feature bf16 tile of h
-constexpr int kNSmemBytes = kNRingBytes + kNCtrlBytes + kNOutStage + 1024;
+constexpr int kNSmemBytes = kNRingBytes + kNCtrlBytes + kNListBytes + kNOutStage + 1024;
 static_assert(kNSmemBytes <= 232448, "shared memory budget of one CTA");
 constexpr int kNTmemCols = 512;
 constexpr int kAccCols = 64;                              // one item slot of one weight tile
@@ -161,7 +166,8 @@ __global__ void __launch_bounds__(kNThreads, 1)
     int* ntiles = item_off + kMaxExperts + 1;        // E entries
     volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
     int* mode_big = const_cast<int*>(epi_flag + 2);   // launch-wide carve-up
-    __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kNCtrlBytes);
+    Item* ilist = reinterpret_cast<Item*>(ctrl + kNCtrlBytes);   // this CTA's items, in hand-out order
+    __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kNCtrlBytes + kNListBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int fw = GATED ? NBM : 2 * NBM;            // output features per item
@@ -260,6 +266,16 @@ __global__ void __launch_bounds__(kNThreads, 1)
     const int off_sb = off_sa1 + kSfaTile;
     const int sfb_rows = big ? kSfbRowsBig : kSfbRows;
     auto item_at = [&](int it) { return decode_item(it, item_off, ntiles, offsets, E, big ? kSliceBig : kSliceN); };
+    // item j of this CTA is hand-out position blockIdx.x + j * gridDim.x
+    const int n_list = static_cast<int>(blockIdx.x) < n_items
+                           ? min((n_items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                     static_cast<int>(gridDim.x),
+                                 kNList)
+                           : 0;
+    if (warp >= 2)
+        for (int j = threadIdx.x - 64; j < n_list; j += kNThreads - 64) ilist[j] = item_at(blockIdx.x + j * gridDim.x);
+    __syncthreads();
+    auto my_item = [&](int j, int it) { return j < kNList ? ilist[j] : item_at(it); };
 
     if (warp == 0) {
         // ---- TMA producer --------------------------------------------------------
@@ -270,8 +286,8 @@ __global__ void __launch_bounds__(kNThreads, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const Item item = item_at(it);
+            for (int it = blockIdx.x, j = 0; ok && it < n_items; it += gridDim.x, ++j) {
+                const Item item = my_item(j, it);
                 const int n16 = (item.rows + 15) / 16;
                 const uint32_t bytes = 2 * kCodeTile + n16 * 16 * 128;              // codes and rows
                 const uint32_t sf_bytes = 2 * kSfaTile + kMmasPerStage * sfb_rows * 4;   // their block scales
@@ -317,8 +333,8 @@ __global__ void __launch_bounds__(kNThreads, 1)
             int slot = 0;
             uint32_t use0 = 0, use1 = 0;   // uses of each accumulator slot so far
             bool ok = true;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const Item item = item_at(it);
+            for (int it = blockIdx.x, j = 0; ok && it < n_items; it += gridDim.x, ++j) {
+                const Item item = my_item(j, it);
                 const int N = (item.rows + 15) / 16 * 16;
                 const uint32_t idesc = idesc_nvf4(NBM, N);
                 // an item of more than 64 rows takes both slots (128 columns per weight tile)
@@ -377,7 +393,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
         uint32_t use0 = 0, use1 = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
-            const Item item = item_at(it);
+            const Item item = my_item(local, it);
             const int buf = local & 1;
             const bool both = item.rows > kSliceN;
             if (both) slot = 0;
@@ -476,8 +492,8 @@ __global__ void __launch_bounds__(kNThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            const int off = item_at(it).row0 & 3;   // the item's first row within the scale box
+        for (int it = blockIdx.x, j = 0; ok && it < n_items; it += gridDim.x, ++j) {
+            const int off = my_item(j, it).row0 & 3;   // the item's first row within the scale box
             for (int js = 0; js < n_st; ++js) {
                 if (!warp_wait_nvf4(&sf_in[s], ph, abort_flag, err)) {
                     ok = false;
