@@ -166,6 +166,11 @@ struct Cfg {
     static constexpr int kRingBytes = 4 * (kA * kATileBytes + BN * BK * 2);  // = 3 x 64 KB
     static constexpr int kTmemCols = 512;
     static constexpr int kCtrlBytes = 4096;  // barriers, TMEM slot, flags, item table (<= 3.3 KB)
+    // the first kList items of the CTA's hand-out sequence, decoded once at
+    // the start (a decode -- a search over the experts and two loads of the
+    // offsets -- takes microseconds under load, on every role's path between items)
+    static constexpr int kList = 512;
+    static constexpr int kListBytes = kList * 16;
     // gate/up: a 32-row x 128-feature bf16 tile of h staged for row-contiguous
     // stores, then (narrow items) the up half of a stacked tile, 64 features x 32
     // rows of fp32 padded to 33 columns
@@ -174,7 +179,7 @@ struct Cfg {
     // or the combine warps' barriers, list of completed tokens and their
     // compact rows (down)
     static constexpr int kFusedBytes = GATED ? 2048 : 1024 + 2 * BN * 4 + 2 * BN * kMaxK * 4;
-    static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kOutStageBytes + 1024;
+    static constexpr int kSmemBytes = kRingBytes + kCtrlBytes + kListBytes + kOutStageBytes + 1024;
     static constexpr int smem_bytes(bool fused) { return kSmemBytes + (fused ? kFusedBytes : 0); }
     static_assert(kSmemBytes + kFusedBytes <= 232448, "shared memory budget of one CTA");
     static_assert(kRingBytes == 3 * (kA * kATileBytes + 2 * BN * BK * 2), "both carve-ups fill the ring");
@@ -215,9 +220,11 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
     volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
     int* mode_big = const_cast<int*>(reinterpret_cast<volatile int*>(epi_flag + 2));   // launch-wide carve-up
     int* order = mode_big + 1;   // experts by descending row count (E entries; row counts while ranking)
-    __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + C::kCtrlBytes);  // gate/up only
-    float* up_stage = reinterpret_cast<float*>(ctrl + C::kCtrlBytes + 32 * BM * 2);     // narrow gate/up only
-    uint8_t* fused_smem = ctrl + C::kCtrlBytes + C::kOutStageBytes;
+    Item* ilist = reinterpret_cast<Item*>(ctrl + C::kCtrlBytes);   // this CTA's items, in hand-out order
+    uint8_t* after_list = ctrl + C::kCtrlBytes + C::kListBytes;
+    __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(after_list);  // gate/up only
+    float* up_stage = reinterpret_cast<float*>(after_list + 32 * BM * 2);     // narrow gate/up only
+    uint8_t* fused_smem = after_list + C::kOutStageBytes;
     int* tok_s = reinterpret_cast<int*>(fused_smem);                  // gather: token of each row of the item
     uint64_t* comb_done = reinterpret_cast<uint64_t*>(fused_smem);    // combine: an item's y rows are stored (2)
     uint64_t* comb_free = comb_done + 2;                               // combine: that barrier phase was consumed (2)
@@ -375,6 +382,16 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
     const int n_st = n_kb / kpb;             // stages per item (K is a multiple of 128)
     const int slice = big ? 2 * BN : BN;                           // rows per work item at most
     auto item_at = [&](int it) { return decode_item_ordered(it, item_off, order, ntiles, offsets, E, slice); };
+    // item j of this CTA is hand-out position blockIdx.x + j * gridDim.x
+    const int n_list = static_cast<int>(blockIdx.x) < n_items
+                           ? min((n_items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                     static_cast<int>(gridDim.x),
+                                 C::kList)
+                           : 0;
+    if (warp >= 2)
+        for (int j = threadIdx.x - 64; j < n_list; j += blockDim.x - 64) ilist[j] = item_at(blockIdx.x + j * gridDim.x);
+    __syncthreads();
+    auto my_item = [&](int j, int it) { return j < C::kList ? ilist[j] : item_at(it); };
 
     if (warp == 0) {
         // ---- TMA producer -------------------------------------------------
@@ -385,8 +402,8 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const Item item = item_at(it);
+            for (int it = blockIdx.x, j = 0; ok && it < n_items; it += gridDim.x, ++j) {
+                const Item item = my_item(j, it);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
                 const int row_bytes = n16 * kBoxRows * BK * 2;   // one k-block of the item's rows
                 // (the fused gate/up kernel's rows come from the gather warp)
@@ -440,8 +457,8 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
             int toggle = 0;            // slot of the next light item
             uint32_t use0 = 0, use1 = 0;  // uses of each accumulator slot so far
             bool ok = true;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-                const Item item = item_at(it);
+            for (int it = blockIdx.x, j = 0; ok && it < n_items; it += gridDim.x, ++j) {
+                const Item item = my_item(j, it);
                 const int n16 = (item.rows + kBoxRows - 1) / kBoxRows;
                 const uint32_t idesc = F8 ? idesc_e4m3(BM, n16 * kBoxRows) : idesc_bf16(BM, n16 * kBoxRows);
                 const bool both = item.rows > BN;
@@ -531,7 +548,7 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
         uint32_t use0 = 0, use1 = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
-            const Item item = item_at(it);
+            const Item item = my_item(local, it);
             const bool both = item.rows > BN;
             const int slot = both ? 0 : toggle;
             const int buf = local & 1;  // flag parity
@@ -696,8 +713,8 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            const Item item = item_at(it);
+        for (int it = blockIdx.x, j = 0; ok && it < n_items; it += gridDim.x, ++j) {
+            const Item item = my_item(j, it);
             const int N = (item.rows + kBoxRows - 1) / kBoxRows * kBoxRows;
             const int row_bytes = N * BK * 2;
             // the token of every row; padding rows repeat the first row
@@ -754,7 +771,7 @@ __global__ void __launch_bounds__(Roles<GATED, FUSED>::kThreads, 1)
         float4* out4 = reinterpret_cast<float4*>(fa.out);
         int local = 0;
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
-            const Item item = item_at(it);
+            const Item item = my_item(local, it);
             const int b = local & 1;
             if (ct == 0) *comb_flag = mbar_wait(&comb_done[b], (local >> 1) & 1u, abort_flag, err) ? 1 : 0;
             combine_sync();
