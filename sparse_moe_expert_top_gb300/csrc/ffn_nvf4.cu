@@ -411,11 +411,23 @@ __global__ void __launch_bounds__(kNThreads, 1)
             const int m = item.mt * fw + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(slot * kAccCols);
+            bool released = false;
             for (int c0 = 0; c0 < item.rows; c0 += 32) {
                 uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
                 tmem_ld32(taddr + 2 * kAccCols + c0, g1);
                 tmem_ld_wait();
+                if (c0 + 32 >= item.rows) {
+                    // last chunk: the warp's tensor-memory reads of the item are done,
+                    // so the slots go back to the MMA thread before this chunk's stores
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&acc_empty[slot]);
+                        if (both) mbar_arrive(&acc_empty[1]);
+                    }
+                    released = true;
+                }
                 float rs[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) rs[j] = c0 + j < item.rows ? __ldg(sb + item.row0 + c0 + j) : 0.f;
@@ -458,11 +470,13 @@ __global__ void __launch_bounds__(kNThreads, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&acc_empty[slot]);
-                if (both) mbar_arrive(&acc_empty[1]);
+            if (!released) {   // an item without rows
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&acc_empty[slot]);
+                    if (both) mbar_arrive(&acc_empty[1]);
+                }
             }
             if (slot) ++use1;
             else ++use0;
