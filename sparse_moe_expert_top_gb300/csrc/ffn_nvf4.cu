@@ -411,21 +411,24 @@ __global__ void __launch_bounds__(kNThreads, 1)
             const int m = item.mt * fw + q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(slot * kAccCols);
+            // the slots go back to the MMA thread as soon as the warp's tensor-memory
+            // reads of the item are done, before its last chunk's stores
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&acc_empty[slot]);
+                    if (both) mbar_arrive(&acc_empty[1]);
+                }
+            };
             bool released = false;
             for (int c0 = 0; c0 < item.rows; c0 += 32) {
                 uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
                 tmem_ld32(taddr + 2 * kAccCols + c0, g1);
                 tmem_ld_wait();
-                if (c0 + 32 >= item.rows) {
-                    // last chunk: the warp's tensor-memory reads of the item are done,
-                    // so the slots go back to the MMA thread before this chunk's stores
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&acc_empty[slot]);
-                        if (both) mbar_arrive(&acc_empty[1]);
-                    }
+                if (c0 + 32 >= item.rows) {   // the last chunk
+                    release();
                     released = true;
                 }
                 float rs[32];
@@ -470,14 +473,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
                     }
                 }
             }
-            if (!released) {   // an item without rows
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&acc_empty[slot]);
-                    if (both) mbar_arrive(&acc_empty[1]);
-                }
-            }
+            if (!released) release();   // an item without rows
             if (slot) ++use1;
             else ++use0;
             if (both) {

@@ -458,23 +458,26 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(slot * 128);
             // down: the second group only for 256-row items (light items' stores are few)
             const int n_groups = (GATED || both) ? 2 : 1;
+            // Hands the accumulator slots back to the MMA thread of the even CTA,
+            // once per warp and item, as soon as the warp's tensor-memory reads of
+            // the item are done: before its last chunk's stores, which need no
+            // ordering against the next MMAs.
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_remote_relaxed(acc_empty_lead + 8u * static_cast<uint32_t>(slot));
+                    if (both) mbar_arrive_remote_relaxed(acc_empty_lead + 8u);
+                }
+            };
             bool released = false;
             for (int c0 = 32 * grp; grp < n_groups && c0 < item.rows; c0 += 32 * n_groups) {
                 uint32_t g[32], g1[32];
                 tmem_ld32(taddr + c0, g);
                 tmem_ld32(taddr + 256 + c0, g1);
                 tmem_ld_wait();
-                if (c0 + 32 * n_groups >= item.rows) {
-                    // the warp's last chunk of the item: its tensor-memory reads are
-                    // done, so the accumulator slots go back to the MMA thread of the
-                    // even CTA before this chunk's stores (the h / y stores need no
-                    // ordering against the next MMAs)
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive_remote_relaxed(acc_empty_lead + 8u * static_cast<uint32_t>(slot));
-                        if (both) mbar_arrive_remote_relaxed(acc_empty_lead + 8u);
-                    }
+                if (c0 + 32 * n_groups >= item.rows) {   // the warp's last chunk of the item
+                    release();
                     released = true;
                 }
                 float rs[32];
@@ -529,15 +532,7 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
                     }
                 }
             }
-            if (!released) {
-                // a warp without a chunk of this item
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive_remote_relaxed(acc_empty_lead + 8u * static_cast<uint32_t>(slot));
-                    if (both) mbar_arrive_remote_relaxed(acc_empty_lead + 8u);
-                }
-            }
+            if (!released) release();   // a warp without a chunk of this item
             if (slot) ++use1;
             else ++use0;
             if (both) {
