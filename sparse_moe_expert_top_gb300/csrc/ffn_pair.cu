@@ -41,11 +41,18 @@ constexpr int kBTile = 128 * kRowBytes;  // 16 KB: the CTA's half of N rows
 constexpr int kStageBytes = 2 * kATile + kBTile;
 constexpr int kRingBytes = kPairStages * kStageBytes;  // 192 KB
 constexpr int kCtrlBytes = 4096;
-// The first kPairList items of a pair's hand-out sequence, decoded once at
-// the start: decoding an item takes a few microseconds of dependent
-// arithmetic and loads, which every role would otherwise pay between items.
-constexpr int kPairList = 512;
-constexpr int kListBytes = kPairList * 16;
+// Dynamic hand-out: the even CTA's producer takes each next position of the
+// hand-out order from a per-launch counter and publishes the decoded item in
+// a ring of kSched slots of both CTAs (one mbarrier per slot).  The decode
+// reads shared copies of the offsets and of the block starts of the order.
+constexpr int kSched = 16;
+constexpr int kListBytes = 8192;
+constexpr int kSchedOff = 0;                                   // kSched items of 16 bytes
+constexpr int kItemFullOff = kSchedOff + kSched * 16;          // kSched mbarriers
+constexpr int kOffsOff = kItemFullOff + kSched * 8;            // offsets[0 .. E]
+constexpr int kBstartOff = kOffsOff + (kMaxExperts + 4) * 4;   // block starts of the hand-out order
+constexpr int kBstartCap = (kListBytes - kBstartOff) / 4;
+static_assert(kBstartCap > 1024, "room for the block-start table");
 constexpr int kSmallBox = 16;            // rows per small TMA box
 constexpr int kLargeBox = 64;            // rows per large TMA box
 constexpr int kTmemCols = 512;           // gate (tile 0) at 0, up (tile 1) at 256; two 128-column slots each
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
                     const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_big,
                     const int32_t* __restrict__ offsets, int cap, int E, int K, int M, void* __restrict__ out,
                     unsigned* err, const float* __restrict__ sa0, const float* __restrict__ sa1,
-                    const float* __restrict__ sb) {
+                    const float* __restrict__ sb, int* __restrict__ ticket) {
     using C = PairCfg<GATED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
@@ -177,7 +184,11 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
     int* order = const_cast<int*>(epi_flag + 2);     // experts: the heavy ones, then the light ones (E entries)
     int* heavy_items = order + kMaxExperts;          // items of the heavy experts
     int* heavy_experts = heavy_items + 1;            // how many experts are heavy
-    Item* plist = reinterpret_cast<Item*>(ctrl + kCtrlBytes);   // this pair's items, in hand-out order
+    uint8_t* lreg = ctrl + kCtrlBytes;
+    Item* sched = reinterpret_cast<Item*>(lreg + kSchedOff);               // published items, slot j % kSched
+    uint64_t* item_full = reinterpret_cast<uint64_t*>(lreg + kItemFullOff);
+    int* soffs = reinterpret_cast<int*>(lreg + kOffsOff);
+    int* bstart = reinterpret_cast<int*>(lreg + kBstartOff);
     __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kCtrlBytes + kListBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -198,6 +209,7 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 2 * C::kEpiWarps);   // the epilogue warps of both CTAs
         }
+        for (int i = 0; i < kSched; ++i) mbar_init(&item_full[i], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -292,14 +304,21 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
     // then the next floor((b+1) L / G) - floor(b L / G) light items (L light
     // items, G groups).  Block b starts at position
     //   B(b) = item_off[b / n_mt] + (b % n_mt) * ntiles + floor(b L / G).
+    const bool table = n_groups <= kBstartCap;
+    auto block_start_of = [&](int b) {
+        const int ei = b / n_mt, mt = b - ei * n_mt;
+        return item_off[ei] + mt * ntiles[order[ei]] + static_cast<int>(static_cast<long long>(b) * n_light / n_groups);
+    };
+    if (warp >= 2) {
+        // shared copies for the decode: the block starts and the offsets
+        for (int b = threadIdx.x - 64; table && b < n_groups; b += 32 * C::kEpiWarps) bstart[b] = block_start_of(b);
+        for (int e = threadIdx.x - 64; e <= E; e += 32 * C::kEpiWarps) soffs[e] = offsets[e];
+    }
+    __syncthreads();
     auto item_at = [&](int p) {
         int u = p;
         if (n_groups > 0) {
-            auto block_start = [&](int b) {
-                const int ei = b / n_mt, mt = b - ei * n_mt;
-                return item_off[ei] + mt * ntiles[order[ei]] +
-                       static_cast<int>(static_cast<long long>(b) * n_light / n_groups);
-            };
+            auto block_start = [&](int b) { return table ? bstart[b] : block_start_of(b); };
             int lo = 0, hi = n_groups - 1;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -308,19 +327,53 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
             }
             const int ei = lo / n_mt, mt = lo - ei * n_mt;
             const int size = ntiles[order[ei]];
-            const int o = p - block_start(lo);
-            u = o < size ? item_off[ei] + mt * size + o
-                         : n_heavy_items + static_cast<int>(static_cast<long long>(lo) * n_light / n_groups) +
-                               (o - size);
+            const int head = item_off[ei] + mt * size;    // the group's first item
+            const int b0 = block_start(lo);
+            const int o = p - b0;
+            // light items handed out before block lo: b0 - head
+            u = o < size ? head + o : n_heavy_items + (b0 - head) + (o - size);
         }
-        return decode_item_ordered(u, item_off, order, ntiles, offsets, E, kPairSlice);
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (item_off[mid] <= u) lo = mid;
+            else hi = mid - 1;
+        }
+        Item r;
+        r.e = order[lo];
+        const int local = u - item_off[lo];
+        const int n = ntiles[r.e];
+        r.mt = local / n;
+        const int nt = local - r.mt * n;
+        r.row0 = soffs[r.e] + nt * kPairSlice;
+        r.rows = min(kPairSlice, soffs[r.e + 1] - r.row0);
+        return r;
     };
-    // item j of this pair is hand-out position pair + j * n_pairs
-    const int n_list = pair < n_items ? min((n_items - pair + n_pairs - 1) / n_pairs, kPairList) : 0;
-    if (warp >= 2)
-        for (int j = threadIdx.x - 64; j < n_list; j += 32 * C::kEpiWarps) plist[j] = item_at(pair + j * n_pairs);
-    __syncthreads();
-    auto my_item = [&](int j, int it) { return j < kPairList ? plist[j] : item_at(it); };
+
+    // Item j of this pair: the even CTA's producer takes hand-out position
+    // `pair` first, then n_pairs + (the counter's next value) for each further
+    // item, and publishes the decoded item (e = -1 past the last position) in
+    // slot j % kSched of both CTAs; every other role waits for the slot.  No
+    // role is kSched items behind the producer: the producer runs at most the
+    // stage ring ahead of the MMA thread, which runs at most two items ahead of
+    // the epilogues of both CTAs.
+    auto publish = [&](int j, const Item& it) {
+        const int q = j % kSched;
+        sched[q] = it;
+        mbar_arrive(&item_full[q]);
+        // the odd CTA's copy: an asynchronous store that completes on its slot barrier
+        const uint32_t rbar = map_to_rank(smem_u32(&item_full[q]), 1);
+        const uint32_t rdst = map_to_rank(smem_u32(&sched[q]), 1);
+        asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], 16;" ::"r"(rbar)
+                     : "memory");
+        asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                         rdst),
+                     "r"(it.e), "r"(it.mt), "r"(it.row0), "r"(it.rows), "r"(rbar)
+                     : "memory");
+    };
+    auto wait_item = [&](int j) {
+        return mbar_wait(&item_full[j % kSched], static_cast<uint32_t>(j / kSched) & 1u, abort_flag, err);
+    };
 
     if (warp == 0) {
         // ---- TMA producer (both CTAs) ------------------------------------------
@@ -332,8 +385,25 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int it = pair, j = 0; ok && it < n_items; it += n_pairs, ++j) {
-                const Item item = my_item(j, it);
+            int t_next = pair;
+            for (int j = 0; ok; ++j) {
+                Item item;
+                if (rank == 0) {
+                    const int t = t_next;
+                    // the next position now, used one item later (the atomic's latency hides behind this item)
+                    if (t < n_items) t_next = n_pairs + atomicAdd(ticket, 1);
+                    if (t < n_items) {
+                        item = item_at(t);
+                    } else {
+                        item.e = -1;
+                        item.mt = item.row0 = item.rows = 0;
+                    }
+                    publish(j, item);
+                } else {
+                    if (!wait_item(j)) break;
+                    item = sched[j % kSched];
+                }
+                if (item.e < 0) break;
                 const int nh = half_rows(item.rows);
                 const int my0 = item.row0 + static_cast<int>(rank) * nh;
                 const uint32_t bytes = 2 * kATile + nh * kRowBytes;   // this CTA's share of a stage
@@ -375,8 +445,10 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
             int toggle = 0;
             uint32_t use0 = 0, use1 = 0;
             bool ok = true;
-            for (int it = pair, j = 0; ok && it < n_items; it += n_pairs, ++j) {
-                const Item item = my_item(j, it);
+            for (int j = 0; ok; ++j) {
+                if (!wait_item(j)) break;
+                const Item item = sched[j % kSched];
+                if (item.e < 0) break;
                 const int N = 2 * half_rows(item.rows);
                 const uint32_t idesc = F8 ? idesc_e4m3(2 * PBM, N) : idesc_bf16(2 * PBM, N);
                 const bool both = item.rows > 128;
@@ -436,21 +508,41 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
         int toggle = 0;
         uint32_t use0 = 0, use1 = 0;
         bool ok = true;
-        for (int it = pair; it < n_items; it += n_pairs, ++local) {
-            const Item item = my_item(local, it);
-            const bool both = item.rows > 128;
-            const int slot = both ? 0 : toggle;
+        for (;; ++local) {
             const int buf = local & 1;
             if (et == 0) {
-                bool got = mbar_wait(&acc_full[slot], (slot ? use1 : use0) & 1u, abort_flag, err);
-                if (got && both) got = mbar_wait(&acc_full[1], use1 & 1u, abort_flag, err);
-                epi_flag[buf] = got ? 1 : 0;
+                // 1: the item's accumulators are ready; 2: no further item; 0: a wait timed out
+                int flag = wait_item(local) ? 1 : 0;
+                if (flag) {
+                    const Item it0 = sched[local % kSched];
+                    if (it0.e < 0) {
+                        flag = 2;
+                    } else {
+                        const bool both0 = it0.rows > 128;
+                        const int slot0 = both0 ? 0 : toggle;
+                        bool got = mbar_wait(&acc_full[slot0], (slot0 ? use1 : use0) & 1u, abort_flag, err);
+                        if (got && both0) got = mbar_wait(&acc_full[1], use1 & 1u, abort_flag, err);
+                        flag = got ? 1 : 0;
+                    }
+                }
+                epi_flag[buf] = flag;
             }
             epilogue_sync_n_pair(kEpiThreads);
-            if (!epi_flag[buf]) {
+            const int flag = epi_flag[buf];
+            if (flag == 2) break;
+            if (flag == 0) {
                 ok = false;
                 break;
             }
+            // the slot's phase has completed (seen by thread 0 of the epilogue): each
+            // thread takes it too before reading the slot
+            for (int spin = 0;
+                 spin < 4096 && !mbar_try_wait(smem_u32(&item_full[local % kSched]), static_cast<uint32_t>(local / kSched) & 1u);
+                 ++spin) {
+            }
+            const Item item = sched[local % kSched];
+            const bool both = item.rows > 128;
+            const int slot = both ? 0 : toggle;
             tc_fence_after();
             // this CTA's features: tile 0 at fb + [0, 128), tile 1 (down) at fb + 256 + [0, 128)
             const int fb = item.mt * C::kFeat + static_cast<int>(rank) * PBM;
@@ -589,6 +681,29 @@ struct PairCache {
 std::mutex g_pair_mutex;
 PairCache g_pair_cache[64][4];
 
+// Hand-out counters, one 128-byte line per launch slot.  Each launch takes
+// the next slot (so launches on different streams do not share a counter)
+// and clears it on its stream just before the kernel.
+constexpr int kTicketSlots = 64;
+__device__ int g_pair_tickets[kTicketSlots * 32];
+int* g_ticket_base[64];
+unsigned long long g_ticket_ctx[64];
+unsigned g_ticket_seq[64];
+
+moe_status next_ticket(int dev, unsigned long long ctx, cudaStream_t st, int** out) {
+    std::lock_guard<std::mutex> lock(g_pair_mutex);
+    if (g_ticket_base[dev] == nullptr || g_ticket_ctx[dev] != ctx) {
+        void* p = nullptr;
+        MOE_CUDA_TRY(cudaGetSymbolAddress(&p, g_pair_tickets));
+        g_ticket_base[dev] = static_cast<int*>(p);
+        g_ticket_ctx[dev] = ctx;
+    }
+    int* t = g_ticket_base[dev] + (g_ticket_seq[dev]++ % kTicketSlots) * 32;
+    MOE_CUDA_TRY(cudaMemsetAsync(t, 0, sizeof(int), st));
+    *out = t;
+    return MOE_OK;
+}
+
 template <bool GATED, bool F8>
 moe_status launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& bb,
                        const int32_t* offsets, int cap, int E, int K, int M, void* out, const float* sa0,
@@ -628,9 +743,11 @@ moe_status launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
         pairs = pc.pairs;
     }
     if (pairs < 1) return MOE_ERR_UNSUPPORTED;
+    int* ticket = nullptr;
+    if ((s = next_ticket(dev, ctx, st, &ticket)) != MOE_OK) return s;
     cfg.gridDim = dim3(2 * pairs);
     MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a0, a1, b, bb, offsets, cap, E, K, M, out, di.error_word, sa0, sa1,
-                                    sb));
+                                    sb, ticket));
     return MOE_OK;
 }
 
