@@ -138,3 +138,31 @@ def test_pair_kernels_reject_inconsistent_offsets():
         M.moe_check_device_error()
     assert exc.value.status == M.MOE_ERR_INVALID_ARG
     M.moe_check_device_error()  # the error word was cleared
+
+
+@pytest.mark.slow
+def test_pair_many_heavy_groups():
+    """Every expert heavy and seven 256-feature tiles of gate/up each: 1,792 heavy groups, more than the
+    shared block-start table of the dynamic hand-out holds, so the decode computes the block starts itself."""
+    T, E, k, d, f = 16384, 256, 6, 128, 1792
+    assert M.moe_ffn_paired(T * k)
+    g = torch.Generator().manual_seed(77)
+    logits = torch.randn(T, E, generator=g)          # uniform routing: ~384 rows per expert
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(E, f, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    wu = (torch.randn(E, f, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    wd = (torch.randn(E, d, f, generator=g) / f ** 0.5).to(torch.bfloat16)
+    bufs = M.MoEBuffers(T, E, k, d, f, torch.bfloat16)
+    out = M.moe_forward(logits.cuda(), x.cuda(), None, wg.cuda(), wu.cuda(), wd.cuda(), k, bufs)
+    M.moe_check_device_error()
+    w = (to_np(wg), to_np(wu), to_np(wd))
+    ref = mo.moe_forward(logits.numpy(), to_np(x), w, k, None)
+    counts = ref["counts"]
+    assert counts.min() > 256            # every expert has more than one 256-row slice
+    for key in ("ids", "counts", "offsets", "row_of_route", "route_of_row"):
+        assert np.array_equal(to_np(getattr(bufs, key)), ref[key]), key
+    R = int(ref["offsets"][-1])
+    assert_close_bf16_rounded(bufs.h[:R], ref["h"])
+    y_ref = mo.grouped_down(bufs.h[:R].cpu(), ref["offsets"], w)
+    assert_close(bufs.y[:R], y_ref, "bf16")
+    assert_close(out, mo.combine(y_ref, ref["row_of_route"], ref["w"], T, k), "bf16")
