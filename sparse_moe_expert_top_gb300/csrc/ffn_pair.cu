@@ -650,6 +650,14 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) {
+        // the last CTA out clears the launch's counter line for the next launch on it
+        __threadfence();
+        if (atomicAdd(ticket + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            ticket[0] = 0;
+            ticket[1] = 0;
+        }
+    }
+    if (threadIdx.x == 0) {
         if (rank == 0 && *abort_flag) {
             // copies still in flight (both CTAs' shares count on these barriers)
             for (int s = 0; s < kPairStages; ++s)
@@ -681,16 +689,18 @@ struct PairCache {
 std::mutex g_pair_mutex;
 PairCache g_pair_cache[64][4];
 
-// Hand-out counters, one 128-byte line per launch slot.  Each launch takes
-// the next slot (so launches on different streams do not share a counter)
-// and clears it on its stream just before the kernel.
+// Hand-out counters: one 128-byte line per launch slot ([0] the counter,
+// [1] the CTAs done).  Each launch takes the next line, so that launches on
+// different streams do not share one, and the last CTA of a launch clears
+// its line for the next launch on it.  (A captured graph keeps its line:
+// replays of one graph run one after another.)
 constexpr int kTicketSlots = 64;
 __device__ int g_pair_tickets[kTicketSlots * 32];
 int* g_ticket_base[64];
 unsigned long long g_ticket_ctx[64];
 unsigned g_ticket_seq[64];
 
-moe_status next_ticket(int dev, unsigned long long ctx, cudaStream_t st, int** out) {
+moe_status next_ticket(int dev, unsigned long long ctx, int** out) {
     std::lock_guard<std::mutex> lock(g_pair_mutex);
     if (g_ticket_base[dev] == nullptr || g_ticket_ctx[dev] != ctx) {
         void* p = nullptr;
@@ -698,9 +708,7 @@ moe_status next_ticket(int dev, unsigned long long ctx, cudaStream_t st, int** o
         g_ticket_base[dev] = static_cast<int*>(p);
         g_ticket_ctx[dev] = ctx;
     }
-    int* t = g_ticket_base[dev] + (g_ticket_seq[dev]++ % kTicketSlots) * 32;
-    MOE_CUDA_TRY(cudaMemsetAsync(t, 0, sizeof(int), st));
-    *out = t;
+    *out = g_ticket_base[dev] + (g_ticket_seq[dev]++ % kTicketSlots) * 32;
     return MOE_OK;
 }
 
@@ -744,7 +752,7 @@ moe_status launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
     }
     if (pairs < 1) return MOE_ERR_UNSUPPORTED;
     int* ticket = nullptr;
-    if ((s = next_ticket(dev, ctx, st, &ticket)) != MOE_OK) return s;
+    if ((s = next_ticket(dev, ctx, &ticket)) != MOE_OK) return s;
     cfg.gridDim = dim3(2 * pairs);
     MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a0, a1, b, bb, offsets, cap, E, K, M, out, di.error_word, sa0, sa1,
                                     sb, ticket));
