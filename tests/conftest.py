@@ -1,5 +1,6 @@
 import os
 import sys
+import zlib
 
 import pytest
 
@@ -26,3 +27,11 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _seed_default_generator(request):
+    """Each test draws from torch's default generator seeded by its own id, so
+    that its inputs do not depend on which tests ran before it."""
+    import torch
+    torch.manual_seed(zlib.crc32(request.node.nodeid.encode()) & 0x7FFFFFFF)
