@@ -301,13 +301,15 @@ __global__ void __launch_bounds__(PairCfg<GATED>::kThreads, 1)
     // The hand-out order is a sequence of blocks, one per heavy group b (in
     // expert, feature-tile order): the group's row slices, consecutive so
     // that pairs running them at the same time share its weight tiles in L2,
-    // then the next floor((b+1) L / G) - floor(b L / G) light items (L light
-    // items, G groups).  Block b starts at position
-    //   B(b) = item_off[b / n_mt] + (b % n_mt) * ntiles + floor(b L / G).
+    // then light items in proportion to the group's slices, so that heavy
+    // and light items keep one ratio along the whole order.  With H_b the
+    // heavy items before block b (H of them, L light ones), block b starts at
+    //   B(b) = H_b + floor(H_b L / H),  H_b = item_off[b / n_mt] + (b % n_mt) * ntiles.
     const bool table = n_groups <= kBstartCap;
     auto block_start_of = [&](int b) {
         const int ei = b / n_mt, mt = b - ei * n_mt;
-        return item_off[ei] + mt * ntiles[order[ei]] + static_cast<int>(static_cast<long long>(b) * n_light / n_groups);
+        const int hb = item_off[ei] + mt * ntiles[order[ei]];
+        return hb + static_cast<int>(static_cast<long long>(hb) * n_light / n_heavy_items);
     };
     if (warp >= 2) {
         // shared copies for the decode: the block starts and the offsets
