@@ -139,6 +139,46 @@ __device__ __forceinline__ bool warp_wait_nvf4(uint64_t* bar, uint32_t parity, v
 // A0 = w_down, M = d, K = f.  Weight row scales sa0 (gate / down) and sa1
 // (up), compact row scales sb.
 // ---------------------------------------------------------------------------
+// Item at hand-out position p.  The order is a sequence of blocks, one per
+// heavy group b (heavy expert, feature tile; in expert, feature-tile order):
+// the group's row slices, consecutive so that CTAs running them at the same
+// time share its weight tiles in L2, then light items in proportion to the
+// group's slices, so that the MMA-bound heavy items and the HBM-bound light
+// ones keep one ratio along the whole order.  With H_b the heavy items before
+// block b (H of them, L light ones), block b starts at B(b) = H_b + floor(H_b L / H).
+// heavy[0] = H, heavy[1] = the number of heavy experts; items are numbered in
+// `order` (heavy experts first) by item_off.
+__device__ __noinline__ Item decode_interleaved(int p, const int* item_off, const int* order, const int* ntiles,
+                                                const int* heavy, const int32_t* offsets, int E, int n_mt,
+                                                int slice) {
+    const int n_heavy_items = heavy[0];
+    const int n_groups = heavy[1] * n_mt;
+    int u = p;
+    if (n_groups > 0) {
+        const long long n_light = item_off[E] - n_heavy_items;
+        auto head_of = [&](int b) {
+            const int ei = b / n_mt, mt = b - ei * n_mt;
+            return item_off[ei] + mt * ntiles[order[ei]];
+        };
+        auto block_start = [&](int b) {
+            const int hb = head_of(b);
+            return hb + static_cast<int>(static_cast<long long>(hb) * n_light / n_heavy_items);
+        };
+        int lo = 0, hi = n_groups - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (block_start(mid) <= p) lo = mid;
+            else hi = mid - 1;
+        }
+        const int head = head_of(lo);
+        const int size = ntiles[order[lo / n_mt]];
+        const int b0 = block_start(lo);
+        const int o = p - b0;
+        u = o < size ? head + o : n_heavy_items + (b0 - head) + (o - size);
+    }
+    return decode_item_ordered(u, item_off, order, ntiles, offsets, E, slice);
+}
+
 template <bool GATED>
 __global__ void __launch_bounds__(kNThreads, 1)
     ffn_nvf4_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
@@ -166,6 +206,9 @@ __global__ void __launch_bounds__(kNThreads, 1)
     int* ntiles = item_off + kMaxExperts + 1;        // E entries
     volatile int* epi_flag = reinterpret_cast<volatile int*>(ntiles + kMaxExperts);  // 2 entries
     int* mode_big = const_cast<int*>(epi_flag + 2);   // launch-wide carve-up
+    int* order = mode_big + 1;                        // experts: the heavy ones, then the light ones (E entries)
+    int* heavy_items = order + kMaxExperts;           // items of the heavy experts
+    int* heavy_experts = heavy_items + 1;             // how many experts are heavy
     Item* ilist = reinterpret_cast<Item*>(ctrl + kNCtrlBytes);   // this CTA's items, in hand-out order
     __nv_bfloat16* out_stage = reinterpret_cast<__nv_bfloat16*>(ctrl + kNCtrlBytes + kNListBytes);
 
@@ -227,15 +270,40 @@ __global__ void __launch_bounds__(kNThreads, 1)
             GATED && rows > 0 && excess * 100 >= static_cast<long long>(MOE_NVF4_BIG_MODE_PCT) * rows;
         const int slice = big ? kSliceBig : kSliceN;
         if (lane == 0) *mode_big = big ? 1 : 0;
-        const int per = (E + 31) / 32;
-        int local = 0;
+        // Experts with more than one row slice ("heavy": their weight tiles serve
+        // several slices from L2, the MMAs set the pace) come first in `order`,
+        // the others ("light": each weight tile streamed from HBM for one slice)
+        // after them, each group in expert-id order; item_off is the exclusive
+        // scan of the item counts in that order.  The items are then handed out
+        // interleaved (item_at below).
+        const int per = (E + 31) / 32;                 // lane j owns experts / positions [j*per, (j+1)*per)
+        const int first = min(lane * per, E);
+        int nheavy = 0;
         for (int i = 0; i < per; ++i) {
             const int e = lane * per + i;
             if (e < E) {
                 const int n = bad ? 0 : offsets[e + 1] - offsets[e];
                 ntiles[e] = (n + slice - 1) / slice;
-                local += ntiles[e] * n_mt;
+                nheavy += ntiles[e] > 1 ? 1 : 0;
             }
+        }
+        int hincl = nheavy;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, hincl, off);
+            if (lane >= off) hincl += o;
+        }
+        const int n_heavy = __shfl_sync(0xffffffffu, hincl, 31);
+        int hpos = hincl - nheavy;                      // heavy experts before this lane's
+        int lpos = n_heavy + (first - hpos);            // light experts go after all heavy ones
+        for (int i = 0; i < per; ++i) {
+            const int e = lane * per + i;
+            if (e < E) order[ntiles[e] > 1 ? hpos++ : lpos++] = e;
+        }
+        __syncwarp();
+        int local = 0;
+        for (int i = 0; i < per; ++i) {
+            const int p = lane * per + i;
+            if (p < E) local += ntiles[order[p]] * n_mt;
         }
         int incl = local;
         for (int off = 1; off < 32; off <<= 1) {
@@ -244,13 +312,18 @@ __global__ void __launch_bounds__(kNThreads, 1)
         }
         int run = incl - local;
         for (int i = 0; i < per; ++i) {
-            const int e = lane * per + i;
-            if (e < E) {
-                item_off[e] = run;
-                run += ntiles[e] * n_mt;
+            const int p = lane * per + i;
+            if (p < E) {
+                item_off[p] = run;
+                run += ntiles[order[p]] * n_mt;
             }
         }
         if (lane == 31) item_off[E] = run;
+        __syncwarp();
+        if (lane == 0) {
+            *heavy_items = item_off[n_heavy];
+            *heavy_experts = n_heavy;
+        }
         if (bad && lane == 0) atomicOr(err, DEVERR_OFFSETS);
     }
     tc_fence_before();
@@ -265,7 +338,9 @@ __global__ void __launch_bounds__(kNThreads, 1)
     const int off_sa1 = off_sa0 + kSfaTile;
     const int off_sb = off_sa1 + kSfaTile;
     const int sfb_rows = big ? kSfbRowsBig : kSfbRows;
-    auto item_at = [&](int it) { return decode_item(it, item_off, ntiles, offsets, E, big ? kSliceBig : kSliceN); };
+    auto item_at = [&](int p) {
+        return decode_interleaved(p, item_off, order, ntiles, heavy_items, offsets, E, n_mt, big ? kSliceBig : kSliceN);
+    };
     // item j of this CTA is hand-out position blockIdx.x + j * gridDim.x
     const int n_list = static_cast<int>(blockIdx.x) < n_items
                            ? min((n_items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
