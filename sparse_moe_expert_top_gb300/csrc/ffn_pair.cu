@@ -10,11 +10,13 @@
 // MMA work, and each SM's shared memory serves half the operand reads.
 //
 // Roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (active in the even
-// CTA of the pair only), then the epilogue warps (4 for gate/up, 8 for down).
-// Both CTAs run the same item loop.  The odd CTA's TMA loads complete on the
-// even CTA's full barrier (the cta_group::2 form of the bulk tensor copy);
-// the MMA thread's commits arrive on the barriers of both CTAs (multicast);
-// the odd CTA's epilogue releases an accumulator on the even CTA's barrier.
+// CTA of the pair only), then eight epilogue warps (two groups of four taking
+// alternate 32-row chunks).  Both CTAs run the same item sequence, which the
+// even CTA's producer takes from a per-launch counter and publishes to both.
+// The odd CTA's TMA loads complete on the even CTA's full barrier (the
+// cta_group::2 form of the bulk tensor copy); the MMA thread's commits arrive
+// on the barriers of both CTAs (multicast); the odd CTA's epilogue releases
+// an accumulator on the even CTA's barrier.
 //
 // Work item: (expert e, a 256-feature tile of gate/up or a 512-feature tile
 // of down, a slice of at most 256 of the expert's compact rows).  The item's
